@@ -1,0 +1,239 @@
+"""fp64 sequential oracle of the ReplaySSM hot path (GDN and KDA).
+
+Test infrastructure only: the CUDA path never imports, links or runs this file.
+Only tests, the package's smoke check and the benchmark's CPU-baseline leg use it.
+
+What it computes, restated from the pages:
+
+* The gated delta rule, one token at a time, for every request slot and value
+  head (value head h reads key head h // G, adjacent value heads sharing a key
+  head: LightLLM PR #1690 "feat: add ReplaySSM state modes for GDN and KDA",
+  commit messages on grouped GDN key groups)::
+
+      GDN:  S <- exp(g) * S                 (one log-decay per value head)
+      KDA:  S <- diag(exp(g)) @ S            (one log-decay per key channel)
+      d    = beta * (v - S^T k)              (the delta; kept fp32 in the ring)
+      S   <- S + k d^T
+      o    = scale * S^T q
+
+* The exact committed state is carried forward. The oracle never replays: the
+  whole point of ReplaySSM is that a checkpoint plus a ring of accepted records
+  reproduces this same state, so the oracle keeps the state itself and, beside
+  it, the checkpoint value the GPU must hold and the ring records the GPU must
+  write (LightLLM PR #1690, PR description: the checkpoint is the canonical SSM
+  state, deltas are stored in fp32).
+* Ring, cursor and fold decisions follow ``oracle.ring``: a window folds when
+  forced or when it would overflow the ring, and the fold makes the checkpoint
+  equal to the committed state (in exact arithmetic a fold changes nothing).
+* Speculative verify (SGLang fork PR jianc99/sglang#2, commits on the verify
+  and the commit): a window of T draft tokens runs from the committed state and
+  writes its T records; commit keeps the first ``a`` tokens, trims the rest,
+  and in fold-every mode folds them into the checkpoint. Rejected positions
+  never reach the committed state: commit re-runs only the accepted tokens.
+
+Inputs are float64 arrays whose values are already the quantised values the
+GPU sees (bf16 inputs widened exactly). Layouts are token-major:
+q, k [B*T, HK, dk]; v [B*T, HV, dv]; beta [B*T, HV]; g [B*T, HV] (GDN) or
+[B*T, HV, dk] (KDA). Row r's token i is index r*T + i; a row whose slot is -1
+is a null row and is skipped entirely.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import ring
+
+__all__ = ["token_step", "ReplayOracle"]
+
+
+def token_step(S, q, k, v, beta, g, scale, algo):
+    """Advance states S [R, HV, dk, dv] by one token.
+
+    q, k: [R, HV, dk] (key heads already mapped onto value heads); v: [R, HV, dv];
+    beta: [R, HV]; g: [R, HV] (gdn) or [R, HV, dk] (kda). Returns the new
+    state, the delta d [R, HV, dv] and the output o [R, HV, dv].
+    """
+    if algo == "gdn":
+        S = np.exp(g)[:, :, None, None] * S
+    elif algo == "kda":
+        S = np.exp(g)[:, :, :, None] * S
+    else:
+        raise ValueError(algo)
+    Stk = np.matmul(k[:, :, None, :], S)[:, :, 0, :]          # S^T k
+    d = beta[:, :, None] * (v - Stk)
+    S = S + k[:, :, :, None] * d[:, :, None, :]
+    o = scale * np.matmul(q[:, :, None, :], S)[:, :, 0, :]     # S^T q
+    return S, d, o
+
+
+class ReplayOracle:
+    """Sequential fp64 model of one ReplaySSM store (all layers, all slots).
+
+    State kept per (layer, slot): ``S`` the exact committed state, ``ckpt`` the
+    value the GPU checkpoint must hold, and the ring records each window wrote.
+    ``cursor`` is shared by all layers of a slot, as on the GPU.
+    """
+
+    def __init__(self, algo, n_layers, n_slots, HK, HV, dk, dv, L, scale, S0):
+        if HV % HK:
+            raise ValueError("HV must be a multiple of HK")
+        self.algo, self.n_layers, self.n_slots = algo, n_layers, n_slots
+        self.HK, self.HV, self.dk, self.dv, self.L = HK, HV, dk, dv, L
+        self.G = HV // HK
+        self.scale = float(scale)
+        S0 = np.asarray(S0, dtype=np.float64)
+        if S0.shape == (n_slots, HV, dk, dv):
+            S0 = np.broadcast_to(S0, (n_layers,) + S0.shape)
+        assert S0.shape == (n_layers, n_slots, HV, dk, dv)
+        self.S = np.array(S0, dtype=np.float64)
+        self.ckpt = self.S.copy()
+        self.cursor = np.zeros(n_slots, dtype=np.int64)
+        ng = () if algo == "gdn" else (dk,)
+        nan = np.nan
+        self.ring_k = np.full((n_layers, n_slots, HK, L, dk), nan)
+        self.ring_d = np.full((n_layers, n_slots, HV, L, dv), nan)
+        self.ring_g = np.full((n_layers, n_slots, HV, L) + ng, nan)
+        self.ring_v = np.full((n_layers, n_slots, HV, L, dv), nan)
+        self.ring_beta = np.full((n_layers, n_slots, HV, L), nan)
+        # positions [base, base+T) written by the last window of each layer
+        self.written = np.zeros((n_layers, n_slots, L), dtype=bool)
+        self._pending: dict[int, dict] = {}
+
+    # ------------------------------------------------------------------ helpers
+    def _expand(self, x):
+        """[R, HK, dk] -> [R, HV, dk]: value head h uses key head h // G."""
+        return np.repeat(x, self.G, axis=1)
+
+    def _decide(self, slots, T, force):
+        B = len(slots)
+        fold = np.zeros(B, dtype=bool)
+        base = np.zeros(B, dtype=np.int64)
+        for r in range(B):
+            s = int(slots[r])
+            if s < 0:
+                continue
+            f, b = ring.fold_decision(int(self.cursor[s]), T, self.L, bool(force[r]))
+            fold[r], base[r] = f, b
+        return fold, base
+
+    def _token_inputs(self, inp, idx):
+        return (self._expand(inp["q"][idx]), self._expand(inp["k"][idx]),
+                inp["v"][idx], inp["beta"][idx], inp["g"][idx])
+
+    # --------------------------------------------------------------- hot path
+    def window(self, layer, slots, inp, T, force=None):
+        """Run one T-token window (decode: T=1) for every live row of one layer.
+
+        Returns (o, fold): o [B*T, HV, dv] with NaN on null rows; fold [B]
+        int8, 1 where the window folded, 0 where not, -1 on null rows.
+        """
+        slots = np.asarray(slots, dtype=np.int64)
+        B = slots.shape[0]
+        force = np.zeros(B, np.uint8) if force is None else np.asarray(force)
+        if not 1 <= T <= self.L:
+            raise ValueError("window must satisfy 1 <= T <= L")
+        fold, base = self._decide(slots, T, force)
+        live = np.nonzero(slots >= 0)[0]
+        o = np.full((B * T, self.HV, self.dv), np.nan)
+        flags = np.where(slots >= 0, fold.astype(np.int8), np.int8(-1))
+        if live.size:
+            sl = slots[live]
+            folded = sl[fold[live]]
+            # A fold makes the checkpoint the committed state and empties the ring.
+            self.ckpt[layer, folded] = self.S[layer, folded]
+            self.written[layer, sl] = False
+            S = self.S[layer, sl].copy()
+            with np.errstate(all="ignore"):
+                for i in range(T):
+                    idx = live * T + i
+                    q, k, v, beta, g = self._token_inputs(inp, idx)
+                    S, d, oi = token_step(S, q, k, v, beta, g, self.scale, self.algo)
+                    o[idx] = oi
+                    pos = base[live] + i
+                    self.ring_k[layer, sl, :, pos] = inp["k"][idx]
+                    self.ring_d[layer, sl, :, pos] = d
+                    self.ring_g[layer, sl, :, pos] = inp["g"][idx]
+                    self.ring_v[layer, sl, :, pos] = v
+                    self.ring_beta[layer, sl, :, pos] = beta
+                    self.written[layer, sl, pos] = True
+        self._pending[layer] = {"slots": slots.copy(), "inp": inp, "T": T,
+                                "force": np.asarray(force).copy(), "base": base}
+        return o, flags
+
+    def _accept(self, layer, accept):
+        """Commit ``accept[r]`` tokens of the pending window of one layer."""
+        pend = self._pending.pop(layer)
+        slots, inp, T = pend["slots"], pend["inp"], pend["T"]
+        live = np.nonzero(slots >= 0)[0]
+        if live.size == 0:
+            return
+        sl = slots[live]
+        S = self.S[layer, sl].copy()
+        a = np.asarray(accept)[live]
+        for i in range(T):
+            keep = np.nonzero(a > i)[0]          # rows that accept token i
+            if keep.size == 0:
+                break
+            idx = live[keep] * T + i
+            q, k, v, beta, g = self._token_inputs(inp, idx)
+            S[keep], _, _ = token_step(S[keep], q, k, v, beta, g, self.scale,
+                                       self.algo)
+        self.S[layer, sl] = S
+
+    def decode(self, layer, slots, inp, force=None, advance=False):
+        """Width-1 decode of one layer; the token is accepted at once.
+
+        The cursor (shared by all layers) moves only when ``advance`` is set,
+        i.e. after the last layer of the step.
+        """
+        o, flags = self.window(layer, slots, inp, 1, force)
+        B = len(slots)
+        self._accept(layer, np.ones(B, dtype=np.int64))
+        if advance:
+            force = np.zeros(B, np.uint8) if force is None else np.asarray(force)
+            for r, s in enumerate(np.asarray(slots)):
+                if s >= 0:
+                    self.cursor[s] = ring.cursor_after_decode(
+                        int(self.cursor[s]), self.L, bool(force[r]))
+        return o, flags
+
+    def commit(self, slots, accept, T, force=None, mode=ring.LAZY):
+        """Commit the pending verify windows of every layer, then the cursor."""
+        slots = np.asarray(slots, dtype=np.int64)
+        B = slots.shape[0]
+        force = np.zeros(B, np.uint8) if force is None else np.asarray(force)
+        accept = np.asarray(accept, dtype=np.int64)
+        for layer in sorted(self._pending):
+            if self._pending[layer]["T"] != T:
+                raise ValueError("commit T differs from the verified window")
+            self._accept(layer, accept)
+        for r, s in enumerate(slots):
+            if s < 0:
+                continue
+            c = int(self.cursor[s])
+            if mode == ring.FOLD_EVERY:
+                self.ckpt[:, s] = self.S[:, s]
+            self.cursor[s] = ring.cursor_after_commit(c, T, self.L, bool(force[r]),
+                                                      int(accept[r]), mode)
+
+    def fold(self, slots):
+        """Explicit fold: checkpoint <- committed state, cursor <- 0."""
+        for s in np.asarray(slots):
+            if s >= 0:
+                self.ckpt[:, s] = self.S[:, s]
+                self.cursor[s] = 0
+
+    def load_checkpoint(self, slot, S):
+        """Install a checkpoint in a slot (restore / state copy)."""
+        self.ckpt[:, slot] = S
+
+    def reset_slots(self, slots):
+        """Restore semantics: cursor <- 0, so the slot's state is its checkpoint."""
+        for s in np.asarray(slots):
+            if s >= 0:
+                self.cursor[s] = 0
+                self.S[:, s] = self.ckpt[:, s]
+
+    def accepted_positions(self, slot):
+        """Ring positions holding committed history: [0, cursor)."""
+        return np.arange(int(self.cursor[slot]))
