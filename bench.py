@@ -1,0 +1,506 @@
+#!/usr/bin/env python3
+"""Throughput of the ReplaySSM hot path on GB300: replayed tokens/s per layer
+and achieved HBM bandwidth of the replay kernel against the measured peak.
+
+Workload (N = 1): a Qwen3.5-4B-shaped Gated DeltaNet decode layer (HK = 16 key
+heads, HV = 32 value heads, dk = dv = 128, batch 64 with 8 null slots, ring
+L = 16, width T = 1, bf16 q/k/v, fp32 checkpoint and deltas, fp16 ring keys),
+48 stacked layers with distinct buffers. A step is one decode pass over all 48
+layers plus the cursor advance, replayed from a CUDA graph. The checkpoints
+(6 GiB) dwarf the 129 MB L2, so nothing is served from cache between steps.
+Rows join a few steps apart before timing, so their cursors are staggered and
+every step folds about one row in sixteen, as in steady serving.
+
+A second workload, reported under "verify", times speculative verify + commit
+(batch 128, T = 8, L = 16, random accept lengths) on the same head shapes.
+
+--impl reference times the fp64 oracle (CPU) on a bounded sample of the same
+workload. Under torchrun each rank runs an independent replica (no
+collective on the data path; weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "replayed tokens/s per layer (decode & verify) and HBM GB/s vs GB300 peak"
+UNIT = "tokens/s/layer"
+WL = dict(workload="Qwen3.5-4B-shaped GDN decode layer", algo="gdn", HK=16, HV=32, dk=128,
+          dv=128, batch=64, null_slots=8, L=16, T=1, in_dtype="bf16", state_dtype="f32",
+          ring_k_dtype="f16", ring_d_dtype="f32", layers=48)
+VERIFY = dict(workload="GDN speculative verify+commit", batch=128, T=8, L=16,
+              state_dtype="f32", commit_mode="lazy", layers=48)
+ESZ = {"f32": 4, "bf16": 2, "f16": 2}
+
+
+# --------------------------------------------------------------- accounting
+def row_bytes(c, T, fold, HK, HV, dk, dv, s_state, s_in, s_k, s_d, n_g=1):
+    """Algorithmic HBM bytes of one live row in one replay launch.
+
+    Reads: the checkpoint tile once, c history records (key per key head,
+    delta and gate per value head), the window's q/k/v/beta/g. Writes: the
+    outputs, T records (key per key head; delta, gate, v, beta per value head)
+    and, on a fold, the folded checkpoint.
+    """
+    state = HV * dk * dv * s_state
+    hist = c * (HK * dk * s_k + HV * dv * s_d + HV * n_g * 4)
+    win = T * (2 * HK * dk * s_in + HV * dv * s_in + HV * (1 + n_g) * 4)
+    out = T * HV * dv * s_in
+    rec = T * (HK * dk * s_k + HV * dv * s_d + HV * n_g * 4 + HV * dv * s_in + HV * 4)
+    return state + hist + win + out + rec + (state if fold else 0)
+
+
+def advance(c, T, L, a):
+    fold = c + T > L
+    return (0 if fold else c) + a, fold
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def ncu_traffic():
+    """Bytes per launch from the committed ncu summary, if its kernel sources
+    still hash to what was profiled; else None."""
+    path = os.path.join(ROOT, "profiles", "replay_gdn_decode_qwen_shapes.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    try:
+        want = vals["sources_sha256"]
+        per_launch = float(vals["dram_bytes_per_launch_full_batch"])
+    except (KeyError, ValueError):
+        return None
+    return per_launch if want == sources_hash() else None
+
+
+def sources_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "linear_attention_state_rssm_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc = index, None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for _, _, r in rows for i, x in enumerate(r)
+                          if x.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": rows[0][1],
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------- device inputs
+def device_inputs(torch, gen, n_layers, B, T, HK, HV, dk, dv, dtype):
+    """Seeded synthetic window inputs for every layer, resident in HBM:
+    q, k ~ N(0,1) L2-normalised per head, v ~ N(0,1), beta = sigmoid(N(0,1)),
+    g = -softplus(N(0,1)); packed so one copy moves a whole step."""
+    n = n_layers * B * T
+    dev = "cuda"
+    q = torch.randn((n, HK, dk), generator=gen, device=dev)
+    k = torch.randn((n, HK, dk), generator=gen, device=dev)
+    q = q / q.norm(dim=-1, keepdim=True)
+    k = k / k.norm(dim=-1, keepdim=True)
+    v = torch.randn((n, HV, dv), generator=gen, device=dev)
+    beta = torch.sigmoid(torch.randn((n, HV), generator=gen, device=dev))
+    g = -torch.nn.functional.softplus(torch.randn((n, HV), generator=gen, device=dev))
+    half = torch.cat([q.reshape(-1), k.reshape(-1), v.reshape(-1)]).to(dtype)
+    flt = torch.cat([beta.reshape(-1), g.reshape(-1)]).float()
+    return half, flt
+
+
+def views(half, flt, layer, n_layers, B, T, HK, HV, dk, dv):
+    nq = n_layers * B * T * HK * dk
+    per_q, per_v, per_s = B * T * HK * dk, B * T * HV * dv, B * T * HV
+    q = half[layer * per_q:(layer + 1) * per_q].view(B * T, HK, dk)
+    k = half[nq + layer * per_q:nq + (layer + 1) * per_q].view(B * T, HK, dk)
+    v = half[2 * nq + layer * per_v:2 * nq + (layer + 1) * per_v].view(B * T, HV, dv)
+    ns = n_layers * B * T * HV
+    beta = flt[layer * per_s:(layer + 1) * per_s].view(B * T, HV)
+    g = flt[ns + layer * per_s:ns + (layer + 1) * per_s].view(B * T, HV)
+    return q, k, v, beta, g
+
+
+# ------------------------------------------------------------------- ours
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from linear_attention_state_rssm_gb300 import build as _build
+    _build.build()
+    from linear_attention_state_rssm_gb300.store import ReplayStore
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = WL
+    nl, B, T, L = args.layers, w["batch"], w["T"], w["L"]
+    HK, HV, dk, dv = w["HK"], w["HV"], w["dk"], w["dv"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+
+    st = ReplayStore("gdn", nl, B, HK, HV, dk, dv, L, 1, w["in_dtype"], w["state_dtype"],
+                     w["ring_k_dtype"], w["ring_d_dtype"], "lazy", device=dev)
+    for layer in range(nl):
+        st.state[layer].normal_(0.0, 0.1, generator=gen)
+    null = torch.randperm(B, generator=torch.Generator().manual_seed(7))[:w["null_slots"]]
+    slots = torch.arange(B, dtype=torch.int32)
+    slots[null] = -1
+    live_rows = [r for r in range(B) if slots[r] >= 0]
+    B_live = len(live_rows)
+    slot_d = slots.to(dev)
+    half, flt = device_inputs(torch, gen, nl, B, T, HK, HV, dk, dv, torch.bfloat16)
+    out = torch.empty((nl, B * T, HV, dv), dtype=torch.bfloat16, device=dev)
+    lv = [views(half, flt, l, nl, B, T, HK, HV, dk, dv) for l in range(nl)]
+
+    def step(slot_t, events=None):
+        for l in range(nl):
+            if events is not None:
+                events[l].record()
+            st.rssm_decode(l, *lv[l], slot_t, out[l], advance_cursor=(l == nl - 1))
+        if events is not None:
+            events[nl].record()
+
+    # stagger: row r joins at step r % L so cursors spread over [0, L)
+    for j in range(L):
+        s = slots.clone()
+        for r in range(B):
+            if r % L > j:
+                s[r] = -1
+        step(s.to(dev))
+    torch.cuda.synchronize()
+    cur = st.cursor.cpu().tolist()
+
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            step(slot_d)
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+
+    def host_advance(cur, steps):
+        """Cursor trajectory and algorithmic bytes per launch for `steps` steps."""
+        per_launch = []
+        for _ in range(steps):
+            tot = 0
+            nxt = list(cur)
+            for r in live_rows:
+                c = cur[r]
+                nxt[r], fold = advance(c, T, L, 1)
+                tot += row_bytes(c, T, fold, HK, HV, dk, dv, 4, 2, 2, 4)
+            per_launch.append(tot)
+            cur = nxt
+        return cur, per_launch
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    cur, _ = host_advance(cur, args.warmup)
+
+    # ---- timed region: K steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local_rank) as clk:
+        e0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_ms = e0.elapsed_time(e1)
+    cur, bytes_timed = host_advance(cur, args.steps)
+    t_max = t_ms
+    if world > 1:
+        tt = torch.tensor([t_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    value = world * B_live * T * nl * args.steps / (t_max / 1e3)
+    ms_per_step = t_max / args.steps
+
+    # ---- per-launch duration of the replay kernel: events between layers on
+    # the launching stream; a GPU sleep queued first lets the host enqueue the
+    # whole step before it starts, so the intervals hold no launch gaps.
+    durs, kbytes = [], []
+    n_inst = max(3, min(args.steps, 10))
+    ev_i = [torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)]
+    for _ in range(n_inst):
+        torch.cuda._sleep(20_000_000)
+        step(slot_d, ev_i)
+        torch.cuda.synchronize()
+        durs += [ev_i[l].elapsed_time(ev_i[l + 1]) for l in range(nl)]
+        cur, b = host_advance(cur, 1)
+        kbytes += [b[0]] * nl
+    # the last layer's interval also holds the cursor kernel: leave it out
+    lay = [d for i, d in enumerate(durs) if i % nl != nl - 1]
+    lay_b = [b for i, b in enumerate(kbytes) if i % nl != nl - 1]
+    k_ms = statistics.mean(lay)
+    k_bytes = statistics.mean(lay_b)
+    achieved = k_bytes / (k_ms / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    traffic = ncu_traffic()
+
+    # ---- end to end through the C ABI with host buffers
+    half_h = half.cpu().pin_memory()
+    flt_h = flt.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    for _ in range(2):
+        half.copy_(half_h, non_blocking=True)
+        flt.copy_(flt_h, non_blocking=True)
+        graph.replay()
+        out_h.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record()
+    for _ in range(args.steps):
+        half.copy_(half_h, non_blocking=True)
+        flt.copy_(flt_h, non_blocking=True)
+        graph.replay()
+        out_h.copy_(out, non_blocking=True)
+    e3.record()
+    torch.cuda.synchronize()
+    te = e2.elapsed_time(e3)
+    if world > 1:
+        tt = torch.tensor([te], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        te = float(tt.item())
+    e2e = {"value": world * B_live * T * nl * args.steps / (te / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": half.numel() * 2 + flt.numel() * 4,
+           "d2h_bytes_per_step": out.numel() * 2}
+    err = st.rssm_get_device_error()
+    del graph, st, half, flt, out, lv
+    torch.cuda.empty_cache()
+
+    ver = run_verify(args, torch, dev, rank) if not args.no_verify else None
+
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded torch RNG on device; distributions of the pages' tiny "
+                "GDN workload)",
+        "config": {"workload": w["workload"], "algo": "gdn", "HK": HK, "HV": HV, "dk": dk,
+                   "dv": dv, "batch": B, "live_rows": B_live, "L": L, "T": T,
+                   "layers": nl, "in_dtype": w["in_dtype"], "state_dtype": w["state_dtype"],
+                   "ring_k_dtype": w["ring_k_dtype"], "ring_d_dtype": w["ring_d_dtype"],
+                   "cuda_graph": True, "replicas": world,
+                   "l2": "inputs larger than L2 (48 distinct layers, 6 GiB of checkpoints)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} (hbm_gbs, burst)",
+                     "traffic": traffic, "kernel": "replay_kernel<GDN, f32, 1>",
+                     "algorithmic_bytes_per_launch": k_bytes, "launch_ms": k_ms},
+        "gpu_launches": args.steps * (nl + 1),
+        "e2e": e2e,
+        "clocks": clk.summary(),
+        "device_error_word": err,
+    }
+    if ver is not None:
+        res["verify"] = ver
+    return res
+
+
+def run_verify(args, torch, dev, rank):
+    """Speculative verify (T = 8) + lazy commit over 48 layers, batch 128."""
+    from linear_attention_state_rssm_gb300.store import ReplayStore
+    w, v = WL, VERIFY
+    nl, B, T, L = args.layers, v["batch"], v["T"], v["L"]
+    HK, HV, dk, dv = w["HK"], w["HV"], w["dk"], w["dv"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2000 + rank)
+    st = ReplayStore("gdn", nl, B, HK, HV, dk, dv, L, T, "bf16", v["state_dtype"], "f16", "f32",
+                     v["commit_mode"], device=dev)
+    for layer in range(nl):
+        st.state[layer].normal_(0.0, 0.1, generator=gen)
+    slot = torch.arange(B, dtype=torch.int32, device=dev)
+    half, flt = device_inputs(torch, gen, nl, B, T, HK, HV, dk, dv, torch.bfloat16)
+    out = torch.empty((nl, B * T, HV, dv), dtype=torch.bfloat16, device=dev)
+    lv = [views(half, flt, l, nl, B, T, HK, HV, dk, dv) for l in range(nl)]
+    n_acc = args.warmup + args.steps + 1
+    acc = torch.randint(0, T + 1, (n_acc, B), generator=gen, device=dev, dtype=torch.int32)
+    acc_cur = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def step():
+        for l in range(nl):
+            st.rssm_verify(l, *lv[l], slot, T, out[l])
+        st.rssm_commit(slot, acc_cur, T)
+
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            step()
+    torch.cuda.current_stream().wait_stream(cap)
+    for i in range(args.warmup):
+        acc_cur.copy_(acc[i])
+        graph.replay()
+    torch.cuda.synchronize()
+    acc_sum = int(acc[args.warmup:args.warmup + args.steps].sum().item())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        acc_cur.copy_(acc[args.warmup + i])
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3
+    err = st.rssm_get_device_error()
+    del graph, st
+    torch.cuda.empty_cache()
+    return {"workload": v["workload"], "batch": B, "T": T, "L": L, "layers": nl,
+            "state_dtype": v["state_dtype"], "commit_mode": v["commit_mode"],
+            "replayed_tokens_per_s_per_layer": B * T * nl * args.steps / t,
+            "accepted_tokens_per_s_per_layer": acc_sum * nl / t,
+            "ms_per_step": t * 1e3 / args.steps, "device_error_word": err}
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample(rows, steps):
+    """Time the fp64 oracle on `rows` rows of the decode workload (1 layer)."""
+    import numpy as np
+    import synth
+    from oracle import ReplayOracle
+    w = WL
+    HK, HV, dk, dv, L = w["HK"], w["HV"], w["dk"], w["dv"], w["L"]
+    S0 = synth.initial_state(1, rows, HV, dk, dv)
+    orc = ReplayOracle("gdn", 1, rows, HK, HV, dk, dv, L, dk ** -0.5, S0)
+    inps = [synth.window_inputs(s, rows, 1, HK, HV, dk, dv, "gdn", "bf16") for s in range(steps)]
+    slots = np.arange(rows)
+    orc.decode(0, slots, inps[0], advance=True)            # warm the allocator
+    c0, t0 = time.process_time(), time.perf_counter()
+    for s in range(steps):
+        orc.decode(0, slots, inps[s], advance=True)
+    wall = time.perf_counter() - t0
+    cpu = time.process_time() - c0
+    return rows * steps / wall, wall, max(1, round(cpu / wall))
+
+
+def run_reference(args):
+    rows, per_step = 8, 1
+    t_total, toks = 0.0, 0
+    for _ in range(args.warmup):
+        oracle_sample(rows, per_step)
+    cores = 1
+    for _ in range(args.steps):
+        v, wall, cores = oracle_sample(rows, per_step)
+        t_total += wall
+        toks += rows * per_step
+    value = toks / t_total
+    sample = f"{rows} rows x 1 layer x 1 decode step per bench step, fp64 numpy oracle"
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WL["workload"], "batch": rows, "L": WL["L"], "T": 1},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=WL["layers"])
+    ap.add_argument("--no-verify", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            v, wall, cores = oracle_sample(8, 20)
+            res["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                   "sample": "8 live rows x 1 layer x 20 decode steps of the "
+                                             f"same workload ({wall:.1f} s wall)"}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,219 @@
+/*
+ * rssm.h — C ABI of the GB300 ReplaySSM hot path (gated delta rule, GDN and KDA).
+ *
+ * What the operations compute, restated from the pages they come from:
+ *
+ *  - LightLLM PR #1690 "feat: add ReplaySSM state modes for GDN and KDA"
+ *    (PR description and commit messages): per request, a canonical checkpoint
+ *    state plus a buffer of accepted-token records with a cursor; decode replays
+ *    checkpoint + history + the new token; a ring that the next window would
+ *    overflow is folded inside the decode kernel; the cursor advances once per
+ *    step after the last layer; a restored slot has its cursor cleared; deltas
+ *    are stored in fp32, keys in fp16 for bf16 activations.
+ *  - SGLang fork PR jianc99/sglang#2 (GDN ReplaySSM for DFLASH/DSPARK), commit
+ *    messages and "Modifications": speculative verify writes its T draft records
+ *    at ring positions [write_pos, write_pos + T) and solves the window in the
+ *    (I + A)^-1 triangular form with causal selects, so non-finite values at
+ *    rejected drafts never reach accepted outputs; commit trims the rejected
+ *    tail and (fold-every mode) folds the accepted window into the checkpoint;
+ *    rows whose state slot is null (-1) are skipped by every kernel.
+ *  - vLLM PR #64699 "[Feature][MRV2] Enable Qwen3.5 GDN ReplaySSM standard
+ *    decode", commit messages: a per-row forced flush (fold) at any boundary.
+ *
+ * Per token t of a (request, value head) with state S[dk][dv]:
+ *   GDN: S <- exp(g_t) S        KDA: S <- diag(exp(g_t)) S   (g_t per key channel)
+ *   d_t = beta_t (v_t - S^T k_t);  S <- S + k_t d_t^T;  o_t = scale S^T q_t.
+ * Value head h reads key head h / (HV/HK).
+ *
+ * Memory ownership: the caller allocates every device buffer and owns every
+ * stream. The library borrows the pointers given to rssm_alloc for the life of
+ * the handle and allocates nothing on the device; the handle itself is a small
+ * host object. All index/length arrays passed per call are DEVICE pointers, so
+ * no call synchronises the device or allocates (rssm_get_device_error excepted,
+ * which synchronises the given stream). Every enqueueing call may be captured
+ * in a CUDA graph.
+ *
+ * Errors: arguments the host can check are validated before anything is
+ * enqueued; a failed check returns RSSM_ERR_INVALID_ARG or
+ * RSSM_ERR_UNSUPPORTED and launches nothing. Conditions only the device can see
+ * (a slot index >= n_slots, a cursor outside [0, L], an accepted length outside
+ * [0, T], a bounded wait that ran out) set bits in the device error word and the
+ * affected row is skipped; the kernels never trap. A null slot (-1) is not an
+ * error: its row is skipped and its outputs are left untouched. Two live rows
+ * of one call must not name the same slot (the result is then undefined).
+ * Launch failures return RSSM_ERR_CUDA. No C++ exception crosses this ABI.
+ *
+ * Layouts (row-major, element counts; "tok" = r*T + i for row r, token i):
+ *   q, k : [B*T][HK][dk]  in_dtype          v, o : [B*T][HV][dv] in_dtype
+ *   beta : [B*T][HV] fp32                   g    : [B*T][HV] (GDN) | [B*T][HV][dk] (KDA) fp32
+ *   state    : [n_layers][n_slots][HV][dk][dv]  state_dtype (the checkpoint)
+ *   ring_k   : [n_layers][n_slots][HK][L][dk]   ring_k_dtype
+ *   ring_d   : [n_layers][n_slots][HV][L][dv]   ring_d_dtype
+ *   ring_g   : [n_layers][n_slots][HV][L]       (GDN) | [..][L][dk] (KDA) fp32
+ *   ring_v   : [n_layers][n_slots][HV][L][dv]   in_dtype
+ *   ring_beta: [n_layers][n_slots][HV][L]       fp32
+ *   cursor   : [n_slots] int32, shared by all layers
+ *   err_word : [1] uint32
+ */
+#ifndef RSSM_H_
+#define RSSM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rssm_status {
+  RSSM_OK = 0,
+  RSSM_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad index or size      */
+  RSSM_ERR_UNSUPPORTED = 2,  /* valid but not built: dims, dtypes, G > 8, smem  */
+  RSSM_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed             */
+  RSSM_ERR_DEVICE = 4        /* rssm_get_device_error found a non-zero word      */
+} rssm_status;
+
+enum { RSSM_ALGO_GDN = 0, RSSM_ALGO_KDA = 1 };
+enum { RSSM_F32 = 0, RSSM_BF16 = 1, RSSM_F16 = 2 };
+enum { RSSM_COMMIT_LAZY = 0, RSSM_COMMIT_FOLD_EVERY = 1 };
+
+/* Bits of the device error word. */
+enum {
+  RSSM_DEVERR_SLOT = 1u,     /* slot index >= n_slots                 */
+  RSSM_DEVERR_CURSOR = 2u,   /* cursor outside [0, L]                 */
+  RSSM_DEVERR_ACCEPT = 4u,   /* accepted length outside [0, T]        */
+  RSSM_DEVERR_TIMEOUT = 8u   /* a bounded wait on a tile copy ran out */
+};
+
+/*
+ * Store configuration. Supported: dk, dv in {32, 64, 128}; HV a multiple of HK
+ * with G = HV/HK <= 8; 1 <= max_T <= 16; max_T <= L <= 256 (a ring shorter than
+ * the widest window is refused, SGLang fork PR jianc99/sglang#2, first commit);
+ * in_dtype F32|BF16; state_dtype F32|BF16; ring_k_dtype F32|F16|BF16;
+ * ring_d_dtype F32|F16. commit_mode selects what rssm_commit does.
+ */
+typedef struct rssm_config {
+  int32_t algo;
+  int32_t n_layers;
+  int32_t n_slots;
+  int32_t HK;
+  int32_t HV;
+  int32_t dk;
+  int32_t dv;
+  int32_t L;
+  int32_t max_T;
+  int32_t in_dtype;
+  int32_t state_dtype;
+  int32_t ring_k_dtype;
+  int32_t ring_d_dtype;
+  int32_t commit_mode;
+  float scale;
+} rssm_config;
+
+/* Device buffers (layouts above). All must be non-null; state, ring_k, ring_d
+ * and ring_v must be 16-byte aligned. Borrowed for the life of the handle. */
+typedef struct rssm_buffers {
+  void *state;
+  void *ring_k;
+  void *ring_d;
+  float *ring_g;
+  void *ring_v;
+  float *ring_beta;
+  int32_t *cursor;
+  uint32_t *err_word;
+} rssm_buffers;
+
+/* Byte sizes of each buffer for a configuration. */
+typedef struct rssm_sizes {
+  size_t state;
+  size_t ring_k;
+  size_t ring_d;
+  size_t ring_g;
+  size_t ring_v;
+  size_t ring_beta;
+  size_t cursor;
+  size_t err_word;
+} rssm_sizes;
+
+typedef struct rssm_handle rssm_handle;
+
+/* Pure host: fills *out for a valid configuration. */
+rssm_status rssm_required_bytes(const rssm_config *cfg, rssm_sizes *out);
+
+/* Validates cfg and buffers, prepares kernel attributes on the current device
+ * and returns a host handle in *out (freed by rssm_free). Does not touch the
+ * buffers' contents: the caller zeroes cursor and err_word and writes the
+ * initial checkpoint. */
+rssm_status rssm_alloc(const rssm_config *cfg, const rssm_buffers *buf,
+                       rssm_handle **out);
+void rssm_free(rssm_handle *h);
+
+/*
+ * Width-1 replay decode of one layer (LightLLM PR #1690, commit messages on
+ * decode and on the fused fold). For each row r with s = slot[r] >= 0:
+ * c = cursor[s]; fold = force[r] || c + 1 > L. On fold the history is folded
+ * into the checkpoint first (S0 <- replayed state) and the new record goes to
+ * ring position 0, else to c. Writes o (B rows), the token's record
+ * (k once per key head, d, g, v, beta) and, if fold_out is non-null,
+ * fold_out[r] = fold (0/1) for live rows. When advance_cursor is non-zero
+ * (the last layer of the step) the cursor kernel then sets
+ * cursor[s] = (fold ? 0 : c) + 1. force and fold_out may be null.
+ * B == 0 is a no-op. Pointers are device pointers; stream is a cudaStream_t.
+ */
+rssm_status rssm_decode(rssm_handle *h, int32_t layer, const void *q,
+                        const void *k, const void *v, const float *beta,
+                        const float *g, const int32_t *slot,
+                        const uint8_t *force, int32_t B, void *o,
+                        uint8_t *fold_out, int32_t advance_cursor,
+                        void *stream);
+
+/*
+ * Speculative verify of one layer: a window of T (1 <= T <= max_T) draft tokens
+ * per row, same rules as decode with c + T > L as the overflow test; writes
+ * T outputs per row and the T records at [base, base + T). Never moves the
+ * cursor (rssm_commit does). Non-finite inputs at positions the later commit
+ * rejects cannot change accepted outputs, accepted records or the state.
+ */
+rssm_status rssm_verify(rssm_handle *h, int32_t layer, const void *q,
+                        const void *k, const void *v, const float *beta,
+                        const float *g, const int32_t *slot,
+                        const uint8_t *force, int32_t B, int32_t T, void *o,
+                        uint8_t *fold_out, void *stream);
+
+/*
+ * Commit the last verify of every layer (SGLang fork PR jianc99/sglang#2,
+ * fourth commit). accept_len[r] in [0, T]; slot/force/T must equal the
+ * verify's. LAZY: cursor[s] = base + a (rejected tail trimmed). FOLD_EVERY:
+ * for every layer S0 <- fold of the base + a records, then cursor[s] = 0.
+ */
+rssm_status rssm_commit(rssm_handle *h, const int32_t *slot,
+                        const uint8_t *force, const int32_t *accept_len,
+                        int32_t B, int32_t T, void *stream);
+
+/* Explicit fold of every layer's history into its checkpoint, then cursor <- 0
+ * (LightLLM PR #1690: materialise the canonical state). */
+rssm_status rssm_fold(rssm_handle *h, const int32_t *slot, int32_t B,
+                      void *stream);
+
+/* Restore semantics: cursor <- 0 for the given slots, so a slot whose
+ * checkpoint was just written (state copy, restore) starts with an empty
+ * history (LightLLM PR #1690, PR description and commit messages). */
+rssm_status rssm_reset_slots(rssm_handle *h, const int32_t *slot, int32_t B,
+                             void *stream);
+
+/* Synchronises `stream`, reads the device error word into *out and clears it
+ * when `clear` is non-zero. Returns RSSM_ERR_DEVICE if the word was non-zero.
+ * For tests and debugging; not capturable. */
+rssm_status rssm_get_device_error(rssm_handle *h, uint32_t *out, int32_t clear,
+                                  void *stream);
+
+const char *rssm_status_string(rssm_status s);
+
+/* ABI version of this header: 1. */
+int32_t rssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RSSM_H_ */

@@ -1,0 +1,352 @@
+// C ABI of librssm: host-side validation, per-layer addressing and launches.
+// See include/rssm.h for the contract of every entry point.
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "../../include/rssm.h"
+#include "rssm_common.cuh"
+#include "rssm_launch.h"
+
+using namespace rssm;
+
+struct rssm_handle {
+  rssm_config cfg;
+  rssm_buffers buf;
+  int G;
+  int max_smem;
+  size_t layer_state, layer_k, layer_d, layer_g, layer_v, layer_beta;  // elements
+};
+
+namespace {
+
+constexpr int kMaxL = 256;
+constexpr int kMaxT = 16;
+constexpr int kMaxGroup = 8;
+constexpr int kMaxGrid = 65535;
+
+bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+int n_gate(const rssm_config& c) { return c.algo == RSSM_ALGO_GDN ? 1 : c.dk; }
+
+rssm_status check_config(const rssm_config* c) {
+  if (c == nullptr) return RSSM_ERR_INVALID_ARG;
+  if (c->algo != RSSM_ALGO_GDN && c->algo != RSSM_ALGO_KDA) return RSSM_ERR_INVALID_ARG;
+  if (c->n_layers < 1 || c->n_slots < 1 || c->HK < 1 || c->HV < 1) return RSSM_ERR_INVALID_ARG;
+  if (c->HV % c->HK != 0) return RSSM_ERR_INVALID_ARG;
+  if (c->max_T < 1 || c->L < 1) return RSSM_ERR_INVALID_ARG;
+  // A ring that cannot hold the widest window is refused up front.
+  if (c->max_T > c->L) return RSSM_ERR_INVALID_ARG;
+  if (c->dk < 1 || c->dv < 1) return RSSM_ERR_INVALID_ARG;
+  if (!(c->in_dtype == RSSM_F32 || c->in_dtype == RSSM_BF16 || c->in_dtype == RSSM_F16))
+    return RSSM_ERR_INVALID_ARG;
+  if (!(c->state_dtype == RSSM_F32 || c->state_dtype == RSSM_BF16 ||
+        c->state_dtype == RSSM_F16))
+    return RSSM_ERR_INVALID_ARG;
+  if (!(c->ring_k_dtype == RSSM_F32 || c->ring_k_dtype == RSSM_BF16 ||
+        c->ring_k_dtype == RSSM_F16))
+    return RSSM_ERR_INVALID_ARG;
+  if (!(c->ring_d_dtype == RSSM_F32 || c->ring_d_dtype == RSSM_BF16 ||
+        c->ring_d_dtype == RSSM_F16))
+    return RSSM_ERR_INVALID_ARG;
+  if (c->commit_mode != RSSM_COMMIT_LAZY && c->commit_mode != RSSM_COMMIT_FOLD_EVERY)
+    return RSSM_ERR_INVALID_ARG;
+  if (!std::isfinite(c->scale)) return RSSM_ERR_INVALID_ARG;
+  // Valid but not built.
+  if (!dim_ok(c->dk) || !dim_ok(c->dv)) return RSSM_ERR_UNSUPPORTED;
+  if (c->HV / c->HK > kMaxGroup) return RSSM_ERR_UNSUPPORTED;
+  if (c->max_T > kMaxT || c->L > kMaxL) return RSSM_ERR_UNSUPPORTED;
+  if (c->in_dtype == RSSM_F16 || c->state_dtype == RSSM_F16 || c->ring_d_dtype == RSSM_BF16)
+    return RSSM_ERR_UNSUPPORTED;
+  if (c->HV > kMaxGrid || c->n_layers > kMaxGrid) return RSSM_ERR_UNSUPPORTED;
+  return RSSM_OK;
+}
+
+size_t esize(int dt) { return dt == RSSM_F32 ? 4 : 2; }
+
+void sizes_of(const rssm_config& c, rssm_sizes* s) {
+  const size_t ls = (size_t)c.n_layers * c.n_slots;
+  s->state = ls * c.HV * c.dk * c.dv * esize(c.state_dtype);
+  s->ring_k = ls * c.HK * c.L * c.dk * esize(c.ring_k_dtype);
+  s->ring_d = ls * c.HV * c.L * c.dv * esize(c.ring_d_dtype);
+  s->ring_g = ls * c.HV * c.L * n_gate(c) * sizeof(float);
+  s->ring_v = ls * c.HV * c.L * c.dv * esize(c.in_dtype);
+  s->ring_beta = ls * c.HV * c.L * sizeof(float);
+  s->cursor = (size_t)c.n_slots * sizeof(int32_t);
+  s->err_word = sizeof(uint32_t);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+rssm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA; }
+
+int state_dt(const rssm_config& c) { return c.state_dtype == RSSM_F32 ? DT_F32 : DT_BF16; }
+
+cudaError_t replay_launch(const rssm_config& c, const ReplayParams& p, int NT, int cluster,
+                          cudaStream_t st) {
+  const bool f32 = c.state_dtype == RSSM_F32;
+  if (c.algo == RSSM_ALGO_GDN) {
+    return f32 ? replay_gdn_f32_launch(p, NT, cluster, st)
+               : replay_gdn_bf16_launch(p, NT, cluster, st);
+  }
+  return f32 ? replay_kda_f32_launch(p, NT, cluster, st)
+             : replay_kda_bf16_launch(p, NT, cluster, st);
+}
+
+cudaError_t replay_prepare(const rssm_config& c, int max_smem) {
+  const bool f32 = c.state_dtype == RSSM_F32;
+  if (c.algo == RSSM_ALGO_GDN) {
+    return f32 ? replay_gdn_f32_prepare(max_smem) : replay_gdn_bf16_prepare(max_smem);
+  }
+  return f32 ? replay_kda_f32_prepare(max_smem) : replay_kda_bf16_prepare(max_smem);
+}
+
+ReplaySmem layout_for(const rssm_config& c, int T) {
+  return replay_layout(c.algo, (int)esize(c.state_dtype), nt_for(T), T, c.L, c.dk, c.dv);
+}
+
+FoldSmem fold_layout_for(const rssm_config& c) {
+  return fold_layout(c.algo, (int)esize(c.state_dtype), c.L, c.dk, c.dv);
+}
+
+template <typename T>
+T* at(void* base, size_t elems, size_t esz) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + elems * esz);
+}
+
+rssm_status window(rssm_handle* h, int32_t layer, const void* q, const void* k, const void* v,
+                   const float* beta, const float* g, const int32_t* slot,
+                   const uint8_t* force, int32_t B, int32_t T, void* o, uint8_t* fold_out,
+                   void* stream) {
+  if (h == nullptr) return RSSM_ERR_INVALID_ARG;
+  const rssm_config& c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers) return RSSM_ERR_INVALID_ARG;
+  if (B < 0 || B > kMaxGrid) return RSSM_ERR_INVALID_ARG;
+  if (T < 1 || T > c.max_T) return RSSM_ERR_INVALID_ARG;
+  if (B == 0) return RSSM_OK;
+  if (!q || !k || !v || !beta || !g || !slot || !o) return RSSM_ERR_INVALID_ARG;
+  if (!aligned4(beta) || !aligned4(g) || !aligned4(slot)) return RSSM_ERR_INVALID_ARG;
+
+  ReplayParams p{};
+  const rssm_buffers& b = h->buf;
+  p.state = at<char>(b.state, layer * h->layer_state, esize(c.state_dtype));
+  p.ring_k = at<char>(b.ring_k, layer * h->layer_k, esize(c.ring_k_dtype));
+  p.ring_d = at<char>(b.ring_d, layer * h->layer_d, esize(c.ring_d_dtype));
+  p.ring_g = b.ring_g + layer * h->layer_g;
+  p.ring_v = at<char>(b.ring_v, layer * h->layer_v, esize(c.in_dtype));
+  p.ring_beta = b.ring_beta + layer * h->layer_beta;
+  p.cursor = b.cursor;
+  p.err = b.err_word;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.beta = beta;
+  p.g = g;
+  p.slot = slot;
+  p.force = force;
+  p.o = o;
+  p.fold_out = fold_out;
+  p.B = B;
+  p.T = T;
+  p.L = c.L;
+  p.n_slots = c.n_slots;
+  p.HK = c.HK;
+  p.HV = c.HV;
+  p.G = h->G;
+  p.dk = c.dk;
+  p.dv = c.dv;
+  p.in_dt = c.in_dtype;
+  p.rk_dt = c.ring_k_dtype;
+  p.rd_dt = c.ring_d_dtype;
+  p.scale = c.scale;
+  p.sm = layout_for(c, T);
+  if ((int)p.sm.total > h->max_smem) return RSSM_ERR_UNSUPPORTED;
+  return from_cuda(replay_launch(c, p, nt_for(T), h->G,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+FoldParams fold_params(const rssm_handle* h, const int32_t* slot, const uint8_t* force,
+                       const int32_t* accept, int B, int T, int mode) {
+  const rssm_config& c = h->cfg;
+  FoldParams p{};
+  p.state = h->buf.state;
+  p.ring_k = h->buf.ring_k;
+  p.ring_d = h->buf.ring_d;
+  p.ring_g = h->buf.ring_g;
+  p.cursor = h->buf.cursor;
+  p.err = h->buf.err_word;
+  p.slot = slot;
+  p.force = force;
+  p.accept = accept;
+  p.layer_state = h->layer_state;
+  p.layer_k = h->layer_k;
+  p.layer_d = h->layer_d;
+  p.layer_g = h->layer_g;
+  p.B = B;
+  p.T = T;
+  p.L = c.L;
+  p.n_slots = c.n_slots;
+  p.HK = c.HK;
+  p.HV = c.HV;
+  p.G = h->G;
+  p.dk = c.dk;
+  p.dv = c.dv;
+  p.rk_dt = c.ring_k_dtype;
+  p.rd_dt = c.ring_d_dtype;
+  p.mode = mode;
+  p.sm = fold_layout_for(c);
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+rssm_status rssm_required_bytes(const rssm_config* cfg, rssm_sizes* out) {
+  if (out == nullptr) return RSSM_ERR_INVALID_ARG;
+  const rssm_status st = check_config(cfg);
+  if (st != RSSM_OK) return st;
+  sizes_of(*cfg, out);
+  return RSSM_OK;
+}
+
+rssm_status rssm_alloc(const rssm_config* cfg, const rssm_buffers* buf, rssm_handle** out) {
+  if (out == nullptr || buf == nullptr) return RSSM_ERR_INVALID_ARG;
+  *out = nullptr;
+  const rssm_status st = check_config(cfg);
+  if (st != RSSM_OK) return st;
+  const rssm_buffers& b = *buf;
+  if (!b.state || !b.ring_k || !b.ring_d || !b.ring_g || !b.ring_v || !b.ring_beta ||
+      !b.cursor || !b.err_word)
+    return RSSM_ERR_INVALID_ARG;
+  if (!aligned16(b.state) || !aligned16(b.ring_k) || !aligned16(b.ring_d) ||
+      !aligned16(b.ring_v) || !aligned4(b.ring_g) || !aligned4(b.ring_beta) ||
+      !aligned4(b.cursor) || !aligned4(b.err_word))
+    return RSSM_ERR_INVALID_ARG;
+
+  int dev = 0, max_smem = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RSSM_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+      cudaSuccess)
+    return RSSM_ERR_CUDA;
+  // The widest window this store allows must fit in shared memory.
+  const ReplaySmem worst = layout_for(*cfg, cfg->max_T);
+  const FoldSmem fworst = fold_layout_for(*cfg);
+  if ((int)worst.total > max_smem || (int)fworst.total > max_smem) return RSSM_ERR_UNSUPPORTED;
+  if (replay_prepare(*cfg, max_smem) != cudaSuccess) return RSSM_ERR_CUDA;
+  if (fold_prepare(cfg->algo, state_dt(*cfg), max_smem) != cudaSuccess) return RSSM_ERR_CUDA;
+
+  rssm_handle* h = new (std::nothrow) rssm_handle;
+  if (h == nullptr) return RSSM_ERR_INVALID_ARG;
+  h->cfg = *cfg;
+  h->buf = b;
+  h->G = cfg->HV / cfg->HK;
+  h->max_smem = max_smem;
+  const size_t slots = (size_t)cfg->n_slots;
+  h->layer_state = slots * cfg->HV * cfg->dk * cfg->dv;
+  h->layer_k = slots * cfg->HK * cfg->L * cfg->dk;
+  h->layer_d = slots * cfg->HV * cfg->L * cfg->dv;
+  h->layer_g = slots * cfg->HV * cfg->L * n_gate(*cfg);
+  h->layer_v = slots * cfg->HV * cfg->L * cfg->dv;
+  h->layer_beta = slots * cfg->HV * cfg->L;
+  *out = h;
+  return RSSM_OK;
+}
+
+void rssm_free(rssm_handle* h) { delete h; }
+
+rssm_status rssm_decode(rssm_handle* h, int32_t layer, const void* q, const void* k,
+                        const void* v, const float* beta, const float* g, const int32_t* slot,
+                        const uint8_t* force, int32_t B, void* o, uint8_t* fold_out,
+                        int32_t advance_cursor, void* stream) {
+  const rssm_status st = window(h, layer, q, k, v, beta, g, slot, force, B, 1, o, fold_out,
+                                stream);
+  if (st != RSSM_OK || B == 0 || !advance_cursor) return st;
+  const rssm_config& c = h->cfg;
+  return from_cuda(cursor_launch(h->buf.cursor, slot, force, nullptr, B, 1, c.L, c.n_slots,
+                                 CURSOR_DECODE, h->buf.err_word,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+rssm_status rssm_verify(rssm_handle* h, int32_t layer, const void* q, const void* k,
+                        const void* v, const float* beta, const float* g, const int32_t* slot,
+                        const uint8_t* force, int32_t B, int32_t T, void* o, uint8_t* fold_out,
+                        void* stream) {
+  return window(h, layer, q, k, v, beta, g, slot, force, B, T, o, fold_out, stream);
+}
+
+rssm_status rssm_commit(rssm_handle* h, const int32_t* slot, const uint8_t* force,
+                        const int32_t* accept_len, int32_t B, int32_t T, void* stream) {
+  if (h == nullptr) return RSSM_ERR_INVALID_ARG;
+  const rssm_config& c = h->cfg;
+  if (B < 0 || B > kMaxGrid || T < 1 || T > c.max_T) return RSSM_ERR_INVALID_ARG;
+  if (B == 0) return RSSM_OK;
+  if (!slot || !accept_len) return RSSM_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c.commit_mode == RSSM_COMMIT_FOLD_EVERY) {
+    const FoldParams p = fold_params(h, slot, force, accept_len, B, T, FOLD_COMMIT);
+    const cudaError_t e = fold_launch(c.algo, state_dt(c), p, c.n_layers, st);
+    if (e != cudaSuccess) return RSSM_ERR_CUDA;
+    return from_cuda(cursor_launch(h->buf.cursor, slot, force, accept_len, B, T, c.L,
+                                   c.n_slots, CURSOR_COMMIT_FOLD, h->buf.err_word, st));
+  }
+  return from_cuda(cursor_launch(h->buf.cursor, slot, force, accept_len, B, T, c.L, c.n_slots,
+                                 CURSOR_COMMIT_LAZY, h->buf.err_word, st));
+}
+
+rssm_status rssm_fold(rssm_handle* h, const int32_t* slot, int32_t B, void* stream) {
+  if (h == nullptr) return RSSM_ERR_INVALID_ARG;
+  if (B < 0 || B > kMaxGrid) return RSSM_ERR_INVALID_ARG;
+  if (B == 0) return RSSM_OK;
+  if (!slot) return RSSM_ERR_INVALID_ARG;
+  const rssm_config& c = h->cfg;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const FoldParams p = fold_params(h, slot, nullptr, nullptr, B, 1, FOLD_ALL);
+  const cudaError_t e = fold_launch(c.algo, state_dt(c), p, c.n_layers, st);
+  if (e != cudaSuccess) return RSSM_ERR_CUDA;
+  return from_cuda(cursor_launch(h->buf.cursor, slot, nullptr, nullptr, B, 1, c.L, c.n_slots,
+                                 CURSOR_ZERO, h->buf.err_word, st));
+}
+
+rssm_status rssm_reset_slots(rssm_handle* h, const int32_t* slot, int32_t B, void* stream) {
+  if (h == nullptr) return RSSM_ERR_INVALID_ARG;
+  if (B < 0 || B > kMaxGrid) return RSSM_ERR_INVALID_ARG;
+  if (B == 0) return RSSM_OK;
+  if (!slot) return RSSM_ERR_INVALID_ARG;
+  const rssm_config& c = h->cfg;
+  return from_cuda(cursor_launch(h->buf.cursor, slot, nullptr, nullptr, B, 1, c.L, c.n_slots,
+                                 CURSOR_ZERO, h->buf.err_word,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+rssm_status rssm_get_device_error(rssm_handle* h, uint32_t* out, int32_t clear, void* stream) {
+  if (h == nullptr || out == nullptr) return RSSM_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return RSSM_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, h->buf.err_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return RSSM_ERR_CUDA;
+  if (clear) {
+    if (cudaMemsetAsync(h->buf.err_word, 0, sizeof(uint32_t), st) != cudaSuccess)
+      return RSSM_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return RSSM_ERR_CUDA;
+  }
+  *out = word;
+  return word == 0 ? RSSM_OK : RSSM_ERR_DEVICE;
+}
+
+const char* rssm_status_string(rssm_status s) {
+  switch (s) {
+    case RSSM_OK: return "ok";
+    case RSSM_ERR_INVALID_ARG: return "invalid argument";
+    case RSSM_ERR_UNSUPPORTED: return "unsupported configuration";
+    case RSSM_ERR_CUDA: return "CUDA runtime error";
+    case RSSM_ERR_DEVICE: return "device error word set";
+  }
+  return "unknown status";
+}
+
+int32_t rssm_version(void) { return 1; }
+
+}  // extern "C"

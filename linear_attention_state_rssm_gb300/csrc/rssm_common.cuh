@@ -1,0 +1,275 @@
+// Shared definitions of the ReplaySSM kernels: launch parameters, the shared
+// memory plan, dtype helpers and the inline-PTX primitives (mbarrier, bulk
+// async copy, cluster barrier) used on sm_103a.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace rssm {
+
+enum : int { ALGO_GDN = 0, ALGO_KDA = 1 };
+enum : int { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
+enum : uint32_t {
+  DEVERR_SLOT = 1u,
+  DEVERR_CURSOR = 2u,
+  DEVERR_ACCEPT = 4u,
+  DEVERR_TIMEOUT = 8u,
+};
+enum : int { CURSOR_DECODE = 0, CURSOR_COMMIT_LAZY = 1, CURSOR_ZERO = 2, CURSOR_COMMIT_FOLD = 3 };
+enum : int { FOLD_ALL = 0, FOLD_COMMIT = 1 };
+
+constexpr int kThreads = 128;  // 4 warps per CTA, one CTA per (row, value head)
+constexpr int kWarps = kThreads / 32;
+constexpr unsigned kFull = 0xffffffffu;
+// A bounded wait gives up after this many nanoseconds of %globaltimer.
+constexpr unsigned long long kWaitLimitNs = 500ull * 1000ull * 1000ull;
+
+__host__ __device__ constexpr int dtype_bytes(int dt) { return dt == DT_F32 ? 4 : 2; }
+__host__ __device__ constexpr uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
+
+// Byte offsets into the dynamic shared memory of the replay kernel.
+struct ReplaySmem {
+  uint32_t mbar;   // kWarps mbarriers (one per row chunk of the state tile)
+  uint32_t wq;     // [T][dk]  window q (fp32)
+  uint32_t wk;     // [T][dk]  window k (fp32)
+  uint32_t wv;     // [T][dv]  window v (fp32)
+  uint32_t wb;     // [NT]     window beta
+  uint32_t wg;     // [T] (GDN) | [T][dk] (KDA): window gates -> inclusive prefix
+  uint32_t scal;   // GDN: es[NT], eG[NT], gam; KDA: egam[dk], gam[dk]
+  uint32_t xh;     // [dk][2NT] mat-vec inputs
+  uint32_t am;     // [NT][NT] window coefficients A (strictly lower)
+  uint32_t fm;     // [NT][NT] window coefficients F (lower incl. diagonal)
+  uint32_t hk;     // [L][dk]  history keys (KDA: decay-scaled)
+  uint32_t hd;     // [L][dv]  history deltas
+  uint32_t hf;     // [L]      GDN: raw gates -> exp(suffix sums)
+  uint32_t hdot;   // [L][2NT] history dot coefficients
+  uint32_t red;    // [kWarps][VB][dv] partial mat-vec sums (unless aliased)
+  uint32_t total;
+  int red_alias;   // partial sums overwrite each warp's own consumed tile rows
+};
+
+struct ReplayParams {
+  // store (layer offset already applied)
+  void* state;
+  void* ring_k;
+  void* ring_d;
+  float* ring_g;
+  void* ring_v;
+  float* ring_beta;
+  const int32_t* cursor;
+  uint32_t* err;
+  // window
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* beta;
+  const float* g;
+  const int32_t* slot;
+  const uint8_t* force;
+  void* o;
+  uint8_t* fold_out;
+  int B, T, L, n_slots, HK, HV, G, dk, dv;
+  int in_dt, rk_dt, rd_dt;
+  float scale;
+  ReplaySmem sm;
+};
+
+struct FoldSmem {
+  uint32_t mbar, hk, hd, hf, scal, total;
+};
+
+struct FoldParams {
+  void* state;
+  const void* ring_k;
+  const void* ring_d;
+  const float* ring_g;
+  const int32_t* cursor;
+  uint32_t* err;
+  const int32_t* slot;
+  const uint8_t* force;
+  const int32_t* accept;
+  size_t layer_state, layer_k, layer_d, layer_g;  // per-layer strides (elements)
+  int B, T, L, n_slots, HK, HV, G, dk, dv;
+  int rk_dt, rd_dt, mode;
+  FoldSmem sm;
+};
+
+// Vector-block width of the mat-vec accumulators.
+__host__ __device__ constexpr int vblock(int NT) { return 2 * NT < 16 ? 2 * NT : 16; }
+
+// Shared memory plan of the replay kernel for a window of T <= NT tokens and a
+// ring of L records.
+__host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, int NT,
+                                                    int T, int L, int dk, int dv) {
+  ReplaySmem m{};
+  const int NV = 2 * NT;
+  const int VB = vblock(NT);
+  uint32_t off = align16((uint32_t)dk * dv * state_bytes);
+  m.mbar = off;  off = align16(off + 8u * kWarps);
+  m.wq = off;    off = align16(off + 4u * T * dk);
+  m.wk = off;    off = align16(off + 4u * T * dk);
+  m.wv = off;    off = align16(off + 4u * T * dv);
+  m.wb = off;    off = align16(off + 4u * NT);
+  m.wg = off;    off = align16(off + 4u * T * (algo == ALGO_GDN ? 1 : dk));
+  m.scal = off;  off = align16(off + 4u * (algo == ALGO_GDN ? 2 * NT + 4 : 2 * dk));
+  m.xh = off;    off = align16(off + 4u * dk * NV);
+  m.am = off;    off = align16(off + 4u * NT * NT);
+  m.fm = off;    off = align16(off + 4u * NT * NT);
+  m.hk = off;    off = align16(off + 4u * L * dk);
+  m.hd = off;    off = align16(off + 4u * L * dv);
+  m.hf = off;    off = align16(off + 4u * L);
+  m.hdot = off;  off = align16(off + 4u * L * NV);
+  // Each warp's partial sums fit in its own rows of the tile when one vector
+  // block covers all vectors and VB*dv*4 <= (dk/4)*dv*state_bytes.
+  m.red_alias = (NV == VB) && (VB * 16 <= dk * state_bytes);
+  m.red = off;
+  if (!m.red_alias) off = align16(off + 4u * kWarps * VB * dv);
+  m.total = off;
+  return m;
+}
+
+__host__ __device__ inline FoldSmem fold_layout(int algo, int state_bytes, int L, int dk,
+                                                int dv) {
+  FoldSmem m{};
+  uint32_t off = align16((uint32_t)dk * dv * state_bytes);
+  m.mbar = off;  off = align16(off + 8u * kWarps);
+  m.hk = off;    off = align16(off + 4u * L * dk);
+  m.hd = off;    off = align16(off + 4u * L * dv);
+  m.hf = off;    off = align16(off + 4u * L);
+  m.scal = off;  off = align16(off + 4u * (algo == ALGO_GDN ? 4 : 2 * dk));
+  m.total = off;
+  return m;
+}
+
+#if defined(__CUDACC__)
+
+// ------------------------------------------------------------------ dtypes
+__device__ __forceinline__ float ld_f32(const void* base, size_t i, int dt) {
+  if (dt == DT_F32) return static_cast<const float*>(base)[i];
+  if (dt == DT_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]);
+  return __half2float(static_cast<const __half*>(base)[i]);
+}
+
+__device__ __forceinline__ void st_f32(void* base, size_t i, int dt, float x) {
+  if (dt == DT_F32) {
+    static_cast<float*>(base)[i] = x;
+  } else if (dt == DT_BF16) {
+    static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(x);
+  } else {
+    static_cast<__half*>(base)[i] = __float2half_rn(x);
+  }
+}
+
+template <typename ST>
+struct StateIO;
+
+template <>
+struct StateIO<float> {
+  static __device__ __forceinline__ float4 load4(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+  }
+  static __device__ __forceinline__ void store4(float* p, float4 x) {
+    *reinterpret_cast<float4*>(p) = x;
+  }
+};
+
+template <>
+struct StateIO<__nv_bfloat16> {
+  static __device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+    const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+    return make_float4(fa.x, fa.y, fb.x, fb.y);
+  }
+  static __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 x) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(x.z, x.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&a);
+    u.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
+};
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// One bulk (non-tensor) async copy global -> shared, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of `bar`, giving up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(kFull, x, off);
+  return x;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace rssm

@@ -1,0 +1,31 @@
+// Host-side entry points of the kernel translation units (internal to librssm).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "rssm_common.cuh"
+
+namespace rssm {
+
+// Window widths the replay kernel is built for; a window of T tokens runs in
+// the smallest width >= T.
+inline int nt_for(int T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16; }
+
+#define RSSM_DECLARE_REPLAY(NAME)                                                      \
+  cudaError_t NAME##_launch(const ReplayParams& p, int NT, int cluster, cudaStream_t st); \
+  cudaError_t NAME##_prepare(int max_smem);
+
+RSSM_DECLARE_REPLAY(replay_gdn_f32)
+RSSM_DECLARE_REPLAY(replay_gdn_bf16)
+RSSM_DECLARE_REPLAY(replay_kda_f32)
+RSSM_DECLARE_REPLAY(replay_kda_bf16)
+#undef RSSM_DECLARE_REPLAY
+
+cudaError_t fold_launch(int algo, int state_dt, const FoldParams& p, int n_layers,
+                        cudaStream_t st);
+cudaError_t fold_prepare(int algo, int state_dt, int max_smem);
+cudaError_t cursor_launch(int32_t* cursor, const int32_t* slot, const uint8_t* force,
+                          const int32_t* accept, int B, int T, int L, int n_slots, int mode,
+                          uint32_t* err, cudaStream_t st);
+
+}  // namespace rssm

@@ -61,7 +61,7 @@ def token_step(S, q, k, v, beta, g, scale, algo):
         raise ValueError(algo)
     Stk = np.matmul(k[:, :, None, :], S)[:, :, 0, :]          # S^T k
     d = beta[:, :, None] * (v - Stk)
-    S = S + k[:, :, :, None] * d[:, :, None, :]
+    S += k[:, :, :, None] * d[:, :, None, :]                  # S is a fresh array here
     o = scale * np.matmul(q[:, :, None, :], S)[:, :, 0, :]     # S^T q
     return S, d, o
 
@@ -98,6 +98,8 @@ class ReplayOracle:
         # positions [base, base+T) written by the last window of each layer
         self.written = np.zeros((n_layers, n_slots, L), dtype=bool)
         self._pending: dict[int, dict] = {}
+        # rows per batch of work: keeps each temporary near 16 MB
+        self._chunk = max(1, (16 << 20) // (HV * dk * dv * 8))
 
     # ------------------------------------------------------------------ helpers
     def _expand(self, x):
@@ -142,43 +144,60 @@ class ReplayOracle:
             # A fold makes the checkpoint the committed state and empties the ring.
             self.ckpt[layer, folded] = self.S[layer, folded]
             self.written[layer, sl] = False
-            S = self.S[layer, sl].copy()
+            final = np.empty((live.size, self.HV, self.dk, self.dv))
             with np.errstate(all="ignore"):
-                for i in range(T):
-                    idx = live * T + i
-                    q, k, v, beta, g = self._token_inputs(inp, idx)
-                    S, d, oi = token_step(S, q, k, v, beta, g, self.scale, self.algo)
-                    o[idx] = oi
-                    pos = base[live] + i
-                    self.ring_k[layer, sl, :, pos] = inp["k"][idx]
-                    self.ring_d[layer, sl, :, pos] = d
-                    self.ring_g[layer, sl, :, pos] = inp["g"][idx]
-                    self.ring_v[layer, sl, :, pos] = v
-                    self.ring_beta[layer, sl, :, pos] = beta
-                    self.written[layer, sl, pos] = True
+                for c0 in range(0, live.size, self._chunk):
+                    rows = live[c0:c0 + self._chunk]
+                    final[c0:c0 + rows.size] = self._run_window(layer, rows, slots, inp, T,
+                                                                base, o)
+        else:
+            final = None
         self._pending[layer] = {"slots": slots.copy(), "inp": inp, "T": T,
-                                "force": np.asarray(force).copy(), "base": base}
+                                "force": np.asarray(force).copy(), "base": base,
+                                "final": final}
         return o, flags
+
+    def _run_window(self, layer, rows, slots, inp, T, base, o):
+        """Run the T window tokens of some live rows; record outputs and ring
+        records; return the rows' states after the window."""
+        sl = slots[rows]
+        S = self.S[layer, sl]                     # fancy indexing: a copy
+        for i in range(T):
+            idx = rows * T + i
+            q, k, v, beta, g = self._token_inputs(inp, idx)
+            S, d, oi = token_step(S, q, k, v, beta, g, self.scale, self.algo)
+            o[idx] = oi
+            pos = base[rows] + i
+            self.ring_k[layer, sl, :, pos] = inp["k"][idx]
+            self.ring_d[layer, sl, :, pos] = d
+            self.ring_g[layer, sl, :, pos] = inp["g"][idx]
+            self.ring_v[layer, sl, :, pos] = v
+            self.ring_beta[layer, sl, :, pos] = beta
+            self.written[layer, sl, pos] = True
+        return S
 
     def _accept(self, layer, accept):
         """Commit ``accept[r]`` tokens of the pending window of one layer."""
         pend = self._pending.pop(layer)
-        slots, inp, T = pend["slots"], pend["inp"], pend["T"]
+        slots, inp, T, final = pend["slots"], pend["inp"], pend["T"], pend["final"]
         live = np.nonzero(slots >= 0)[0]
-        if live.size == 0:
-            return
-        sl = slots[live]
-        S = self.S[layer, sl].copy()
-        a = np.asarray(accept)[live]
-        for i in range(T):
-            keep = np.nonzero(a > i)[0]          # rows that accept token i
-            if keep.size == 0:
-                break
-            idx = live[keep] * T + i
-            q, k, v, beta, g = self._token_inputs(inp, idx)
-            S[keep], _, _ = token_step(S[keep], q, k, v, beta, g, self.scale,
-                                       self.algo)
-        self.S[layer, sl] = S
+        a_live = np.asarray(accept)[live]
+        for c0 in range(0, live.size, self._chunk):
+            rows = live[c0:c0 + self._chunk]
+            a = a_live[c0:c0 + rows.size]
+            sl = slots[rows]
+            S = self.S[layer, sl]                 # fancy indexing: a copy
+            full = a == T                         # whole window accepted: final state
+            S[full] = final[c0:c0 + rows.size][full]
+            for i in range(T):
+                keep = np.nonzero(~full & (a > i))[0]   # rows that accept token i
+                if keep.size == 0:
+                    break
+                idx = rows[keep] * T + i
+                q, k, v, beta, g = self._token_inputs(inp, idx)
+                S[keep], _, _ = token_step(S[keep], q, k, v, beta, g, self.scale,
+                                           self.algo)
+            self.S[layer, sl] = S
 
     def decode(self, layer, slots, inp, force=None, advance=False):
         """Width-1 decode of one layer; the token is accepted at once.

@@ -1,0 +1,129 @@
+"""Drive the CUDA store (through the C ABI) and the fp64 oracle on the same
+seeded inputs, and measure their differences. Test-side only."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import synth
+from oracle import ReplayOracle, ring
+
+TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+SENTINEL = 12345.0
+
+
+def dev(x, dtype):
+    """Exact upload of values already on the dtype grid."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64)).to(
+        device="cuda", dtype=TORCH[dtype])
+
+
+def rel_err(a, b, mask=None):
+    """max|a - b| / max|b| over the (masked) elements; both float64."""
+    if mask is not None:
+        a, b = a[mask], b[mask]
+    if b.size == 0:
+        return 0.0
+    den = np.max(np.abs(b))
+    return float(np.max(np.abs(a - b)) / den) if den > 0 else float(np.max(np.abs(a - b)))
+
+
+class Run:
+    """One store on the GPU and its oracle, over rows ``sample`` of the batch."""
+
+    def __init__(self, *, algo="gdn", HK, HV, dk, dv, L, max_T, slots, n_slots=None,
+                 n_layers=1, in_dtype="f32", state_dtype="f32", ring_k_dtype=None,
+                 ring_d_dtype="f32", commit_mode="lazy", config_id=0, sample=None):
+        from linear_attention_state_rssm_gb300 import ReplayStore
+        self.algo, self.HK, self.HV, self.dk, self.dv, self.L = algo, HK, HV, dk, dv, L
+        self.in_dtype, self.state_dtype, self.config_id = in_dtype, state_dtype, config_id
+        self.commit_mode = commit_mode
+        self.slots = np.asarray(slots, dtype=np.int32)
+        self.B = self.slots.size
+        self.n_slots = int(n_slots if n_slots is not None else max(self.slots.max() + 1, 1))
+        self.n_layers = n_layers
+        self.store = ReplayStore(algo, n_layers, self.n_slots, HK, HV, dk, dv, L, max_T,
+                                 in_dtype, state_dtype, ring_k_dtype, ring_d_dtype, commit_mode)
+        S0 = np.stack([synth.initial_state(synth.seed_for(config_id, 10_000, l), self.n_slots,
+                                           HV, dk, dv, state_dtype) for l in range(n_layers)])
+        self.store.state.copy_(dev(S0, state_dtype))
+        self.slot_t = torch.from_numpy(self.slots).cuda()
+        # oracle over the sampled rows' slots (rows are independent)
+        self.sample = np.arange(self.B) if sample is None else np.asarray(sample)
+        live_slots = sorted({int(self.slots[r]) for r in self.sample if self.slots[r] >= 0})
+        self.orc_index = {s: j for j, s in enumerate(live_slots)}
+        self.orc_slots = np.array([self.orc_index.get(int(self.slots[r]), -1)
+                                   for r in self.sample], dtype=np.int64)
+        self.orc_gpu_slots = np.array(live_slots, dtype=np.int64)
+        self.orc = ReplayOracle(algo, n_layers, max(len(live_slots), 1), HK, HV, dk, dv, L,
+                                self.store.scale, S0[:, live_slots] if live_slots else
+                                S0[:, :1])
+
+    # ------------------------------------------------------------------ inputs
+    def inputs(self, step, layer, T):
+        return synth.window_inputs(synth.seed_for(self.config_id, step, layer), self.B, T,
+                                   self.HK, self.HV, self.dk, self.dv, self.algo, self.in_dtype)
+
+    def _sub(self, inp, T):
+        tok = (self.sample[:, None] * T + np.arange(T)[None, :]).reshape(-1)
+        return {key: val[tok] for key, val in inp.items()}
+
+    def _gpu_inputs(self, inp):
+        return (dev(inp["q"], self.in_dtype), dev(inp["k"], self.in_dtype),
+                dev(inp["v"], self.in_dtype), dev(inp["beta"], "f32"), dev(inp["g"], "f32"))
+
+    # ------------------------------------------------------------------ steps
+    def window(self, layer, inp, T, force=None, decode=False, advance=False):
+        """Run one layer's window on both sides. Returns (o_gpu_all, o_gpu,
+        o_orc, fold_gpu, fold_orc): the GPU output of every row, then the GPU
+        output, oracle output and fold flags of the sampled rows."""
+        q, k, v, beta, g = self._gpu_inputs(inp)
+        o = torch.full((self.B * T, self.HV, self.dv), SENTINEL, dtype=TORCH[self.in_dtype],
+                       device="cuda")
+        fold_out = torch.full((self.B,), 7, dtype=torch.uint8, device="cuda")
+        force_t = None if force is None else torch.from_numpy(np.asarray(force, np.uint8)).cuda()
+        if decode:
+            self.store.rssm_decode(layer, q, k, v, beta, g, self.slot_t, o, force=force_t,
+                                   fold_out=fold_out, advance_cursor=advance)
+        else:
+            self.store.rssm_verify(layer, q, k, v, beta, g, self.slot_t, T, o, force=force_t,
+                                   fold_out=fold_out)
+        sub = self._sub(inp, T)
+        fsub = None if force is None else np.asarray(force)[self.sample]
+        if decode:
+            o_orc, f_orc = self.orc.decode(layer, self.orc_slots, sub, fsub, advance)
+        else:
+            o_orc, f_orc = self.orc.window(layer, self.orc_slots, sub, T, fsub)
+        o_gpu = o.double().cpu().numpy()
+        tok = (self.sample[:, None] * T + np.arange(T)[None, :]).reshape(-1)
+        return o_gpu, o_gpu[tok], o_orc, fold_out.cpu().numpy()[self.sample], f_orc
+
+    def commit(self, accept, T, force=None):
+        acc_t = torch.from_numpy(np.asarray(accept, np.int32)).cuda()
+        force_t = None if force is None else torch.from_numpy(np.asarray(force, np.uint8)).cuda()
+        self.store.rssm_commit(self.slot_t, acc_t, T, force=force_t)
+        mode = ring.FOLD_EVERY if self.commit_mode == "fold_every" else ring.LAZY
+        fsub = None if force is None else np.asarray(force)[self.sample]
+        self.orc.commit(self.orc_slots, np.asarray(accept)[self.sample], T, fsub, mode)
+
+    # ------------------------------------------------------------- inspection
+    def cursor_gpu(self):
+        return self.store.cursor.cpu().numpy()
+
+    def check_cursors(self):
+        """GPU cursors of the oracle's slots equal the oracle's, bit for bit."""
+        cur = self.cursor_gpu()
+        np.testing.assert_array_equal(cur[self.orc_gpu_slots], self.orc.cursor[:len(self.orc_gpu_slots)])
+
+    def state_err(self):
+        """Checkpoint (GPU) vs the checkpoint the oracle says it must hold."""
+        S = self.store.state.double().cpu().numpy()[:, self.orc_gpu_slots]
+        return rel_err(S, self.orc.ckpt[:, :len(self.orc_gpu_slots)])
+
+    def ring_d_err(self):
+        """Committed history records d[0, cursor) vs the oracle's."""
+        d = self.store.ring_d.double().cpu().numpy()[:, self.orc_gpu_slots]
+        mask = np.zeros(d.shape, dtype=bool)
+        for j, s in enumerate(self.orc_gpu_slots):
+            mask[:, j, :, :int(self.orc.cursor[j])] = True
+        return rel_err(d, self.orc.ring_d[:, :len(self.orc_gpu_slots)], mask)

@@ -1,0 +1,95 @@
+"""The C ABI library builds, loads and exports every symbol include/rssm.h
+declares; host-only entry points work without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_state_rssm_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "rssm.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"\b(rssm_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding():
+    assert _declared() == sorted(_lib.SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version_and_status_strings(lib):
+    assert _lib.rssm_version() == 1
+    assert _lib.rssm_status_string(0) == "ok"
+    assert _lib.rssm_status_string(2) == "unsupported configuration"
+
+
+def test_required_bytes_matches_layouts(lib):
+    cfg = _lib.make_config("gdn", n_layers=3, n_slots=5, HK=16, HV=32, dk=128, dv=128, L=16,
+                           max_T=8, in_dtype="bf16", state_dtype="f32")
+    s = _lib.rssm_required_bytes(cfg)
+    assert s.state == 3 * 5 * 32 * 128 * 128 * 4
+    assert s.ring_k == 3 * 5 * 16 * 16 * 128 * 2          # fp16 keys for bf16 inputs
+    assert s.ring_d == 3 * 5 * 32 * 16 * 128 * 4
+    assert s.ring_g == 3 * 5 * 32 * 16 * 4
+    assert s.ring_v == 3 * 5 * 32 * 16 * 128 * 2
+    assert s.ring_beta == 3 * 5 * 32 * 16 * 4
+    assert s.cursor == 5 * 4 and s.err_word == 4
+    kda = _lib.make_config("kda", n_layers=1, n_slots=2, HK=4, HV=4, dk=64, dv=32, L=8,
+                           max_T=3, in_dtype="f32", state_dtype="bf16", ring_d_dtype="f16")
+    s = _lib.rssm_required_bytes(kda)
+    assert s.state == 2 * 4 * 64 * 32 * 2 and s.ring_g == 2 * 4 * 8 * 64 * 4
+    assert s.ring_d == 2 * 4 * 8 * 32 * 2
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(max_T=17, L=32), 2),           # window wider than built
+    (dict(max_T=8, L=4), 1),             # ring shorter than the window
+    (dict(dk=96), 2),                    # head size not built
+    (dict(HK=3, HV=8), 1),               # HV not a multiple of HK
+    (dict(HK=1, HV=16), 2),              # GQA group above 8
+    (dict(n_slots=0), 1),
+    (dict(L=300, max_T=1), 2),
+])
+def test_host_validation(lib, kw, status):
+    base = dict(algo="gdn", n_layers=1, n_slots=2, HK=2, HV=4, dk=64, dv=64, L=8, max_T=2,
+                in_dtype="f32", state_dtype="f32")
+    base.update(kw)
+    cfg = _lib.make_config(**base)
+    with pytest.raises(_lib.RssmError) as e:
+        _lib.rssm_required_bytes(cfg)
+    assert e.value.status == status
+
+
+def test_alloc_refuses_bad_buffers_before_touching_the_device(lib):
+    cfg = _lib.make_config("gdn", 1, 2, 2, 4, 64, 64, 8, 2, "f32", "f32")
+    bufs = _lib.rssm_buffers(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0, 0x8000)
+    with pytest.raises(_lib.RssmError) as e:              # null cursor
+        _lib.rssm_alloc(cfg, bufs)
+    assert e.value.status == 1
+    bufs = _lib.rssm_buffers(0x1004, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000)
+    with pytest.raises(_lib.RssmError) as e:              # misaligned state
+        _lib.rssm_alloc(cfg, bufs)
+    assert e.value.status == 1
+
+
+def test_null_handle_is_refused(lib):
+    with pytest.raises(_lib.RssmError):
+        _lib.rssm_commit(None, None, None, None, 1, 1, stream=0)
+    with pytest.raises(_lib.RssmError):
+        _lib.rssm_fold(None, None, 1, stream=0)
