@@ -12,5 +12,5 @@ never calls it; there is no CPU fallback anywhere in the product.
 Pins (tests that check the oracle against something other than itself) live
 in ``tests/test_oracle_pins.py`` and ``tests/test_ring_rules.py``.
 """
-from .recurrence import ReplayOracle, token_step  # noqa: F401
+from .recurrence import ReplayOracle, round_bf16, token_step  # noqa: F401
 from . import ring  # noqa: F401

@@ -43,7 +43,22 @@ import numpy as np
 
 from . import ring
 
-__all__ = ["token_step", "ReplayOracle"]
+__all__ = ["token_step", "ReplayOracle", "round_bf16"]
+
+
+def round_bf16(x):
+    """Round float64 values to the nearest bfloat16 value, ties to even.
+
+    bfloat16 keeps 8 significant bits (1 implicit + 7 stored) and the float32
+    exponent range. With x = m * 2**e, 0.5 <= |m| < 1, the nearest value is
+    rint(m * 2**8) * 2**(e - 8); numpy's rint rounds halves to even. Non-finite
+    values pass through. (Values below the float32 normal range, never met
+    here, keep 8 bits instead of becoming bfloat16 subnormals.)
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    r = np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+    return np.where(np.isfinite(x), r, x)
 
 
 def token_step(S, q, k, v, beta, g, scale, algo):
@@ -74,13 +89,21 @@ class ReplayOracle:
     ``cursor`` is shared by all layers of a slot, as on the GPU.
     """
 
-    def __init__(self, algo, n_layers, n_slots, HK, HV, dk, dv, L, scale, S0):
+    def __init__(self, algo, n_layers, n_slots, HK, HV, dk, dv, L, scale, S0,
+                 ckpt_round=None):
+        """``ckpt_round="bf16"`` models a bf16 checkpoint: at every fold the
+        committed state is rounded to bf16 and the chain continues from the
+        rounded value, as the GPU does (vLLM PR #64699, commit message on
+        accounting for BF16 state rounding between flushes)."""
         if HV % HK:
             raise ValueError("HV must be a multiple of HK")
         self.algo, self.n_layers, self.n_slots = algo, n_layers, n_slots
         self.HK, self.HV, self.dk, self.dv, self.L = HK, HV, dk, dv, L
         self.G = HV // HK
         self.scale = float(scale)
+        if ckpt_round not in (None, "bf16"):
+            raise ValueError(ckpt_round)
+        self.ckpt_round = ckpt_round
         S0 = np.asarray(S0, dtype=np.float64)
         if S0.shape == (n_slots, HV, dk, dv):
             S0 = np.broadcast_to(S0, (n_layers,) + S0.shape)
@@ -118,6 +141,13 @@ class ReplayOracle:
             fold[r], base[r] = f, b
         return fold, base
 
+    def _checkpoint(self, layer, slots):
+        """Fold: the checkpoint takes the committed state (rounded to the
+        checkpoint dtype when modelled; the chain then continues from it)."""
+        if self.ckpt_round == "bf16":
+            self.S[layer, slots] = round_bf16(self.S[layer, slots])
+        self.ckpt[layer, slots] = self.S[layer, slots]
+
     def _token_inputs(self, inp, idx):
         return (self._expand(inp["q"][idx]), self._expand(inp["k"][idx]),
                 inp["v"][idx], inp["beta"][idx], inp["g"][idx])
@@ -142,7 +172,7 @@ class ReplayOracle:
             sl = slots[live]
             folded = sl[fold[live]]
             # A fold makes the checkpoint the committed state and empties the ring.
-            self.ckpt[layer, folded] = self.S[layer, folded]
+            self._checkpoint(layer, folded)
             self.written[layer, sl] = False
             final = np.empty((live.size, self.HV, self.dk, self.dv))
             with np.errstate(all="ignore"):
@@ -231,7 +261,7 @@ class ReplayOracle:
                 continue
             c = int(self.cursor[s])
             if mode == ring.FOLD_EVERY:
-                self.ckpt[:, s] = self.S[:, s]
+                self._checkpoint(slice(None), s)
             self.cursor[s] = ring.cursor_after_commit(c, T, self.L, bool(force[r]),
                                                       int(accept[r]), mode)
 
@@ -239,7 +269,7 @@ class ReplayOracle:
         """Explicit fold: checkpoint <- committed state, cursor <- 0."""
         for s in np.asarray(slots):
             if s >= 0:
-                self.ckpt[:, s] = self.S[:, s]
+                self._checkpoint(slice(None), s)
                 self.cursor[s] = 0
 
     def load_checkpoint(self, slot, S):

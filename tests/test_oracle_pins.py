@@ -322,3 +322,49 @@ def test_restore_clears_history():
     orc.reset_slots([1])
     np.testing.assert_array_equal(orc.S[:, 1], orc.S[:, 0])
     assert orc.cursor[1] == 0
+
+
+# ---------------------------------------------- 7. bf16 checkpoint rounding
+def test_round_bf16_known_values_and_ties():
+    from oracle import round_bf16
+    one = 1.0
+    cases = {
+        one: one,
+        one + 2.0 ** -9: one,                       # below half an ulp (ulp = 2^-7)
+        one + 2.0 ** -8: one,                       # exact tie, mantissa even: down
+        one + 3 * 2.0 ** -8: one + 2.0 ** -6,       # exact tie, odd below: up to even
+        one + 2.0 ** -7: one + 2.0 ** -7,           # representable
+        -3.0 - 2.0 ** -7: -3.0,                     # ulp at 3 is 2^-6
+        0.1: 0.10009765625,                         # nearest with 8 significant bits
+        2.0 ** 100 * 1.5: 2.0 ** 100 * 1.5,
+    }
+    for x, want in cases.items():
+        assert round_bf16(np.array(x)) == want, x
+    nf = round_bf16(np.array([np.inf, -np.inf, np.nan]))
+    assert nf[0] == np.inf and nf[1] == -np.inf and np.isnan(nf[2])
+
+
+def test_round_bf16_matches_torch_on_float32_values():
+    import torch
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    from oracle import round_bf16
+    np.testing.assert_array_equal(round_bf16(x.astype(np.float64)), want)
+
+
+def test_bf16_checkpoint_mode_rounds_only_at_folds():
+    from oracle import round_bf16
+    HK, HV, dk, dv, B = 1, 2, 8, 8, 2
+    S0 = round_bf16(synth.initial_state(4, B, HV, dk, dv))
+    exact = ReplayOracle("gdn", 1, B, HK, HV, dk, dv, 6, 0.5, S0)
+    rounded = ReplayOracle("gdn", 1, B, HK, HV, dk, dv, 6, 0.5, S0, ckpt_round="bf16")
+    for t in range(20):
+        inp = synth.window_inputs(t, B, 1, HK, HV, dk, dv)
+        o1, f = exact.decode(0, [0, 1], inp, advance=True)
+        o2, _ = rounded.decode(0, [0, 1], inp, advance=True)
+        if t < 6:                                 # before the first fold: identical
+            np.testing.assert_array_equal(o1, o2)
+        np.testing.assert_array_equal(round_bf16(rounded.ckpt), rounded.ckpt)
+        assert np.max(np.abs(o1 - o2)) <= 1e-2 * np.max(np.abs(o1))
+    assert not np.array_equal(exact.ckpt, rounded.ckpt)
