@@ -60,6 +60,22 @@ def row_bytes(c, T, fold, HK, HV, dk, dv, s_state, s_in, s_k, s_d, n_g=1):
     return state + hist + win + out + rec + (state if fold else 0)
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Largest value of x over all ranks (the slowest replica's time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: float, world: int, t_max_s: float) -> float:
+    """Whole-job throughput of `world` independent replicas (weak scaling)."""
+    return world * tokens_per_rank / t_max_s
+
+
 def advance(c, T, L, a):
     fold = c + T > L
     return (0 if fold else c) + a, fold
@@ -273,12 +289,8 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     t_ms = e0.elapsed_time(e1)
     cur, bytes_timed = host_advance(cur, args.steps)
-    t_max = t_ms
-    if world > 1:
-        tt = torch.tensor([t_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
-    value = world * B_live * T * nl * args.steps / (t_max / 1e3)
+    t_max = max_over_ranks(t_ms, world, dev)
+    value = job_throughput(B_live * T * nl * args.steps, world, t_max / 1e3)
     ms_per_step = t_max / args.steps
 
     # ---- per-launch duration of the replay kernel: events between layers on
@@ -324,12 +336,8 @@ def run_ours(args, rank, world, local_rank):
         out_h.copy_(out, non_blocking=True)
     e3.record()
     torch.cuda.synchronize()
-    te = e2.elapsed_time(e3)
-    if world > 1:
-        tt = torch.tensor([te], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        te = float(tt.item())
-    e2e = {"value": world * B_live * T * nl * args.steps / (te / 1e3), "unit": UNIT,
+    te = max_over_ranks(e2.elapsed_time(e3), world, dev)
+    e2e = {"value": job_throughput(B_live * T * nl * args.steps, world, te / 1e3), "unit": UNIT,
            "h2d_bytes_per_step": half.numel() * 2 + flt.numel() * 4,
            "d2h_bytes_per_step": out.numel() * 2}
     err = st.rssm_get_device_error()

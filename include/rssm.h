@@ -110,8 +110,9 @@ typedef struct rssm_config {
   float scale;
 } rssm_config;
 
-/* Device buffers (layouts above). All must be non-null; state, ring_k, ring_d
- * and ring_v must be 16-byte aligned. Borrowed for the life of the handle. */
+/* Device buffers (layouts above). All must be non-null; state, ring_k, ring_d,
+ * ring_g and ring_v must be 16-byte aligned (they move by bulk async copies).
+ * Borrowed for the life of the handle. */
 typedef struct rssm_buffers {
   void *state;
   void *ring_k;
@@ -155,7 +156,8 @@ void rssm_free(rssm_handle *h);
  * into the checkpoint first (S0 <- replayed state) and the new record goes to
  * ring position 0, else to c. Writes o (B rows), the token's record
  * (k once per key head, d, g, v, beta) and, if fold_out is non-null,
- * fold_out[r] = fold (0/1) for live rows. When advance_cursor is non-zero
+ * fold_out[r] = fold (0/1) for live rows. q, k, v (and g for KDA) must be
+ * 16-byte aligned; beta, g (GDN) and slot 4-byte aligned. When advance_cursor is non-zero
  * (the last layer of the step) the cursor kernel then sets
  * cursor[s] = (fold ? 0 : c) + 1. force and fold_out may be null.
  * B == 0 is a no-op. Pointers are device pointers; stream is a cudaStream_t.

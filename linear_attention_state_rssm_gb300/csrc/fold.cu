@@ -49,41 +49,64 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
   }
   if (n == 0) return;
 
-  ST* tile = reinterpret_cast<ST*>(smem);
+  const ColMap cm(dk, dv, tid);
+  ST* gtile = static_cast<ST*>(p.state) + layer * p.layer_state +
+              ((size_t)s * HV + h) * (size_t)dk * dv;
+  ST* gcol = gtile + cm.col;
+
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + p.sm.mbar);
   float* hk = reinterpret_cast<float*>(smem + p.sm.hk);
   float* hd = reinterpret_cast<float*>(smem + p.sm.hd);
+  float* hg = reinterpret_cast<float*>(smem + p.sm.hg);
   float* hf = reinterpret_cast<float*>(smem + p.sm.hf);
   float* scal = reinterpret_cast<float*>(smem + p.sm.scal);
-  // GDN: scal[0] = Gam, scal[1] = exp(Gam). KDA: egam[dk] = exp(Gam[ch]), then Gam[dk].
+  unsigned char* hkraw = smem + p.sm.hkraw;
+  unsigned char* hdraw = smem + p.sm.hdraw;
+  // GDN: scal[0] = Gam, scal[1] = exp(Gam). KDA: egam[dk] = exp(Gam[ch]).
   float* egam = scal;
 
-  ST* gtile = static_cast<ST*>(p.state) + layer * p.layer_state +
-              ((size_t)s * HV + h) * (size_t)dk * dv;
   const size_t kbase = layer * p.layer_k + ((size_t)s * HK + kh) * L * dk;
   const size_t dbase = layer * p.layer_d + ((size_t)s * HV + h) * L * dv;
   const size_t gbase = layer * p.layer_g + ((size_t)s * HV + h) * L * (ALGO == ALGO_GDN ? 1 : dk);
 
+  const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv);
   if (tid == 0) {
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) mbar_init(&mbar[w], 1);
+    mbar_init(&mbar[kMbarWin], 1);
+    mbar_init(&mbar[kMbarHist], 1);
+    pipe.init();
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0) load_tile_async(tile, gtile, dk, dv, mbar);
-
-  stage_history<ALGO>(n, dk, dv, p.ring_k, kbase, p.rk_dt, p.ring_d, dbase, p.rd_dt, p.ring_g,
-                      gbase, hk, hd, hf, tid);
-  __syncthreads();
-  history_decay<ALGO>(n, dk, hk, hf, scal, ALGO == ALGO_KDA ? scal + dk : nullptr, egam,
-                      p.ring_g, gbase, tid, warp, lane);
-  const bool ok = mbar_wait_bounded(&mbar[warp], 0);
+  if (tid == 0) {
+    pipe.prime();
+    issue_history<ALGO>(n, dk, dv, p.ring_k, kbase, p.rk_dt, p.ring_d, dbase, p.rd_dt, p.ring_g,
+                        gbase, hk, hkraw, hd, hdraw, hg, &mbar[kMbarHist]);
+  }
+  if (ALGO == ALGO_GDN) {
+    for (int m = tid; m < n; m += kThreads) hf[m] = p.ring_g[gbase + m];
+  }
+  const bool ok = mbar_wait_bounded(&mbar[kMbarHist], 0);
   if (!ok) {
-    atomicOr(p.err, DEVERR_TIMEOUT);
-    mbar_wait_bounded(&mbar[warp], 0);
+    if (tid == 0) atomicOr(p.err, DEVERR_TIMEOUT);
+    mbar_wait_bounded(&mbar[kMbarHist], 0);
+    pipe.drain();
     return;
   }
-  fold_rows<ALGO, ST>(tile, gtile, n, dk, dv, hk, hd, scal[1], egam, warp, lane);
+  widen_history(n, dk, dv, p.rk_dt, p.rd_dt, hk, hkraw, hd, hdraw, tid);
+  __syncthreads();
+  if (ALGO == ALGO_GDN) {
+    if (warp == 0) gdn_history_scan(n, hf, scal, lane);
+  } else {
+    for (int ch = tid; ch < dk; ch += kThreads) {
+      egam[ch] = __expf(kda_history_channel(n, dk, ch, hk, hg));
+    }
+  }
+  __syncthreads();
+  float unused[1] = {0.f};
+  if (!stream_tile<ALGO, ST, 0, true>(pipe, unused, gcol, cm, dk, dv, n, hk, hd, hf, scal[1], egam,
+                                      nullptr, tid, lane)) {
+    if (tid == 0) atomicOr(p.err, DEVERR_TIMEOUT);
+  }
 }
 
 __global__ void cursor_kernel(int32_t* cursor, const int32_t* slot, const uint8_t* force,

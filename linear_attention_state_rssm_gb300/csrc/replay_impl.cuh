@@ -9,24 +9,28 @@
 // rewritten; here the wait is a hardware cluster barrier, which always makes
 // progress because cluster CTAs are co-scheduled).
 //
+// The (slot, head) checkpoint tile S0 [dk][dv] streams through a ring of four
+// shared-memory stages (8 KB row chunks, one bulk async copy each, full/empty
+// mbarriers); thread tid consumes value column tid % dv of every chunk. The
+// small ring lets several CTAs share an SM, each with 32 KB of the tile in
+// flight from its first microsecond.
+//
 // Per CTA, with c = cursor[slot], fold = force || c + T > L:
-//  1. the checkpoint tile S0 [dk][dv] streams into shared memory by bulk async
-//     copies (one row chunk per warp), overlapped with loading the window and
-//     the c history records;
-//  2. history gates become decay-scaled keys k~_m (rssm_history.cuh);
-//  3. window coefficients, for j <= i < T, G_i the inclusive in-window gate
-//     prefix (per channel for KDA):
+//  1. bulk async copies: the first tile chunks and the window rows (they need
+//     only the slot) and, once the cursor is known, the c history records;
+//  2. gates: history decay factors and in-window inclusive prefixes G_i;
+//  3. window coefficients for j <= i < T (per key channel for KDA)
 //        A_ij = beta_i sum_ch e^{G_i-G_j} k_j k_i   (j < i)
 //        F_ij =        sum_ch e^{G_i-G_j} k_j q_i   (j <= i)
-//  4. fold: S0 <- exp(Gam) S0 + sum_m k~_m d_m^T, written back, history emptied;
-//     no fold: history dot coefficients H[m][x] = k~_m . (e^{G_i} x) for every
-//     window vector x in {k_i, q_i};
-//  5. one pass over the tile computes S0^T (e^{Gam_e + G_i} x) for all 2T
-//     vectors at once (the only O(dk dv) work);
-//  6. per value column: a_i, b_i = state part + sum_m H d_m; the triangular
-//     solve d_i = beta_i (v_i - a_i) - sum_{j<i} A_ij d_j (forward
-//     substitution of (I + A) D = R) and o_i = scale (b_i + sum_{j<=i} F_ij d_j);
-//  7. the T records go to ring positions base + i (base = fold ? 0 : c).
+//     and, without a fold, history dot coefficients H[m][x] = k~_m . (e^{G_i} x)
+//     for every window vector x in {k_i, q_i};
+//  4. stream the tile: on a fold S0 <- e^{Gam} S0 + sum_m k~_m d_m^T (stored
+//     back), and y_x = S0^T (e^{Gam_e + G_i} x) for all 2T vectors in one pass
+//     (a GDN window without a fold streams first, while its history lands);
+//  5. per column: a_i, b_i = y + sum_m H d_m; the triangular solve
+//     d_i = beta_i (v_i - a_i) - sum_{j<i} A_ij d_j (forward substitution of
+//     (I + A) D = R) and o_i = scale (b_i + sum_{j<=i} F_ij d_j); the records of
+//     the window go to ring positions base + i (base = fold ? 0 : c).
 // Every window sum runs over j <= i only, so a NaN or Inf at a later (rejected)
 // position is never read by an earlier output: the causal selection is
 // structural, never a multiplication by zero (SGLang fork PR jianc99/sglang#2,
@@ -40,8 +44,7 @@ namespace rssm {
 
 template <int ALGO, typename ST, int NT>
 __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) {
-  constexpr int NV = 2 * NT;     // mat-vec vectors: k_i at [0, NT), q_i at [NT, 2NT)
-  constexpr int VB = vblock(NT);  // vectors per accumulator block
+  constexpr int NV = 2 * NT;             // mat-vec vectors: k_i at [0, NT), q_i at [NT, 2NT)
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int h = blockIdx.x;
@@ -50,109 +53,175 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
   const int T = p.T, dk = p.dk, dv = p.dv, L = p.L, HV = p.HV, HK = p.HK;
   const int kh = h / p.G;
 
-  // ---- row resolve and fold decision (uniform over the CTA and its cluster)
+  // ---- row resolve (uniform over the CTA and its cluster)
   const int s = p.slot[r];
   if (s < 0) return;
   if (s >= p.n_slots) {
     if (h == 0 && tid == 0) atomicOr(p.err, DEVERR_SLOT);
     return;
   }
-  const int c = p.cursor[s];
-  if (c < 0 || c > L) {
-    if (h == 0 && tid == 0) atomicOr(p.err, DEVERR_CURSOR);
-    return;
-  }
-  const bool fold = (p.force != nullptr && p.force[r] != 0) || (c + T > L);
-  const int base = fold ? 0 : c;
-  const int nh = c;
-  const bool group_sync = fold && p.G > 1;
 
-  ST* tile = reinterpret_cast<ST*>(smem);
+  const ColMap cm(dk, dv, tid);
+  ST* gtile = static_cast<ST*>(p.state) + ((size_t)s * HV + h) * dk * dv;
+  ST* gcol = gtile + cm.col;
+
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + p.sm.mbar);
   float* wq = reinterpret_cast<float*>(smem + p.sm.wq);
   float* wk = reinterpret_cast<float*>(smem + p.sm.wk);
   float* wv = reinterpret_cast<float*>(smem + p.sm.wv);
   float* wb = reinterpret_cast<float*>(smem + p.sm.wb);
   float* wg = reinterpret_cast<float*>(smem + p.sm.wg);
+  float* yk = reinterpret_cast<float*>(smem + p.sm.yk);
+  float* yq = reinterpret_cast<float*>(smem + p.sm.yq);
   float* scal = reinterpret_cast<float*>(smem + p.sm.scal);
   float* xh = reinterpret_cast<float*>(smem + p.sm.xh);
   float* am = reinterpret_cast<float*>(smem + p.sm.am);
   float* fm = reinterpret_cast<float*>(smem + p.sm.fm);
   float* hk = reinterpret_cast<float*>(smem + p.sm.hk);
   float* hd = reinterpret_cast<float*>(smem + p.sm.hd);
+  float* hg = reinterpret_cast<float*>(smem + p.sm.hg);
   float* hf = reinterpret_cast<float*>(smem + p.sm.hf);
   float* hdot = reinterpret_cast<float*>(smem + p.sm.hdot);
-  // GDN scalars: es[NT] = e^{Gam_e + G_i}, eG[NT] = e^{G_i}, scal[2NT..] = Gam, e^Gam.
-  // KDA vectors: egam[dk] = e^{Gam[ch]}, gam[dk] = Gam[ch].
+  float* red = reinterpret_cast<float*>(smem + p.sm.red);
+  unsigned char* wraw = smem + p.sm.wraw;
+  unsigned char* hkraw = smem + p.sm.hkraw;
+  unsigned char* hdraw = smem + p.sm.hdraw;
+  // GDN scalars: es[i] = e^{Gam_e + G_i}, eG[i] = e^{G_i}, hscal = {Gam, e^Gam}.
+  // KDA vectors: egam[ch] = e^{Gam[ch]}, gam[ch] = Gam[ch].
   float* es = scal;
   float* eG = scal + NT;
   float* hscal = scal + 2 * NT;
   float* egam = scal;
   float* gam = scal + dk;
 
-  const size_t tile_elems = (size_t)dk * dv;
-  ST* gtile = static_cast<ST*>(p.state) + ((size_t)s * HV + h) * tile_elems;
+  const size_t tok0 = (size_t)r * T;
+  const int s_in = dtype_bytes(p.in_dt);
+  const uint32_t qrow = (uint32_t)(dk * s_in), vrow = (uint32_t)(dv * s_in);
 
-  // ---- 1. checkpoint tile -> shared memory (async), window + history loads
+  // ---- 1. bulk async copies: window rows now, history once the cursor is
+  //         known. One thread issues every copy of a barrier after registering
+  //         its byte count.
+  const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv);
   if (tid == 0) {
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) mbar_init(&mbar[w], 1);
+    mbar_init(&mbar[kMbarWin], 1);
+    mbar_init(&mbar[kMbarHist], 1);
+    pipe.init();
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0) load_tile_async(tile, gtile, dk, dv, mbar);
-
-  const size_t tok0 = (size_t)r * T;
-  for (int e = tid; e < T * dk; e += kThreads) {
-    const int i = e / dk, ch = e - i * dk;
-    const size_t gi = ((tok0 + i) * HK + kh) * dk + ch;
-    wq[e] = ld_f32(p.q, gi, p.in_dt);
-    wk[e] = ld_f32(p.k, gi, p.in_dt);
-  }
-  for (int e = tid; e < T * dv; e += kThreads) {
-    const int i = e / dv, col = e - i * dv;
-    wv[e] = ld_f32(p.v, ((tok0 + i) * HV + h) * dv + col, p.in_dt);
-  }
-  if (tid < T) wb[tid] = p.beta[(tok0 + tid) * HV + h];
-  if (ALGO == ALGO_GDN) {
-    if (tid < T) wg[tid] = p.g[(tok0 + tid) * HV + h];
-  } else {
-    for (int e = tid; e < T * dk; e += kThreads) {
-      const int i = e / dk, ch = e - i * dk;
-      wg[e] = p.g[((tok0 + i) * HV + h) * dk + ch];
+  if (tid == 0) {
+    pipe.prime();
+    const bool f32in = p.in_dt == DT_F32;
+    mbar_expect_tx(&mbar[kMbarWin],
+                   T * (2 * qrow + vrow) + (ALGO == ALGO_KDA ? (uint32_t)(T * dk * 4) : 0u));
+    for (int i = 0; i < T; ++i) {
+      const size_t tok = tok0 + i;
+      const size_t qoff = ((tok * HK + kh) * dk) * s_in;
+      const size_t voff = ((tok * HV + h) * dv) * s_in;
+      bulk_g2s(f32in ? static_cast<void*>(wq + i * dk) : wraw + i * qrow,
+               static_cast<const char*>(p.q) + qoff, qrow, &mbar[kMbarWin]);
+      bulk_g2s(f32in ? static_cast<void*>(wk + i * dk) : wraw + (T + i) * qrow,
+               static_cast<const char*>(p.k) + qoff, qrow, &mbar[kMbarWin]);
+      bulk_g2s(f32in ? static_cast<void*>(wv + i * dv) : wraw + 2 * T * qrow + i * vrow,
+               static_cast<const char*>(p.v) + voff, vrow, &mbar[kMbarWin]);
+      if (ALGO == ALGO_KDA) {
+        bulk_g2s(wg + i * dk, p.g + (tok * HV + h) * dk, (uint32_t)(dk * 4), &mbar[kMbarWin]);
+      }
     }
   }
+  const int c = p.cursor[s];
+  if (tid < T) {
+    wb[tid] = p.beta[(tok0 + tid) * HV + h];
+    if (ALGO == ALGO_GDN) wg[tid] = p.g[(tok0 + tid) * HV + h];
+  }
+  if (c < 0 || c > L) {
+    if (h == 0 && tid == 0) atomicOr(p.err, DEVERR_CURSOR);
+    // copies are in flight into this CTA's shared memory: let them land
+    mbar_wait_bounded(&mbar[kMbarWin], 0);
+    pipe.drain();
+    return;
+  }
+  // fold decision (uniform over the CTA and its cluster)
+  const bool fold = (p.force != nullptr && p.force[r] != 0) || (c + T > L);
+  const int base = fold ? 0 : c;
+  const int nh = c;
+  const bool group_sync = fold && p.G > 1;
   const size_t kbase = ((size_t)s * HK + kh) * L * dk;
   const size_t dbase = ((size_t)s * HV + h) * L * dv;
   const size_t gbase = ((size_t)s * HV + h) * L * (ALGO == ALGO_GDN ? 1 : dk);
-  if (nh > 0) {
-    stage_history<ALGO>(nh, dk, dv, p.ring_k, kbase, p.rk_dt, p.ring_d, dbase, p.rd_dt,
-                        p.ring_g, gbase, hk, hd, hf, tid);
+  if (nh > 0 && tid == 0) {
+    issue_history<ALGO>(nh, dk, dv, p.ring_k, kbase, p.rk_dt, p.ring_d, dbase, p.rd_dt, p.ring_g,
+                        gbase, hk, hkraw, hd, hdraw, hg, &mbar[kMbarHist]);
+  }
+  if (ALGO == ALGO_GDN) {
+    for (int m = tid; m < nh; m += kThreads) hf[m] = p.ring_g[gbase + m];
+  }
+  bool copies_ok = mbar_wait_bounded(&mbar[kMbarWin], 0);
+  if (p.in_dt != DT_F32) {
+    widen16(wq, wraw, T * dk, p.in_dt, tid, kThreads);
+    widen16(wk, wraw + T * qrow, T * dk, p.in_dt, tid, kThreads);
+    widen16(wv, wraw + 2 * T * qrow, T * dv, p.in_dt, tid, kThreads);
   }
   __syncthreads();
-  // This CTA has read every old key record it needs; a folding sibling may
-  // overwrite them once all of the key group has arrived.
-  if (group_sync) cluster_arrive_release();
 
-  // ---- 2. gates: history decay factors, in-window prefixes
-  if (nh > 0) {
-    history_decay<ALGO>(nh, dk, hk, hf, hscal, gam, egam, p.ring_g, gbase, tid, warp, lane);
-  } else {
-    if (ALGO == ALGO_GDN) {
-      if (tid == 0) {
+  // ---- records that need no result of the window: keys (once per key head),
+  //      gates and betas, at ring positions base + i. Each thread writes the
+  //      key channels it owns in step 2 below. A folding window writes over
+  //      positions [0, T) of the history it reads: it first waits for its own
+  //      history copy, then until the whole key group has read the old keys.
+  if (fold && nh > 0) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
+  if (group_sync) {
+    cluster_arrive_release();
+    cluster_wait_acquire();
+  }
+  for (int ch = tid; ch < dk; ch += kThreads) {
+    for (int i = 0; i < T; ++i) {
+      if (h % p.G == 0) {
+        st_f32(p.ring_k, kbase + (size_t)(base + i) * dk + ch, p.rk_dt, wk[i * dk + ch]);
+      }
+      if (ALGO == ALGO_KDA) p.ring_g[gbase + (size_t)(base + i) * dk + ch] = wg[i * dk + ch];
+    }
+  }
+  if (tid < T) {
+    p.ring_beta[((size_t)s * HV + h) * L + base + tid] = wb[tid];
+    if (ALGO == ALGO_GDN) p.ring_g[gbase + base + tid] = wg[tid];
+  }
+
+  float y[NV];
+#pragma unroll
+  for (int vv = 0; vv < NV; ++vv) y[vv] = 0.f;
+  // GDN mat-vec inputs are the raw window vectors (their scalar decay goes on
+  // the column results); without a fold the tile streams now, before the
+  // history is needed.
+  const bool early = ALGO == ALGO_GDN && !fold;
+  if (ALGO == ALGO_GDN) {
+    for (int e = tid; e < dk * NV; e += kThreads) {
+      const int ch = e / NV, vv = e - ch * NV;
+      const int i = vv < NT ? vv : vv - NT;
+      xh[e] = i < T ? (vv < NT ? wk[i * dk + ch] : wq[i * dk + ch]) : 0.f;
+    }
+    if (early) {
+      __syncthreads();
+      copies_ok = stream_tile<ALGO, ST, NV, false>(pipe, y, gcol, cm, dk, dv, 0, hk, hd, hf, 1.f,
+                                                   egam, xh, tid, lane) && copies_ok;
+    }
+  }
+  if (nh > 0 && !fold) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
+  if (nh > 0) widen_history(nh, dk, dv, p.rk_dt, p.rd_dt, hk, hkraw, hd, hdraw, tid);
+  if (!copies_ok) atomicOr(p.err, DEVERR_TIMEOUT);
+  __syncthreads();
+
+  // ---- 2. gates
+  if (ALGO == ALGO_GDN) {
+    if (warp == 0) {
+      if (nh > 0) {
+        gdn_history_scan(nh, hf, hscal, lane);
+      } else if (lane == 0) {
         hscal[0] = 0.f;
         hscal[1] = 1.f;
       }
-    } else {
-      for (int ch = tid; ch < dk; ch += kThreads) {
-        gam[ch] = 0.f;
-        egam[ch] = 1.f;
-      }
-    }
-    __syncthreads();
-  }
-  if (ALGO == ALGO_GDN) {
-    if (warp == 0) {
+      __syncwarp();
+      // in-window inclusive prefix of the gates (T <= 16 lanes)
       const float gv = lane < T ? wg[lane] : 0.f;
       float incl = gv;
 #pragma unroll
@@ -168,17 +237,34 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
       }
     }
   } else {
+    // one thread per key channel: history decay, window prefix, scaled vectors
     for (int ch = tid; ch < dk; ch += kThreads) {
+      const float gm = nh > 0 ? kda_history_channel(nh, dk, ch, hk, hg) : 0.f;
+      gam[ch] = gm;
+      egam[ch] = __expf(gm);
+      const float gam_e = fold ? 0.f : gm;
       float G = 0.f;
-      for (int i = 0; i < T; ++i) {
-        G += wg[i * dk + ch];
-        wg[i * dk + ch] = G;
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        float xk = 0.f, xq = 0.f;
+        if (i < T) {
+          G += wg[i * dk + ch];
+          wg[i * dk + ch] = G;
+          const float eg = __expf(G);
+          yk[i * dk + ch] = eg * wk[i * dk + ch];
+          yq[i * dk + ch] = eg * wq[i * dk + ch];
+          const float ex = __expf(gam_e + G);
+          xk = ex * wk[i * dk + ch];
+          xq = ex * wq[i * dk + ch];
+        }
+        xh[ch * NV + i] = xk;
+        xh[ch * NV + NT + i] = xq;
       }
     }
   }
   __syncthreads();
 
-  // ---- 3. window coefficients A, F (j <= i only) and mat-vec inputs
+  // ---- 3. window coefficients A, F (j <= i only) and history dot coefficients
   {
     int pi = 0;
     for (int i = 0; i < T; ++i) {
@@ -201,38 +287,10 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
       }
     }
   }
-  for (int e = tid; e < dk * NV; e += kThreads) {
-    const int ch = e / NV, vv = e - ch * NV;
-    const int i = vv < NT ? vv : vv - NT;
-    float x = 0.f;
-    if (i < T) {
-      x = vv < NT ? wk[i * dk + ch] : wq[i * dk + ch];
-      if (ALGO == ALGO_KDA) x *= __expf((fold ? 0.f : gam[ch]) + wg[i * dk + ch]);
-    }
-    xh[e] = x;
-  }
-  __syncthreads();
-  if (ALGO == ALGO_KDA && !fold && nh > 0) {
-    // history dots use e^{G_i} x (the history keys carry their own decay)
-    for (int e = tid; e < T * dk; e += kThreads) {
-      const float eg = __expf(wg[e]);
-      wk[e] *= eg;
-      wq[e] *= eg;
-    }
-    __syncthreads();
-  }
-
-  // ---- 4. fold, or history dot coefficients
-  bool tile_ok = true;
-  bool waited = false;
-  if (fold) {
-    if (nh > 0) {
-      tile_ok = mbar_wait_bounded(&mbar[warp], 0);
-      waited = true;
-      fold_rows<ALGO, ST>(tile, gtile, nh, dk, dv, hk, hd, hscal[1], egam, warp, lane);
-      __syncwarp();
-    }
-  } else if (nh > 0) {
+  if (!fold) {
+    // GDN: raw keys, coefficient hf[m] * e^{G_i}; KDA: decayed keys and e^{G_i} x
+    const float* xk = ALGO == ALGO_GDN ? wk : yk;
+    const float* xq = ALGO == ALGO_GDN ? wq : yq;
     for (int m = warp; m < nh; m += kWarps) {
       float part[NV];
 #pragma unroll
@@ -242,7 +300,7 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
 #pragma unroll
         for (int vv = 0; vv < NV; ++vv) {
           const int i = vv < NT ? vv : vv - NT;
-          if (i < T) part[vv] = fmaf(km, (vv < NT ? wk : wq)[i * dk + ch], part[vv]);
+          if (i < T) part[vv] = fmaf(km, (vv < NT ? xk : xq)[i * dk + ch], part[vv]);
         }
       }
 #pragma unroll
@@ -252,95 +310,45 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
         for (int vv = 0; vv < NV; ++vv) {
           const int i = vv < NT ? vv : vv - NT;
           float hv = 0.f;
-          if (i < T) hv = (ALGO == ALGO_GDN) ? part[vv] * eG[i] : part[vv];
+          if (i < T) hv = (ALGO == ALGO_GDN) ? part[vv] * hf[m] * eG[i] : part[vv];
           hdot[m * NV + vv] = hv;
         }
       }
     }
   }
+  __syncthreads();
 
-  // ---- 5. S^T x for all window vectors, one pass over the tile
-  if (!waited) tile_ok = mbar_wait_bounded(&mbar[warp], 0);
-  if (!tile_ok) atomicOr(p.err, DEVERR_TIMEOUT);
-
-  const TileMap tm(dk, dv, warp, lane);
-  float y[NV];  // per value column (thread tid < dv): reduced S^T x
-#pragma unroll
-  for (int vv = 0; vv < NV; ++vv) y[vv] = 0.f;
-
-#pragma unroll
-  for (int v0 = 0; v0 < NV; v0 += VB) {
-    float acc[VB][4];
-#pragma unroll
-    for (int v = 0; v < VB; ++v) acc[v][0] = acc[v][1] = acc[v][2] = acc[v][3] = 0.f;
-    for (int t = 0; t < tm.rpt; ++t) {
-      const int row = tm.row0 + t;
-      const float4 s4 = StateIO<ST>::load4(tile + (size_t)row * dv + 4 * tm.cc);
-      const float* xr = xh + (size_t)row * NV + v0;
-      if constexpr (VB % 4 == 0) {
-#pragma unroll
-        for (int q4 = 0; q4 < VB / 4; ++q4) {
-          const float4 x = reinterpret_cast<const float4*>(xr)[q4];
-          const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            acc[4 * q4 + u][0] = fmaf(xs[u], s4.x, acc[4 * q4 + u][0]);
-            acc[4 * q4 + u][1] = fmaf(xs[u], s4.y, acc[4 * q4 + u][1]);
-            acc[4 * q4 + u][2] = fmaf(xs[u], s4.z, acc[4 * q4 + u][2]);
-            acc[4 * q4 + u][3] = fmaf(xs[u], s4.w, acc[4 * q4 + u][3]);
-          }
-        }
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(xr);
-        const float xs[2] = {x.x, x.y};
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          acc[u][0] = fmaf(xs[u], s4.x, acc[u][0]);
-          acc[u][1] = fmaf(xs[u], s4.y, acc[u][1]);
-          acc[u][2] = fmaf(xs[u], s4.z, acc[u][2]);
-          acc[u][3] = fmaf(xs[u], s4.w, acc[u][3]);
-        }
-      }
+  // ---- 4. stream the checkpoint tile (unless done early): fold, then S^T x
+  if (!early) {
+    bool ok;
+    if (fold && nh > 0) {
+      ok = stream_tile<ALGO, ST, NV, true>(pipe, y, gcol, cm, dk, dv, nh, hk, hd, hf, hscal[1],
+                                           egam, xh, tid, lane);
+    } else {
+      ok = stream_tile<ALGO, ST, NV, false>(pipe, y, gcol, cm, dk, dv, 0, hk, hd, hf, 1.f, egam,
+                                            xh, tid, lane);
     }
-    // reduce over the lanes that share columns (row sub-lanes)
-    for (int off = tm.ccw; off < 32; off <<= 1) {
-#pragma unroll
-      for (int v = 0; v < VB; ++v) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) acc[v][u] += __shfl_xor_sync(kFull, acc[v][u], off);
-      }
+    if (!ok) {
+      atomicOr(p.err, DEVERR_TIMEOUT);
+      copies_ok = false;
     }
-    float* red = p.sm.red_alias
-                     ? reinterpret_cast<float*>(smem + (size_t)warp * (dk / kWarps) * dv * sizeof(ST))
-                     : reinterpret_cast<float*>(smem + p.sm.red) + (size_t)warp * VB * dv;
-    if (p.sm.red_alias) __syncwarp();  // every lane is done with this warp's tile rows
-    if (tm.rs == 0) {
+  }
+  if (cm.RG > 1) {
+    // dv < kThreads: several row groups share a column; add their sums
 #pragma unroll
-      for (int v = 0; v < VB; ++v) {
-        *reinterpret_cast<float4*>(red + (size_t)v * dv + 4 * tm.cc) =
-            make_float4(acc[v][0], acc[v][1], acc[v][2], acc[v][3]);
-      }
-    }
+    for (int vv = 0; vv < NV; ++vv) red[(cm.rg * NV + vv) * dv + cm.col] = y[vv];
     __syncthreads();
-    if (tid < dv) {
-      const size_t wstride =
-          p.sm.red_alias ? (size_t)(dk / kWarps) * dv * sizeof(ST) / sizeof(float) : (size_t)VB * dv;
-      const float* red0 = p.sm.red_alias ? reinterpret_cast<const float*>(smem)
-                                         : reinterpret_cast<const float*>(smem + p.sm.red);
+    if (cm.rg == 0) {
+      for (int g2 = 1; g2 < cm.RG; ++g2) {
 #pragma unroll
-      for (int v = 0; v < VB; ++v) {
-        float sum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) sum += red0[w * wstride + (size_t)v * dv + tid];
-        y[v0 + v] = sum;
+        for (int vv = 0; vv < NV; ++vv) y[vv] += red[(g2 * NV + vv) * dv + cm.col];
       }
     }
-    if (v0 + VB < NV) __syncthreads();
   }
 
-  // ---- 6. per value column: corrections, triangular solve, outputs, deltas
-  if (tid < dv) {
-    const int col = tid;
+  // ---- 5. per value column: corrections, triangular solve, outputs, deltas
+  if (cm.rg == 0) {
+    const int col = cm.col;
     if (ALGO == ALGO_GDN) {
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
@@ -379,29 +387,11 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
       }
     }
   }
-
-  // ---- 7. remaining records: keys (once per key head), gates, beta
-  if (group_sync) cluster_wait_acquire();
-  if (h % p.G == 0) {
-    for (int e = tid; e < T * dk; e += kThreads) {
-      const int i = e / dk, ch = e - i * dk;
-      const float kv = ld_f32(p.k, ((tok0 + i) * HK + kh) * dk + ch, p.in_dt);
-      st_f32(p.ring_k, kbase + (size_t)(base + i) * dk + ch, p.rk_dt, kv);
-    }
-  }
-  if (tid < T) p.ring_beta[((size_t)s * HV + h) * L + base + tid] = p.beta[(tok0 + tid) * HV + h];
-  if (ALGO == ALGO_GDN) {
-    if (tid < T) p.ring_g[gbase + base + tid] = p.g[(tok0 + tid) * HV + h];
-  } else {
-    for (int e = tid; e < T * dk; e += kThreads) {
-      const int i = e / dk, ch = e - i * dk;
-      p.ring_g[gbase + (size_t)(base + i) * dk + ch] = p.g[((tok0 + i) * HV + h) * dk + ch];
-    }
-  }
   if (h == 0 && tid == 0 && p.fold_out != nullptr) p.fold_out[r] = fold ? 1 : 0;
-  if (!tile_ok) {
-    // give the copy that did not arrive a second bounded chance before exit
-    mbar_wait_bounded(&mbar[warp], 0);
+  if (!copies_ok) {
+    // give copies that did not arrive a second bounded chance before exit
+    mbar_wait_bounded(&mbar[kMbarWin], 0);
+    if (nh > 0) mbar_wait_bounded(&mbar[kMbarHist], 0);
   }
 }
 

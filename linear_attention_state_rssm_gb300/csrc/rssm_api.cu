@@ -103,11 +103,13 @@ cudaError_t replay_prepare(const rssm_config& c, int max_smem) {
 }
 
 ReplaySmem layout_for(const rssm_config& c, int T) {
-  return replay_layout(c.algo, (int)esize(c.state_dtype), nt_for(T), T, c.L, c.dk, c.dv);
+  return replay_layout(c.algo, (int)esize(c.state_dtype), nt_for(T), T, c.L, c.dk, c.dv,
+                       c.in_dtype, c.ring_k_dtype, c.ring_d_dtype);
 }
 
 FoldSmem fold_layout_for(const rssm_config& c) {
-  return fold_layout(c.algo, (int)esize(c.state_dtype), c.L, c.dk, c.dv);
+  return fold_layout(c.algo, (int)esize(c.state_dtype), c.L, c.dk, c.dv, c.ring_k_dtype,
+                     c.ring_d_dtype);
 }
 
 template <typename T>
@@ -126,7 +128,10 @@ rssm_status window(rssm_handle* h, int32_t layer, const void* q, const void* k, 
   if (T < 1 || T > c.max_T) return RSSM_ERR_INVALID_ARG;
   if (B == 0) return RSSM_OK;
   if (!q || !k || !v || !beta || !g || !slot || !o) return RSSM_ERR_INVALID_ARG;
-  if (!aligned4(beta) || !aligned4(g) || !aligned4(slot)) return RSSM_ERR_INVALID_ARG;
+  if (!aligned4(beta) || !aligned4(slot)) return RSSM_ERR_INVALID_ARG;
+  // window rows move by bulk copies: 16-byte aligned sources
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return RSSM_ERR_INVALID_ARG;
+  if (c.algo == RSSM_ALGO_KDA ? !aligned16(g) : !aligned4(g)) return RSSM_ERR_INVALID_ARG;
 
   ReplayParams p{};
   const rssm_buffers& b = h->buf;
@@ -221,7 +226,7 @@ rssm_status rssm_alloc(const rssm_config* cfg, const rssm_buffers* buf, rssm_han
       !b.cursor || !b.err_word)
     return RSSM_ERR_INVALID_ARG;
   if (!aligned16(b.state) || !aligned16(b.ring_k) || !aligned16(b.ring_d) ||
-      !aligned16(b.ring_v) || !aligned4(b.ring_g) || !aligned4(b.ring_beta) ||
+      !aligned16(b.ring_v) || !aligned16(b.ring_g) || !aligned4(b.ring_beta) ||
       !aligned4(b.cursor) || !aligned4(b.err_word))
     return RSSM_ERR_INVALID_ARG;
 

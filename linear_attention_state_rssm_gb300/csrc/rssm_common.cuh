@@ -32,25 +32,60 @@ constexpr unsigned long long kWaitLimitNs = 500ull * 1000ull * 1000ull;
 __host__ __device__ constexpr int dtype_bytes(int dt) { return dt == DT_F32 ? 4 : 2; }
 __host__ __device__ constexpr uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
 
+// The checkpoint tile streams through a ring of kStages shared-memory stages,
+// each holding one chunk of whole rows (at most kChunkBytes) moved by one bulk
+// async copy.
+constexpr int kStages = 4;
+constexpr int kChunkBytes = 8192;
+
+// mbarriers of one CTA: the window rows, the history records, then one "full"
+// and one "empty" barrier per stage of the tile ring.
+constexpr int kMbarWin = 0;
+constexpr int kMbarHist = 1;
+constexpr int kMbarFull = 2;
+constexpr int kMbarEmpty = 2 + kStages;
+constexpr int kMbars = 2 + 2 * kStages;
+
+// Geometry of the tile ring for a [dk][dv] tile of `state_bytes`-byte elements.
+struct TileRing {
+  int cr;       // rows per chunk
+  int nchunk;   // chunks per tile
+  int ns;       // stages in use
+  uint32_t chunk_bytes;
+  __host__ __device__ TileRing(int dk, int dv, int state_bytes) {
+    const int rowb = dv * state_bytes;
+    cr = kChunkBytes / rowb < dk ? kChunkBytes / rowb : dk;
+    nchunk = dk / cr;
+    ns = nchunk < kStages ? nchunk : kStages;
+    chunk_bytes = (uint32_t)(cr * rowb);
+  }
+};
+
 // Byte offsets into the dynamic shared memory of the replay kernel.
 struct ReplaySmem {
-  uint32_t mbar;   // kWarps mbarriers (one per row chunk of the state tile)
+  uint32_t ring;   // tile ring: ns stages of one chunk each (offset 0)
+  uint32_t mbar;   // kMbars mbarriers
   uint32_t wq;     // [T][dk]  window q (fp32)
   uint32_t wk;     // [T][dk]  window k (fp32)
   uint32_t wv;     // [T][dv]  window v (fp32)
+  uint32_t wraw;   // raw 16-bit window rows q [T][dk], k [T][dk], v [T][dv] (16-bit inputs)
   uint32_t wb;     // [NT]     window beta
   uint32_t wg;     // [T] (GDN) | [T][dk] (KDA): window gates -> inclusive prefix
-  uint32_t scal;   // GDN: es[NT], eG[NT], gam; KDA: egam[dk], gam[dk]
+  uint32_t yk;     // KDA [T][dk]: e^{G_i} * k_i (history dots)
+  uint32_t yq;     // KDA [T][dk]: e^{G_i} * q_i
+  uint32_t scal;   // GDN: es[NT], eG[NT], Gam, e^Gam; KDA: egam[dk], gam[dk]
   uint32_t xh;     // [dk][2NT] mat-vec inputs
   uint32_t am;     // [NT][NT] window coefficients A (strictly lower)
   uint32_t fm;     // [NT][NT] window coefficients F (lower incl. diagonal)
-  uint32_t hk;     // [L][dk]  history keys (KDA: decay-scaled)
-  uint32_t hd;     // [L][dv]  history deltas
+  uint32_t hk;     // [L][dk]  history keys (fp32; KDA: decay-scaled in place)
+  uint32_t hkraw;  // [L][dk]  raw 16-bit history keys (16-bit ring keys)
+  uint32_t hd;     // [L][dv]  history deltas (fp32)
+  uint32_t hdraw;  // [L][dv]  raw 16-bit history deltas (16-bit ring deltas)
+  uint32_t hg;     // [L][dk]  KDA history gates
   uint32_t hf;     // [L]      GDN: raw gates -> exp(suffix sums)
   uint32_t hdot;   // [L][2NT] history dot coefficients
-  uint32_t red;    // [kWarps][VB][dv] partial mat-vec sums (unless aliased)
+  uint32_t red;    // [RG][2NT][dv] partial column sums when dv < kThreads
   uint32_t total;
-  int red_alias;   // partial sums overwrite each warp's own consumed tile rows
 };
 
 struct ReplayParams {
@@ -80,7 +115,7 @@ struct ReplayParams {
 };
 
 struct FoldSmem {
-  uint32_t mbar, hk, hd, hf, scal, total;
+  uint32_t ring, mbar, hk, hkraw, hd, hdraw, hg, hf, scal, total;
 };
 
 struct FoldParams {
@@ -99,49 +134,60 @@ struct FoldParams {
   FoldSmem sm;
 };
 
-// Vector-block width of the mat-vec accumulators.
-__host__ __device__ constexpr int vblock(int NT) { return 2 * NT < 16 ? 2 * NT : 16; }
+
 
 // Shared memory plan of the replay kernel for a window of T <= NT tokens and a
 // ring of L records.
-__host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, int NT,
-                                                    int T, int L, int dk, int dv) {
+__host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, int NT, int T,
+                                                    int L, int dk, int dv, int in_dt, int rk_dt,
+                                                    int rd_dt) {
   ReplaySmem m{};
   const int NV = 2 * NT;
-  const int VB = vblock(NT);
-  uint32_t off = align16((uint32_t)dk * dv * state_bytes);
-  m.mbar = off;  off = align16(off + 8u * kWarps);
+  const bool kda = algo == ALGO_KDA;
+  const int RG = kThreads / dv;
+  const TileRing tr(dk, dv, state_bytes);
+  uint32_t off = 0;
+  m.ring = off;  off = align16(off + tr.ns * tr.chunk_bytes);
+  m.mbar = off;  off = align16(off + 8u * kMbars);
   m.wq = off;    off = align16(off + 4u * T * dk);
   m.wk = off;    off = align16(off + 4u * T * dk);
   m.wv = off;    off = align16(off + 4u * T * dv);
+  m.wraw = off;  if (in_dt != DT_F32) off = align16(off + 2u * T * (2 * dk + dv));
   m.wb = off;    off = align16(off + 4u * NT);
-  m.wg = off;    off = align16(off + 4u * T * (algo == ALGO_GDN ? 1 : dk));
-  m.scal = off;  off = align16(off + 4u * (algo == ALGO_GDN ? 2 * NT + 4 : 2 * dk));
+  m.wg = off;    off = align16(off + 4u * T * (kda ? dk : 1));
+  m.yk = off;    if (kda) off = align16(off + 4u * T * dk);
+  m.yq = off;    if (kda) off = align16(off + 4u * T * dk);
+  m.scal = off;  off = align16(off + 4u * (kda ? 2 * dk : 2 * NT + 4));
   m.xh = off;    off = align16(off + 4u * dk * NV);
   m.am = off;    off = align16(off + 4u * NT * NT);
   m.fm = off;    off = align16(off + 4u * NT * NT);
   m.hk = off;    off = align16(off + 4u * L * dk);
+  m.hkraw = off; if (rk_dt != DT_F32) off = align16(off + 2u * L * dk);
   m.hd = off;    off = align16(off + 4u * L * dv);
+  m.hdraw = off; if (rd_dt != DT_F32) off = align16(off + 2u * L * dv);
+  m.hg = off;    if (kda) off = align16(off + 4u * L * dk);
   m.hf = off;    off = align16(off + 4u * L);
   m.hdot = off;  off = align16(off + 4u * L * NV);
-  // Each warp's partial sums fit in its own rows of the tile when one vector
-  // block covers all vectors and VB*dv*4 <= (dk/4)*dv*state_bytes.
-  m.red_alias = (NV == VB) && (VB * 16 <= dk * state_bytes);
-  m.red = off;
-  if (!m.red_alias) off = align16(off + 4u * kWarps * VB * dv);
+  m.red = off;   if (RG > 1) off = align16(off + 4u * RG * NV * dv);
   m.total = off;
   return m;
 }
 
-__host__ __device__ inline FoldSmem fold_layout(int algo, int state_bytes, int L, int dk,
-                                                int dv) {
+__host__ __device__ inline FoldSmem fold_layout(int algo, int state_bytes, int L, int dk, int dv,
+                                                int rk_dt, int rd_dt) {
   FoldSmem m{};
-  uint32_t off = align16((uint32_t)dk * dv * state_bytes);
-  m.mbar = off;  off = align16(off + 8u * kWarps);
+  const bool kda = algo == ALGO_KDA;
+  const TileRing tr(dk, dv, state_bytes);
+  uint32_t off = 0;
+  m.ring = off;  off = align16(off + tr.ns * tr.chunk_bytes);
+  m.mbar = off;  off = align16(off + 8u * kMbars);
   m.hk = off;    off = align16(off + 4u * L * dk);
+  m.hkraw = off; if (rk_dt != DT_F32) off = align16(off + 2u * L * dk);
   m.hd = off;    off = align16(off + 4u * L * dv);
+  m.hdraw = off; if (rd_dt != DT_F32) off = align16(off + 2u * L * dv);
+  m.hg = off;    if (kda) off = align16(off + 4u * L * dk);
   m.hf = off;    off = align16(off + 4u * L);
-  m.scal = off;  off = align16(off + 4u * (algo == ALGO_GDN ? 4 : 2 * dk));
+  m.scal = off;  off = align16(off + 4u * (kda ? 2 * dk : 4));
   m.total = off;
   return m;
 }
@@ -155,6 +201,18 @@ __device__ __forceinline__ float ld_f32(const void* base, size_t i, int dt) {
   return __half2float(static_cast<const __half*>(base)[i]);
 }
 
+// Widen n 16-bit values (bf16 or fp16) in shared memory to fp32.
+__device__ __forceinline__ void widen16(float* dst, const void* src, int n, int dt, int tid,
+                                        int nthreads) {
+  if (dt == DT_BF16) {
+    const __nv_bfloat16* s = static_cast<const __nv_bfloat16*>(src);
+    for (int e = tid; e < n; e += nthreads) dst[e] = __bfloat162float(s[e]);
+  } else {
+    const __half* s = static_cast<const __half*>(src);
+    for (int e = tid; e < n; e += nthreads) dst[e] = __half2float(s[e]);
+  }
+}
+
 __device__ __forceinline__ void st_f32(void* base, size_t i, int dt, float x) {
   if (dt == DT_F32) {
     static_cast<float*>(base)[i] = x;
@@ -164,38 +222,6 @@ __device__ __forceinline__ void st_f32(void* base, size_t i, int dt, float x) {
     static_cast<__half*>(base)[i] = __float2half_rn(x);
   }
 }
-
-template <typename ST>
-struct StateIO;
-
-template <>
-struct StateIO<float> {
-  static __device__ __forceinline__ float4 load4(const float* p) {
-    return *reinterpret_cast<const float4*>(p);
-  }
-  static __device__ __forceinline__ void store4(float* p, float4 x) {
-    *reinterpret_cast<float4*>(p) = x;
-  }
-};
-
-template <>
-struct StateIO<__nv_bfloat16> {
-  static __device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
-    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
-    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
-    const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
-    return make_float4(fa.x, fa.y, fb.x, fb.y);
-  }
-  static __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 x) {
-    const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(x.z, x.w);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t*>(&a);
-    u.y = *reinterpret_cast<const uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(p) = u;
-  }
-};
 
 // ------------------------------------------------------------------ PTX
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -209,6 +235,10 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {

@@ -1,6 +1,8 @@
 // Device helpers shared by the replay kernel and the fold kernel: staging the
-// ring history, turning its gates into decay factors, and folding it into the
-// checkpoint tile.
+// ring history with bulk async copies, turning its gates into decay factors,
+// and streaming the checkpoint tile through a ring of shared-memory stages,
+// each thread consuming one value column (with the fold and the mat-vecs of
+// the window fused in).
 //
 // Replay identity (LightLLM PR #1690 "feat: add ReplaySSM state modes for GDN
 // and KDA": the checkpoint is the canonical state and the ring holds the
@@ -14,147 +16,252 @@
 
 namespace rssm {
 
-// Stage n history records of one (slot, key head, value head) into shared
-// memory as fp32: keys [n][dk], deltas [n][dv]; GDN raw gates [n] into hf.
+// Issue the bulk copies of n history records of one (slot, key head, value
+// head), completing on `bar` (one thread, after the mbarrier is initialised):
+// keys [n][dk] -> hk (fp32 ring) or hkraw (16-bit ring), deltas [n][dv] -> hd
+// or hdraw, KDA gates [n][dk] -> hg. The ring is head-major, so each run is
+// contiguous; every run is a multiple of 16 bytes (dk, dv >= 32).
 template <int ALGO>
-__device__ __forceinline__ void stage_history(int n, int dk, int dv, const void* ring_k,
+__device__ __forceinline__ void issue_history(int n, int dk, int dv, const void* ring_k,
                                               size_t kbase, int rk_dt, const void* ring_d,
                                               size_t dbase, int rd_dt, const float* ring_g,
-                                              size_t gbase, float* hk, float* hd, float* hf,
-                                              int tid) {
-  for (int e = tid; e < n * dk; e += kThreads) hk[e] = ld_f32(ring_k, kbase + e, rk_dt);
-  for (int e = tid; e < n * dv; e += kThreads) hd[e] = ld_f32(ring_d, dbase + e, rd_dt);
-  if (ALGO == ALGO_GDN) {
-    for (int m = tid; m < n; m += kThreads) hf[m] = ring_g[gbase + m];
-  }
+                                              size_t gbase, float* hk, void* hkraw, float* hd,
+                                              void* hdraw, float* hg, uint64_t* bar) {
+  const int sk = dtype_bytes(rk_dt), sd = dtype_bytes(rd_dt);
+  const uint32_t kb = (uint32_t)(n * dk * sk), db = (uint32_t)(n * dv * sd);
+  const uint32_t gb = ALGO == ALGO_KDA ? (uint32_t)(n * dk * 4) : 0u;
+  mbar_expect_tx(bar, kb + db + gb);
+  bulk_g2s(rk_dt == DT_F32 ? static_cast<void*>(hk) : hkraw,
+           static_cast<const char*>(ring_k) + kbase * sk, kb, bar);
+  bulk_g2s(rd_dt == DT_F32 ? static_cast<void*>(hd) : hdraw,
+           static_cast<const char*>(ring_d) + dbase * sd, db, bar);
+  if (ALGO == ALGO_KDA) bulk_g2s(hg, ring_g + gbase, gb, bar);
 }
 
-// Turn staged history into decay-scaled keys k~_m (in place in hk) and the total
-// decay. Needs a __syncthreads() between stage_history and this call; ends with
-// one. GDN: scal[0] <- Gam, scal[1] <- exp(Gam). KDA: gam[ch] <- Gam[ch],
-// egam[ch] <- exp(Gam[ch]); the KDA record gates are read from global memory
-// (ring_g + gbase, [n][dk]).
-template <int ALGO>
-__device__ __forceinline__ void history_decay(int n, int dk, float* hk, float* hf, float* scal,
-                                              float* gam, float* egam, const float* ring_g,
-                                              size_t gbase, int tid, int warp, int lane) {
-  if (ALGO == ALGO_GDN) {
-    if (warp == 0) {
-      // Exclusive suffix sums of the record gates, 32 records at a time from
-      // the newest: hf[m] <- exp(sum_{m' > m} g_m').
-      float carry = 0.f;
-      for (int hi = n; hi > 0; hi -= 32) {
-        const int m = hi - 1 - lane;
-        const float gv = (m >= 0) ? hf[m] : 0.f;
-        float incl = gv;
+// Once the history copies have landed: widen 16-bit records to fp32.
+__device__ __forceinline__ void widen_history(int n, int dk, int dv, int rk_dt, int rd_dt,
+                                              float* hk, const void* hkraw, float* hd,
+                                              const void* hdraw, int tid) {
+  if (rk_dt != DT_F32) widen16(hk, hkraw, n * dk, rk_dt, tid, kThreads);
+  if (rd_dt != DT_F32) widen16(hd, hdraw, n * dv, rd_dt, tid, kThreads);
+}
+
+// GDN, warp 0: hf[m] holds the raw record gates g_m; replaces them with
+// exp(sum_{m' > m} g_m') and writes Gam, exp(Gam) to scal[0], scal[1].
+__device__ __forceinline__ void gdn_history_scan(int n, float* hf, float* scal, int lane) {
+  float carry = 0.f;
+  for (int hi = n; hi > 0; hi -= 32) {
+    const int m = hi - 1 - lane;  // newest record first
+    const float gv = (m >= 0) ? hf[m] : 0.f;
+    float incl = gv;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const float t = __shfl_up_sync(kFull, incl, off);
-          if (lane >= off) incl += t;
-        }
-        float excl = __shfl_up_sync(kFull, incl, 1);
-        if (lane == 0) excl = 0.f;
-        if (m >= 0) hf[m] = __expf(carry + excl);
-        carry += __shfl_sync(kFull, incl, 31);
-      }
-      if (lane == 0) {
-        scal[0] = carry;
-        scal[1] = __expf(carry);
-      }
+    for (int off = 1; off < 32; off <<= 1) {
+      const float t = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += t;
     }
-    __syncthreads();
-    for (int e = tid; e < n * dk; e += kThreads) hk[e] *= hf[e / dk];
-    __syncthreads();
-  } else {
-    for (int ch = tid; ch < dk; ch += kThreads) {
-      float suf = 0.f;
-      for (int m = n - 1; m >= 0; --m) {
-        hk[m * dk + ch] *= __expf(suf);
-        suf += ring_g[gbase + (size_t)m * dk + ch];
-      }
-      gam[ch] = suf;
-      egam[ch] = __expf(suf);
-    }
-    __syncthreads();
+    float excl = __shfl_up_sync(kFull, incl, 1);
+    if (lane == 0) excl = 0.f;
+    if (m >= 0) hf[m] = __expf(carry + excl);
+    carry += __shfl_sync(kFull, incl, 31);
+  }
+  if (lane == 0) {
+    scal[0] = carry;
+    scal[1] = __expf(carry);
   }
 }
 
-// Thread mapping of one warp over its quarter of the state tile: rows
-// [warp*dk/4, (warp+1)*dk/4), a lane owning 4 consecutive columns of
-// `rows_per_thread` consecutive rows.
-struct TileMap {
-  int cc, rs, ccw, rsw, rpt, row0;
-  __device__ __forceinline__ TileMap(int dk, int dv, int warp, int lane) {
-    const int rpw = dk / kWarps;
-    ccw = dv / 4 < 32 ? dv / 4 : 32;
-    rsw = 32 / ccw;
-    cc = lane % ccw;
-    rs = lane / ccw;
-    rpt = rpw / rsw;
-    row0 = warp * rpw + rs * rpt;
+// KDA, one key channel: scale the staged keys of channel ch by their decay to
+// the end of the history (k~_m[ch], in place) and return Gam[ch]. hg holds the
+// record gates [n][dk].
+__device__ __forceinline__ float kda_history_channel(int n, int dk, int ch, float* hk,
+                                                     const float* hg) {
+  float suf = 0.f;
+  for (int m = n - 1; m >= 0; --m) {
+    hk[m * dk + ch] *= __expf(suf);
+    suf += hg[m * dk + ch];
+  }
+  return suf;
+}
+
+// Column mapping of a CTA over one (slot, head) checkpoint tile [dk][dv]:
+// thread tid owns value column col = tid % dv and rows rg, rg + RG, ... with
+// RG = kThreads / dv row groups. A warp's load of one row is 32 consecutive
+// columns (128 bytes for fp32).
+struct ColMap {
+  int col, rg, RG, nrow;
+  __device__ __forceinline__ ColMap(int dk, int dv, int tid) {
+    RG = kThreads / dv;
+    col = tid % dv;
+    rg = tid / dv;
+    nrow = dk / RG;
+  }
+  __device__ __forceinline__ int row(int j) const { return rg + RG * j; }
+};
+
+template <typename ST>
+__device__ __forceinline__ float st_load(const ST* p);
+template <>
+__device__ __forceinline__ float st_load<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float st_load<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+
+// Round to the checkpoint dtype, store, and return the stored value.
+template <typename ST>
+__device__ __forceinline__ float st_store(ST* p, float x);
+template <>
+__device__ __forceinline__ float st_store<float>(float* p, float x) {
+  *p = x;
+  return x;
+}
+template <>
+__device__ __forceinline__ float st_store<__nv_bfloat16>(__nv_bfloat16* p, float x) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(x);
+  *p = b;
+  return __bfloat162float(b);
+}
+
+// Consume one register batch of this thread's column:
+//  - FOLD: S[row] <- decay(row) S[row] + sum_m k~_m[row] d~_m   (d~_m = f_m d_m[col]),
+//    stored back to the checkpoint in its dtype; the stored value is used below;
+//  - NV > 0: y[v] += x_v[row] S[row] for every mat-vec vector (xh [dk][NV]).
+// GDN: hk holds raw keys and f_m = hf[m], decay = gdn_decay; KDA: hk holds k~
+// and f_m = 1, decay(row) = egam[row].
+template <int ALGO, typename ST, int RB, int NV, bool FOLD>
+__device__ __forceinline__ void consume_rows(float (&buf)[RB], float (&y)[NV > 0 ? NV : 1],
+                                             ST* gcol, int j0, const ColMap& cm, int dk, int dv,
+                                             int n, const float* hk, const float* hd,
+                                             const float* hf, float gdn_decay,
+                                             const float* egam, const float* xh) {
+  if (FOLD) {
+    float acc[RB];
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+      const int row = cm.row(min(j0 + u, cm.nrow - 1));
+      const float dec = (ALGO == ALGO_GDN) ? gdn_decay : egam[row];
+      acc[u] = dec * buf[u];
+    }
+    for (int m = 0; m < n; ++m) {
+      float dm = hd[m * dv + cm.col];
+      if (ALGO == ALGO_GDN) dm *= hf[m];
+      const float* km = hk + (size_t)m * dk;
+#pragma unroll
+      for (int u = 0; u < RB; ++u) {
+        acc[u] = fmaf(km[cm.row(min(j0 + u, cm.nrow - 1))], dm, acc[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+      const int j = j0 + u;
+      if (j < cm.nrow) buf[u] = st_store<ST>(gcol + (size_t)cm.row(j) * dv, acc[u]);
+    }
+  }
+  if constexpr (NV > 0) {
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+      const int j = j0 + u;
+      if (j < cm.nrow) {
+        const float* xr = xh + (size_t)cm.row(j) * NV;
+        if constexpr (NV % 4 == 0) {
+#pragma unroll
+          for (int q4 = 0; q4 < NV / 4; ++q4) {
+            const float4 x = reinterpret_cast<const float4*>(xr)[q4];
+            y[4 * q4 + 0] = fmaf(x.x, buf[u], y[4 * q4 + 0]);
+            y[4 * q4 + 1] = fmaf(x.y, buf[u], y[4 * q4 + 1]);
+            y[4 * q4 + 2] = fmaf(x.z, buf[u], y[4 * q4 + 2]);
+            y[4 * q4 + 3] = fmaf(x.w, buf[u], y[4 * q4 + 3]);
+          }
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(xr);
+          y[0] = fmaf(x.x, buf[u], y[0]);
+          y[1] = fmaf(x.y, buf[u], y[1]);
+        }
+      }
+    }
+  }
+}
+
+// Ring of shared-memory stages over the row chunks of one checkpoint tile.
+// One thread produces (bulk async copies), every warp consumes; stage
+// j % ns holds chunk j; "full" completes when a chunk has landed, "empty"
+// when all warps have consumed it.
+template <typename ST>
+struct TilePipe {
+  ST* ring;
+  uint64_t* full;
+  uint64_t* empty;
+  const ST* gtile;
+  int dv;
+  TileRing tr;
+  __device__ __forceinline__ TilePipe(ST* ring_, uint64_t* mbar, const ST* gtile_, int dk, int dv_)
+      : ring(ring_), full(mbar + kMbarFull), empty(mbar + kMbarEmpty), gtile(gtile_), dv(dv_),
+        tr(dk, dv_, (int)sizeof(ST)) {}
+  // mbarrier set-up (one thread, before the CTA-wide fence and barrier)
+  __device__ __forceinline__ void init() const {
+    for (int st = 0; st < tr.ns; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kWarps);
+    }
+  }
+  __device__ __forceinline__ void issue(int j) const {
+    const int st = j % tr.ns;
+    mbar_expect_tx(&full[st], tr.chunk_bytes);
+    bulk_g2s(ring + (size_t)st * tr.cr * dv, gtile + (size_t)j * tr.cr * dv, tr.chunk_bytes,
+             &full[st]);
+  }
+  // producer: the first ns chunks
+  __device__ __forceinline__ void prime() const {
+    for (int j = 0; j < tr.ns; ++j) issue(j);
+  }
+  __device__ __forceinline__ bool wait_full(int j) const {
+    return mbar_wait_bounded(&full[j % tr.ns], (uint32_t)((j / tr.ns) & 1));
+  }
+  // every warp, once it has consumed chunk j
+  __device__ __forceinline__ void release(int j, int lane) const {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[j % tr.ns]);
+  }
+  // producer, after its own release of chunk j: refill that stage with chunk j + ns
+  __device__ __forceinline__ bool refill(int j) const {
+    if (j + tr.ns >= tr.nchunk) return true;
+    const bool ok = mbar_wait_bounded(&empty[j % tr.ns], (uint32_t)((j / tr.ns) & 1));
+    if (ok) issue(j + tr.ns);
+    return ok;
+  }
+  // a CTA that leaves early lets the primed chunks land first
+  __device__ __forceinline__ void drain() const {
+    for (int j = 0; j < tr.ns; ++j) mbar_wait_bounded(&full[j], 0);
   }
 };
 
-// Fold n staged records into this warp's rows of the tile:
-//   S[row][:] <- decay(row) S[row][:] + sum_m k~_m[row] d_m[:]
-// and write the folded rows to shared memory and to the checkpoint in global
-// memory. decay(row) = exp(Gam) (GDN) or exp(Gam[row]) (KDA).
-template <int ALGO, typename ST>
-__device__ __forceinline__ void fold_rows(ST* tile, ST* gtile, int n, int dk, int dv,
-                                          const float* hk, const float* hd, float gdn_decay,
-                                          const float* egam, int warp, int lane) {
-  const TileMap tm(dk, dv, warp, lane);
-  for (int t0 = 0; t0 < tm.rpt; t0 += 8) {
-    const int nr = tm.rpt - t0 < 8 ? tm.rpt - t0 : 8;
-    const int rbase = tm.row0 + t0;
-    float4 acc[8];
+// Stream the checkpoint tile through the ring; each thread consumes its
+// column's rows of every chunk (fold and/or mat-vecs, see consume_rows).
+// Returns false if a bounded wait ran out.
+template <int ALGO, typename ST, int NV, bool FOLD>
+__device__ __forceinline__ bool stream_tile(const TilePipe<ST>& pipe, float (&y)[NV > 0 ? NV : 1],
+                                            ST* gcol, const ColMap& cm, int dk, int dv, int n,
+                                            const float* hk, const float* hd, const float* hf,
+                                            float gdn_decay, const float* egam, const float* xh,
+                                            int tid, int lane) {
+  constexpr int RB = 8;  // rows of a chunk held in registers at a time
+  const int rpc = pipe.tr.cr / cm.RG;  // this thread's rows per chunk (a multiple of 8)
+  bool ok = true;
+  for (int j = 0; j < pipe.tr.nchunk; ++j) {
+    ok = pipe.wait_full(j) && ok;
+    const ST* stg = pipe.ring + (size_t)(j % pipe.tr.ns) * pipe.tr.cr * dv +
+                    (size_t)cm.rg * dv + cm.col;
+    for (int u0 = 0; u0 < rpc; u0 += RB) {
+      float buf[RB];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < nr) {
-        const int row = rbase + j;
-        const float4 s4 = StateIO<ST>::load4(tile + (size_t)row * dv + 4 * tm.cc);
-        const float dec = (ALGO == ALGO_GDN) ? gdn_decay : egam[row];
-        acc[j] = make_float4(dec * s4.x, dec * s4.y, dec * s4.z, dec * s4.w);
-      }
+      for (int u = 0; u < RB; ++u) buf[u] = st_load<ST>(stg + (size_t)cm.RG * (u0 + u) * dv);
+      consume_rows<ALGO, ST, RB, NV, FOLD>(buf, y, gcol, j * rpc + u0, cm, dk, dv, n, hk, hd, hf,
+                                           gdn_decay, egam, xh);
     }
-    for (int m = 0; m < n; ++m) {
-      const float4 d4 = *reinterpret_cast<const float4*>(hd + (size_t)m * dv + 4 * tm.cc);
-      const float* km = hk + (size_t)m * dk + rbase;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j < nr) {
-          const float kt = km[j];
-          acc[j].x = fmaf(kt, d4.x, acc[j].x);
-          acc[j].y = fmaf(kt, d4.y, acc[j].y);
-          acc[j].z = fmaf(kt, d4.z, acc[j].z);
-          acc[j].w = fmaf(kt, d4.w, acc[j].w);
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < nr) {
-        const size_t off = (size_t)(rbase + j) * dv + 4 * tm.cc;
-        StateIO<ST>::store4(tile + off, acc[j]);
-        StateIO<ST>::store4(gtile + off, acc[j]);
-      }
-    }
+    pipe.release(j, lane);
+    if (tid == 0) ok = pipe.refill(j) && ok;
   }
-}
-
-// Issue the bulk copies of one (slot, head) state tile: one row chunk per warp,
-// each completing on its own mbarrier. Called by one thread after the
-// mbarriers are initialised and the initialisation is visible to the CTA.
-template <typename ST>
-__device__ __forceinline__ void load_tile_async(ST* tile, const ST* gtile, int dk, int dv,
-                                                uint64_t* mbar) {
-  const int rpw = dk / kWarps;
-  const uint32_t bytes = (uint32_t)(rpw * dv * (int)sizeof(ST));
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    mbar_expect_tx(&mbar[w], bytes);
-    bulk_g2s(tile + (size_t)w * rpw * dv, gtile + (size_t)w * rpw * dv, bytes, &mbar[w]);
-  }
+  return ok;
 }
 
 }  // namespace rssm
