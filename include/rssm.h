@@ -47,7 +47,7 @@
  *   q, k : [B*T][HK][dk]  in_dtype          v, o : [B*T][HV][dv] in_dtype
  *   beta : [B*T][HV] fp32                   g    : [B*T][HV] (GDN) | [B*T][HV][dk] (KDA) fp32
  *   state    : [n_layers][n_slots][HV][dk][dv]  state_dtype (the checkpoint)
- *   ring_k   : [n_layers][n_slots][HK][L][dk]   ring_k_dtype
+ *   ring_k   : [n_layers][n_slots][HV][L][dk]   ring_k_dtype (one copy per value head)
  *   ring_d   : [n_layers][n_slots][HV][L][dv]   ring_d_dtype
  *   ring_g   : [n_layers][n_slots][HV][L]       (GDN) | [..][L][dk] (KDA) fp32
  *   ring_v   : [n_layers][n_slots][HV][L][dv]   in_dtype
@@ -68,7 +68,7 @@ extern "C" {
 typedef enum rssm_status {
   RSSM_OK = 0,
   RSSM_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad index or size      */
-  RSSM_ERR_UNSUPPORTED = 2,  /* valid but not built: dims, dtypes, G > 8, smem  */
+  RSSM_ERR_UNSUPPORTED = 2,  /* valid but not built: dims, dtypes, smem limits  */
   RSSM_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed             */
   RSSM_ERR_DEVICE = 4        /* rssm_get_device_error found a non-zero word      */
 } rssm_status;
@@ -86,8 +86,8 @@ enum {
 };
 
 /*
- * Store configuration. Supported: dk, dv in {32, 64, 128}; HV a multiple of HK
- * with G = HV/HK <= 8; 1 <= max_T <= 16; max_T <= L <= 256 (a ring shorter than
+ * Store configuration. Supported: dk, dv in {32, 64, 128}; HV a multiple of HK;
+ * 1 <= max_T <= 16; max_T <= L <= 256 (a ring shorter than
  * the widest window is refused, SGLang fork PR jianc99/sglang#2, first commit);
  * in_dtype F32|BF16; state_dtype F32|BF16; ring_k_dtype F32|F16|BF16;
  * ring_d_dtype F32|F16. commit_mode selects what rssm_commit does.
@@ -155,7 +155,8 @@ void rssm_free(rssm_handle *h);
  * c = cursor[s]; fold = force[r] || c + 1 > L. On fold the history is folded
  * into the checkpoint first (S0 <- replayed state) and the new record goes to
  * ring position 0, else to c. Writes o (B rows), the token's record
- * (k once per key head, d, g, v, beta) and, if fold_out is non-null,
+ * (k, d, g, v, beta; each value head keeps its own copy of the key) and, if
+ * fold_out is non-null,
  * fold_out[r] = fold (0/1) for live rows. q, k, v (and g for KDA) must be
  * 16-byte aligned; beta, g (GDN) and slot 4-byte aligned. When advance_cursor is non-zero
  * (the last layer of the step) the cursor kernel then sets

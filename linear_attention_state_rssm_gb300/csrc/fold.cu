@@ -22,8 +22,7 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int h = blockIdx.x, r = blockIdx.y, layer = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int dk = p.dk, dv = p.dv, L = p.L, HV = p.HV, HK = p.HK;
-  const int kh = h / p.G;
+  const int dk = p.dk, dv = p.dv, L = p.L, HV = p.HV;
 
   const int s = p.slot[r];
   if (s < 0) return;
@@ -65,7 +64,7 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
   // GDN: scal[0] = Gam, scal[1] = exp(Gam). KDA: egam[dk] = exp(Gam[ch]).
   float* egam = scal;
 
-  const size_t kbase = layer * p.layer_k + ((size_t)s * HK + kh) * L * dk;
+  const size_t kbase = layer * p.layer_k + ((size_t)s * HV + h) * L * dk;
   const size_t dbase = layer * p.layer_d + ((size_t)s * HV + h) * L * dv;
   const size_t gbase = layer * p.layer_g + ((size_t)s * HV + h) * L * (ALGO == ALGO_GDN ? 1 : dk);
 

@@ -1,19 +1,19 @@
 // Replay kernel: decode (T = 1) and speculative verify (T <= 16) of one layer,
 // with the ring-overflow fold fused in.
 //
-// One CTA of 4 warps per (request row, value head); for GQA the G value heads
-// of a key head form a thread-block cluster, whose barrier orders their reads
-// of the shared key records before a folding window overwrites them (LightLLM
-// PR #1690 "feat: add ReplaySSM state modes for GDN and KDA", commit message on
-// waiting until every value tile has read the old prefix before slot 0 is
-// rewritten; here the wait is a hardware cluster barrier, which always makes
-// progress because cluster CTAs are co-scheduled).
+// One CTA of 4 warps per (request row, value head). The (slot, head)
+// checkpoint tile S0 [dk][dv] streams through a ring of four shared-memory
+// stages (8 KB row chunks, one bulk async copy each, full/empty mbarriers); a
+// lane owns CW consecutive value columns of some rows of every chunk, so one
+// vector load feeds CW x 2T fused multiply-adds. The stream is the only
+// O(dk dv) work, and the kernel keeps the instructions spent around it small.
 //
-// The (slot, head) checkpoint tile S0 [dk][dv] streams through a ring of four
-// shared-memory stages (8 KB row chunks, one bulk async copy each, full/empty
-// mbarriers); thread tid consumes value column tid % dv of every chunk. The
-// small ring lets several CTAs share an SM, each with 32 KB of the tile in
-// flight from its first microsecond.
+// Ring keys are stored per value head, so every CTA reads and writes only its
+// own records: a folding window (which writes positions [0, T) of the history
+// it reads) waits for nothing but its own history copy. (LightLLM PR #1690
+// "feat: add ReplaySSM state modes for GDN and KDA" shares one key buffer
+// across the value heads of a key group and needs a counted cross-CTA barrier
+// for that reason; its author notes the barrier has no progress guarantee.)
 //
 // Per CTA, with c = cursor[slot], fold = force || c + T > L:
 //  1. bulk async copies: the first tile chunks and the window rows (they need
@@ -27,7 +27,7 @@
 //  4. stream the tile: on a fold S0 <- e^{Gam} S0 + sum_m k~_m d_m^T (stored
 //     back), and y_x = S0^T (e^{Gam_e + G_i} x) for all 2T vectors in one pass
 //     (a GDN window without a fold streams first, while its history lands);
-//  5. per column: a_i, b_i = y + sum_m H d_m; the triangular solve
+//  5. per value column: a_i, b_i = y + sum_m H d_m; the triangular solve
 //     d_i = beta_i (v_i - a_i) - sum_{j<i} A_ij d_j (forward substitution of
 //     (I + A) D = R) and o_i = scale (b_i + sum_{j<=i} F_ij d_j); the records of
 //     the window go to ring positions base + i (base = fold ? 0 : c).
@@ -42,9 +42,18 @@
 
 namespace rssm {
 
+// Dot products of key-channel vectors: lanes take float4 groups of channels,
+// then a warp reduction.
+__device__ __forceinline__ float4 ld4(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+
+// Narrow windows keep four CTAs per SM (at most 128 registers per thread);
+// wide verify windows trade occupancy for their larger accumulator tiles.
 template <int ALGO, typename ST, int NT>
-__global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) {
+__global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const ReplayParams p) {
   constexpr int NV = 2 * NT;             // mat-vec vectors: k_i at [0, NT), q_i at [NT, 2NT)
+  constexpr int CW = quad_width(NT);     // value columns per lane in the tile stream
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int h = blockIdx.x;
@@ -53,7 +62,7 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
   const int T = p.T, dk = p.dk, dv = p.dv, L = p.L, HV = p.HV, HK = p.HK;
   const int kh = h / p.G;
 
-  // ---- row resolve (uniform over the CTA and its cluster)
+  // ---- row resolve
   const int s = p.slot[r];
   if (s < 0) return;
   if (s >= p.n_slots) {
@@ -61,10 +70,7 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
     return;
   }
 
-  const ColMap cm(dk, dv, tid);
   ST* gtile = static_cast<ST*>(p.state) + ((size_t)s * HV + h) * dk * dv;
-  ST* gcol = gtile + cm.col;
-
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + p.sm.mbar);
   float* wq = reinterpret_cast<float*>(smem + p.sm.wq);
   float* wk = reinterpret_cast<float*>(smem + p.sm.wk);
@@ -98,9 +104,8 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
   const int s_in = dtype_bytes(p.in_dt);
   const uint32_t qrow = (uint32_t)(dk * s_in), vrow = (uint32_t)(dv * s_in);
 
-  // ---- 1. bulk async copies: window rows now, history once the cursor is
-  //         known. One thread issues every copy of a barrier after registering
-  //         its byte count.
+  // ---- 1. bulk async copies. One thread issues every copy of a barrier after
+  //         registering its byte count.
   const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv);
   if (tid == 0) {
     mbar_init(&mbar[kMbarWin], 1);
@@ -141,12 +146,11 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
     pipe.drain();
     return;
   }
-  // fold decision (uniform over the CTA and its cluster)
+  // fold decision (uniform over the CTA)
   const bool fold = (p.force != nullptr && p.force[r] != 0) || (c + T > L);
   const int base = fold ? 0 : c;
   const int nh = c;
-  const bool group_sync = fold && p.G > 1;
-  const size_t kbase = ((size_t)s * HK + kh) * L * dk;
+  const size_t kbase = ((size_t)s * HV + h) * L * dk;
   const size_t dbase = ((size_t)s * HV + h) * L * dv;
   const size_t gbase = ((size_t)s * HV + h) * L * (ALGO == ALGO_GDN ? 1 : dk);
   if (nh > 0 && tid == 0) {
@@ -162,23 +166,17 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
     widen16(wk, wraw + T * qrow, T * dk, p.in_dt, tid, kThreads);
     widen16(wv, wraw + 2 * T * qrow, T * dv, p.in_dt, tid, kThreads);
   }
+  // A folding window writes over positions [0, T) of the history it reads:
+  // its history copy must have landed before the records below.
+  if (fold && nh > 0) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
   __syncthreads();
 
-  // ---- records that need no result of the window: keys (once per key head),
-  //      gates and betas, at ring positions base + i. Each thread writes the
-  //      key channels it owns in step 2 below. A folding window writes over
-  //      positions [0, T) of the history it reads: it first waits for its own
-  //      history copy, then until the whole key group has read the old keys.
-  if (fold && nh > 0) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
-  if (group_sync) {
-    cluster_arrive_release();
-    cluster_wait_acquire();
-  }
+  // ---- records that need no result of the window: keys, gates and betas at
+  //      ring positions base + i. Each thread writes the key channels it owns
+  //      in step 2 below.
   for (int ch = tid; ch < dk; ch += kThreads) {
     for (int i = 0; i < T; ++i) {
-      if (h % p.G == 0) {
-        st_f32(p.ring_k, kbase + (size_t)(base + i) * dk + ch, p.rk_dt, wk[i * dk + ch]);
-      }
+      st_f32(p.ring_k, kbase + (size_t)(base + i) * dk + ch, p.rk_dt, wk[i * dk + ch]);
       if (ALGO == ALGO_KDA) p.ring_g[gbase + (size_t)(base + i) * dk + ch] = wg[i * dk + ch];
     }
   }
@@ -187,12 +185,16 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
     if (ALGO == ALGO_GDN) p.ring_g[gbase + base + tid] = wg[tid];
   }
 
-  float y[NV];
+  const QuadLayout qlay(dv, CW);
+  const QuadLane qlane(qlay, CW, warp, lane);
+  float acc[NV][CW];
 #pragma unroll
-  for (int vv = 0; vv < NV; ++vv) y[vv] = 0.f;
+  for (int vv = 0; vv < NV; ++vv) {
+#pragma unroll
+    for (int cc = 0; cc < CW; ++cc) acc[vv][cc] = 0.f;
+  }
   // GDN mat-vec inputs are the raw window vectors (their scalar decay goes on
-  // the column results); without a fold the tile streams now, before the
-  // history is needed.
+  // the column results); without a fold the tile streams now.
   const bool early = ALGO == ALGO_GDN && !fold;
   if (ALGO == ALGO_GDN) {
     for (int e = tid; e < dk * NV; e += kThreads) {
@@ -202,8 +204,9 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
     }
     if (early) {
       __syncthreads();
-      copies_ok = stream_tile<ALGO, ST, NV, false>(pipe, y, gcol, cm, dk, dv, 0, hk, hd, hf, 1.f,
-                                                   egam, xh, tid, lane) && copies_ok;
+      copies_ok = stream_quads<ALGO, ST, NV, CW, false>(pipe, qlane, acc, gtile, dk, dv, 0, hk,
+                                                        hd, hf, 1.f, egam, xh, tid, lane) &&
+                  copies_ok;
     }
   }
   if (nh > 0 && !fold) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
@@ -271,11 +274,18 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
       for (int j = 0; j <= i; ++j, ++pi) {
         if ((pi & (kWarps - 1)) != warp) continue;
         float skk = 0.f, skq = 0.f;
-        for (int ch = lane; ch < dk; ch += 32) {
-          float kj = wk[j * dk + ch];
-          if (ALGO == ALGO_KDA) kj *= __expf(wg[i * dk + ch] - wg[j * dk + ch]);
-          skk = fmaf(kj, wk[i * dk + ch], skk);
-          skq = fmaf(kj, wq[i * dk + ch], skq);
+        for (int c4 = 4 * lane; c4 < dk; c4 += 128) {
+          float4 kj = ld4(wk + j * dk + c4);
+          if (ALGO == ALGO_KDA) {
+            const float4 gi = ld4(wg + i * dk + c4), gj = ld4(wg + j * dk + c4);
+            kj.x *= __expf(gi.x - gj.x);
+            kj.y *= __expf(gi.y - gj.y);
+            kj.z *= __expf(gi.z - gj.z);
+            kj.w *= __expf(gi.w - gj.w);
+          }
+          const float4 ki = ld4(wk + i * dk + c4), qi = ld4(wq + i * dk + c4);
+          skk = fmaf(kj.x, ki.x, fmaf(kj.y, ki.y, fmaf(kj.z, ki.z, fmaf(kj.w, ki.w, skk))));
+          skq = fmaf(kj.x, qi.x, fmaf(kj.y, qi.y, fmaf(kj.z, qi.z, fmaf(kj.w, qi.w, skq))));
         }
         skk = warp_sum(skk);
         skq = warp_sum(skq);
@@ -295,12 +305,15 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
       float part[NV];
 #pragma unroll
       for (int vv = 0; vv < NV; ++vv) part[vv] = 0.f;
-      for (int ch = lane; ch < dk; ch += 32) {
-        const float km = hk[m * dk + ch];
+      for (int c4 = 4 * lane; c4 < dk; c4 += 128) {
+        const float4 km = ld4(hk + m * dk + c4);
 #pragma unroll
         for (int vv = 0; vv < NV; ++vv) {
           const int i = vv < NT ? vv : vv - NT;
-          if (i < T) part[vv] = fmaf(km, (vv < NT ? xk : xq)[i * dk + ch], part[vv]);
+          if (i < T) {
+            const float4 x = ld4((vv < NT ? xk : xq) + i * dk + c4);
+            part[vv] = fmaf(km.x, x.x, fmaf(km.y, x.y, fmaf(km.z, x.z, fmaf(km.w, x.w, part[vv]))));
+          }
         }
       }
 #pragma unroll
@@ -316,39 +329,45 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
       }
     }
   }
-  __syncthreads();
 
   // ---- 4. stream the checkpoint tile (unless done early): fold, then S^T x
   if (!early) {
+    __syncthreads();
     bool ok;
     if (fold && nh > 0) {
-      ok = stream_tile<ALGO, ST, NV, true>(pipe, y, gcol, cm, dk, dv, nh, hk, hd, hf, hscal[1],
-                                           egam, xh, tid, lane);
+      ok = stream_quads<ALGO, ST, NV, CW, true>(pipe, qlane, acc, gtile, dk, dv, nh, hk, hd, hf,
+                                                hscal[1], egam, xh, tid, lane);
     } else {
-      ok = stream_tile<ALGO, ST, NV, false>(pipe, y, gcol, cm, dk, dv, 0, hk, hd, hf, 1.f, egam,
-                                            xh, tid, lane);
+      ok = stream_quads<ALGO, ST, NV, CW, false>(pipe, qlane, acc, gtile, dk, dv, 0, hk, hd, hf,
+                                                 1.f, egam, xh, tid, lane);
     }
     if (!ok) {
       atomicOr(p.err, DEVERR_TIMEOUT);
       copies_ok = false;
     }
   }
-  if (cm.RG > 1) {
-    // dv < kThreads: several row groups share a column; add their sums
+  // partial column sums of the warp row groups -> shared memory (the ring is
+  // free once every warp has consumed the last chunk)
+  __syncthreads();
+  if (qlane.first) {
 #pragma unroll
-    for (int vv = 0; vv < NV; ++vv) red[(cm.rg * NV + vv) * dv + cm.col] = y[vv];
-    __syncthreads();
-    if (cm.rg == 0) {
-      for (int g2 = 1; g2 < cm.RG; ++g2) {
+    for (int vv = 0; vv < NV; ++vv) {
 #pragma unroll
-        for (int vv = 0; vv < NV; ++vv) y[vv] += red[(g2 * NV + vv) * dv + cm.col];
-      }
+      for (int cc = 0; cc < CW; ++cc) red[(qlane.rg * NV + vv) * dv + qlane.col0 + cc] = acc[vv][cc];
     }
   }
+  __syncthreads();
 
   // ---- 5. per value column: corrections, triangular solve, outputs, deltas
-  if (cm.rg == 0) {
-    const int col = cm.col;
+  if (tid < dv) {
+    const int col = tid;
+    float y[NV];
+#pragma unroll
+    for (int vv = 0; vv < NV; ++vv) {
+      float sum = 0.f;
+      for (int g2 = 0; g2 < qlay.rgw; ++g2) sum += red[(g2 * NV + vv) * dv + col];
+      y[vv] = sum;
+    }
     if (ALGO == ALGO_GDN) {
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
@@ -371,10 +390,10 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
     for (int i = 0; i < NT; ++i) {
       d[i] = 0.f;
       if (i < T) {
-        float acc = wb[i] * (wv[i * dv + col] - y[i]);
+        float a = wb[i] * (wv[i * dv + col] - y[i]);
 #pragma unroll
-        for (int j = 0; j < i; ++j) acc = fmaf(-am[i * NT + j], d[j], acc);
-        d[i] = acc;
+        for (int j = 0; j < i; ++j) a = fmaf(-am[i * NT + j], d[j], a);
+        d[i] = a;
         float o = y[NT + i];
 #pragma unroll
         for (int j = 0; j <= i; ++j) o = fmaf(fm[i * NT + j], d[j], o);
@@ -382,7 +401,7 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
         const size_t tok = tok0 + i;
         st_f32(p.o, (tok * HV + h) * dv + col, p.in_dt, o);
         const size_t rec = dbase + (size_t)(base + i) * dv + col;
-        st_f32(p.ring_d, rec, p.rd_dt, acc);
+        st_f32(p.ring_d, rec, p.rd_dt, a);
         st_f32(p.ring_v, rec, p.in_dt, wv[i * dv + col]);
       }
     }
@@ -392,6 +411,7 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const ReplayParams p) 
     // give copies that did not arrive a second bounded chance before exit
     mbar_wait_bounded(&mbar[kMbarWin], 0);
     if (nh > 0) mbar_wait_bounded(&mbar[kMbarHist], 0);
+    pipe.drain();
   }
 }
 

@@ -8,24 +8,12 @@
 
 namespace rssm {
 
+// One CTA per (value head, request row).
 template <int ALGO, typename ST, int NT>
-static cudaError_t replay_launch_one(const ReplayParams& p, int cluster, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.HV, (unsigned)p.B, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = p.sm.total;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  cfg.numAttrs = 0;
-  if (cluster > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.numAttrs = 1;
-  }
-  cfg.attrs = attr;
-  return cudaLaunchKernelEx(&cfg, replay_kernel<ALGO, ST, NT>, p);
+static cudaError_t replay_launch_one(const ReplayParams& p, cudaStream_t st) {
+  const dim3 grid((unsigned)p.HV, (unsigned)p.B, 1);
+  replay_kernel<ALGO, ST, NT><<<grid, kThreads, p.sm.total, st>>>(p);
+  return cudaGetLastError();
 }
 
 template <int ALGO, typename ST, int NT>
@@ -41,13 +29,13 @@ static cudaError_t replay_prepare_one(int max_smem) {
 
 #define RSSM_DEFINE_REPLAY(NAME, ALGO, ST)                                                  \
   namespace rssm {                                                                          \
-  cudaError_t NAME##_launch(const ReplayParams& p, int NT, int cluster, cudaStream_t st) {  \
+  cudaError_t NAME##_launch(const ReplayParams& p, int NT, cudaStream_t st) {             \
     switch (NT) {                                                                           \
-      case 1: return replay_launch_one<ALGO, ST, 1>(p, cluster, st);                        \
-      case 2: return replay_launch_one<ALGO, ST, 2>(p, cluster, st);                        \
-      case 4: return replay_launch_one<ALGO, ST, 4>(p, cluster, st);                        \
-      case 8: return replay_launch_one<ALGO, ST, 8>(p, cluster, st);                        \
-      case 16: return replay_launch_one<ALGO, ST, 16>(p, cluster, st);                      \
+      case 1: return replay_launch_one<ALGO, ST, 1>(p, st);                                 \
+      case 2: return replay_launch_one<ALGO, ST, 2>(p, st);                                 \
+      case 4: return replay_launch_one<ALGO, ST, 4>(p, st);                                 \
+      case 8: return replay_launch_one<ALGO, ST, 8>(p, st);                                 \
+      case 16: return replay_launch_one<ALGO, ST, 16>(p, st);                               \
       default: return cudaErrorInvalidValue;                                                \
     }                                                                                       \
   }                                                                                         \

@@ -15,6 +15,7 @@ struct rssm_handle {
   rssm_buffers buf;
   int G;
   int max_smem;
+  int num_sms;
   size_t layer_state, layer_k, layer_d, layer_g, layer_v, layer_beta;  // elements
 };
 
@@ -22,7 +23,6 @@ namespace {
 
 constexpr int kMaxL = 256;
 constexpr int kMaxT = 16;
-constexpr int kMaxGroup = 8;
 constexpr int kMaxGrid = 65535;
 
 bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
@@ -54,7 +54,6 @@ rssm_status check_config(const rssm_config* c) {
   if (!std::isfinite(c->scale)) return RSSM_ERR_INVALID_ARG;
   // Valid but not built.
   if (!dim_ok(c->dk) || !dim_ok(c->dv)) return RSSM_ERR_UNSUPPORTED;
-  if (c->HV / c->HK > kMaxGroup) return RSSM_ERR_UNSUPPORTED;
   if (c->max_T > kMaxT || c->L > kMaxL) return RSSM_ERR_UNSUPPORTED;
   if (c->in_dtype == RSSM_F16 || c->state_dtype == RSSM_F16 || c->ring_d_dtype == RSSM_BF16)
     return RSSM_ERR_UNSUPPORTED;
@@ -67,7 +66,7 @@ size_t esize(int dt) { return dt == RSSM_F32 ? 4 : 2; }
 void sizes_of(const rssm_config& c, rssm_sizes* s) {
   const size_t ls = (size_t)c.n_layers * c.n_slots;
   s->state = ls * c.HV * c.dk * c.dv * esize(c.state_dtype);
-  s->ring_k = ls * c.HK * c.L * c.dk * esize(c.ring_k_dtype);
+  s->ring_k = ls * c.HV * c.L * c.dk * esize(c.ring_k_dtype);
   s->ring_d = ls * c.HV * c.L * c.dv * esize(c.ring_d_dtype);
   s->ring_g = ls * c.HV * c.L * n_gate(c) * sizeof(float);
   s->ring_v = ls * c.HV * c.L * c.dv * esize(c.in_dtype);
@@ -83,15 +82,13 @@ rssm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RSSM_OK : RSSM_
 
 int state_dt(const rssm_config& c) { return c.state_dtype == RSSM_F32 ? DT_F32 : DT_BF16; }
 
-cudaError_t replay_launch(const rssm_config& c, const ReplayParams& p, int NT, int cluster,
+cudaError_t replay_launch(const rssm_config& c, const ReplayParams& p, int NT,
                           cudaStream_t st) {
   const bool f32 = c.state_dtype == RSSM_F32;
   if (c.algo == RSSM_ALGO_GDN) {
-    return f32 ? replay_gdn_f32_launch(p, NT, cluster, st)
-               : replay_gdn_bf16_launch(p, NT, cluster, st);
+    return f32 ? replay_gdn_f32_launch(p, NT, st) : replay_gdn_bf16_launch(p, NT, st);
   }
-  return f32 ? replay_kda_f32_launch(p, NT, cluster, st)
-             : replay_kda_bf16_launch(p, NT, cluster, st);
+  return f32 ? replay_kda_f32_launch(p, NT, st) : replay_kda_bf16_launch(p, NT, st);
 }
 
 cudaError_t replay_prepare(const rssm_config& c, int max_smem) {
@@ -167,8 +164,7 @@ rssm_status window(rssm_handle* h, int32_t layer, const void* q, const void* k, 
   p.scale = c.scale;
   p.sm = layout_for(c, T);
   if ((int)p.sm.total > h->max_smem) return RSSM_ERR_UNSUPPORTED;
-  return from_cuda(replay_launch(c, p, nt_for(T), h->G,
-                                 static_cast<cudaStream_t>(stream)));
+  return from_cuda(replay_launch(c, p, nt_for(T), static_cast<cudaStream_t>(stream)));
 }
 
 FoldParams fold_params(const rssm_handle* h, const int32_t* slot, const uint8_t* force,
@@ -230,10 +226,12 @@ rssm_status rssm_alloc(const rssm_config* cfg, const rssm_buffers* buf, rssm_han
       !aligned4(b.cursor) || !aligned4(b.err_word))
     return RSSM_ERR_INVALID_ARG;
 
-  int dev = 0, max_smem = 0;
+  int dev = 0, max_smem = 0, num_sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return RSSM_ERR_CUDA;
   if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
       cudaSuccess)
+    return RSSM_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return RSSM_ERR_CUDA;
   // The widest window this store allows must fit in shared memory.
   const ReplaySmem worst = layout_for(*cfg, cfg->max_T);
@@ -248,9 +246,10 @@ rssm_status rssm_alloc(const rssm_config* cfg, const rssm_buffers* buf, rssm_han
   h->buf = b;
   h->G = cfg->HV / cfg->HK;
   h->max_smem = max_smem;
+  h->num_sms = num_sms;
   const size_t slots = (size_t)cfg->n_slots;
   h->layer_state = slots * cfg->HV * cfg->dk * cfg->dv;
-  h->layer_k = slots * cfg->HK * cfg->L * cfg->dk;
+  h->layer_k = slots * cfg->HV * cfg->L * cfg->dk;
   h->layer_d = slots * cfg->HV * cfg->L * cfg->dv;
   h->layer_g = slots * cfg->HV * cfg->L * n_gate(*cfg);
   h->layer_v = slots * cfg->HV * cfg->L * cfg->dv;

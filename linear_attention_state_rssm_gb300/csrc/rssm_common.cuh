@@ -1,6 +1,6 @@
 // Shared definitions of the ReplaySSM kernels: launch parameters, the shared
-// memory plan, dtype helpers and the inline-PTX primitives (mbarrier, bulk
-// async copy, cluster barrier) used on sm_103a.
+// memory plans, dtype helpers and the inline-PTX primitives (mbarrier, bulk
+// async copy) used on sm_103a.
 #pragma once
 
 #include <cstddef>
@@ -84,9 +84,28 @@ struct ReplaySmem {
   uint32_t hg;     // [L][dk]  KDA history gates
   uint32_t hf;     // [L]      GDN: raw gates -> exp(suffix sums)
   uint32_t hdot;   // [L][2NT] history dot coefficients
-  uint32_t red;    // [RG][2NT][dv] partial column sums when dv < kThreads
+  uint32_t red;    // [row groups][2NT][dv] partial column sums (on the ring when it fits)
   uint32_t total;
 };
+
+// Lane layout of the tile stream: a lane owns CW consecutive value columns
+// (one vector load per row); the lanes of a row may span several warps
+// (column blocks) and a warp instruction may cover several rows.
+struct QuadLayout {
+  int lpr;   // lanes per row (dv / CW)
+  int wcb;   // warps per row (column blocks)
+  int rsw;   // rows covered by one warp instruction
+  int rgw;   // warp row groups (kWarps / wcb): partial sums to add
+  __host__ __device__ QuadLayout(int dv, int CW) {
+    lpr = dv / CW;
+    wcb = lpr > 32 ? lpr / 32 : 1;
+    rsw = lpr < 32 ? 32 / lpr : 1;
+    rgw = kWarps / wcb;
+  }
+};
+
+// Columns per lane in the tile stream for a window width.
+__host__ __device__ constexpr int quad_width(int NT) { return NT <= 8 ? 4 : 2; }
 
 struct ReplayParams {
   // store (layer offset already applied)
@@ -144,8 +163,8 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
   ReplaySmem m{};
   const int NV = 2 * NT;
   const bool kda = algo == ALGO_KDA;
-  const int RG = kThreads / dv;
   const TileRing tr(dk, dv, state_bytes);
+  const QuadLayout ql(dv, quad_width(NT));
   uint32_t off = 0;
   m.ring = off;  off = align16(off + tr.ns * tr.chunk_bytes);
   m.mbar = off;  off = align16(off + 8u * kMbars);
@@ -154,7 +173,7 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
   m.wv = off;    off = align16(off + 4u * T * dv);
   m.wraw = off;  if (in_dt != DT_F32) off = align16(off + 2u * T * (2 * dk + dv));
   m.wb = off;    off = align16(off + 4u * NT);
-  m.wg = off;    off = align16(off + 4u * T * (kda ? dk : 1));
+  m.wg = off;    off = align16(off + 4u * (kda ? T * dk : NT));
   m.yk = off;    if (kda) off = align16(off + 4u * T * dk);
   m.yq = off;    if (kda) off = align16(off + 4u * T * dk);
   m.scal = off;  off = align16(off + 4u * (kda ? 2 * dk : 2 * NT + 4));
@@ -168,7 +187,14 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
   m.hg = off;    if (kda) off = align16(off + 4u * L * dk);
   m.hf = off;    off = align16(off + 4u * L);
   m.hdot = off;  off = align16(off + 4u * L * NV);
-  m.red = off;   if (RG > 1) off = align16(off + 4u * RG * NV * dv);
+  // partial column sums go to the ring once the tile is consumed, if they fit
+  const uint32_t red_bytes = 4u * ql.rgw * NV * dv;
+  if (red_bytes <= tr.ns * tr.chunk_bytes) {
+    m.red = m.ring;
+  } else {
+    m.red = off;
+    off = align16(off + red_bytes);
+  }
   m.total = off;
   return m;
 }
@@ -286,13 +312,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
-}
 
-__device__ __forceinline__ void cluster_wait_acquire() {
-  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
-}
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll

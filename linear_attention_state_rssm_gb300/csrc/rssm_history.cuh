@@ -264,4 +264,194 @@ __device__ __forceinline__ bool stream_tile(const TilePipe<ST>& pipe, float (&y)
   return ok;
 }
 
+// CW consecutive checkpoint values <-> fp32 (shared-memory loads, global stores
+// that round to the checkpoint dtype and return the stored values).
+template <typename ST, int CW>
+__device__ __forceinline__ void ld_cols(const ST* p, float (&v)[CW]);
+template <>
+__device__ __forceinline__ void ld_cols<float, 4>(const float* p, float (&v)[4]) {
+  const float4 x = *reinterpret_cast<const float4*>(p);
+  v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+template <>
+__device__ __forceinline__ void ld_cols<float, 2>(const float* p, float (&v)[2]) {
+  const float2 x = *reinterpret_cast<const float2*>(p);
+  v[0] = x.x; v[1] = x.y;
+}
+template <>
+__device__ __forceinline__ void ld_cols<__nv_bfloat16, 4>(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+template <>
+__device__ __forceinline__ void ld_cols<__nv_bfloat16, 2>(const __nv_bfloat16* p, float (&v)[2]) {
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+  v[0] = a.x; v[1] = a.y;
+}
+
+template <typename ST, int CW>
+__device__ __forceinline__ void st_cols(ST* p, float (&v)[CW]);
+template <>
+__device__ __forceinline__ void st_cols<float, 4>(float* p, float (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <>
+__device__ __forceinline__ void st_cols<float, 2>(float* p, float (&v)[2]) {
+  *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+}
+template <>
+__device__ __forceinline__ void st_cols<__nv_bfloat16, 4>(__nv_bfloat16* p, float (&v)[4]) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&a);
+  u.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+  const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+  v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
+}
+template <>
+__device__ __forceinline__ void st_cols<__nv_bfloat16, 2>(__nv_bfloat16* p, float (&v)[2]) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+  *reinterpret_cast<__nv_bfloat162*>(p) = a;
+  const float2 fa = __bfloat1622float2(a);
+  v[0] = fa.x; v[1] = fa.y;
+}
+
+// Lane position in the tile stream (see QuadLayout).
+struct QuadLane {
+  int col0;   // first of this lane's CW columns
+  int lr0;    // first local row of a chunk handled by this lane
+  int rstep;  // distance between this lane's rows
+  int rg;     // warp row group (index of the partial sum)
+  int first;  // 1 on the lane that holds the row group's sum after the reduction
+  int lanes;  // lanes of one row within a warp
+  __device__ __forceinline__ QuadLane(const QuadLayout& ql, int CW, int warp, int lane) {
+    lanes = ql.lpr < 32 ? ql.lpr : 32;
+    const int cb = warp % ql.wcb;
+    rg = warp / ql.wcb;
+    col0 = CW * (cb * 32 + lane % lanes);
+    const int rl = lane / lanes;
+    lr0 = rg * ql.rsw + rl;
+    rstep = ql.rgw * ql.rsw;
+    first = rl == 0;
+  }
+};
+
+// Stream the checkpoint tile through the ring: each lane takes CW columns of
+// some rows of every chunk, four rows at a time. FOLD: S[row] <- decay(row)
+// S[row] + sum_m k~_m[row] d_m, a rank-n update blocked over 4 records held
+// in registers (hk [n][dk] and hd [n][dv]; GDN: k~_m = hf[m] k_m, decay =
+// gdn_decay; KDA: hk holds k~, decay = egam[row]), stored back to the
+// checkpoint rounded to its dtype; then acc[v] += x_v[row] S[row] for the NV
+// mat-vec vectors (xh [dk][NV]). Sums over the rows of one warp instruction
+// are reduced before returning.
+template <int ALGO, typename ST, int NV, int CW, bool FOLD>
+__device__ __forceinline__ bool stream_quads(const TilePipe<ST>& pipe, const QuadLane& ql,
+                                             float (&acc)[NV][CW], ST* gtile, int dk, int dv,
+                                             int n, const float* hk, const float* hd,
+                                             const float* hf, float gdn_decay,
+                                             const float* egam, const float* xh, int tid,
+                                             int lane) {
+  constexpr int RS = 4;  // rows held in registers at a time
+  constexpr int MB = 4;  // history records per fold block
+  const int rpl = pipe.tr.cr / ql.rstep;  // this lane's rows per chunk
+  bool ok = true;
+  for (int j = 0; j < pipe.tr.nchunk; ++j) {
+    ok = pipe.wait_full(j) && ok;
+    const ST* stg = pipe.ring + (size_t)(j % pipe.tr.ns) * pipe.tr.cr * dv + ql.col0;
+    const int row0 = j * pipe.tr.cr;
+    for (int u0 = 0; u0 < rpl; u0 += RS) {
+      float s[RS][CW];
+      int rows[RS];
+#pragma unroll
+      for (int u = 0; u < RS; ++u) {
+        const int uu = u0 + u < rpl ? u0 + u : rpl - 1;  // a repeated row is never used
+        const int lr = ql.lr0 + uu * ql.rstep;
+        rows[u] = row0 + lr;
+        ld_cols<ST, CW>(stg + (size_t)lr * dv, s[u]);
+      }
+      if (FOLD) {
+#pragma unroll
+        for (int u = 0; u < RS; ++u) {
+          const float dec = ALGO == ALGO_GDN ? gdn_decay : egam[rows[u]];
+#pragma unroll
+          for (int c = 0; c < CW; ++c) s[u][c] *= dec;
+        }
+        for (int m0 = 0; m0 < n; m0 += MB) {
+          float dm[MB][CW];
+#pragma unroll
+          for (int m = 0; m < MB; ++m) {
+            if (m0 + m < n) {
+              const float* src = hd + (size_t)(m0 + m) * dv + ql.col0;
+              const float f = ALGO == ALGO_GDN ? hf[m0 + m] : 1.f;
+              if constexpr (CW == 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src);
+                dm[m][0] = f * x.x; dm[m][1] = f * x.y; dm[m][2] = f * x.z; dm[m][3] = f * x.w;
+              } else {
+                const float2 x = *reinterpret_cast<const float2*>(src);
+                dm[m][0] = f * x.x; dm[m][1] = f * x.y;
+              }
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < MB; ++m) {
+            if (m0 + m < n) {
+              const float* km = hk + (size_t)(m0 + m) * dk;
+#pragma unroll
+              for (int u = 0; u < RS; ++u) {
+                const float kv = km[rows[u]];
+#pragma unroll
+                for (int c = 0; c < CW; ++c) s[u][c] = fmaf(kv, dm[m][c], s[u][c]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < RS; ++u) {
+          if (u0 + u < rpl) st_cols<ST, CW>(gtile + (size_t)rows[u] * dv + ql.col0, s[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < RS; ++u) {
+        if (u0 + u < rpl) {
+          const float* xr = xh + (size_t)rows[u] * NV;
+          if constexpr (NV % 4 == 0) {
+#pragma unroll
+            for (int q4 = 0; q4 < NV / 4; ++q4) {
+              const float4 x = reinterpret_cast<const float4*>(xr)[q4];
+#pragma unroll
+              for (int c = 0; c < CW; ++c) {
+                acc[4 * q4 + 0][c] = fmaf(x.x, s[u][c], acc[4 * q4 + 0][c]);
+                acc[4 * q4 + 1][c] = fmaf(x.y, s[u][c], acc[4 * q4 + 1][c]);
+                acc[4 * q4 + 2][c] = fmaf(x.z, s[u][c], acc[4 * q4 + 2][c]);
+                acc[4 * q4 + 3][c] = fmaf(x.w, s[u][c], acc[4 * q4 + 3][c]);
+              }
+            }
+          } else {
+            const float2 x = *reinterpret_cast<const float2*>(xr);
+#pragma unroll
+            for (int c = 0; c < CW; ++c) {
+              acc[0][c] = fmaf(x.x, s[u][c], acc[0][c]);
+              acc[1][c] = fmaf(x.y, s[u][c], acc[1][c]);
+            }
+          }
+        }
+      }
+    }
+    pipe.release(j, lane);
+    if (tid == 0) ok = pipe.refill(j) && ok;
+  }
+  for (int off = ql.lanes; off < 32; off <<= 1) {
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+#pragma unroll
+      for (int c = 0; c < CW; ++c) acc[v][c] += __shfl_xor_sync(kFull, acc[v][c], off);
+    }
+  }
+  return ok;
+}
+
 }  // namespace rssm

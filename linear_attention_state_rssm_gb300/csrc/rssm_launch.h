@@ -12,7 +12,7 @@ namespace rssm {
 inline int nt_for(int T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16; }
 
 #define RSSM_DECLARE_REPLAY(NAME)                                                      \
-  cudaError_t NAME##_launch(const ReplayParams& p, int NT, int cluster, cudaStream_t st); \
+  cudaError_t NAME##_launch(const ReplayParams& p, int NT, cudaStream_t st); \
   cudaError_t NAME##_prepare(int max_smem);
 
 RSSM_DECLARE_REPLAY(replay_gdn_f32)

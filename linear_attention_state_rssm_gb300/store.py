@@ -16,7 +16,7 @@ class ReplayStore:
 
     Buffers (row-major):
       state     [n_layers, n_slots, HV, dk, dv]    state_dtype
-      ring_k    [n_layers, n_slots, HK, L, dk]     ring_k_dtype
+      ring_k    [n_layers, n_slots, HV, L, dk]     ring_k_dtype (one copy per value head)
       ring_d    [n_layers, n_slots, HV, L, dv]     ring_d_dtype
       ring_g    [n_layers, n_slots, HV, L] (+ [dk] for KDA)  fp32
       ring_v    [n_layers, n_slots, HV, L, dv]     in_dtype
@@ -42,7 +42,7 @@ class ReplayStore:
         ng = () if algo == "gdn" else (dk,)
         dev = self.device
         self.state = torch.zeros(ls + (HV, dk, dv), dtype=_TORCH[state_dtype], device=dev)
-        self.ring_k = torch.zeros(ls + (HK, L, dk), dtype=_TORCH[self.ring_k_dtype], device=dev)
+        self.ring_k = torch.zeros(ls + (HV, L, dk), dtype=_TORCH[self.ring_k_dtype], device=dev)
         self.ring_d = torch.zeros(ls + (HV, L, dv), dtype=_TORCH[ring_d_dtype], device=dev)
         self.ring_g = torch.zeros(ls + (HV, L) + ng, dtype=torch.float32, device=dev)
         self.ring_v = torch.zeros(ls + (HV, L, dv), dtype=_TORCH[in_dtype], device=dev)

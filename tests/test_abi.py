@@ -44,7 +44,7 @@ def test_required_bytes_matches_layouts(lib):
                            max_T=8, in_dtype="bf16", state_dtype="f32")
     s = _lib.rssm_required_bytes(cfg)
     assert s.state == 3 * 5 * 32 * 128 * 128 * 4
-    assert s.ring_k == 3 * 5 * 16 * 16 * 128 * 2          # fp16 keys for bf16 inputs
+    assert s.ring_k == 3 * 5 * 32 * 16 * 128 * 2          # fp16 keys, one copy per value head
     assert s.ring_d == 3 * 5 * 32 * 16 * 128 * 4
     assert s.ring_g == 3 * 5 * 32 * 16 * 4
     assert s.ring_v == 3 * 5 * 32 * 16 * 128 * 2
@@ -62,7 +62,7 @@ def test_required_bytes_matches_layouts(lib):
     (dict(max_T=8, L=4), 1),             # ring shorter than the window
     (dict(dk=96), 2),                    # head size not built
     (dict(HK=3, HV=8), 1),               # HV not a multiple of HK
-    (dict(HK=1, HV=16), 2),              # GQA group above 8
+    (dict(ring_d_dtype="bf16"), 2),      # bf16 deltas not built
     (dict(n_slots=0), 1),
     (dict(L=300, max_T=1), 2),
 ])
