@@ -78,8 +78,10 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
   __syncthreads();
   if (tid == 0) {
     pipe.prime();
-    issue_history<ALGO>(n, dk, dv, p.ring_k, kbase, p.rk_dt, p.ring_d, dbase, p.rd_dt, p.ring_g,
-                        gbase, hk, hkraw, hd, hdraw, hg, &mbar[kMbarHist]);
+    issue_history<ALGO>(n, dk, dv, p.ring_k, kbase, p.rk_dt,
+                        p.rk_dt == DT_F32 ? static_cast<void*>(hk) : hkraw, p.ring_d, dbase,
+                        p.rd_dt, p.rd_dt == DT_F32 ? static_cast<void*>(hd) : hdraw, p.ring_g,
+                        gbase, hg, &mbar[kMbarHist]);
   }
   if (ALGO == ALGO_GDN) {
     for (int m = tid; m < n; m += kThreads) hf[m] = p.ring_g[gbase + m];

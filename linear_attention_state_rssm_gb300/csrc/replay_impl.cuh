@@ -6,7 +6,8 @@
 // stages (8 KB row chunks, one bulk async copy each, full/empty mbarriers); a
 // lane owns CW consecutive value columns of some rows of every chunk, so one
 // vector load feeds CW x 2T fused multiply-adds. The stream is the only
-// O(dk dv) work, and the kernel keeps the instructions spent around it small.
+// O(dk dv) work; everything else is arranged so that a CTA spends as little
+// time as possible outside it.
 //
 // Ring keys are stored per value head, so every CTA reads and writes only its
 // own records: a folding window (which writes positions [0, T) of the history
@@ -16,21 +17,24 @@
 // for that reason; its author notes the barrier has no progress guarantee.)
 //
 // Per CTA, with c = cursor[slot], fold = force || c + T > L:
-//  1. bulk async copies: the first tile chunks and the window rows (they need
-//     only the slot) and, once the cursor is known, the c history records;
-//  2. gates: history decay factors and in-window inclusive prefixes G_i;
-//  3. window coefficients for j <= i < T (per key channel for KDA)
+//  0. bulk async copies: the window rows first (they need only the request
+//     row), then the first tile chunks (once the slot is known) and the c
+//     history records (once the cursor is known);
+//  1. gates: history decay factors and in-window inclusive prefixes G_i;
+//  2. window coefficients for j <= i < T (per key channel for KDA)
 //        A_ij = beta_i sum_ch e^{G_i-G_j} k_j k_i   (j < i)
 //        F_ij =        sum_ch e^{G_i-G_j} k_j q_i   (j <= i)
 //     and, without a fold, history dot coefficients H[m][x] = k~_m . (e^{G_i} x)
 //     for every window vector x in {k_i, q_i};
-//  4. stream the tile: on a fold S0 <- e^{Gam} S0 + sum_m k~_m d_m^T (stored
-//     back), and y_x = S0^T (e^{Gam_e + G_i} x) for all 2T vectors in one pass
-//     (a GDN window without a fold streams first, while its history lands);
-//  5. per value column: a_i, b_i = y + sum_m H d_m; the triangular solve
+//  3. stream the tile: on a fold S0 <- e^{Gam} S0 + sum_m k~_m d_m^T (stored
+//     back), and y_x = S0^T (e^{Gam_e + G_i} x) for all 2T vectors in one pass;
+//  4. per value column: a_i, b_i = y + sum_m H d_m; the triangular solve
 //     d_i = beta_i (v_i - a_i) - sum_{j<i} A_ij d_j (forward substitution of
 //     (I + A) D = R) and o_i = scale (b_i + sum_{j<=i} F_ij d_j); the records of
 //     the window go to ring positions base + i (base = fold ? 0 : c).
+// A narrow GDN window without a fold runs steps 1-2 (and the history part of
+// step 4) on two warps while the other two stream the tile: its mat-vec inputs
+// are the raw window vectors, whose scalar decay goes on the column results.
 // Every window sum runs over j <= i only, so a NaN or Inf at a later (rejected)
 // position is never read by an earlier output: the causal selection is
 // structural, never a multiplication by zero (SGLang fork PR jianc99/sglang#2,
@@ -42,10 +46,111 @@
 
 namespace rssm {
 
-// Dot products of key-channel vectors: lanes take float4 groups of channels,
-// then a warp reduction.
 __device__ __forceinline__ float4 ld4(const float* p) {
   return *reinterpret_cast<const float4*>(p);
+}
+
+// GDN, one warp: history decay factors (hf, hscal = {Gam, e^Gam}) and the
+// in-window inclusive gate prefixes gp[i] = G_i of the raw gates wg (T <= 16
+// lanes; wg itself is left as it is, the ring records copy it) with eG[i] =
+// e^{G_i} and es[i] = e^{Gam_e + G_i} (Gam_e = Gam unless the window folds).
+__device__ __forceinline__ void gdn_gates(int nh, int T, bool fold, float* hf, float* hscal,
+                                          const float* wg, float* gp, float* eG, float* es,
+                                          int lane) {
+  if (nh > 0) {
+    gdn_history_scan(nh, hf, hscal, lane);
+  } else if (lane == 0) {
+    hscal[0] = 0.f;
+    hscal[1] = 1.f;
+  }
+  __syncwarp();
+  const float gv = lane < T ? wg[lane] : 0.f;
+  float incl = gv;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float t = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += t;
+  }
+  const float gam_e = fold ? 0.f : hscal[0];
+  if (lane < T) {
+    gp[lane] = incl;
+    eG[lane] = __expf(incl);
+    es[lane] = __expf(gam_e + incl);
+  }
+}
+
+// Window coefficients A_ij (j < i) and F_ij (j <= i) of the pairs that fall to
+// warp w of nw; lanes take float4 groups of key channels, then a warp sum.
+// wg holds the inclusive gate prefixes (GDN [T], KDA [T][dk]).
+template <int ALGO, int NT>
+__device__ __forceinline__ void window_pairs(int T, int dk, const float* wk, const float* wq,
+                                             const float* wg, const float* wb, float* am,
+                                             float* fm, int w, int nw, int lane) {
+  int pi = 0;
+  for (int i = 0; i < T; ++i) {
+    for (int j = 0; j <= i; ++j, ++pi) {
+      if (pi % nw != w) continue;
+      float skk = 0.f, skq = 0.f;
+      for (int c4 = 4 * lane; c4 < dk; c4 += 128) {
+        float4 kj = ld4(wk + j * dk + c4);
+        if (ALGO == ALGO_KDA) {
+          const float4 gi = ld4(wg + i * dk + c4), gj = ld4(wg + j * dk + c4);
+          kj.x *= __expf(gi.x - gj.x);
+          kj.y *= __expf(gi.y - gj.y);
+          kj.z *= __expf(gi.z - gj.z);
+          kj.w *= __expf(gi.w - gj.w);
+        }
+        const float4 ki = ld4(wk + i * dk + c4), qi = ld4(wq + i * dk + c4);
+        skk = fmaf(kj.x, ki.x, fmaf(kj.y, ki.y, fmaf(kj.z, ki.z, fmaf(kj.w, ki.w, skk))));
+        skq = fmaf(kj.x, qi.x, fmaf(kj.y, qi.y, fmaf(kj.z, qi.z, fmaf(kj.w, qi.w, skq))));
+      }
+      skk = warp_sum(skk);
+      skq = warp_sum(skq);
+      if (lane == 0) {
+        const float wgt = (ALGO == ALGO_GDN) ? __expf(wg[i] - wg[j]) : 1.f;
+        fm[i * NT + j] = wgt * skq;
+        am[i * NT + j] = (j < i) ? wb[i] * wgt * skk : 0.f;
+      }
+    }
+  }
+}
+
+// History dot coefficients hdot[m][v] of the records m = w, w + nw, ...:
+// GDN: raw keys against raw window vectors, times hf[m] e^{G_i};
+// KDA: decayed keys against e^{G_i} x (xk, xq = yk, yq).
+template <int ALGO, int NT>
+__device__ __forceinline__ void history_dots(int nh, int T, int dk, const float* hk,
+                                             const float* xk, const float* xq, const float* hf,
+                                             const float* eG, float* hdot, int w, int nw,
+                                             int lane) {
+  constexpr int NV = 2 * NT;
+  for (int m = w; m < nh; m += nw) {
+    float part[NV];
+#pragma unroll
+    for (int vv = 0; vv < NV; ++vv) part[vv] = 0.f;
+    for (int c4 = 4 * lane; c4 < dk; c4 += 128) {
+      const float4 km = ld4(hk + m * dk + c4);
+#pragma unroll
+      for (int vv = 0; vv < NV; ++vv) {
+        const int i = vv < NT ? vv : vv - NT;
+        if (i < T) {
+          const float4 x = ld4((vv < NT ? xk : xq) + i * dk + c4);
+          part[vv] = fmaf(km.x, x.x, fmaf(km.y, x.y, fmaf(km.z, x.z, fmaf(km.w, x.w, part[vv]))));
+        }
+      }
+    }
+#pragma unroll
+    for (int vv = 0; vv < NV; ++vv) part[vv] = warp_sum(part[vv]);
+    if (lane == 0) {
+#pragma unroll
+      for (int vv = 0; vv < NV; ++vv) {
+        const int i = vv < NT ? vv : vv - NT;
+        float hv = 0.f;
+        if (i < T) hv = (ALGO == ALGO_GDN) ? part[vv] * hf[m] * eG[i] : part[vv];
+        hdot[m * NV + vv] = hv;
+      }
+    }
+  }
 }
 
 // Narrow windows keep four CTAs per SM (at most 128 registers per thread);
@@ -54,6 +159,7 @@ template <int ALGO, typename ST, int NT>
 __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const ReplayParams p) {
   constexpr int NV = 2 * NT;             // mat-vec vectors: k_i at [0, NT), q_i at [NT, 2NT)
   constexpr int CW = quad_width(NT);     // value columns per lane in the tile stream
+  constexpr int MR = fold_reg_records(NT);
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int h = blockIdx.x;
@@ -62,15 +168,6 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   const int T = p.T, dk = p.dk, dv = p.dv, L = p.L, HV = p.HV, HK = p.HK;
   const int kh = h / p.G;
 
-  // ---- row resolve
-  const int s = p.slot[r];
-  if (s < 0) return;
-  if (s >= p.n_slots) {
-    if (h == 0 && tid == 0) atomicOr(p.err, DEVERR_SLOT);
-    return;
-  }
-
-  ST* gtile = static_cast<ST*>(p.state) + ((size_t)s * HV + h) * dk * dv;
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + p.sm.mbar);
   float* wq = reinterpret_cast<float*>(smem + p.sm.wq);
   float* wk = reinterpret_cast<float*>(smem + p.sm.wk);
@@ -92,31 +189,30 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   unsigned char* wraw = smem + p.sm.wraw;
   unsigned char* hkraw = smem + p.sm.hkraw;
   unsigned char* hdraw = smem + p.sm.hdraw;
+  float* hc = reinterpret_cast<float*>(smem + p.sm.hkraw);  // split windows, after widening
   // GDN scalars: es[i] = e^{Gam_e + G_i}, eG[i] = e^{G_i}, hscal = {Gam, e^Gam}.
   // KDA vectors: egam[ch] = e^{Gam[ch]}, gam[ch] = Gam[ch].
   float* es = scal;
   float* eG = scal + NT;
   float* hscal = scal + 2 * NT;
+  float* gp = scal + 2 * NT + 4;  // GDN in-window gate prefixes
   float* egam = scal;
   float* gam = scal + dk;
 
   const size_t tok0 = (size_t)r * T;
   const int s_in = dtype_bytes(p.in_dt);
+  const bool f32in = p.in_dt == DT_F32;
   const uint32_t qrow = (uint32_t)(dk * s_in), vrow = (uint32_t)(dv * s_in);
 
-  // ---- 1. bulk async copies. One thread issues every copy of a barrier after
-  //         registering its byte count.
-  const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv);
+  // ---- 0. bulk async copies; one thread issues every copy of a barrier after
+  //         registering its byte count. The window rows need only the request
+  //         row: they are under way while the slot index loads.
+  const int s = p.slot[r];
   if (tid == 0) {
     mbar_init(&mbar[kMbarWin], 1);
     mbar_init(&mbar[kMbarHist], 1);
-    pipe.init();
+    TilePipe<ST>::init_full(mbar);
     fence_mbar_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    pipe.prime();
-    const bool f32in = p.in_dt == DT_F32;
     mbar_expect_tx(&mbar[kMbarWin],
                    T * (2 * qrow + vrow) + (ALGO == ALGO_KDA ? (uint32_t)(T * dk * 4) : 0u));
     for (int i = 0; i < T; ++i) {
@@ -134,37 +230,78 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
       }
     }
   }
-  const int c = p.cursor[s];
+  float wbeta = 0.f, wgate = 0.f;
   if (tid < T) {
-    wb[tid] = p.beta[(tok0 + tid) * HV + h];
-    if (ALGO == ALGO_GDN) wg[tid] = p.g[(tok0 + tid) * HV + h];
+    wbeta = p.beta[(tok0 + tid) * HV + h];
+    if (ALGO == ALGO_GDN) wgate = p.g[(tok0 + tid) * HV + h];
   }
+  if (s < 0 || s >= p.n_slots) {
+    // null row (or a slot out of range): let the window copies land, leave
+    if (tid == 0) {
+      if (s >= p.n_slots && h == 0) atomicOr(p.err, DEVERR_SLOT);
+      mbar_wait_bounded(&mbar[kMbarWin], 0);
+    }
+    return;
+  }
+  ST* gtile = static_cast<ST*>(p.state) + ((size_t)s * HV + h) * dk * dv;
+  const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv);
+  if (tid == 0) pipe.prime();
+  const int c = p.cursor[s];
   if (c < 0 || c > L) {
-    if (h == 0 && tid == 0) atomicOr(p.err, DEVERR_CURSOR);
-    // copies are in flight into this CTA's shared memory: let them land
-    mbar_wait_bounded(&mbar[kMbarWin], 0);
-    pipe.drain();
+    if (tid == 0) {
+      if (h == 0) atomicOr(p.err, DEVERR_CURSOR);
+      mbar_wait_bounded(&mbar[kMbarWin], 0);
+      pipe.drain();
+    }
     return;
   }
   // fold decision (uniform over the CTA)
   const bool fold = (p.force != nullptr && p.force[r] != 0) || (c + T > L);
   const int base = fold ? 0 : c;
   const int nh = c;
+  const bool split = can_split(ALGO, NT) && !fold;
+  const int sw = split ? kSplitWarps : kWarps;  // warps that stream the tile
   const size_t kbase = ((size_t)s * HV + h) * L * dk;
   const size_t dbase = ((size_t)s * HV + h) * L * dv;
   const size_t gbase = ((size_t)s * HV + h) * L * (ALGO == ALGO_GDN ? 1 : dk);
-  if (nh > 0 && tid == 0) {
-    issue_history<ALGO>(nh, dk, dv, p.ring_k, kbase, p.rk_dt, p.ring_d, dbase, p.rd_dt, p.ring_g,
-                        gbase, hk, hkraw, hd, hdraw, hg, &mbar[kMbarHist]);
+  if (tid == 0) {
+    pipe.init_empty(sw);
+    if (nh > 0) {
+      void* kdst = (ALGO == ALGO_KDA && p.rk_dt == DT_F32) ? static_cast<void*>(hk) : hkraw;
+      issue_history<ALGO>(nh, dk, dv, p.ring_k, kbase, p.rk_dt, kdst, p.ring_d, dbase, p.rd_dt,
+                          p.rd_dt == DT_F32 ? static_cast<void*>(hd) : hdraw, p.ring_g, gbase,
+                          hg, &mbar[kMbarHist]);
+    }
   }
-  if (ALGO == ALGO_GDN) {
-    for (int m = tid; m < nh; m += kThreads) hf[m] = p.ring_g[gbase + m];
-  }
+  // GDN history gates: loaded now, stored once the window has landed
+  float hgate = 0.f;
+  if (ALGO == ALGO_GDN && tid < nh) hgate = p.ring_g[gbase + tid];
+  __syncthreads();  // every mbarrier is initialised
+
+  // ---- window rows -> fp32; GDN mat-vec inputs xh[ch][v] are the raw window
+  //      vectors (their scalar decay goes on the column results)
   bool copies_ok = mbar_wait_bounded(&mbar[kMbarWin], 0);
-  if (p.in_dt != DT_F32) {
+  if (!f32in) {
     widen16(wq, wraw, T * dk, p.in_dt, tid, kThreads);
     widen16(wk, wraw + T * qrow, T * dk, p.in_dt, tid, kThreads);
     widen16(wv, wraw + 2 * T * qrow, T * dv, p.in_dt, tid, kThreads);
+  }
+  if (ALGO == ALGO_GDN) {
+    const void* qsrc = f32in ? static_cast<const void*>(wq) : wraw;
+    const void* ksrc = f32in ? static_cast<const void*>(wk) : wraw + T * qrow;
+    for (int e = tid; e < dk * NV; e += kThreads) {
+      const int ch = e / NV, vv = e - ch * NV;
+      const int i = vv < NT ? vv : vv - NT;
+      xh[e] = i < T ? ld_f32(vv < NT ? ksrc : qsrc, (size_t)i * dk + ch, p.in_dt) : 0.f;
+    }
+  }
+  if (tid < T) {
+    wb[tid] = wbeta;
+    if (ALGO == ALGO_GDN) wg[tid] = wgate;
+  }
+  if (ALGO == ALGO_GDN) {
+    if (tid < nh) hf[tid] = hgate;
+    for (int m = tid + kThreads; m < nh; m += kThreads) hf[m] = p.ring_g[gbase + m];
   }
   // A folding window writes over positions [0, T) of the history it reads:
   // its history copy must have landed before the records below.
@@ -172,8 +309,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   __syncthreads();
 
   // ---- records that need no result of the window: keys, gates and betas at
-  //      ring positions base + i. Each thread writes the key channels it owns
-  //      in step 2 below.
+  //      ring positions base + i
   for (int ch = tid; ch < dk; ch += kThreads) {
     for (int i = 0; i < T; ++i) {
       st_f32(p.ring_k, kbase + (size_t)(base + i) * dk + ch, p.rk_dt, wk[i * dk + ch]);
@@ -185,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
     if (ALGO == ALGO_GDN) p.ring_g[gbase + base + tid] = wg[tid];
   }
 
-  const QuadLayout qlay(dv, CW);
+  const QuadLayout qlay(dv, CW, sw);
   const QuadLane qlane(qlay, CW, warp, lane);
   float acc[NV][CW];
 #pragma unroll
@@ -193,163 +329,134 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
 #pragma unroll
     for (int cc = 0; cc < CW; ++cc) acc[vv][cc] = 0.f;
   }
-  // GDN mat-vec inputs are the raw window vectors (their scalar decay goes on
-  // the column results); without a fold the tile streams now.
-  const bool early = ALGO == ALGO_GDN && !fold;
-  if (ALGO == ALGO_GDN) {
-    for (int e = tid; e < dk * NV; e += kThreads) {
-      const int ch = e / NV, vv = e - ch * NV;
-      const int i = vv < NT ? vv : vv - NT;
-      xh[e] = i < T ? (vv < NT ? wk[i * dk + ch] : wq[i * dk + ch]) : 0.f;
-    }
-    if (early) {
-      __syncthreads();
-      copies_ok = stream_quads<ALGO, ST, NV, CW, false>(pipe, qlane, acc, gtile, dk, dv, 0, hk,
-                                                        hd, hf, 1.f, egam, xh, tid, lane) &&
-                  copies_ok;
-    }
-  }
-  if (nh > 0 && !fold) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
-  if (nh > 0) widen_history(nh, dk, dv, p.rk_dt, p.rd_dt, hk, hkraw, hd, hdraw, tid);
-  if (!copies_ok) atomicOr(p.err, DEVERR_TIMEOUT);
-  __syncthreads();
 
-  // ---- 2. gates
-  if (ALGO == ALGO_GDN) {
-    if (warp == 0) {
+  if (split) {
+    if (warp < sw) {
+      // ---- 3. stream warps: y_x = S0^T x for the raw window vectors
+      copies_ok = stream_quads<ALGO, ST, NV, CW, MR, false>(pipe, qlane, acc, gtile, dk, dv, 0,
+                                                            hk, hd, hf, 1.f, egam, xh, tid,
+                                                            lane) &&
+                  copies_ok;
+    } else {
+      // ---- 1, 2 and the history part of 4 on the other warps
+      const int ht = tid - sw * 32, hw = warp - sw;
+      const int nht = kThreads - sw * 32, nhw = kWarps - sw;
       if (nh > 0) {
-        gdn_history_scan(nh, hf, hscal, lane);
-      } else if (lane == 0) {
-        hscal[0] = 0.f;
-        hscal[1] = 1.f;
+        copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
+        widen_keys(hk, hkraw, nh * dk, p.rk_dt, ht, nht);
+        if (p.rd_dt != DT_F32) widen16(hd, hdraw, nh * dv, p.rd_dt, ht, nht);
       }
-      __syncwarp();
-      // in-window inclusive prefix of the gates (T <= 16 lanes)
-      const float gv = lane < T ? wg[lane] : 0.f;
-      float incl = gv;
+      named_sync(1, nht);
+      if (hw == 0) gdn_gates(nh, T, false, hf, hscal, wg, gp, eG, es, lane);
+      named_sync(1, nht);
+      window_pairs<ALGO, NT>(T, dk, wk, wq, gp, wb, am, fm, hw, nhw, lane);
+      history_dots<ALGO, NT>(nh, T, dk, hk, wk, wq, hf, eG, hdot, hw, nhw, lane);
+      named_sync(1, nht);
+      // history correction of every column: hc[v][col] = sum_m H[m][v] d_m[col]
+      // (hc reuses the landing zone of the keys, widened above)
+      for (int col = ht; col < dv; col += nht) {
+        float y[NV];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float t = __shfl_up_sync(kFull, incl, off);
-        if (lane >= off) incl += t;
-      }
-      const float gam_e = fold ? 0.f : hscal[0];
-      if (lane < T) {
-        wg[lane] = incl;
-        eG[lane] = __expf(incl);
-        es[lane] = __expf(gam_e + incl);
+        for (int vv = 0; vv < NV; ++vv) y[vv] = 0.f;
+        for (int m = 0; m < nh; ++m) {
+          const float dm = hd[m * dv + col];
+#pragma unroll
+          for (int vv = 0; vv < NV; ++vv) y[vv] = fmaf(hdot[m * NV + vv], dm, y[vv]);
+        }
+#pragma unroll
+        for (int vv = 0; vv < NV; ++vv) hc[vv * dv + col] = y[vv];
       }
     }
   } else {
-    // one thread per key channel: history decay, window prefix, scaled vectors
-    for (int ch = tid; ch < dk; ch += kThreads) {
-      const float gm = nh > 0 ? kda_history_channel(nh, dk, ch, hk, hg) : 0.f;
-      gam[ch] = gm;
-      egam[ch] = __expf(gm);
-      const float gam_e = fold ? 0.f : gm;
-      float G = 0.f;
-#pragma unroll
-      for (int i = 0; i < NT; ++i) {
-        float xk = 0.f, xq = 0.f;
-        if (i < T) {
-          G += wg[i * dk + ch];
-          wg[i * dk + ch] = G;
-          const float eg = __expf(G);
-          yk[i * dk + ch] = eg * wk[i * dk + ch];
-          yq[i * dk + ch] = eg * wq[i * dk + ch];
-          const float ex = __expf(gam_e + G);
-          xk = ex * wk[i * dk + ch];
-          xq = ex * wq[i * dk + ch];
-        }
-        xh[ch * NV + i] = xk;
-        xh[ch * NV + NT + i] = xq;
-      }
+    // A wide GDN window without a fold streams first, while its history lands.
+    const bool early = ALGO == ALGO_GDN && !fold;
+    if (early) {
+      copies_ok = stream_quads<ALGO, ST, NV, CW, MR, false>(pipe, qlane, acc, gtile, dk, dv, 0,
+                                                            hk, hd, hf, 1.f, egam, xh, tid,
+                                                            lane) &&
+                  copies_ok;
     }
-  }
-  __syncthreads();
-
-  // ---- 3. window coefficients A, F (j <= i only) and history dot coefficients
-  {
-    int pi = 0;
-    for (int i = 0; i < T; ++i) {
-      for (int j = 0; j <= i; ++j, ++pi) {
-        if ((pi & (kWarps - 1)) != warp) continue;
-        float skk = 0.f, skq = 0.f;
-        for (int c4 = 4 * lane; c4 < dk; c4 += 128) {
-          float4 kj = ld4(wk + j * dk + c4);
-          if (ALGO == ALGO_KDA) {
-            const float4 gi = ld4(wg + i * dk + c4), gj = ld4(wg + j * dk + c4);
-            kj.x *= __expf(gi.x - gj.x);
-            kj.y *= __expf(gi.y - gj.y);
-            kj.z *= __expf(gi.z - gj.z);
-            kj.w *= __expf(gi.w - gj.w);
-          }
-          const float4 ki = ld4(wk + i * dk + c4), qi = ld4(wq + i * dk + c4);
-          skk = fmaf(kj.x, ki.x, fmaf(kj.y, ki.y, fmaf(kj.z, ki.z, fmaf(kj.w, ki.w, skk))));
-          skq = fmaf(kj.x, qi.x, fmaf(kj.y, qi.y, fmaf(kj.z, qi.z, fmaf(kj.w, qi.w, skq))));
-        }
-        skk = warp_sum(skk);
-        skq = warp_sum(skq);
-        if (lane == 0) {
-          const float w = (ALGO == ALGO_GDN) ? __expf(wg[i] - wg[j]) : 1.f;
-          fm[i * NT + j] = w * skq;
-          am[i * NT + j] = (j < i) ? wb[i] * w * skk : 0.f;
+    if (nh > 0 && !fold) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
+    if (nh > 0) {
+      if (p.rd_dt != DT_F32) widen16(hd, hdraw, nh * dv, p.rd_dt, tid, kThreads);
+      if (ALGO == ALGO_GDN) {
+        if (fold) {
+          transpose_keys(hk, hkraw, nh, dk, p.rk_dt, tid, kThreads);
+        } else {
+          widen_keys(hk, hkraw, nh * dk, p.rk_dt, tid, kThreads);
         }
       }
     }
-  }
-  if (!fold) {
-    // GDN: raw keys, coefficient hf[m] * e^{G_i}; KDA: decayed keys and e^{G_i} x
-    const float* xk = ALGO == ALGO_GDN ? wk : yk;
-    const float* xq = ALGO == ALGO_GDN ? wq : yq;
-    for (int m = warp; m < nh; m += kWarps) {
-      float part[NV];
-#pragma unroll
-      for (int vv = 0; vv < NV; ++vv) part[vv] = 0.f;
-      for (int c4 = 4 * lane; c4 < dk; c4 += 128) {
-        const float4 km = ld4(hk + m * dk + c4);
-#pragma unroll
-        for (int vv = 0; vv < NV; ++vv) {
-          const int i = vv < NT ? vv : vv - NT;
-          if (i < T) {
-            const float4 x = ld4((vv < NT ? xk : xq) + i * dk + c4);
-            part[vv] = fmaf(km.x, x.x, fmaf(km.y, x.y, fmaf(km.z, x.z, fmaf(km.w, x.w, part[vv]))));
-          }
-        }
-      }
-#pragma unroll
-      for (int vv = 0; vv < NV; ++vv) part[vv] = warp_sum(part[vv]);
-      if (lane == 0) {
-#pragma unroll
-        for (int vv = 0; vv < NV; ++vv) {
-          const int i = vv < NT ? vv : vv - NT;
-          float hv = 0.f;
-          if (i < T) hv = (ALGO == ALGO_GDN) ? part[vv] * hf[m] * eG[i] : part[vv];
-          hdot[m * NV + vv] = hv;
-        }
-      }
-    }
-  }
-
-  // ---- 4. stream the checkpoint tile (unless done early): fold, then S^T x
-  if (!early) {
     __syncthreads();
-    bool ok;
-    if (fold && nh > 0) {
-      ok = stream_quads<ALGO, ST, NV, CW, true>(pipe, qlane, acc, gtile, dk, dv, nh, hk, hd, hf,
-                                                hscal[1], egam, xh, tid, lane);
+
+    // ---- 1. gates
+    if (ALGO == ALGO_GDN) {
+      if (warp == 0) gdn_gates(nh, T, fold, hf, hscal, wg, gp, eG, es, lane);
     } else {
-      ok = stream_quads<ALGO, ST, NV, CW, false>(pipe, qlane, acc, gtile, dk, dv, 0, hk, hd, hf,
-                                                 1.f, egam, xh, tid, lane);
+      // one thread per key channel: decayed history keys k~ (in hk, [nh][dk]),
+      // history decay, window prefix, scaled window vectors
+      const bool f32k = p.rk_dt == DT_F32;
+      for (int ch = tid; ch < dk; ch += kThreads) {
+        float suf = 0.f;
+        for (int m = nh - 1; m >= 0; --m) {
+          const float kraw = f32k ? hk[m * dk + ch] : ld_f32(hkraw, (size_t)m * dk + ch, p.rk_dt);
+          hk[m * dk + ch] = kraw * __expf(suf);
+          suf += hg[m * dk + ch];
+        }
+        gam[ch] = suf;
+        egam[ch] = __expf(suf);
+        const float gam_e = fold ? 0.f : suf;
+        float G = 0.f;
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          float xk = 0.f, xq = 0.f;
+          if (i < T) {
+            G += wg[i * dk + ch];
+            wg[i * dk + ch] = G;
+            const float eg = __expf(G);
+            yk[i * dk + ch] = eg * wk[i * dk + ch];
+            yq[i * dk + ch] = eg * wq[i * dk + ch];
+            const float ex = __expf(gam_e + G);
+            xk = ex * wk[i * dk + ch];
+            xq = ex * wq[i * dk + ch];
+          }
+          xh[ch * NV + i] = xk;
+          xh[ch * NV + NT + i] = xq;
+        }
+      }
     }
-    if (!ok) {
-      atomicOr(p.err, DEVERR_TIMEOUT);
-      copies_ok = false;
+    __syncthreads();
+
+    // ---- 2. window coefficients A, F (j <= i only) and history dot coefficients;
+    //         a folding KDA window transposes its decayed keys over its gates
+    if (ALGO == ALGO_KDA && fold && nh > 0) transpose_keys(hg, hk, nh, dk, DT_F32, tid, kThreads);
+    window_pairs<ALGO, NT>(T, dk, wk, wq, ALGO == ALGO_GDN ? gp : wg, wb, am, fm, warp, kWarps,
+                           lane);
+    if (!fold) {
+      history_dots<ALGO, NT>(nh, T, dk, hk, ALGO == ALGO_GDN ? wk : yk,
+                             ALGO == ALGO_GDN ? wq : yq, hf, eG, hdot, warp, kWarps, lane);
+    }
+
+    // ---- 3. stream the checkpoint tile (unless done early): fold, then S^T x
+    if (!early) {
+      __syncthreads();
+      if (fold && nh > 0) {
+        copies_ok = stream_quads<ALGO, ST, NV, CW, MR, true>(pipe, qlane, acc, gtile, dk, dv, nh,
+                                                             ALGO == ALGO_KDA ? hg : hk, hd, hf,
+                                                             hscal[1], egam, xh, tid, lane) &&
+                    copies_ok;
+      } else {
+        copies_ok = stream_quads<ALGO, ST, NV, CW, MR, false>(pipe, qlane, acc, gtile, dk, dv, 0,
+                                                              hk, hd, hf, 1.f, egam, xh, tid,
+                                                              lane) &&
+                    copies_ok;
+      }
     }
   }
   // partial column sums of the warp row groups -> shared memory (the ring is
   // free once every warp has consumed the last chunk)
   __syncthreads();
-  if (qlane.first) {
+  if (warp < sw && qlane.first) {
 #pragma unroll
     for (int vv = 0; vv < NV; ++vv) {
 #pragma unroll
@@ -358,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   }
   __syncthreads();
 
-  // ---- 5. per value column: corrections, triangular solve, outputs, deltas
+  // ---- 4. per value column: corrections, triangular solve, outputs, deltas
   if (tid < dv) {
     const int col = tid;
     float y[NV];
@@ -377,7 +484,10 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
         }
       }
     }
-    if (!fold) {
+    if (split) {
+#pragma unroll
+      for (int vv = 0; vv < NV; ++vv) y[vv] += hc[vv * dv + col];
+    } else if (!fold) {
       for (int m = 0; m < nh; ++m) {
         const float dm = hd[m * dv + col];
         const float* hm = hdot + m * NV;
@@ -408,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   }
   if (h == 0 && tid == 0 && p.fold_out != nullptr) p.fold_out[r] = fold ? 1 : 0;
   if (!copies_ok) {
+    atomicOr(p.err, DEVERR_TIMEOUT);
     // give copies that did not arrive a second bounded chance before exit
     mbar_wait_bounded(&mbar[kMbarWin], 0);
     if (nh > 0) mbar_wait_bounded(&mbar[kMbarHist], 0);

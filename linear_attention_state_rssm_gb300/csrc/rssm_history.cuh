@@ -16,34 +16,75 @@
 
 namespace rssm {
 
-// Issue the bulk copies of n history records of one (slot, key head, value
-// head), completing on `bar` (one thread, after the mbarrier is initialised):
-// keys [n][dk] -> hk (fp32 ring) or hkraw (16-bit ring), deltas [n][dv] -> hd
-// or hdraw, KDA gates [n][dk] -> hg. The ring is head-major, so each run is
-// contiguous; every run is a multiple of 16 bytes (dk, dv >= 32).
+// Issue the bulk copies of n history records of one (slot, value head),
+// completing on `bar` (one thread, after the mbarrier is initialised): keys
+// [n][dk] -> kdst and deltas [n][dv] -> ddst, both as stored in the ring; KDA
+// gates [n][dk] -> hg. The ring is head-major, so each run is contiguous;
+// every run is a multiple of 16 bytes (dk, dv >= 32).
 template <int ALGO>
-__device__ __forceinline__ void issue_history(int n, int dk, int dv, const void* ring_k,
-                                              size_t kbase, int rk_dt, const void* ring_d,
-                                              size_t dbase, int rd_dt, const float* ring_g,
-                                              size_t gbase, float* hk, void* hkraw, float* hd,
-                                              void* hdraw, float* hg, uint64_t* bar) {
-  const int sk = dtype_bytes(rk_dt), sd = dtype_bytes(rd_dt);
-  const uint32_t kb = (uint32_t)(n * dk * sk), db = (uint32_t)(n * dv * sd);
-  const uint32_t gb = ALGO == ALGO_KDA ? (uint32_t)(n * dk * 4) : 0u;
-  mbar_expect_tx(bar, kb + db + gb);
-  bulk_g2s(rk_dt == DT_F32 ? static_cast<void*>(hk) : hkraw,
-           static_cast<const char*>(ring_k) + kbase * sk, kb, bar);
-  bulk_g2s(rd_dt == DT_F32 ? static_cast<void*>(hd) : hdraw,
-           static_cast<const char*>(ring_d) + dbase * sd, db, bar);
-  if (ALGO == ALGO_KDA) bulk_g2s(hg, ring_g + gbase, gb, bar);
+__host__ __device__ __forceinline__ uint32_t history_bytes(int n, int dk, int dv, int rk_dt,
+                                                           int rd_dt) {
+  return (uint32_t)(n * (dk * dtype_bytes(rk_dt) + dv * dtype_bytes(rd_dt) +
+                         (ALGO == ALGO_KDA ? dk * 4 : 0)));
 }
 
-// Once the history copies have landed: widen 16-bit records to fp32.
+// The copies alone; the caller has registered history_bytes() on `bar`.
+template <int ALGO>
+__device__ __forceinline__ void history_copies(int n, int dk, int dv, const void* ring_k,
+                                               size_t kbase, int rk_dt, void* kdst,
+                                               const void* ring_d, size_t dbase, int rd_dt,
+                                               void* ddst, const float* ring_g, size_t gbase,
+                                               float* hg, uint64_t* bar) {
+  const int sk = dtype_bytes(rk_dt), sd = dtype_bytes(rd_dt);
+  bulk_g2s(kdst, static_cast<const char*>(ring_k) + kbase * sk, (uint32_t)(n * dk * sk), bar);
+  bulk_g2s(ddst, static_cast<const char*>(ring_d) + dbase * sd, (uint32_t)(n * dv * sd), bar);
+  if (ALGO == ALGO_KDA) bulk_g2s(hg, ring_g + gbase, (uint32_t)(n * dk * 4), bar);
+}
+
+template <int ALGO>
+__device__ __forceinline__ void issue_history(int n, int dk, int dv, const void* ring_k,
+                                              size_t kbase, int rk_dt, void* kdst,
+                                              const void* ring_d, size_t dbase, int rd_dt,
+                                              void* ddst, const float* ring_g, size_t gbase,
+                                              float* hg, uint64_t* bar) {
+  mbar_expect_tx(bar, history_bytes<ALGO>(n, dk, dv, rk_dt, rd_dt));
+  history_copies<ALGO>(n, dk, dv, ring_k, kbase, rk_dt, kdst, ring_d, dbase, rd_dt, ddst, ring_g,
+                       gbase, hg, bar);
+}
+
+// Once the history copies have landed: widen 16-bit records to fp32 (fold
+// kernel: fp32 records land in place).
 __device__ __forceinline__ void widen_history(int n, int dk, int dv, int rk_dt, int rd_dt,
                                               float* hk, const void* hkraw, float* hd,
                                               const void* hdraw, int tid) {
   if (rk_dt != DT_F32) widen16(hk, hkraw, n * dk, rk_dt, tid, kThreads);
   if (rd_dt != DT_F32) widen16(hd, hdraw, n * dv, rd_dt, tid, kThreads);
+}
+
+// Ring keys [n][dk] as stored (any dtype) -> fp32 [n][dk]; threads t of nt.
+__device__ __forceinline__ void widen_keys(float* hk, const void* raw, int count, int dt, int t,
+                                           int nt) {
+  if (dt == DT_F32) {
+    const float4* s = static_cast<const float4*>(raw);
+    float4* d = reinterpret_cast<float4*>(hk);
+    for (int e = t; e < count / 4; e += nt) d[e] = s[e];
+  } else {
+    widen16(hk, raw, count, dt, t, nt);
+  }
+}
+
+// Keys [n][dk] (any dtype) -> transposed fp32 keys hkt[ch][m] with row stride
+// ks = round4(n); the padding entries m in [n, ks) are zero.
+__device__ __forceinline__ void transpose_keys(float* hkt, const void* raw, int n, int dk, int dt,
+                                               int t, int nt) {
+  const int ks = round4(n);
+  for (int e = t; e < dk * (ks / 4); e += nt) {
+    const int ch = e % dk, m0 = 4 * (e / dk);
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = m0 + j < n ? ld_f32(raw, (size_t)(m0 + j) * dk + ch, dt) : 0.f;
+    *reinterpret_cast<float4*>(hkt + (size_t)ch * ks + m0) = make_float4(v[0], v[1], v[2], v[3]);
+  }
 }
 
 // GDN, warp 0: hf[m] holds the raw record gates g_m; replaces them with
@@ -197,12 +238,18 @@ struct TilePipe {
   __device__ __forceinline__ TilePipe(ST* ring_, uint64_t* mbar, const ST* gtile_, int dk, int dv_)
       : ring(ring_), full(mbar + kMbarFull), empty(mbar + kMbarEmpty), gtile(gtile_), dv(dv_),
         tr(dk, dv_, (int)sizeof(ST)) {}
-  // mbarrier set-up (one thread, before the CTA-wide fence and barrier)
+  // mbarrier set-up (one thread): "full" before the first copy (and the fence
+  // that makes initialisation visible to the copies), "empty" with the number
+  // of consuming warps before the CTA barrier that precedes the stream.
+  static __device__ __forceinline__ void init_full(uint64_t* mbar) {
+    for (int st = 0; st < kStages; ++st) mbar_init(&mbar[kMbarFull + st], 1);
+  }
+  __device__ __forceinline__ void init_empty(int warps) const {
+    for (int st = 0; st < tr.ns; ++st) mbar_init(&empty[st], warps);
+  }
   __device__ __forceinline__ void init() const {
-    for (int st = 0; st < tr.ns; ++st) {
-      mbar_init(&full[st], 1);
-      mbar_init(&empty[st], kWarps);
-    }
+    for (int st = 0; st < tr.ns; ++st) mbar_init(&full[st], 1);
+    init_empty(kWarps);
   }
   __device__ __forceinline__ void issue(int j) const {
     const int st = j % tr.ns;
@@ -232,6 +279,15 @@ struct TilePipe {
   // a CTA that leaves early lets the primed chunks land first
   __device__ __forceinline__ void drain() const {
     for (int j = 0; j < tr.ns; ++j) mbar_wait_bounded(&full[j], 0);
+  }
+  // interface of stream_quads: stage data of chunk j, wait for it, hand it back
+  __device__ __forceinline__ const ST* stage(int j) const {
+    return ring + (size_t)(j % tr.ns) * tr.cr * dv;
+  }
+  __device__ __forceinline__ bool wait(int j) const { return wait_full(j); }
+  __device__ __forceinline__ bool done(int j, int tid, int lane) const {
+    release(j, lane);
+    return tid == 0 ? refill(j) : true;
   }
 };
 
@@ -341,27 +397,44 @@ struct QuadLane {
 };
 
 // Stream the checkpoint tile through the ring: each lane takes CW columns of
-// some rows of every chunk, four rows at a time. FOLD: S[row] <- decay(row)
-// S[row] + sum_m k~_m[row] d_m, a rank-n update blocked over 4 records held
-// in registers (hk [n][dk] and hd [n][dv]; GDN: k~_m = hf[m] k_m, decay =
-// gdn_decay; KDA: hk holds k~, decay = egam[row]), stored back to the
-// checkpoint rounded to its dtype; then acc[v] += x_v[row] S[row] for the NV
-// mat-vec vectors (xh [dk][NV]). Sums over the rows of one warp instruction
-// are reduced before returning.
-template <int ALGO, typename ST, int NV, int CW, bool FOLD>
-__device__ __forceinline__ bool stream_quads(const TilePipe<ST>& pipe, const QuadLane& ql,
+// some rows of every chunk, a few rows at a time. FOLD: S[row] <- decay(row)
+// S[row] + sum_m k~_m[row] d_m, stored back to the checkpoint rounded to its
+// dtype; hkt holds the keys transposed ([dk][round4(n)], zero padded; GDN: raw
+// keys with k~_m = hf[m] k_m and decay = gdn_decay; KDA: k~ itself, decay =
+// egam[row]). A lane's columns never change, so the deltas of the first MR
+// records stay in registers for the whole tile and every row costs one
+// broadcast vector load per four records; records past MR come from hd
+// [n][dv]. Then acc[v] += x_v[row] S[row] for the NV mat-vec vectors (xh
+// [dk][NV]). Sums over the rows of one warp instruction are reduced before
+// returning.
+template <int ALGO, typename ST, int NV, int CW, int MR, bool FOLD, class PIPE>
+__device__ __forceinline__ bool stream_quads(const PIPE& pipe, const QuadLane& ql,
                                              float (&acc)[NV][CW], ST* gtile, int dk, int dv,
-                                             int n, const float* hk, const float* hd,
+                                             int n, const float* hkt, const float* hd,
                                              const float* hf, float gdn_decay,
                                              const float* egam, const float* xh, int tid,
                                              int lane) {
-  constexpr int RS = 4;  // rows held in registers at a time
-  constexpr int MB = 4;  // history records per fold block
+  constexpr int RS = FOLD ? 2 : 4;  // rows held in registers at a time
+  constexpr int MRR = FOLD ? MR : 1;
+  const int ks = round4(n);
+  float dr[MRR][CW];
+  if (FOLD) {
+#pragma unroll
+    for (int m = 0; m < MRR; ++m) {
+#pragma unroll
+      for (int c = 0; c < CW; ++c) dr[m][c] = 0.f;
+      if (m < n) {
+        const float f = ALGO == ALGO_GDN ? hf[m] : 1.f;
+#pragma unroll
+        for (int c = 0; c < CW; ++c) dr[m][c] = f * hd[(size_t)m * dv + ql.col0 + c];
+      }
+    }
+  }
   const int rpl = pipe.tr.cr / ql.rstep;  // this lane's rows per chunk
   bool ok = true;
   for (int j = 0; j < pipe.tr.nchunk; ++j) {
-    ok = pipe.wait_full(j) && ok;
-    const ST* stg = pipe.ring + (size_t)(j % pipe.tr.ns) * pipe.tr.cr * dv + ql.col0;
+    ok = pipe.wait(j) && ok;
+    const ST* stg = pipe.stage(j) + ql.col0;
     const int row0 = j * pipe.tr.cr;
     for (int u0 = 0; u0 < rpl; u0 += RS) {
       float s[RS][CW];
@@ -377,34 +450,32 @@ __device__ __forceinline__ bool stream_quads(const TilePipe<ST>& pipe, const Qua
 #pragma unroll
         for (int u = 0; u < RS; ++u) {
           const float dec = ALGO == ALGO_GDN ? gdn_decay : egam[rows[u]];
+          const float* kr = hkt + (size_t)rows[u] * ks;
 #pragma unroll
           for (int c = 0; c < CW; ++c) s[u][c] *= dec;
-        }
-        for (int m0 = 0; m0 < n; m0 += MB) {
-          float dm[MB][CW];
 #pragma unroll
-          for (int m = 0; m < MB; ++m) {
-            if (m0 + m < n) {
-              const float* src = hd + (size_t)(m0 + m) * dv + ql.col0;
-              const float f = ALGO == ALGO_GDN ? hf[m0 + m] : 1.f;
-              if constexpr (CW == 4) {
-                const float4 x = *reinterpret_cast<const float4*>(src);
-                dm[m][0] = f * x.x; dm[m][1] = f * x.y; dm[m][2] = f * x.z; dm[m][3] = f * x.w;
-              } else {
-                const float2 x = *reinterpret_cast<const float2*>(src);
-                dm[m][0] = f * x.x; dm[m][1] = f * x.y;
+          for (int q4 = 0; q4 < MRR / 4; ++q4) {
+            if (4 * q4 < n) {
+              const float4 k4 = *reinterpret_cast<const float4*>(kr + 4 * q4);
+#pragma unroll
+              for (int c = 0; c < CW; ++c) {
+                s[u][c] = fmaf(k4.x, dr[4 * q4 + 0][c], s[u][c]);
+                s[u][c] = fmaf(k4.y, dr[4 * q4 + 1][c], s[u][c]);
+                s[u][c] = fmaf(k4.z, dr[4 * q4 + 2][c], s[u][c]);
+                s[u][c] = fmaf(k4.w, dr[4 * q4 + 3][c], s[u][c]);
               }
             }
           }
+          for (int m0 = MRR; m0 < n; m0 += 4) {
+            const float4 k4 = *reinterpret_cast<const float4*>(kr + m0);
+            const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-          for (int m = 0; m < MB; ++m) {
-            if (m0 + m < n) {
-              const float* km = hk + (size_t)(m0 + m) * dk;
+            for (int m = 0; m < 4; ++m) {
+              if (m0 + m < n) {
+                const float* src = hd + (size_t)(m0 + m) * dv + ql.col0;
+                const float kf = (ALGO == ALGO_GDN ? hf[m0 + m] : 1.f) * kv[m];
 #pragma unroll
-              for (int u = 0; u < RS; ++u) {
-                const float kv = km[rows[u]];
-#pragma unroll
-                for (int c = 0; c < CW; ++c) s[u][c] = fmaf(kv, dm[m][c], s[u][c]);
+                for (int c = 0; c < CW; ++c) s[u][c] = fmaf(kf, src[c], s[u][c]);
               }
             }
           }
@@ -441,8 +512,7 @@ __device__ __forceinline__ bool stream_quads(const TilePipe<ST>& pipe, const Qua
         }
       }
     }
-    pipe.release(j, lane);
-    if (tid == 0) ok = pipe.refill(j) && ok;
+    ok = pipe.done(j, tid, lane) && ok;
   }
   for (int off = ql.lanes; off < 32; off <<= 1) {
 #pragma unroll
