@@ -224,96 +224,6 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
   return m;
 }
 
-// ---------------------------------------------------------------- persistent
-// Persistent replay kernel: 4 consumer warps (the warps of the per-CTA kernel),
-// one warp that feeds the tile ring and one that prepares the next items.
-constexpr int kPWarps = kWarps + 2;
-constexpr int kPThreads = 32 * kPWarps;
-constexpr int kPFeedWarp = kWarps;
-constexpr int kPPrepWarp = kWarps + 1;
-constexpr int kPBuffers = 2;     // items prepared ahead of the consumers
-constexpr int kPMaxStages = 8;   // tile ring stages
-// mbarriers: ring full / empty per stage, then per item buffer: contents
-// landed, descriptor written, released by the consumers.
-constexpr int kPFull = 0;
-constexpr int kPEmpty = kPMaxStages;
-constexpr int kPItemFull = 2 * kPMaxStages;
-constexpr int kPDesc = kPItemFull + kPBuffers;
-constexpr int kPBufEmpty = kPDesc + kPBuffers;
-constexpr int kPMbars = kPBufEmpty + kPBuffers;
-// Window widths served by the persistent kernel (wider ones keep the
-// accumulator tiles of the per-CTA kernel).
-__host__ __device__ constexpr bool persistent_nt(int NT) { return NT <= 4; }
-// Fold records held in registers by the persistent kernel (it runs three CTAs
-// of 192 threads per SM, at most 112 registers a thread).
-__host__ __device__ constexpr int persistent_reg_records(int NT) { return NT == 1 ? 8 : 4; }
-
-struct PSmem {
-  uint32_t ring;      // ns stages of one chunk each
-  uint32_t mbar;      // kPMbars mbarriers
-  uint32_t desc;      // kPBuffers item descriptors (int4: slot, cursor, fold, base)
-  uint32_t flag;      // abort flag (int)
-  uint32_t buf0;      // item buffer b at buf0 + b * buf_bytes, laid out as:
-  uint32_t buf_bytes;
-  uint32_t b_wraw;    //   window rows q [T][dk], k [T][dk], v [T][dv] (input dtype)
-  uint32_t b_wgk;     //   KDA window gates [T][dk]
-  uint32_t b_wbg;     //   window betas [NT], GDN window gates [NT]
-  uint32_t b_hkraw;   //   history keys [L][dk] (ring dtype); split windows: hc [NV][dv]
-  uint32_t b_hd;      //   history deltas [L][dv] (ring dtype)
-  uint32_t b_hg;      //   KDA history gates [L][dk] (a fold: transposed decayed keys)
-  uint32_t b_hf;      //   GDN history gates [L]
-  // consumer working memory
-  uint32_t wq, wk, wv, yk, yq, scal, xh, am, fm, hk, hdw, hdot, red;
-  int ns;             // tile ring stages in use
-  uint32_t total;
-};
-
-__host__ __device__ inline PSmem persistent_layout(int algo, int state_bytes, int NT, int T,
-                                                   int L, int dk, int dv, int in_dt, int rk_dt,
-                                                   int rd_dt, int ns) {
-  PSmem m{};
-  const int NV = 2 * NT;
-  const bool kda = algo == ALGO_KDA;
-  const TileRing tr(dk, dv, state_bytes);
-  const QuadLayout ql(dv, quad_width(NT), kWarps);
-  m.ns = ns;
-  uint32_t off = 0;
-  m.ring = off;  off = align16(off + ns * tr.chunk_bytes);
-  m.mbar = off;  off = align16(off + 8u * kPMbars);
-  m.desc = off;  off = align16(off + 16u * kPBuffers);
-  m.flag = off;  off = align16(off + 16u);
-  {
-    uint32_t b = 0;
-    m.b_wraw = b;  b = align16(b + (uint32_t)(dtype_bytes(in_dt) * T * (2 * dk + dv)));
-    m.b_wgk = b;   if (kda) b = align16(b + 4u * T * dk);
-    m.b_wbg = b;   b = align16(b + 8u * NT);
-    const uint32_t raw = (uint32_t)(dtype_bytes(rk_dt) * L * dk);
-    const uint32_t hc = can_split(algo, NT) ? 4u * NV * dv : 0u;
-    m.b_hkraw = b; b = align16(b + (raw > hc ? raw : hc));
-    m.b_hd = b;    b = align16(b + (uint32_t)(dtype_bytes(rd_dt) * L * dv));
-    m.b_hg = b;    if (kda) b = align16(b + 4u * round4(L) * dk);
-    m.b_hf = b;    if (!kda) b = align16(b + 4u * L);
-    m.buf_bytes = b;
-    m.buf0 = off;
-    off = align16(off + kPBuffers * b);
-  }
-  m.wq = off;    off = align16(off + 4u * T * dk);
-  m.wk = off;    off = align16(off + 4u * T * dk);
-  m.wv = off;    off = align16(off + 4u * T * dv);
-  m.yk = off;    if (kda) off = align16(off + 4u * T * dk);
-  m.yq = off;    if (kda) off = align16(off + 4u * T * dk);
-  m.scal = off;  off = align16(off + 4u * (kda ? 2 * dk : 3 * NT + 4));
-  m.xh = off;    off = align16(off + 4u * dk * NV);
-  m.am = off;    off = align16(off + 4u * NT * NT);
-  m.fm = off;    off = align16(off + 4u * NT * NT);
-  m.hk = off;    off = align16(off + 4u * round4(L) * dk);
-  m.hdw = off;   if (rd_dt != DT_F32) off = align16(off + 4u * L * dv);
-  m.hdot = off;  off = align16(off + 4u * L * NV);
-  m.red = off;   off = align16(off + 4u * ql.rgw * NV * dv);
-  m.total = off;
-  return m;
-}
-
 __host__ __device__ inline FoldSmem fold_layout(int algo, int state_bytes, int L, int dk, int dv,
                                                 int rk_dt, int rd_dt) {
   FoldSmem m{};
@@ -428,38 +338,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 
-
-// One arrival that counts as `cnt` on `bar`.
-__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t cnt) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(cnt)
-               : "memory");
-}
-
-// As mbar_wait_bounded, but also gives up as soon as *abort is set.
-__device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t parity,
-                                                    const volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort != 0 || global_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
-// Barrier over `count` threads naming barrier `id` that returns whether any of
-// them passed pred = true (the same answer in every thread).
-__device__ __forceinline__ bool named_any(int id, int count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
 
 // Barrier over the `count` threads (a multiple of 32) that name barrier `id`
 // (id 0 is the one __syncthreads uses).

@@ -472,10 +472,11 @@ __device__ __forceinline__ bool stream_quads(const PIPE& pipe, const QuadLane& q
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
               if (m0 + m < n) {
-                const float* src = hd + (size_t)(m0 + m) * dv + ql.col0;
+                float dv4[CW];
+                ld_cols<float, CW>(hd + (size_t)(m0 + m) * dv + ql.col0, dv4);
                 const float kf = (ALGO == ALGO_GDN ? hf[m0 + m] : 1.f) * kv[m];
 #pragma unroll
-                for (int c = 0; c < CW; ++c) s[u][c] = fmaf(kf, src[c], s[u][c]);
+                for (int c = 0; c < CW; ++c) s[u][c] = fmaf(kf, dv4[c], s[u][c]);
               }
             }
           }
