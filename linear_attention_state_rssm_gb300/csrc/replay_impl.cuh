@@ -163,7 +163,6 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int h = blockIdx.x;
-  const int r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = p.T, dk = p.dk, dv = p.dv, L = p.L, HV = p.HV, HK = p.HK;
   const int kh = h / p.G;
@@ -199,15 +198,69 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   float* egam = scal;
   float* gam = scal + dk;
 
-  const size_t tok0 = (size_t)r * T;
   const int s_in = dtype_bytes(p.in_dt);
   const bool f32in = p.in_dt == DT_F32;
   const uint32_t qrow = (uint32_t)(dk * s_in), vrow = (uint32_t)(dv * s_in);
 
+  // ---- row order. A folding row's CTAs live several times longer than the
+  //      others; started last they would set the end of the launch. For
+  //      decode (about one row in L folds) with up to kThreads rows, every CTA
+  //      ranks the rows the same way (folding rows first, rows without a slot
+  //      last, stable) and takes the blockIdx.y-th; its own slot and cursor
+  //      come out of the same loads. (Wider verify windows fold a large share
+  //      of their rows, and the ranking's extra latency does not pay there.)
+  int r = blockIdx.y, s, c = 0;
+  bool have_c = false;
+  if (NT == 1 && p.B <= kThreads) {
+    int* order = reinterpret_cast<int*>(smem + p.sm.ring);  // the ring is unused yet
+    int* rslot = order + kThreads;
+    int* rcur = rslot + kThreads;
+    int* wcount = rcur + kThreads;  // [kWarps][3]
+    int key = 3, sv = -1, cv = 0;
+    if (tid < p.B) {
+      sv = p.slot[tid];
+      key = 2;
+      if (sv >= 0 && sv < p.n_slots) {
+        cv = p.cursor[sv];
+        const bool fr = (p.force != nullptr && p.force[tid] != 0) || (cv + T > L);
+        key = fr ? 0 : 1;
+      }
+      rslot[tid] = sv;
+      rcur[tid] = cv;
+    }
+    unsigned below = 0, cnt[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const unsigned m = __ballot_sync(kFull, key == k);
+      cnt[k] = __popc(m);
+      if (key == k) below = __popc(m & ((1u << lane) - 1u));
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < 3; ++k) wcount[warp * 3 + k] = (int)cnt[k];
+    }
+    __syncthreads();
+    if (key < 3) {
+      int rank = (int)below;
+      for (int k = 0; k < key; ++k) {
+        for (int w2 = 0; w2 < kWarps; ++w2) rank += wcount[w2 * 3 + k];
+      }
+      for (int w2 = 0; w2 < warp; ++w2) rank += wcount[w2 * 3 + key];
+      order[rank] = tid;
+    }
+    __syncthreads();
+    r = order[blockIdx.y];
+    s = rslot[r];
+    c = rcur[r];
+    have_c = true;
+    __syncthreads();  // the ring's first chunks land over these arrays
+  } else {
+    s = p.slot[r];
+  }
+  const size_t tok0 = (size_t)r * T;
+
   // ---- 0. bulk async copies; one thread issues every copy of a barrier after
-  //         registering its byte count. The window rows need only the request
-  //         row: they are under way while the slot index loads.
-  const int s = p.slot[r];
+  //         registering its byte count.
   if (tid == 0) {
     mbar_init(&mbar[kMbarWin], 1);
     mbar_init(&mbar[kMbarHist], 1);
@@ -246,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   ST* gtile = static_cast<ST*>(p.state) + ((size_t)s * HV + h) * dk * dv;
   const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv);
   if (tid == 0) pipe.prime();
-  const int c = p.cursor[s];
+  if (!have_c) c = p.cursor[s];
   if (c < 0 || c > L) {
     if (tid == 0) {
       if (h == 0) atomicOr(p.err, DEVERR_CURSOR);

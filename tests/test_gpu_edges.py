@@ -250,3 +250,29 @@ def test_multi_layer_decode_moves_cursor_once_per_step():
             np.testing.assert_array_equal(f_gpu, f_orc)
         run.check_cursors()
     assert run.state_err() <= TOL32
+
+
+@pytest.mark.parametrize("B", [128, 160])
+def test_decode_row_order_either_side_of_the_ranked_batch_limit(B):
+    """Decode launches of up to 128 rows start their folding rows first (each
+    CTA ranks the rows by fold decision); wider batches keep the grid order.
+    On both sides of that limit, with permuted slots, null rows and forced
+    folds, every row matches the oracle and null rows stay untouched."""
+    rng = np.random.default_rng(31 + B)
+    slots = rng.permutation(B + 8)[:B].astype(np.int32)
+    null = rng.choice(B, 9, replace=False)
+    slots[null] = -1
+    run = Run(algo="gdn", HK=1, HV=2, dk=32, dv=32, L=4, max_T=1, slots=slots, n_slots=B + 8,
+              config_id=32)
+    live_rows = run.orc_slots >= 0
+    for step in range(10):
+        force = synth.force_flags(3200 + step, B, 0.1)
+        o_all, o_gpu, o_orc, f_gpu, f_orc = run.window(0, run.inputs(step, 0, 1), 1, force=force,
+                                                       decode=True, advance=True)
+        assert rel_err(o_gpu[live_rows], o_orc[live_rows]) <= TOL32, step
+        np.testing.assert_array_equal(f_gpu[live_rows], f_orc[live_rows])
+        assert np.all(o_all[null] == SENTINEL), "null rows must be left untouched"
+        run.check_cursors()
+    assert run.state_err() <= TOL32
+    assert run.ring_d_err() <= TOL32
+    assert run.store.rssm_get_device_error() == 0
