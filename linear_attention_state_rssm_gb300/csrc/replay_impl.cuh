@@ -115,6 +115,38 @@ __device__ __forceinline__ void window_pairs(int T, int dk, const float* wk, con
   }
 }
 
+// GDN window coefficients with one thread per pair (i, j), j <= i: plain dot
+// products over copies of the window keys and queries whose rows are padded
+// to `pitch` floats (so the rows a warp reads fall in different banks); no
+// shuffles. gp holds the inclusive gate prefixes.
+template <int NT>
+__device__ __forceinline__ void window_pairs_flat(int T, int dk, const float* kp,
+                                                  const float* qp, int pitch, const float* gp,
+                                                  const float* wb, float* am, float* fm, int t,
+                                                  int nt) {
+  const int npairs = T * (T + 1) / 2;
+  for (int pidx = t; pidx < npairs; pidx += nt) {
+    int i = 0;
+    while ((i + 1) * (i + 2) / 2 <= pidx) ++i;
+    const int j = pidx - i * (i + 1) / 2;
+    const float* kj = kp + j * pitch;
+    const float* ki = kp + i * pitch;
+    const float* qi = qp + i * pitch;
+    float sk0 = 0.f, sk1 = 0.f, sq0 = 0.f, sq1 = 0.f;
+    for (int c4 = 0; c4 < dk; c4 += 8) {
+      const float4 a = ld4(kj + c4), b = ld4(ki + c4), c = ld4(qi + c4);
+      const float4 a2 = ld4(kj + c4 + 4), b2 = ld4(ki + c4 + 4), c2 = ld4(qi + c4 + 4);
+      sk0 = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, sk0))));
+      sq0 = fmaf(a.x, c.x, fmaf(a.y, c.y, fmaf(a.z, c.z, fmaf(a.w, c.w, sq0))));
+      sk1 = fmaf(a2.x, b2.x, fmaf(a2.y, b2.y, fmaf(a2.z, b2.z, fmaf(a2.w, b2.w, sk1))));
+      sq1 = fmaf(a2.x, c2.x, fmaf(a2.y, c2.y, fmaf(a2.z, c2.z, fmaf(a2.w, c2.w, sq1))));
+    }
+    const float wgt = __expf(gp[i] - gp[j]);
+    fm[i * NT + j] = wgt * (sq0 + sq1);
+    am[i * NT + j] = (j < i) ? wb[i] * wgt * (sk0 + sk1) : 0.f;
+  }
+}
+
 // History dot coefficients hdot[m][v] of the records m = w, w + nw, ...:
 // GDN: raw keys against raw window vectors, times hf[m] e^{G_i};
 // KDA: decayed keys against e^{G_i} x (xk, xq = yk, yq).
@@ -442,9 +474,28 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
     }
     __syncthreads();
 
+    // Windows of four or more tokens compute the GDN window coefficients one
+    // thread per pair on padded copies of the window keys and queries in the
+    // drained tile ring: a window without a fold has streamed already; a
+    // folding one computes them after its stream (only the per-column solve
+    // needs them).
+    const int wpitch = dk + 4;
+    float* kpad = reinterpret_cast<float*>(smem + p.sm.ring);
+    float* qpad = kpad + T * wpitch;
+    const bool flat = ALGO == ALGO_GDN && NT >= 4 &&
+                      (uint32_t)(8 * T * wpitch) <= pipe.tr.ns * pipe.tr.chunk_bytes;
+    auto pad_window = [&]() {
+      for (int e = tid; e < T * dk / 4; e += kThreads) {
+        const int i = e / (dk / 4), c4 = 4 * (e - i * (dk / 4));
+        *reinterpret_cast<float4*>(kpad + i * wpitch + c4) = ld4(wk + i * dk + c4);
+        *reinterpret_cast<float4*>(qpad + i * wpitch + c4) = ld4(wq + i * dk + c4);
+      }
+    };
+
     // ---- 1. gates
     if (ALGO == ALGO_GDN) {
       if (warp == 0) gdn_gates(nh, T, fold, hf, hscal, wg, gp, eG, es, lane);
+      if (flat && early) pad_window();
     } else {
       // one thread per key channel: decayed history keys k~ (in hk, [nh][dk]),
       // history decay, window prefix, scaled window vectors
@@ -483,8 +534,12 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
     // ---- 2. window coefficients A, F (j <= i only) and history dot coefficients;
     //         a folding KDA window transposes its decayed keys over its gates
     if (ALGO == ALGO_KDA && fold && nh > 0) transpose_keys(hg, hk, nh, dk, DT_F32, tid, kThreads);
-    window_pairs<ALGO, NT>(T, dk, wk, wq, ALGO == ALGO_GDN ? gp : wg, wb, am, fm, warp, kWarps,
-                           lane);
+    if (flat) {
+      if (early) window_pairs_flat<NT>(T, dk, kpad, qpad, wpitch, gp, wb, am, fm, tid, kThreads);
+    } else {
+      window_pairs<ALGO, NT>(T, dk, wk, wq, ALGO == ALGO_GDN ? gp : wg, wb, am, fm, warp, kWarps,
+                             lane);
+    }
     if (!fold) {
       history_dots<ALGO, NT>(nh, T, dk, hk, ALGO == ALGO_GDN ? wk : yk,
                              ALGO == ALGO_GDN ? wq : yq, hf, eG, hdot, warp, kWarps, lane);
@@ -503,6 +558,12 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
                                                               hk, hd, hf, 1.f, egam, xh, tid,
                                                               lane) &&
                     copies_ok;
+      }
+      if (flat) {
+        __syncthreads();  // the ring is drained
+        pad_window();
+        __syncthreads();
+        window_pairs_flat<NT>(T, dk, kpad, qpad, wpitch, gp, wb, am, fm, tid, kThreads);
       }
     }
   }
