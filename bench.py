@@ -329,6 +329,36 @@ def run_ours(args, rank, world, local_rank):
            "h2d_bytes_per_step": half.numel() * 2 + flt.numel() * 4,
            "d2h_bytes_per_step": out.numel() * 2}
     err = st.rssm_get_device_error()
+
+    # ---- comparison point: native fused-recurrent decode on the same shapes
+    # (the state read and written every token; ring unused), 48 layers per step
+    native = None
+    if not args.no_native:
+        with torch.cuda.stream(cap):
+            ngraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(ngraph, stream=cap):
+                for l in range(nl):
+                    st.rssm_native_decode(l, *lv[l], slot_d, out[l])
+        torch.cuda.current_stream().wait_stream(cap)
+        for _ in range(args.warmup):
+            ngraph.replay()
+        torch.cuda.synchronize()
+        n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0.record()
+        for _ in range(args.steps):
+            ngraph.replay()
+        n1.record()
+        torch.cuda.synchronize()
+        tn = n0.elapsed_time(n1) / 1e3
+        n_bytes = B_live * (2 * HV * dk * dv * 4 + 2 * HK * dk * 2 + HV * dv * 2 + 2 * HV * 4
+                            + HV * dv * 2)
+        native = {"kernel": "native_decode_kernel<GDN, f32>",
+                  "tokens_per_s_per_layer": B_live * nl * args.steps / tn,
+                  "launch_ms": tn * 1e3 / (args.steps * nl),
+                  "achieved_gbs": n_bytes * nl * args.steps / tn / 1e9,
+                  "bytes_per_launch": n_bytes}
+        err |= st.rssm_get_device_error()
+        del ngraph
     del graph, st, half, flt, out, lv
     torch.cuda.empty_cache()
 
@@ -350,11 +380,13 @@ def run_ours(args, rank, world, local_rank):
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} (hbm_gbs, burst)",
                      "traffic": traffic, "kernel": "replay_kernel<GDN, f32, 1>",
                      "algorithmic_bytes_per_launch": k_bytes, "launch_ms": k_ms},
-        "gpu_launches": args.steps * (nl + 1),
+        "gpu_launches": args.steps * (nl + 1),  # the timed region: replay layers + cursor
         "e2e": e2e,
         "clocks": clk.summary(),
         "device_error_word": err,
     }
+    if native is not None:
+        res["native_decode"] = native
     if ver is not None:
         res["verify"] = ver
     return res
@@ -468,6 +500,8 @@ def main():
     ap.add_argument("--layers", type=int, default=WL["layers"])
     ap.add_argument("--no-verify", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-native", action="store_true",
+                    help="skip the native fused-recurrent decode comparison line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -184,6 +184,23 @@ rssm_status rssm_verify(rssm_handle *h, int32_t layer, const void *q,
                         uint8_t *fold_out, void *stream);
 
 /*
+ * Native fused-recurrent decode of one layer, the path ReplaySSM replaces
+ * (LightLLM PR #1690, PR description: the native mode writes the recurrent
+ * state back every step). It is here as a comparison point: for each row r
+ * with s = slot[r] >= 0 it treats the layer's checkpoint of (s, h) as the live
+ * state and applies one token, S <- decay(g) S; d = beta (v - S^T k);
+ * S <- S + k d^T; o = scale S^T q, storing S back (rounded to the state dtype)
+ * and writing o (B rows, input dtype). The ring and the cursor are neither
+ * read nor written, so mixing it with rssm_decode on the same slots is only
+ * meaningful while their rings are empty. Same input layout, alignment and
+ * error rules as rssm_decode; null slots are skipped.
+ */
+rssm_status rssm_native_decode(rssm_handle *h, int32_t layer, const void *q,
+                               const void *k, const void *v, const float *beta,
+                               const float *g, const int32_t *slot, int32_t B,
+                               void *o, void *stream);
+
+/*
  * Commit the last verify of every layer (SGLang fork PR jianc99/sglang#2,
  * fourth commit). accept_len[r] in [0, T]; slot/force/T must equal the
  * verify's. LAZY: cursor[s] = base + a (rejected tail trimmed). FOLD_EVERY:

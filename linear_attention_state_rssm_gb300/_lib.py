@@ -23,8 +23,8 @@ DEVERR = {"slot": 1, "cursor": 2, "accept": 4, "timeout": 8}
 
 # Every entry point declared in include/rssm.h.
 SYMBOLS = ("rssm_required_bytes", "rssm_alloc", "rssm_free", "rssm_decode", "rssm_verify",
-           "rssm_commit", "rssm_fold", "rssm_reset_slots", "rssm_get_device_error",
-           "rssm_status_string", "rssm_version")
+           "rssm_native_decode", "rssm_commit", "rssm_fold", "rssm_reset_slots",
+           "rssm_get_device_error", "rssm_status_string", "rssm_version")
 
 
 class RssmError(RuntimeError):
@@ -77,6 +77,7 @@ def load() -> ctypes.CDLL:
         "rssm_free": ([_P], None),
         "rssm_decode": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _P], _I),
         "rssm_verify": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P], _I),
+        "rssm_native_decode": ([_P, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P], _I),
         "rssm_commit": ([_P, _P, _P, _P, _I, _I, _P], _I),
         "rssm_fold": ([_P, _P, _I, _P], _I),
         "rssm_reset_slots": ([_P, _P, _I, _P], _I),
@@ -155,6 +156,12 @@ def rssm_verify(handle, layer, q, k, v, beta, g, slot, force, B, T, o, fold_out,
     _check(load().rssm_verify(handle, layer, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
                               _ptr(slot), _ptr(force), B, T, _ptr(o), _ptr(fold_out),
                               _stream(stream)), "rssm_verify")
+
+
+def rssm_native_decode(handle, layer, q, k, v, beta, g, slot, B, o, stream=None):
+    _check(load().rssm_native_decode(handle, layer, _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                     _ptr(g), _ptr(slot), B, _ptr(o), _stream(stream)),
+           "rssm_native_decode")
 
 
 def rssm_commit(handle, slot, force, accept_len, B, T, stream=None):

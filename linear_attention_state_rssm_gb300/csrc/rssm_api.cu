@@ -114,10 +114,12 @@ T* at(void* base, size_t elems, size_t esz) {
   return reinterpret_cast<T*>(static_cast<char*>(base) + elems * esz);
 }
 
-rssm_status window(rssm_handle* h, int32_t layer, const void* q, const void* k, const void* v,
-                   const float* beta, const float* g, const int32_t* slot,
-                   const uint8_t* force, int32_t B, int32_t T, void* o, uint8_t* fold_out,
-                   void* stream) {
+// Validates the window arguments shared by decode, verify and native decode
+// and fills the launch parameters (all but the shared memory plan).
+rssm_status window_params(const rssm_handle* h, int32_t layer, const void* q, const void* k,
+                          const void* v, const float* beta, const float* g,
+                          const int32_t* slot, const uint8_t* force, int32_t B, int32_t T,
+                          void* o, uint8_t* fold_out, ReplayParams* out) {
   if (h == nullptr) return RSSM_ERR_INVALID_ARG;
   const rssm_config& c = h->cfg;
   if (layer < 0 || layer >= c.n_layers) return RSSM_ERR_INVALID_ARG;
@@ -130,7 +132,8 @@ rssm_status window(rssm_handle* h, int32_t layer, const void* q, const void* k, 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return RSSM_ERR_INVALID_ARG;
   if (c.algo == RSSM_ALGO_KDA ? !aligned16(g) : !aligned4(g)) return RSSM_ERR_INVALID_ARG;
 
-  ReplayParams p{};
+  ReplayParams& p = *out;
+  p = ReplayParams{};
   const rssm_buffers& b = h->buf;
   p.state = at<char>(b.state, layer * h->layer_state, esize(c.state_dtype));
   p.ring_k = at<char>(b.ring_k, layer * h->layer_k, esize(c.ring_k_dtype));
@@ -162,9 +165,24 @@ rssm_status window(rssm_handle* h, int32_t layer, const void* q, const void* k, 
   p.rk_dt = c.ring_k_dtype;
   p.rd_dt = c.ring_d_dtype;
   p.scale = c.scale;
-  p.sm = layout_for(c, T);
+  return RSSM_OK;
+}
+
+rssm_status window(rssm_handle* h, int32_t layer, const void* q, const void* k, const void* v,
+                   const float* beta, const float* g, const int32_t* slot,
+                   const uint8_t* force, int32_t B, int32_t T, void* o, uint8_t* fold_out,
+                   void* stream) {
+  ReplayParams p;
+  const rssm_status st = window_params(h, layer, q, k, v, beta, g, slot, force, B, T, o,
+                                       fold_out, &p);
+  if (st != RSSM_OK || B == 0) return st;
+  p.sm = layout_for(h->cfg, T);
   if ((int)p.sm.total > h->max_smem) return RSSM_ERR_UNSUPPORTED;
-  return from_cuda(replay_launch(c, p, nt_for(T), static_cast<cudaStream_t>(stream)));
+  return from_cuda(replay_launch(h->cfg, p, nt_for(T), static_cast<cudaStream_t>(stream)));
+}
+
+NativeSmem native_layout_for(const rssm_config& c) {
+  return native_layout(c.algo, (int)esize(c.state_dtype), c.dk, c.dv, c.in_dtype);
 }
 
 FoldParams fold_params(const rssm_handle* h, const int32_t* slot, const uint8_t* force,
@@ -239,6 +257,12 @@ rssm_status rssm_alloc(const rssm_config* cfg, const rssm_buffers* buf, rssm_han
   if ((int)worst.total > max_smem || (int)fworst.total > max_smem) return RSSM_ERR_UNSUPPORTED;
   if (replay_prepare(*cfg, max_smem) != cudaSuccess) return RSSM_ERR_CUDA;
   if (fold_prepare(cfg->algo, state_dt(*cfg), max_smem) != cudaSuccess) return RSSM_ERR_CUDA;
+  // the comparison kernel needs the whole tile in shared memory; configurations
+  // where it does not fit still allocate, and rssm_native_decode reports
+  // RSSM_ERR_UNSUPPORTED for them
+  if ((int)native_layout_for(*cfg).total <= max_smem &&
+      native_prepare(cfg->algo, state_dt(*cfg), max_smem) != cudaSuccess)
+    return RSSM_ERR_CUDA;
 
   rssm_handle* h = new (std::nothrow) rssm_handle;
   if (h == nullptr) return RSSM_ERR_INVALID_ARG;
@@ -278,6 +302,19 @@ rssm_status rssm_verify(rssm_handle* h, int32_t layer, const void* q, const void
                         const uint8_t* force, int32_t B, int32_t T, void* o, uint8_t* fold_out,
                         void* stream) {
   return window(h, layer, q, k, v, beta, g, slot, force, B, T, o, fold_out, stream);
+}
+
+rssm_status rssm_native_decode(rssm_handle* h, int32_t layer, const void* q, const void* k,
+                               const void* v, const float* beta, const float* g,
+                               const int32_t* slot, int32_t B, void* o, void* stream) {
+  ReplayParams p;
+  const rssm_status st = window_params(h, layer, q, k, v, beta, g, slot, nullptr, B, 1, o,
+                                       nullptr, &p);
+  if (st != RSSM_OK || B == 0) return st;
+  const NativeSmem sm = native_layout_for(h->cfg);
+  if ((int)sm.total > h->max_smem) return RSSM_ERR_UNSUPPORTED;
+  return from_cuda(native_launch(h->cfg.algo, state_dt(h->cfg), p, sm,
+                                 static_cast<cudaStream_t>(stream)));
 }
 
 rssm_status rssm_commit(rssm_handle* h, const int32_t* slot, const uint8_t* force,

@@ -66,6 +66,12 @@ class ReplayStore:
         _lib.rssm_verify(self.handle, layer, q, k, v, beta, g, slot, force, slot.numel(), T, o,
                          fold_out, stream)
 
+    def rssm_native_decode(self, layer, q, k, v, beta, g, slot, o, stream=None):
+        """The per-token state read/write path ReplaySSM replaces (comparison
+        point): the checkpoint is the live state; ring and cursor untouched."""
+        _lib.rssm_native_decode(self.handle, layer, q, k, v, beta, g, slot, slot.numel(), o,
+                                stream)
+
     def rssm_commit(self, slot, accept_len, T, force=None, stream=None):
         _lib.rssm_commit(self.handle, slot, force, accept_len, slot.numel(), T, stream)
 
