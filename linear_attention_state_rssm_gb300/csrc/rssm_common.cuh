@@ -52,11 +52,11 @@ struct TileRing {
   int nchunk;   // chunks per tile
   int ns;       // stages in use
   uint32_t chunk_bytes;
-  __host__ __device__ TileRing(int dk, int dv, int state_bytes) {
+  __host__ __device__ TileRing(int dk, int dv, int state_bytes, int stages = kStages) {
     const int rowb = dv * state_bytes;
     cr = kChunkBytes / rowb < dk ? kChunkBytes / rowb : dk;
     nchunk = dk / cr;
-    ns = nchunk < kStages ? nchunk : kStages;
+    ns = nchunk < stages ? nchunk : stages;
     chunk_bytes = (uint32_t)(cr * rowb);
   }
 };
@@ -220,6 +220,33 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
     m.red = off;
     off = align16(off + red_bytes);
   }
+  m.total = off;
+  return m;
+}
+
+// Native fused-recurrent decode: the whole tile, one mbarrier for the window
+// and one per chunk, the window, the mat-vec inputs and the partial sums.
+struct NativeSmem {
+  uint32_t ring, mbar, wq, wk, wv, wraw, wg, xh, red, dsh, scal, total;
+};
+
+__host__ __device__ inline NativeSmem native_layout(int algo, int state_bytes, int dk, int dv,
+                                                    int in_dt) {
+  NativeSmem m{};
+  const TileRing tr(dk, dv, state_bytes, 1 << 30);
+  const QuadLayout ql(dv, 4, kWarps);
+  uint32_t off = 0;
+  m.ring = off;  off = align16(off + tr.nchunk * tr.chunk_bytes);
+  m.mbar = off;  off = align16(off + 8u * (1 + tr.nchunk));
+  m.wq = off;    off = align16(off + 4u * dk);
+  m.wk = off;    off = align16(off + 4u * dk);
+  m.wv = off;    off = align16(off + 4u * dv);
+  m.wraw = off;  if (in_dt != DT_F32) off = align16(off + 2u * (2 * dk + dv));
+  m.wg = off;    if (algo == ALGO_KDA) off = align16(off + 4u * dk);
+  m.xh = off;    off = align16(off + 8u * dk);
+  m.red = off;   off = align16(off + 8u * ql.rgw * dv);
+  m.dsh = off;   off = align16(off + 4u * dv);
+  m.scal = off;  off = align16(off + 4u * kWarps);
   m.total = off;
   return m;
 }
