@@ -417,11 +417,20 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
 
   if (split) {
     if (warp < sw) {
-      // ---- 3. stream warps: y_x = S0^T x for the raw window vectors
-      copies_ok = stream_quads<ALGO, ST, NV, CW, MR, false>(pipe, qlane, acc, gtile, dk, dv, 0,
-                                                            hk, hd, hf, 1.f, egam, xh, tid,
-                                                            lane) &&
-                  copies_ok;
+      // ---- 3. stream warps: y_x = S0^T x for the raw window vectors (decode
+      //         with 128 value columns takes the unrolled fixed-geometry loop)
+      constexpr int kFixedRpl = 8192 / (128 * (int)sizeof(ST)) / (2 * kSplitWarps / 2);
+      if (NT == 1 && dv == 128 && qlane.rstep == kSplitWarps &&
+          pipe.tr.cr / qlane.rstep == kFixedRpl) {
+        copies_ok = stream_fixed<ST, NV, CW, kFixedRpl, kSplitWarps, 128>(pipe, qlane, acc, xh,
+                                                                         tid, lane) &&
+                    copies_ok;
+      } else {
+        copies_ok = stream_quads<ALGO, ST, NV, CW, MR, false>(pipe, qlane, acc, gtile, dk, dv, 0,
+                                                              hk, hd, hf, 1.f, egam, xh, tid,
+                                                              lane) &&
+                    copies_ok;
+      }
     } else {
       // ---- 1, 2 and the history part of 4 on the other warps
       const int ht = tid - sw * 32, hw = warp - sw;

@@ -525,4 +525,56 @@ __device__ __forceinline__ bool stream_quads(const PIPE& pipe, const QuadLane& q
   return ok;
 }
 
+// stream_quads without a fold for a fixed geometry: RPL rows per lane per
+// chunk, RSTEP rows between a lane's rows, DV value columns. Every offset is a
+// compile-time constant and a chunk is one fully unrolled block of loads and
+// FMAs, which halves the instructions per row of the general loop.
+template <typename ST, int NV, int CW, int RPL, int RSTEP, int DV, class PIPE>
+__device__ __forceinline__ bool stream_fixed(const PIPE& pipe, const QuadLane& ql,
+                                             float (&acc)[NV][CW], const float* xh, int tid,
+                                             int lane) {
+  bool ok = true;
+  const int cr = pipe.tr.cr;
+  for (int j = 0; j < pipe.tr.nchunk; ++j) {
+    ok = pipe.wait(j) && ok;
+    const ST* stg = pipe.stage(j) + ql.col0 + ql.lr0 * DV;
+    const float* xr = xh + (size_t)(j * cr + ql.lr0) * NV;
+    float sv[RPL][CW];
+#pragma unroll
+    for (int u = 0; u < RPL; ++u) ld_cols<ST, CW>(stg + u * RSTEP * DV, sv[u]);
+#pragma unroll
+    for (int u = 0; u < RPL; ++u) {
+      if constexpr (NV == 2) {
+        const float2 x = *reinterpret_cast<const float2*>(xr + u * RSTEP * NV);
+#pragma unroll
+        for (int c = 0; c < CW; ++c) {
+          acc[0][c] = fmaf(x.x, sv[u][c], acc[0][c]);
+          acc[1][c] = fmaf(x.y, sv[u][c], acc[1][c]);
+        }
+      } else {
+#pragma unroll
+        for (int q4 = 0; q4 < NV / 4; ++q4) {
+          const float4 x = *reinterpret_cast<const float4*>(xr + u * RSTEP * NV + 4 * q4);
+#pragma unroll
+          for (int c = 0; c < CW; ++c) {
+            acc[4 * q4 + 0][c] = fmaf(x.x, sv[u][c], acc[4 * q4 + 0][c]);
+            acc[4 * q4 + 1][c] = fmaf(x.y, sv[u][c], acc[4 * q4 + 1][c]);
+            acc[4 * q4 + 2][c] = fmaf(x.z, sv[u][c], acc[4 * q4 + 2][c]);
+            acc[4 * q4 + 3][c] = fmaf(x.w, sv[u][c], acc[4 * q4 + 3][c]);
+          }
+        }
+      }
+    }
+    ok = pipe.done(j, tid, lane) && ok;
+  }
+  for (int off = ql.lanes; off < 32; off <<= 1) {
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+#pragma unroll
+      for (int c = 0; c < CW; ++c) acc[v][c] += __shfl_xor_sync(kFull, acc[v][c], off);
+    }
+  }
+  return ok;
+}
+
 }  // namespace rssm
