@@ -115,6 +115,70 @@ __device__ __forceinline__ void window_pairs(int T, int dk, const float* wk, con
   }
 }
 
+// Four consecutive ring keys (as stored: fp32, fp16 or bf16) as fp32.
+__device__ __forceinline__ float4 ld4_key(const void* raw, size_t i, int dt) {
+  if (dt == DT_F32) return *reinterpret_cast<const float4*>(static_cast<const float*>(raw) + i);
+  const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(raw) + i);
+  float2 a, b;
+  if (dt == DT_F16) {
+    a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  } else {
+    a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  }
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// Warp reduce-scatter of 32 values: afterwards lane l holds the sum over the
+// warp of value l (31 shuffles in five independent levels).
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int lvl = 0; lvl < 5; ++lvl) {
+    const int off = 16 >> lvl, half = 16 >> lvl;
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFull, send, off);
+    }
+  }
+  return v[0];
+}
+
+// Decode (one window token), one warp: raw history dots hraw[m][0] = k_m . k,
+// hraw[m][1] = k_m . q for m < nh (keys as stored in the ring, 16 records per
+// pass of one reduce-scatter) and the window pair F_00 = k . q (A_00 = 0).
+__device__ __forceinline__ void decode_dots(int nh, int dk, const void* hkraw, int rk_dt,
+                                            const float* wk, const float* wq, float* hraw,
+                                            float* am, float* fm, int lane) {
+  const int c4 = 4 * lane;
+  const bool has = c4 < dk;
+  const float4 xk = has ? ld4(wk + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 xq = has ? ld4(wq + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int m0 = 0; m0 < nh; m0 += 16) {
+    float v[32];
+#pragma unroll
+    for (int mm = 0; mm < 16; ++mm) {
+      v[2 * mm] = 0.f;
+      v[2 * mm + 1] = 0.f;
+      if (m0 + mm < nh && has) {
+        const float4 km = ld4_key(hkraw, (size_t)(m0 + mm) * dk + c4, rk_dt);
+        v[2 * mm] = fmaf(km.x, xk.x, fmaf(km.y, xk.y, fmaf(km.z, xk.z, km.w * xk.w)));
+        v[2 * mm + 1] = fmaf(km.x, xq.x, fmaf(km.y, xq.y, fmaf(km.z, xq.z, km.w * xq.w)));
+      }
+    }
+    const float r = warp_reduce_scatter32(v, lane);
+    if (m0 + lane / 2 < nh) hraw[2 * m0 + lane] = r;
+  }
+  const float kq = warp_sum(fmaf(xk.x, xq.x, fmaf(xk.y, xq.y, fmaf(xk.z, xq.z, xk.w * xq.w))));
+  if (lane == 0) {
+    fm[0] = kq;
+    am[0] = 0.f;
+  }
+}
+
 // GDN window coefficients with one thread per pair (i, j), j <= i: plain dot
 // products over copies of the window keys and queries whose rows are padded
 // to `pitch` floats (so the rows a warp reads fall in different banks); no
@@ -435,16 +499,29 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
       // ---- 1, 2 and the history part of 4 on the other warps
       const int ht = tid - sw * 32, hw = warp - sw;
       const int nht = kThreads - sw * 32, nhw = kWarps - sw;
+      // decode: the gate scan on one history warp while the other takes every
+      // raw history dot straight from the ring keys (gate factors go on in the
+      // column correction below)
+      const bool decode1 = NT == 1 && nhw == 2;
       if (nh > 0) {
         copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
-        widen_keys(hk, hkraw, nh * dk, p.rk_dt, ht, nht);
+        if (!decode1) widen_keys(hk, hkraw, nh * dk, p.rk_dt, ht, nht);
         if (p.rd_dt != DT_F32) widen16(hd, hdraw, nh * dv, p.rd_dt, ht, nht);
       }
-      named_sync(1, nht);
-      if (hw == 0) gdn_gates(nh, T, false, hf, hscal, wg, gp, eG, es, lane);
-      named_sync(1, nht);
-      window_pairs<ALGO, NT>(T, dk, wk, wq, gp, wb, am, fm, hw, nhw, lane);
-      history_dots<ALGO, NT>(nh, T, dk, hk, wk, wq, hf, eG, hdot, hw, nhw, lane);
+      if (decode1) {
+        if (p.rd_dt != DT_F32) named_sync(1, nht);
+        if (hw == 0) {
+          gdn_gates(nh, T, false, hf, hscal, wg, gp, eG, es, lane);
+        } else {
+          decode_dots(nh, dk, hkraw, p.rk_dt, wk, wq, hdot, am, fm, lane);
+        }
+      } else {
+        named_sync(1, nht);
+        if (hw == 0) gdn_gates(nh, T, false, hf, hscal, wg, gp, eG, es, lane);
+        named_sync(1, nht);
+        window_pairs<ALGO, NT>(T, dk, wk, wq, gp, wb, am, fm, hw, nhw, lane);
+        history_dots<ALGO, NT>(nh, T, dk, hk, wk, wq, hf, eG, hdot, hw, nhw, lane);
+      }
       named_sync(1, nht);
       // history correction of every column: hc[v][col] = sum_m H[m][v] d_m[col]
       // (hc reuses the landing zone of the keys, widened above)
@@ -453,12 +530,13 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
 #pragma unroll
         for (int vv = 0; vv < NV; ++vv) y[vv] = 0.f;
         for (int m = 0; m < nh; ++m) {
-          const float dm = hd[m * dv + col];
+          const float dm = decode1 ? hd[m * dv + col] * hf[m] : hd[m * dv + col];
 #pragma unroll
           for (int vv = 0; vv < NV; ++vv) y[vv] = fmaf(hdot[m * NV + vv], dm, y[vv]);
         }
+        const float f = decode1 ? eG[0] : 1.f;
 #pragma unroll
-        for (int vv = 0; vv < NV; ++vv) hc[vv * dv + col] = y[vv];
+        for (int vv = 0; vv < NV; ++vv) hc[vv * dv + col] = f * y[vv];
       }
     }
   } else {
