@@ -249,6 +249,42 @@ __device__ __forceinline__ void history_dots(int nh, int T, int dk, const float*
   }
 }
 
+// Decode row order: with fmask holding one bit per request row (set for a row
+// that folds; kWarps words, row = 32 word + bit) and F folding rows, the
+// position-y CTA takes row y, except that the i-th non-folding row in front of
+// F and the i-th folding row at or behind F trade places. Uniform over the CTA.
+__device__ __forceinline__ int nth_row(const unsigned* fmask, int k, bool folding) {
+  for (int w = 0; w < kWarps; ++w) {
+    unsigned m = folding ? fmask[w] : ~fmask[w];
+    const int n = __popc(m);
+    if (k < n) {
+      for (; k > 0; --k) m &= m - 1u;
+      return w * 32 + __ffs(m) - 1;
+    }
+    k -= n;
+  }
+  return 0;  // not reached: k is below the count it is taken from
+}
+
+__device__ __forceinline__ int folding_below(const unsigned* fmask, int row) {
+  int n = 0;
+  for (int w = 0; w < (row >> 5); ++w) n += __popc(fmask[w]);
+  if (row & 31) n += __popc(fmask[row >> 5] & ((1u << (row & 31)) - 1u));
+  return n;
+}
+
+__device__ __forceinline__ int swap_rank(const unsigned* fmask, int y) {
+  int F = 0;
+  for (int w = 0; w < kWarps; ++w) F += __popc(fmask[w]);
+  const bool fy = (fmask[y >> 5] >> (y & 31)) & 1u;
+  if (y < F && !fy) {
+    // the (y - folding_below(y))-th non-folding row in front of F
+    return nth_row(fmask, folding_below(fmask, F) + (y - folding_below(fmask, y)), true);
+  }
+  if (y >= F && fy) return nth_row(fmask, folding_below(fmask, y) - folding_below(fmask, F), false);
+  return y;
+}
+
 // Narrow windows keep four CTAs per SM (at most 128 registers per thread);
 // wide verify windows trade occupancy for their larger accumulator tiles.
 template <int ALGO, typename ST, int NT>
@@ -298,74 +334,16 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   const bool f32in = p.in_dt == DT_F32;
   const uint32_t qrow = (uint32_t)(dk * s_in), vrow = (uint32_t)(dv * s_in);
 
-  // ---- row order. A folding row's CTAs live several times longer than the
-  //      others; started last they would set the end of the launch. For
-  //      decode (about one row in L folds) with up to kThreads rows, every CTA
-  //      ranks the rows the same way (folding rows first, rows without a slot
-  //      last, stable) and takes the blockIdx.y-th; its own slot and cursor
-  //      come out of the same loads. (Wider verify windows fold a large share
-  //      of their rows, and the ranking's extra latency does not pay there.)
-  int r = blockIdx.y, s, c = 0;
-  bool have_c = false;
-  if (NT == 1 && p.B <= kThreads) {
-    int* order = reinterpret_cast<int*>(smem + p.sm.ring);  // the ring is unused yet
-    int* rslot = order + kThreads;
-    int* rcur = rslot + kThreads;
-    int* wcount = rcur + kThreads;  // [kWarps][3]
-    int key = 3, sv = -1, cv = 0;
-    if (tid < p.B) {
-      sv = p.slot[tid];
-      key = 2;
-      if (sv >= 0 && sv < p.n_slots) {
-        cv = p.cursor[sv];
-        const bool fr = (p.force != nullptr && p.force[tid] != 0) || (cv + T > L);
-        key = fr ? 0 : 1;
-      }
-      rslot[tid] = sv;
-      rcur[tid] = cv;
-    }
-    unsigned below = 0, cnt[3];
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      const unsigned m = __ballot_sync(kFull, key == k);
-      cnt[k] = __popc(m);
-      if (key == k) below = __popc(m & ((1u << lane) - 1u));
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int k = 0; k < 3; ++k) wcount[warp * 3 + k] = (int)cnt[k];
-    }
-    __syncthreads();
-    if (key < 3) {
-      int rank = (int)below;
-      for (int k = 0; k < key; ++k) {
-        for (int w2 = 0; w2 < kWarps; ++w2) rank += wcount[w2 * 3 + k];
-      }
-      for (int w2 = 0; w2 < warp; ++w2) rank += wcount[w2 * 3 + key];
-      order[rank] = tid;
-    }
-    __syncthreads();
-    r = order[blockIdx.y];
-    s = rslot[r];
-    c = rcur[r];
-    have_c = true;
-    __syncthreads();  // the ring's first chunks land over these arrays
-  } else {
-    s = p.slot[r];
-  }
-  const size_t tok0 = (size_t)r * T;
-
-  // ---- 0. bulk async copies; one thread issues every copy of a barrier after
-  //         registering its byte count.
-  if (tid == 0) {
-    mbar_init(&mbar[kMbarWin], 1);
-    mbar_init(&mbar[kMbarHist], 1);
-    TilePipe<ST>::init_full(mbar);
-    fence_mbar_init();
+  // ---- copies of one request row: the window rows (they need only the row),
+  //      the first tile chunks of a slot, the n history records of a slot
+  auto tile_of = [&](int slot) {
+    return static_cast<ST*>(p.state) + ((size_t)slot * HV + h) * dk * dv;
+  };
+  auto issue_window = [&](int row) {
     mbar_expect_tx(&mbar[kMbarWin],
                    T * (2 * qrow + vrow) + (ALGO == ALGO_KDA ? (uint32_t)(T * dk * 4) : 0u));
     for (int i = 0; i < T; ++i) {
-      const size_t tok = tok0 + i;
+      const size_t tok = (size_t)row * T + i;
       const size_t qoff = ((tok * HK + kh) * dk) * s_in;
       const size_t voff = ((tok * HV + h) * dv) * s_in;
       bulk_g2s(f32in ? static_cast<void*>(wq + i * dk) : wraw + i * qrow,
@@ -378,6 +356,60 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
         bulk_g2s(wg + i * dk, p.g + (tok * HV + h) * dk, (uint32_t)(dk * 4), &mbar[kMbarWin]);
       }
     }
+  };
+  auto issue_hist = [&](int slot, int n) {
+    const size_t sh = (size_t)slot * HV + h;
+    void* kdst = (ALGO == ALGO_KDA && p.rk_dt == DT_F32) ? static_cast<void*>(hk) : hkraw;
+    issue_history<ALGO>(n, dk, dv, p.ring_k, sh * L * dk, p.rk_dt, kdst, p.ring_d, sh * L * dv,
+                        p.rd_dt, p.rd_dt == DT_F32 ? static_cast<void*>(hd) : hdraw, p.ring_g,
+                        sh * L * (ALGO == ALGO_GDN ? 1 : dk), hg, &mbar[kMbarHist]);
+  };
+  // ---- row order. A folding row's CTAs live several times longer than the
+  //      others; started last they would set the end of the launch. For
+  //      decode (about one row in L folds) with up to kThreads rows, every CTA
+  //      computes the same order from one load of every row's slot, cursor
+  //      and force flag: each folding row behind position F (the number of
+  //      folding rows) trades places with a non-folding row in front of it,
+  //      the i-th with the i-th, and every other row keeps its place. Its own
+  //      slot and cursor come out of the same loads. (Wider verify windows
+  //      fold a large share of their rows, and the ranking's extra latency
+  //      does not pay there.)
+  const int y = blockIdx.y;
+  int r = y, s, c = 0;
+  bool have_c = false;
+  if (NT == 1 && p.B <= kThreads) {
+    int2* rsc = reinterpret_cast<int2*>(smem + p.sm.rank);  // [kThreads] (slot, cursor)
+    unsigned* fmask = reinterpret_cast<unsigned*>(rsc + kThreads);  // [kWarps] folding rows
+    int sv = -1, cv = 0, fv = 0;
+    if (tid < p.B) {
+      sv = p.slot[tid];
+      if (p.force != nullptr) fv = p.force[tid];
+    }
+    const bool sv_ok = sv >= 0 && sv < p.n_slots;
+    if (sv_ok) cv = p.cursor[sv];
+    const bool fr = sv_ok && (fv != 0 || cv + T > L);
+    if (tid < p.B) rsc[tid] = make_int2(sv, cv);
+    const unsigned m = __ballot_sync(kFull, fr);
+    if (lane == 0) fmask[warp] = m;
+    __syncthreads();
+    r = swap_rank(fmask, y);
+    const int2 e = rsc[r];
+    s = e.x;
+    c = e.y;
+    have_c = true;
+  } else {
+    s = p.slot[r];
+  }
+  const size_t tok0 = (size_t)r * T;
+
+  // ---- 0. bulk async copies; one thread issues every copy of a barrier after
+  //         registering its byte count.
+  if (tid == 0) {
+    mbar_init(&mbar[kMbarWin], 1);
+    mbar_init(&mbar[kMbarHist], 1);
+    TilePipe<ST>::init_full(mbar);
+    fence_mbar_init();
+    issue_window(r);
   }
   float wbeta = 0.f, wgate = 0.f;
   if (tid < T) {
@@ -392,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
     }
     return;
   }
-  ST* gtile = static_cast<ST*>(p.state) + ((size_t)s * HV + h) * dk * dv;
+  ST* gtile = tile_of(s);
   const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv);
   if (tid == 0) pipe.prime();
   if (!have_c) c = p.cursor[s];
@@ -415,12 +447,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   const size_t gbase = ((size_t)s * HV + h) * L * (ALGO == ALGO_GDN ? 1 : dk);
   if (tid == 0) {
     pipe.init_empty(sw);
-    if (nh > 0) {
-      void* kdst = (ALGO == ALGO_KDA && p.rk_dt == DT_F32) ? static_cast<void*>(hk) : hkraw;
-      issue_history<ALGO>(nh, dk, dv, p.ring_k, kbase, p.rk_dt, kdst, p.ring_d, dbase, p.rd_dt,
-                          p.rd_dt == DT_F32 ? static_cast<void*>(hd) : hdraw, p.ring_g, gbase,
-                          hg, &mbar[kMbarHist]);
-    }
+    if (nh > 0) issue_hist(s, nh);
   }
   // GDN history gates: loaded now, stored once the window has landed
   float hgate = 0.f;

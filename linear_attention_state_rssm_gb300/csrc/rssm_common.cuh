@@ -88,6 +88,7 @@ struct ReplaySmem {
   uint32_t hf;     // [L]      GDN: raw gates -> exp(suffix sums)
   uint32_t hdot;   // [L][2NT] history dot coefficients
   uint32_t red;    // [row groups][2NT][dv] partial column sums (on the ring when it fits)
+  uint32_t rank;   // decode row order: [kThreads] (slot, cursor), [kWarps] fold masks
   uint32_t total;
 };
 
@@ -174,6 +175,8 @@ struct FoldParams {
 
 
 
+constexpr uint32_t kRankBytes = 8u * kThreads + 4u * kWarps;
+
 // Shared memory plan of the replay kernel for a window of T <= NT tokens and a
 // ring of L records.
 __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, int NT, int T,
@@ -219,6 +222,14 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
   } else {
     m.red = off;
     off = align16(off + red_bytes);
+  }
+  // The decode row order sits in the fp32 history keys: nothing writes there
+  // before the CTA barrier that follows the copies (16-bit ring keys land in
+  // hkraw), unless KDA fp32 keys land in place.
+  m.rank = m.hk;
+  if (NT == 1 && ((kda && rk_dt == DT_F32) || 4u * round4(L) * dk < kRankBytes)) {
+    m.rank = off;
+    off = align16(off + kRankBytes);
   }
   m.total = off;
   return m;
