@@ -121,22 +121,38 @@ def sources_hash():
 
 # ------------------------------------------------------------------ clocks
 class Clocks:
+    """nvidia-smi samples of the SM clock and throttle reasons while the GPU is
+    loaded. The sampler is started (and its first, idle sample read) before
+    the timed region; `keep_loaded` then repeats the timed step, untimed,
+    until the sampler has covered at least `min_s` of load."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, index):
-        self.index, self.proc = index, None
+        self.index, self.proc, self.t0 = index, None, None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc.stdout.readline()  # the sampler runs; this sample predates the load
         except OSError:
             self.proc = None
+        self.t0 = time.perf_counter()
         return self
+
+    def keep_loaded(self, step, min_s=0.5):
+        """Run `step()` (untimed) until min_s has passed since the sampler's
+        first sample; returns how many steps ran."""
+        n = 0
+        while self.proc is not None and time.perf_counter() - self.t0 < min_s:
+            step()
+            n += 1
+        return n
 
     def __exit__(self, *exc):
         self.out = ""
@@ -285,10 +301,17 @@ def run_ours(args, rank, world, local_rank):
             graph.replay()
         e1.record()
         torch.cuda.synchronize()
+
+        def pad_step():
+            for _ in range(16):
+                graph.replay()
+            torch.cuda.synchronize()
+        pad = 16 * clk.keep_loaded(pad_step)
     if world > 1:
         dist.barrier()
     t_ms = e0.elapsed_time(e1)
     cur, bytes_timed = host_advance(cur, args.steps)
+    cur, _ = host_advance(cur, pad)  # untimed steps that kept the clock sampler loaded
     t_max = max_over_ranks(t_ms, world, dev)
     value = job_throughput(B_live * T * nl * args.steps, world, t_max / 1e3)
     ms_per_step = t_max / args.steps
