@@ -129,15 +129,16 @@ class ReplayOracle:
         """[R, HK, dk] -> [R, HV, dk]: value head h uses key head h // G."""
         return np.repeat(x, self.G, axis=1)
 
-    def _decide(self, slots, T, force):
+    def _decide(self, slots, lens, force):
         B = len(slots)
         fold = np.zeros(B, dtype=bool)
         base = np.zeros(B, dtype=np.int64)
         for r in range(B):
             s = int(slots[r])
-            if s < 0:
+            if s < 0 or lens[r] == 0:
                 continue
-            f, b = ring.fold_decision(int(self.cursor[s]), T, self.L, bool(force[r]))
+            f, b = ring.fold_decision(int(self.cursor[s]), int(lens[r]), self.L,
+                                      bool(force[r]))
             fold[r], base[r] = f, b
         return fold, base
 
@@ -159,15 +160,38 @@ class ReplayOracle:
         Returns (o, fold): o [B*T, HV, dv] with NaN on null rows; fold [B]
         int8, 1 where the window folded, 0 where not, -1 on null rows.
         """
+        B = len(slots)
+        if not 1 <= T <= self.L:
+            raise ValueError("window must satisfy 1 <= T <= L")
+        starts = np.arange(B, dtype=np.int64) * T
+        lens = np.full(B, T, dtype=np.int64)
+        return self._window(layer, slots, inp, starts, lens, B * T, T, force)
+
+    def window_ragged(self, layer, slots, inp, cu_seqlens, force=None):
+        """Windows of different lengths packed into one token list: row r's
+        tokens are [cu_seqlens[r], cu_seqlens[r+1]) (LightLLM PR #1690, commit
+        messages: request windows read from cu_seqlens over [tokens, heads,
+        dim] inputs; SGLang fork PR jianc99/sglang#2, "Related upstream work":
+        verify on packed ragged tokens). A row with no tokens is idle this
+        step, like a null row: no fold, no output, no record.
+
+        Returns (o, fold) as ``window`` does, o over the packed tokens.
+        """
+        cu = np.asarray(cu_seqlens, dtype=np.int64)
+        lens = np.diff(cu)
+        if cu.shape[0] != len(slots) + 1 or np.any(lens < 0) or np.any(lens > self.L):
+            raise ValueError("cu_seqlens must be non-decreasing with windows of at most L")
+        return self._window(layer, slots, inp, cu[:-1].copy(), lens, int(cu[-1]), None, force)
+
+    def _window(self, layer, slots, inp, starts, lens, n_tok, T, force):
         slots = np.asarray(slots, dtype=np.int64)
         B = slots.shape[0]
         force = np.zeros(B, np.uint8) if force is None else np.asarray(force)
-        if not 1 <= T <= self.L:
-            raise ValueError("window must satisfy 1 <= T <= L")
-        fold, base = self._decide(slots, T, force)
-        live = np.nonzero(slots >= 0)[0]
-        o = np.full((B * T, self.HV, self.dv), np.nan)
-        flags = np.where(slots >= 0, fold.astype(np.int8), np.int8(-1))
+        fold, base = self._decide(slots, lens, force)
+        active = (slots >= 0) & (lens > 0)
+        live = np.nonzero(active)[0]
+        o = np.full((n_tok, self.HV, self.dv), np.nan)
+        flags = np.where(active, fold.astype(np.int8), np.int8(-1))
         if live.size:
             sl = slots[live]
             folded = sl[fold[live]]
@@ -178,52 +202,55 @@ class ReplayOracle:
             with np.errstate(all="ignore"):
                 for c0 in range(0, live.size, self._chunk):
                     rows = live[c0:c0 + self._chunk]
-                    final[c0:c0 + rows.size] = self._run_window(layer, rows, slots, inp, T,
-                                                                base, o)
+                    final[c0:c0 + rows.size] = self._run_window(layer, rows, slots, inp, starts,
+                                                                lens, base, o)
         else:
             final = None
-        self._pending[layer] = {"slots": slots.copy(), "inp": inp, "T": T,
-                                "force": np.asarray(force).copy(), "base": base,
+        self._pending[layer] = {"slots": slots.copy(), "inp": inp, "T": T, "starts": starts,
+                                "lens": lens, "force": np.asarray(force).copy(), "base": base,
                                 "final": final}
         return o, flags
 
-    def _run_window(self, layer, rows, slots, inp, T, base, o):
-        """Run the T window tokens of some live rows; record outputs and ring
-        records; return the rows' states after the window."""
+    def _run_window(self, layer, rows, slots, inp, starts, lens, base, o):
+        """Run the window tokens of some live rows; record outputs and ring
+        records; return the rows' states after their windows."""
         sl = slots[rows]
         S = self.S[layer, sl]                     # fancy indexing: a copy
-        for i in range(T):
-            idx = rows * T + i
+        for i in range(int(lens[rows].max())):
+            on = np.nonzero(lens[rows] > i)[0]   # rows whose window has token i
+            r_i, s_i = rows[on], sl[on]
+            idx = starts[r_i] + i
             q, k, v, beta, g = self._token_inputs(inp, idx)
-            S, d, oi = token_step(S, q, k, v, beta, g, self.scale, self.algo)
+            S[on], d, oi = token_step(S[on], q, k, v, beta, g, self.scale, self.algo)
             o[idx] = oi
-            pos = base[rows] + i
-            self.ring_k[layer, sl, :, pos] = inp["k"][idx]
-            self.ring_d[layer, sl, :, pos] = d
-            self.ring_g[layer, sl, :, pos] = inp["g"][idx]
-            self.ring_v[layer, sl, :, pos] = v
-            self.ring_beta[layer, sl, :, pos] = beta
-            self.written[layer, sl, pos] = True
+            pos = base[r_i] + i
+            self.ring_k[layer, s_i, :, pos] = inp["k"][idx]
+            self.ring_d[layer, s_i, :, pos] = d
+            self.ring_g[layer, s_i, :, pos] = inp["g"][idx]
+            self.ring_v[layer, s_i, :, pos] = v
+            self.ring_beta[layer, s_i, :, pos] = beta
+            self.written[layer, s_i, pos] = True
         return S
 
     def _accept(self, layer, accept):
         """Commit ``accept[r]`` tokens of the pending window of one layer."""
         pend = self._pending.pop(layer)
-        slots, inp, T, final = pend["slots"], pend["inp"], pend["T"], pend["final"]
-        live = np.nonzero(slots >= 0)[0]
+        slots, inp, final = pend["slots"], pend["inp"], pend["final"]
+        starts, lens = pend["starts"], pend["lens"]
+        live = np.nonzero((slots >= 0) & (lens > 0))[0]
         a_live = np.asarray(accept)[live]
         for c0 in range(0, live.size, self._chunk):
             rows = live[c0:c0 + self._chunk]
             a = a_live[c0:c0 + rows.size]
             sl = slots[rows]
             S = self.S[layer, sl]                 # fancy indexing: a copy
-            full = a == T                         # whole window accepted: final state
+            full = a == lens[rows]                # whole window accepted: final state
             S[full] = final[c0:c0 + rows.size][full]
-            for i in range(T):
+            for i in range(int(lens[rows].max())):
                 keep = np.nonzero(~full & (a > i))[0]   # rows that accept token i
                 if keep.size == 0:
                     break
-                idx = rows[keep] * T + i
+                idx = starts[rows[keep]] + i
                 q, k, v, beta, g = self._token_inputs(inp, idx)
                 S[keep], _, _ = token_step(S[keep], q, k, v, beta, g, self.scale,
                                            self.algo)
@@ -248,22 +275,37 @@ class ReplayOracle:
 
     def commit(self, slots, accept, T, force=None, mode=ring.LAZY):
         """Commit the pending verify windows of every layer, then the cursor."""
+        for layer in sorted(self._pending):
+            if self._pending[layer]["T"] != T:
+                raise ValueError("commit T differs from the verified window")
+        B = len(slots)
+        self._commit(slots, accept, np.full(B, T, dtype=np.int64), force, mode)
+
+    def commit_ragged(self, slots, accept, cu_seqlens, force=None, mode=ring.LAZY):
+        """Commit pending ragged windows: row r accepts accept[r] of its
+        cu_seqlens[r+1] - cu_seqlens[r] tokens; an idle row (no tokens) keeps
+        its cursor and checkpoint."""
+        lens = np.diff(np.asarray(cu_seqlens, dtype=np.int64))
+        for layer in sorted(self._pending):
+            if not np.array_equal(self._pending[layer]["lens"], lens):
+                raise ValueError("commit windows differ from the verified ones")
+        self._commit(slots, accept, lens, force, mode)
+
+    def _commit(self, slots, accept, lens, force, mode):
         slots = np.asarray(slots, dtype=np.int64)
         B = slots.shape[0]
         force = np.zeros(B, np.uint8) if force is None else np.asarray(force)
         accept = np.asarray(accept, dtype=np.int64)
         for layer in sorted(self._pending):
-            if self._pending[layer]["T"] != T:
-                raise ValueError("commit T differs from the verified window")
             self._accept(layer, accept)
         for r, s in enumerate(slots):
-            if s < 0:
+            if s < 0 or lens[r] == 0:
                 continue
             c = int(self.cursor[s])
             if mode == ring.FOLD_EVERY:
                 self._checkpoint(slice(None), s)
-            self.cursor[s] = ring.cursor_after_commit(c, T, self.L, bool(force[r]),
-                                                      int(accept[r]), mode)
+            self.cursor[s] = ring.cursor_after_commit(c, int(lens[r]), self.L,
+                                                      bool(force[r]), int(accept[r]), mode)
 
     def fold(self, slots):
         """Explicit fold: checkpoint <- committed state, cursor <- 0."""
