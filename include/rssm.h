@@ -82,7 +82,8 @@ enum {
   RSSM_DEVERR_SLOT = 1u,     /* slot index >= n_slots                 */
   RSSM_DEVERR_CURSOR = 2u,   /* cursor outside [0, L]                 */
   RSSM_DEVERR_ACCEPT = 4u,   /* accepted length outside [0, T]        */
-  RSSM_DEVERR_TIMEOUT = 8u   /* a bounded wait on a tile copy ran out */
+  RSSM_DEVERR_TIMEOUT = 8u,  /* a bounded wait on a tile copy ran out */
+  RSSM_DEVERR_SEQLEN = 16u   /* ragged window offsets out of order or wider than max_T */
 };
 
 /*
@@ -184,6 +185,33 @@ rssm_status rssm_verify(rssm_handle *h, int32_t layer, const void *q,
                         uint8_t *fold_out, void *stream);
 
 /*
+ * Ragged speculative verify of one layer: windows of different lengths packed
+ * into one token list (LightLLM PR #1690, commit messages: request windows
+ * read from cu_seqlens over [tokens, heads, dim] inputs; SGLang fork PR
+ * jianc99/sglang#2, "Related upstream work": verify on packed ragged tokens).
+ * cu_seqlens is a device int32[B + 1]; row r's window is tokens
+ * [cu_seqlens[r], cu_seqlens[r+1]) of q, k [N, HK, dk], v [N, HV, dv],
+ * beta [N, HV], g [N, HV] (GDN) or [N, HV, dk] (KDA) and o [N, HV, dv], with
+ * N = cu_seqlens[B]. Per row the rules of rssm_verify hold with T_r =
+ * cu_seqlens[r+1] - cu_seqlens[r] in place of T (fold = force[r] ||
+ * c + T_r > L). A row with T_r == 0 is idle: nothing is read or written for
+ * it, fold_out[r] is left as it is. max_T (1 <= max_T <= the configuration's
+ * max_T) bounds every T_r and picks the kernel width; a row whose offsets
+ * are negative, decreasing or wider than max_T sets RSSM_DEVERR_SEQLEN and is
+ * skipped. cu_seqlens must be 4-byte aligned; other alignment and error
+ * rules as rssm_verify. Per-row forced folds (force) cover a caller that
+ * must hold the exact state at its own block boundaries (vLLM PR #64699,
+ * commit messages on align mode).
+ */
+rssm_status rssm_verify_ragged(rssm_handle *h, int32_t layer, const void *q,
+                               const void *k, const void *v,
+                               const float *beta, const float *g,
+                               const int32_t *cu_seqlens,
+                               const int32_t *slot, const uint8_t *force,
+                               int32_t B, int32_t max_T, void *o,
+                               uint8_t *fold_out, void *stream);
+
+/*
  * Native fused-recurrent decode of one layer, the path ReplaySSM replaces
  * (LightLLM PR #1690, PR description: the native mode writes the recurrent
  * state back every step). It is here as a comparison point: for each row r
@@ -209,6 +237,17 @@ rssm_status rssm_native_decode(rssm_handle *h, int32_t layer, const void *q,
 rssm_status rssm_commit(rssm_handle *h, const int32_t *slot,
                         const uint8_t *force, const int32_t *accept_len,
                         int32_t B, int32_t T, void *stream);
+
+/*
+ * Commit the last ragged verify of every layer: as rssm_commit with T_r =
+ * cu_seqlens[r+1] - cu_seqlens[r] per row and accept_len[r] in [0, T_r];
+ * slot, force, cu_seqlens and max_T must equal the verify's. Idle rows
+ * (T_r == 0) keep their cursor and checkpoint.
+ */
+rssm_status rssm_commit_ragged(rssm_handle *h, const int32_t *slot,
+                               const uint8_t *force, const int32_t *accept_len,
+                               const int32_t *cu_seqlens, int32_t B,
+                               int32_t max_T, void *stream);
 
 /* Explicit fold of every layer's history into its checkpoint, then cursor <- 0
  * (LightLLM PR #1690: materialise the canonical state). */

@@ -19,11 +19,12 @@ STATUS_NAMES = {0: "RSSM_OK", 1: "RSSM_ERR_INVALID_ARG", 2: "RSSM_ERR_UNSUPPORTE
 ALGO = {"gdn": 0, "kda": 1}
 DTYPE = {"f32": 0, "bf16": 1, "f16": 2}
 COMMIT = {"lazy": 0, "fold_every": 1}
-DEVERR = {"slot": 1, "cursor": 2, "accept": 4, "timeout": 8}
+DEVERR = {"slot": 1, "cursor": 2, "accept": 4, "timeout": 8, "seqlen": 16}
 
 # Every entry point declared in include/rssm.h.
 SYMBOLS = ("rssm_required_bytes", "rssm_alloc", "rssm_free", "rssm_decode", "rssm_verify",
-           "rssm_native_decode", "rssm_commit", "rssm_fold", "rssm_reset_slots",
+           "rssm_verify_ragged", "rssm_native_decode", "rssm_commit", "rssm_commit_ragged",
+           "rssm_fold", "rssm_reset_slots",
            "rssm_get_device_error", "rssm_status_string", "rssm_version")
 
 
@@ -77,8 +78,11 @@ def load() -> ctypes.CDLL:
         "rssm_free": ([_P], None),
         "rssm_decode": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _P], _I),
         "rssm_verify": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P], _I),
+        "rssm_verify_ragged": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P],
+                               _I),
         "rssm_native_decode": ([_P, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P], _I),
         "rssm_commit": ([_P, _P, _P, _P, _I, _I, _P], _I),
+        "rssm_commit_ragged": ([_P, _P, _P, _P, _P, _I, _I, _P], _I),
         "rssm_fold": ([_P, _P, _I, _P], _I),
         "rssm_reset_slots": ([_P, _P, _I, _P], _I),
         "rssm_get_device_error": ([_P, ctypes.POINTER(ctypes.c_uint32), _I, _P], _I),
@@ -158,6 +162,14 @@ def rssm_verify(handle, layer, q, k, v, beta, g, slot, force, B, T, o, fold_out,
                               _stream(stream)), "rssm_verify")
 
 
+def rssm_verify_ragged(handle, layer, q, k, v, beta, g, cu_seqlens, slot, force, B, max_T, o,
+                       fold_out, stream=None):
+    _check(load().rssm_verify_ragged(handle, layer, _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                     _ptr(g), _ptr(cu_seqlens), _ptr(slot), _ptr(force), B,
+                                     max_T, _ptr(o), _ptr(fold_out), _stream(stream)),
+           "rssm_verify_ragged")
+
+
 def rssm_native_decode(handle, layer, q, k, v, beta, g, slot, B, o, stream=None):
     _check(load().rssm_native_decode(handle, layer, _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
                                      _ptr(g), _ptr(slot), B, _ptr(o), _stream(stream)),
@@ -167,6 +179,12 @@ def rssm_native_decode(handle, layer, q, k, v, beta, g, slot, B, o, stream=None)
 def rssm_commit(handle, slot, force, accept_len, B, T, stream=None):
     _check(load().rssm_commit(handle, _ptr(slot), _ptr(force), _ptr(accept_len), B, T,
                               _stream(stream)), "rssm_commit")
+
+
+def rssm_commit_ragged(handle, slot, force, accept_len, cu_seqlens, B, max_T, stream=None):
+    _check(load().rssm_commit_ragged(handle, _ptr(slot), _ptr(force), _ptr(accept_len),
+                                     _ptr(cu_seqlens), B, max_T, _stream(stream)),
+           "rssm_commit_ragged")
 
 
 def rssm_fold(handle, slot, B, stream=None):

@@ -38,12 +38,19 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
   }
   int n = c;
   if (p.mode == FOLD_COMMIT) {
+    size_t tok0;
+    int T;
+    if (!row_window(p.cu, r, p.T, tok0, T)) {
+      if (reporter) atomicOr(p.err, DEVERR_SEQLEN);
+      return;
+    }
+    if (T == 0) return;  // an idle row keeps its checkpoint
     const int a = p.accept[r];
-    if (a < 0 || a > p.T) {
+    if (a < 0 || a > T) {
       if (reporter) atomicOr(p.err, DEVERR_ACCEPT);
       return;
     }
-    const bool fold = (p.force != nullptr && p.force[r] != 0) || (c + p.T > L);
+    const bool fold = (p.force != nullptr && p.force[r] != 0) || (c + T > L);
     n = (fold ? 0 : c) + a;
   }
   if (n == 0) return;
@@ -111,8 +118,8 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
 }
 
 __global__ void cursor_kernel(int32_t* cursor, const int32_t* slot, const uint8_t* force,
-                              const int32_t* accept, int B, int T, int L, int n_slots, int mode,
-                              uint32_t* err) {
+                              const int32_t* accept, const int32_t* cu, int B, int maxT, int L,
+                              int n_slots, int mode, uint32_t* err) {
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= B) return;
   const int s = slot[r];
@@ -136,6 +143,13 @@ __global__ void cursor_kernel(int32_t* cursor, const int32_t* slot, const uint8_
     cursor[s] = (fold ? 0 : c) + 1;
     return;
   }
+  size_t tok0;
+  int T;
+  if (!row_window(cu, r, maxT, tok0, T)) {
+    atomicOr(err, DEVERR_SEQLEN);
+    return;
+  }
+  if (T == 0) return;  // an idle row keeps its cursor
   const int a = accept[r];
   if (a < 0 || a > T) {
     atomicOr(err, DEVERR_ACCEPT);
@@ -185,12 +199,12 @@ cudaError_t fold_prepare(int algo, int state_dt, int max_smem) {
 }
 
 cudaError_t cursor_launch(int32_t* cursor, const int32_t* slot, const uint8_t* force,
-                          const int32_t* accept, int B, int T, int L, int n_slots, int mode,
-                          uint32_t* err, cudaStream_t st) {
+                          const int32_t* accept, const int32_t* cu, int B, int T, int L,
+                          int n_slots, int mode, uint32_t* err, cudaStream_t st) {
   const int threads = 128;
   const int blocks = (B + threads - 1) / threads;
-  cursor_kernel<<<blocks, threads, 0, st>>>(cursor, slot, force, accept, B, T, L, n_slots, mode,
-                                            err);
+  cursor_kernel<<<blocks, threads, 0, st>>>(cursor, slot, force, accept, cu, B, T, L, n_slots,
+                                            mode, err);
   return cudaGetLastError();
 }
 

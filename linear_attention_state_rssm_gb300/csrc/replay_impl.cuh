@@ -287,7 +287,9 @@ __device__ __forceinline__ int swap_rank(const unsigned* fmask, int y) {
 
 // Narrow windows keep four CTAs per SM (at most 128 registers per thread);
 // wide verify windows trade occupancy for their larger accumulator tiles.
-template <int ALGO, typename ST, int NT>
+// RAGGED: windows of different lengths from p.cu (verify widths only); the
+// uniform kernels keep the window length a launch constant.
+template <int ALGO, typename ST, int NT, bool RAGGED>
 __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const ReplayParams p) {
   constexpr int NV = 2 * NT;             // mat-vec vectors: k_i at [0, NT), q_i at [NT, 2NT)
   constexpr int CW = quad_width(NT);     // value columns per lane in the tile stream
@@ -296,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
 
   const int h = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int T = p.T, dk = p.dk, dv = p.dv, L = p.L, HV = p.HV, HK = p.HK;
+  const int dk = p.dk, dv = p.dv, L = p.L, HV = p.HV, HK = p.HK;
+  int T = p.T;  // this row's window (RAGGED: set once the row is known)
   const int kh = h / p.G;
 
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + p.sm.mbar);
@@ -339,11 +342,11 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   auto tile_of = [&](int slot) {
     return static_cast<ST*>(p.state) + ((size_t)slot * HV + h) * dk * dv;
   };
-  auto issue_window = [&](int row) {
+  auto issue_window = [&](size_t t0) {
     mbar_expect_tx(&mbar[kMbarWin],
                    T * (2 * qrow + vrow) + (ALGO == ALGO_KDA ? (uint32_t)(T * dk * 4) : 0u));
     for (int i = 0; i < T; ++i) {
-      const size_t tok = (size_t)row * T + i;
+      const size_t tok = t0 + i;
       const size_t qoff = ((tok * HK + kh) * dk) * s_in;
       const size_t voff = ((tok * HV + h) * dv) * s_in;
       bulk_g2s(f32in ? static_cast<void*>(wq + i * dk) : wraw + i * qrow,
@@ -377,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   const int y = blockIdx.y;
   int r = y, s, c = 0;
   bool have_c = false;
-  if (NT == 1 && p.B <= kThreads) {
+  if (NT == 1 && !RAGGED && p.B <= kThreads) {
     int2* rsc = reinterpret_cast<int2*>(smem + p.sm.rank);  // [kThreads] (slot, cursor)
     unsigned* fmask = reinterpret_cast<unsigned*>(rsc + kThreads);  // [kWarps] folding rows
     int sv = -1, cv = 0, fv = 0;
@@ -400,7 +403,14 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
   } else {
     s = p.slot[r];
   }
-  const size_t tok0 = (size_t)r * T;
+  size_t tok0 = (size_t)r * T;
+  if (RAGGED) {
+    if (!row_window(p.cu, r, p.T, tok0, T)) {
+      if (tid == 0 && h == 0) atomicOr(p.err, DEVERR_SEQLEN);
+      return;
+    }
+    if (T == 0) return;  // no tokens for this row in this step: left as it is
+  }
 
   // ---- 0. bulk async copies; one thread issues every copy of a barrier after
   //         registering its byte count.
@@ -409,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
     mbar_init(&mbar[kMbarHist], 1);
     TilePipe<ST>::init_full(mbar);
     fence_mbar_init();
-    issue_window(r);
+    issue_window(tok0);
   }
   float wbeta = 0.f, wgate = 0.f;
   if (tid < T) {

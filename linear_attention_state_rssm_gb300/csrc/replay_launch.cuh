@@ -9,19 +9,19 @@
 namespace rssm {
 
 // One CTA per (value head, request row).
-template <int ALGO, typename ST, int NT>
+template <int ALGO, typename ST, int NT, bool RAGGED>
 static cudaError_t replay_launch_one(const ReplayParams& p, cudaStream_t st) {
   const dim3 grid((unsigned)p.HV, (unsigned)p.B, 1);
-  replay_kernel<ALGO, ST, NT><<<grid, kThreads, p.sm.total, st>>>(p);
+  replay_kernel<ALGO, ST, NT, RAGGED><<<grid, kThreads, p.sm.total, st>>>(p);
   return cudaGetLastError();
 }
 
-template <int ALGO, typename ST, int NT>
+template <int ALGO, typename ST, int NT, bool RAGGED>
 static cudaError_t replay_prepare_one(int max_smem) {
-  cudaError_t e = cudaFuncSetAttribute(replay_kernel<ALGO, ST, NT>,
+  cudaError_t e = cudaFuncSetAttribute(replay_kernel<ALGO, ST, NT, RAGGED>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(replay_kernel<ALGO, ST, NT>,
+  return cudaFuncSetAttribute(replay_kernel<ALGO, ST, NT, RAGGED>,
                               cudaFuncAttributePreferredSharedMemoryCarveout, 100);
 }
 
@@ -31,20 +31,42 @@ static cudaError_t replay_prepare_one(int max_smem) {
   namespace rssm {                                                                          \
   cudaError_t NAME##_launch(const ReplayParams& p, int NT, cudaStream_t st) {             \
     switch (NT) {                                                                           \
-      case 1: return replay_launch_one<ALGO, ST, 1>(p, st);                                 \
-      case 2: return replay_launch_one<ALGO, ST, 2>(p, st);                                 \
-      case 4: return replay_launch_one<ALGO, ST, 4>(p, st);                                 \
-      case 8: return replay_launch_one<ALGO, ST, 8>(p, st);                                 \
-      case 16: return replay_launch_one<ALGO, ST, 16>(p, st);                               \
+      case 1: return replay_launch_one<ALGO, ST, 1, false>(p, st);                          \
+      case 2: return replay_launch_one<ALGO, ST, 2, false>(p, st);                          \
+      case 4: return replay_launch_one<ALGO, ST, 4, false>(p, st);                          \
+      case 8: return replay_launch_one<ALGO, ST, 8, false>(p, st);                          \
+      case 16: return replay_launch_one<ALGO, ST, 16, false>(p, st);                        \
       default: return cudaErrorInvalidValue;                                                \
     }                                                                                       \
   }                                                                                         \
   cudaError_t NAME##_prepare(int max_smem) {                                                \
     cudaError_t e;                                                                          \
-    if ((e = replay_prepare_one<ALGO, ST, 1>(max_smem)) != cudaSuccess) return e;           \
-    if ((e = replay_prepare_one<ALGO, ST, 2>(max_smem)) != cudaSuccess) return e;           \
-    if ((e = replay_prepare_one<ALGO, ST, 4>(max_smem)) != cudaSuccess) return e;           \
-    if ((e = replay_prepare_one<ALGO, ST, 8>(max_smem)) != cudaSuccess) return e;           \
-    return replay_prepare_one<ALGO, ST, 16>(max_smem);                                      \
+    if ((e = replay_prepare_one<ALGO, ST, 1, false>(max_smem)) != cudaSuccess) return e;    \
+    if ((e = replay_prepare_one<ALGO, ST, 2, false>(max_smem)) != cudaSuccess) return e;    \
+    if ((e = replay_prepare_one<ALGO, ST, 4, false>(max_smem)) != cudaSuccess) return e;    \
+    if ((e = replay_prepare_one<ALGO, ST, 8, false>(max_smem)) != cudaSuccess) return e;    \
+    return replay_prepare_one<ALGO, ST, 16, false>(max_smem);                               \
+  }                                                                                         \
+  }
+
+// Ragged windows (cu_seqlens): the verify widths 2..16; a ragged launch of
+// windows of at most one token takes width 2.
+#define RSSM_DEFINE_REPLAY_RAGGED(NAME, ALGO, ST)                                           \
+  namespace rssm {                                                                          \
+  cudaError_t NAME##_launch(const ReplayParams& p, int NT, cudaStream_t st) {             \
+    switch (NT) {                                                                           \
+      case 2: return replay_launch_one<ALGO, ST, 2, true>(p, st);                           \
+      case 4: return replay_launch_one<ALGO, ST, 4, true>(p, st);                           \
+      case 8: return replay_launch_one<ALGO, ST, 8, true>(p, st);                           \
+      case 16: return replay_launch_one<ALGO, ST, 16, true>(p, st);                         \
+      default: return cudaErrorInvalidValue;                                                \
+    }                                                                                       \
+  }                                                                                         \
+  cudaError_t NAME##_prepare(int max_smem) {                                                \
+    cudaError_t e;                                                                          \
+    if ((e = replay_prepare_one<ALGO, ST, 2, true>(max_smem)) != cudaSuccess) return e;     \
+    if ((e = replay_prepare_one<ALGO, ST, 4, true>(max_smem)) != cudaSuccess) return e;     \
+    if ((e = replay_prepare_one<ALGO, ST, 8, true>(max_smem)) != cudaSuccess) return e;     \
+    return replay_prepare_one<ALGO, ST, 16, true>(max_smem);                                \
   }                                                                                         \
   }

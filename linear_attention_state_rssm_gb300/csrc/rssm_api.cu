@@ -85,6 +85,14 @@ int state_dt(const rssm_config& c) { return c.state_dtype == RSSM_F32 ? DT_F32 :
 cudaError_t replay_launch(const rssm_config& c, const ReplayParams& p, int NT,
                           cudaStream_t st) {
   const bool f32 = c.state_dtype == RSSM_F32;
+  if (p.cu != nullptr) {
+    if (c.algo == RSSM_ALGO_GDN) {
+      return f32 ? replay_gdn_f32_ragged_launch(p, NT, st)
+                 : replay_gdn_bf16_ragged_launch(p, NT, st);
+    }
+    return f32 ? replay_kda_f32_ragged_launch(p, NT, st)
+               : replay_kda_bf16_ragged_launch(p, NT, st);
+  }
   if (c.algo == RSSM_ALGO_GDN) {
     return f32 ? replay_gdn_f32_launch(p, NT, st) : replay_gdn_bf16_launch(p, NT, st);
   }
@@ -93,16 +101,24 @@ cudaError_t replay_launch(const rssm_config& c, const ReplayParams& p, int NT,
 
 cudaError_t replay_prepare(const rssm_config& c, int max_smem) {
   const bool f32 = c.state_dtype == RSSM_F32;
+  cudaError_t e;
   if (c.algo == RSSM_ALGO_GDN) {
-    return f32 ? replay_gdn_f32_prepare(max_smem) : replay_gdn_bf16_prepare(max_smem);
+    e = f32 ? replay_gdn_f32_prepare(max_smem) : replay_gdn_bf16_prepare(max_smem);
+    if (e != cudaSuccess) return e;
+    return f32 ? replay_gdn_f32_ragged_prepare(max_smem)
+               : replay_gdn_bf16_ragged_prepare(max_smem);
   }
-  return f32 ? replay_kda_f32_prepare(max_smem) : replay_kda_bf16_prepare(max_smem);
+  e = f32 ? replay_kda_f32_prepare(max_smem) : replay_kda_bf16_prepare(max_smem);
+  if (e != cudaSuccess) return e;
+  return f32 ? replay_kda_f32_ragged_prepare(max_smem) : replay_kda_bf16_ragged_prepare(max_smem);
 }
 
-ReplaySmem layout_for(const rssm_config& c, int T) {
-  return replay_layout(c.algo, (int)esize(c.state_dtype), nt_for(T), T, c.L, c.dk, c.dv,
-                       c.in_dtype, c.ring_k_dtype, c.ring_d_dtype);
+ReplaySmem layout_for(const rssm_config& c, int T, int NT) {
+  return replay_layout(c.algo, (int)esize(c.state_dtype), NT, T, c.L, c.dk, c.dv, c.in_dtype,
+                       c.ring_k_dtype, c.ring_d_dtype);
 }
+
+ReplaySmem layout_for(const rssm_config& c, int T) { return layout_for(c, T, nt_for(T)); }
 
 FoldSmem fold_layout_for(const rssm_config& c) {
   return fold_layout(c.algo, (int)esize(c.state_dtype), c.L, c.dk, c.dv, c.ring_k_dtype,
@@ -171,14 +187,16 @@ rssm_status window_params(const rssm_handle* h, int32_t layer, const void* q, co
 rssm_status window(rssm_handle* h, int32_t layer, const void* q, const void* k, const void* v,
                    const float* beta, const float* g, const int32_t* slot,
                    const uint8_t* force, int32_t B, int32_t T, void* o, uint8_t* fold_out,
-                   void* stream) {
+                   void* stream, const int32_t* cu = nullptr) {
   ReplayParams p;
   const rssm_status st = window_params(h, layer, q, k, v, beta, g, slot, force, B, T, o,
                                        fold_out, &p);
   if (st != RSSM_OK || B == 0) return st;
-  p.sm = layout_for(h->cfg, T);
+  p.cu = cu;
+  const int NT = cu != nullptr ? nt_for_ragged(T) : nt_for(T);
+  p.sm = layout_for(h->cfg, T, NT);
   if ((int)p.sm.total > h->max_smem) return RSSM_ERR_UNSUPPORTED;
-  return from_cuda(replay_launch(h->cfg, p, nt_for(T), static_cast<cudaStream_t>(stream)));
+  return from_cuda(replay_launch(h->cfg, p, NT, static_cast<cudaStream_t>(stream)));
 }
 
 NativeSmem native_layout_for(const rssm_config& c) {
@@ -216,6 +234,29 @@ FoldParams fold_params(const rssm_handle* h, const int32_t* slot, const uint8_t*
   p.mode = mode;
   p.sm = fold_layout_for(c);
   return p;
+}
+
+// Commit of uniform (cu == null, T tokens per row) or ragged windows (at most
+// T tokens per row).
+rssm_status commit(rssm_handle* h, const int32_t* slot, const uint8_t* force,
+                   const int32_t* accept_len, const int32_t* cu, int32_t B, int32_t T,
+                   void* stream) {
+  if (h == nullptr) return RSSM_ERR_INVALID_ARG;
+  const rssm_config& c = h->cfg;
+  if (B < 0 || B > kMaxGrid || T < 1 || T > c.max_T) return RSSM_ERR_INVALID_ARG;
+  if (B == 0) return RSSM_OK;
+  if (!slot || !accept_len) return RSSM_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c.commit_mode == RSSM_COMMIT_FOLD_EVERY) {
+    FoldParams p = fold_params(h, slot, force, accept_len, B, T, FOLD_COMMIT);
+    p.cu = cu;
+    const cudaError_t e = fold_launch(c.algo, state_dt(c), p, c.n_layers, st);
+    if (e != cudaSuccess) return RSSM_ERR_CUDA;
+    return from_cuda(cursor_launch(h->buf.cursor, slot, force, accept_len, cu, B, T, c.L,
+                                   c.n_slots, CURSOR_COMMIT_FOLD, h->buf.err_word, st));
+  }
+  return from_cuda(cursor_launch(h->buf.cursor, slot, force, accept_len, cu, B, T, c.L,
+                                 c.n_slots, CURSOR_COMMIT_LAZY, h->buf.err_word, st));
 }
 
 }  // namespace
@@ -292,7 +333,7 @@ rssm_status rssm_decode(rssm_handle* h, int32_t layer, const void* q, const void
                                 stream);
   if (st != RSSM_OK || B == 0 || !advance_cursor) return st;
   const rssm_config& c = h->cfg;
-  return from_cuda(cursor_launch(h->buf.cursor, slot, force, nullptr, B, 1, c.L, c.n_slots,
+  return from_cuda(cursor_launch(h->buf.cursor, slot, force, nullptr, nullptr, B, 1, c.L, c.n_slots,
                                  CURSOR_DECODE, h->buf.err_word,
                                  static_cast<cudaStream_t>(stream)));
 }
@@ -302,6 +343,16 @@ rssm_status rssm_verify(rssm_handle* h, int32_t layer, const void* q, const void
                         const uint8_t* force, int32_t B, int32_t T, void* o, uint8_t* fold_out,
                         void* stream) {
   return window(h, layer, q, k, v, beta, g, slot, force, B, T, o, fold_out, stream);
+}
+
+rssm_status rssm_verify_ragged(rssm_handle* h, int32_t layer, const void* q, const void* k,
+                               const void* v, const float* beta, const float* g,
+                               const int32_t* cu_seqlens, const int32_t* slot,
+                               const uint8_t* force, int32_t B, int32_t max_T, void* o,
+                               uint8_t* fold_out, void* stream) {
+  if (B > 0 && (cu_seqlens == nullptr || !aligned4(cu_seqlens))) return RSSM_ERR_INVALID_ARG;
+  return window(h, layer, q, k, v, beta, g, slot, force, B, max_T, o, fold_out, stream,
+                cu_seqlens);
 }
 
 rssm_status rssm_native_decode(rssm_handle* h, int32_t layer, const void* q, const void* k,
@@ -319,21 +370,14 @@ rssm_status rssm_native_decode(rssm_handle* h, int32_t layer, const void* q, con
 
 rssm_status rssm_commit(rssm_handle* h, const int32_t* slot, const uint8_t* force,
                         const int32_t* accept_len, int32_t B, int32_t T, void* stream) {
-  if (h == nullptr) return RSSM_ERR_INVALID_ARG;
-  const rssm_config& c = h->cfg;
-  if (B < 0 || B > kMaxGrid || T < 1 || T > c.max_T) return RSSM_ERR_INVALID_ARG;
-  if (B == 0) return RSSM_OK;
-  if (!slot || !accept_len) return RSSM_ERR_INVALID_ARG;
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (c.commit_mode == RSSM_COMMIT_FOLD_EVERY) {
-    const FoldParams p = fold_params(h, slot, force, accept_len, B, T, FOLD_COMMIT);
-    const cudaError_t e = fold_launch(c.algo, state_dt(c), p, c.n_layers, st);
-    if (e != cudaSuccess) return RSSM_ERR_CUDA;
-    return from_cuda(cursor_launch(h->buf.cursor, slot, force, accept_len, B, T, c.L,
-                                   c.n_slots, CURSOR_COMMIT_FOLD, h->buf.err_word, st));
-  }
-  return from_cuda(cursor_launch(h->buf.cursor, slot, force, accept_len, B, T, c.L, c.n_slots,
-                                 CURSOR_COMMIT_LAZY, h->buf.err_word, st));
+  return commit(h, slot, force, accept_len, nullptr, B, T, stream);
+}
+
+rssm_status rssm_commit_ragged(rssm_handle* h, const int32_t* slot, const uint8_t* force,
+                               const int32_t* accept_len, const int32_t* cu_seqlens, int32_t B,
+                               int32_t max_T, void* stream) {
+  if (B > 0 && (cu_seqlens == nullptr || !aligned4(cu_seqlens))) return RSSM_ERR_INVALID_ARG;
+  return commit(h, slot, force, accept_len, cu_seqlens, B, max_T, stream);
 }
 
 rssm_status rssm_fold(rssm_handle* h, const int32_t* slot, int32_t B, void* stream) {
@@ -346,7 +390,7 @@ rssm_status rssm_fold(rssm_handle* h, const int32_t* slot, int32_t B, void* stre
   const FoldParams p = fold_params(h, slot, nullptr, nullptr, B, 1, FOLD_ALL);
   const cudaError_t e = fold_launch(c.algo, state_dt(c), p, c.n_layers, st);
   if (e != cudaSuccess) return RSSM_ERR_CUDA;
-  return from_cuda(cursor_launch(h->buf.cursor, slot, nullptr, nullptr, B, 1, c.L, c.n_slots,
+  return from_cuda(cursor_launch(h->buf.cursor, slot, nullptr, nullptr, nullptr, B, 1, c.L, c.n_slots,
                                  CURSOR_ZERO, h->buf.err_word, st));
 }
 
@@ -356,7 +400,7 @@ rssm_status rssm_reset_slots(rssm_handle* h, const int32_t* slot, int32_t B, voi
   if (B == 0) return RSSM_OK;
   if (!slot) return RSSM_ERR_INVALID_ARG;
   const rssm_config& c = h->cfg;
-  return from_cuda(cursor_launch(h->buf.cursor, slot, nullptr, nullptr, B, 1, c.L, c.n_slots,
+  return from_cuda(cursor_launch(h->buf.cursor, slot, nullptr, nullptr, nullptr, B, 1, c.L, c.n_slots,
                                  CURSOR_ZERO, h->buf.err_word,
                                  static_cast<cudaStream_t>(stream)));
 }

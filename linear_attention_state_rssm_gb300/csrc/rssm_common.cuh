@@ -19,6 +19,7 @@ enum : uint32_t {
   DEVERR_CURSOR = 2u,
   DEVERR_ACCEPT = 4u,
   DEVERR_TIMEOUT = 8u,
+  DEVERR_SEQLEN = 16u,
 };
 enum : int { CURSOR_DECODE = 0, CURSOR_COMMIT_LAZY = 1, CURSOR_ZERO = 2, CURSOR_COMMIT_FOLD = 3 };
 enum : int { FOLD_ALL = 0, FOLD_COMMIT = 1 };
@@ -145,9 +146,10 @@ struct ReplayParams {
   const float* g;
   const int32_t* slot;
   const uint8_t* force;
+  const int32_t* cu;  // ragged windows: row r's tokens [cu[r], cu[r+1]); null: r*T + [0, T)
   void* o;
   uint8_t* fold_out;
-  int B, T, L, n_slots, HK, HV, G, dk, dv;
+  int B, T, L, n_slots, HK, HV, G, dk, dv;  // T: the window (ragged: the widest allowed)
   int in_dt, rk_dt, rd_dt;
   float scale;
   ReplaySmem sm;
@@ -167,6 +169,7 @@ struct FoldParams {
   const int32_t* slot;
   const uint8_t* force;
   const int32_t* accept;
+  const int32_t* cu;  // ragged windows (as in ReplayParams), or null
   size_t layer_state, layer_k, layer_d, layer_g;  // per-layer strides (elements)
   int B, T, L, n_slots, HK, HV, G, dk, dv;
   int rk_dt, rd_dt, mode;
@@ -174,6 +177,22 @@ struct FoldParams {
 };
 
 
+
+// Window of request row r: its first token and length. Uniform windows hold
+// T tokens at r*T; ragged ones cu[r+1] - cu[r] tokens at cu[r] (at most T).
+// Returns false for offsets out of order or a window wider than T.
+__device__ __forceinline__ bool row_window(const int32_t* cu, int r, int T, size_t& tok0,
+                                           int& n) {
+  if (cu == nullptr) {
+    tok0 = (size_t)r * T;
+    n = T;
+    return true;
+  }
+  const int a = cu[r], b = cu[r + 1];
+  tok0 = (size_t)(a < 0 ? 0 : a);
+  n = b - a;
+  return a >= 0 && n >= 0 && n <= T;
+}
 
 constexpr uint32_t kRankBytes = 8u * kThreads + 4u * kWarps;
 

@@ -10,6 +10,8 @@ namespace rssm {
 // Window widths the replay kernel is built for; a window of T tokens runs in
 // the smallest width >= T.
 inline int nt_for(int T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16; }
+// Ragged windows of at most T tokens (kernels built for the verify widths).
+inline int nt_for_ragged(int T) { return T <= 2 ? 2 : nt_for(T); }
 
 #define RSSM_DECLARE_REPLAY(NAME)                                                      \
   cudaError_t NAME##_launch(const ReplayParams& p, int NT, cudaStream_t st); \
@@ -19,6 +21,10 @@ RSSM_DECLARE_REPLAY(replay_gdn_f32)
 RSSM_DECLARE_REPLAY(replay_gdn_bf16)
 RSSM_DECLARE_REPLAY(replay_kda_f32)
 RSSM_DECLARE_REPLAY(replay_kda_bf16)
+RSSM_DECLARE_REPLAY(replay_gdn_f32_ragged)
+RSSM_DECLARE_REPLAY(replay_gdn_bf16_ragged)
+RSSM_DECLARE_REPLAY(replay_kda_f32_ragged)
+RSSM_DECLARE_REPLAY(replay_kda_bf16_ragged)
 #undef RSSM_DECLARE_REPLAY
 
 cudaError_t fold_launch(int algo, int state_dt, const FoldParams& p, int n_layers,
@@ -28,7 +34,7 @@ cudaError_t native_launch(int algo, int state_dt, const ReplayParams& p, const N
                           cudaStream_t st);
 cudaError_t native_prepare(int algo, int state_dt, int max_smem);
 cudaError_t cursor_launch(int32_t* cursor, const int32_t* slot, const uint8_t* force,
-                          const int32_t* accept, int B, int T, int L, int n_slots, int mode,
-                          uint32_t* err, cudaStream_t st);
+                          const int32_t* accept, const int32_t* cu, int B, int T, int L,
+                          int n_slots, int mode, uint32_t* err, cudaStream_t st);
 
 }  // namespace rssm

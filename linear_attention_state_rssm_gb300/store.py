@@ -66,6 +66,13 @@ class ReplayStore:
         _lib.rssm_verify(self.handle, layer, q, k, v, beta, g, slot, force, slot.numel(), T, o,
                          fold_out, stream)
 
+    def rssm_verify_ragged(self, layer, q, k, v, beta, g, cu_seqlens, slot, max_T, o,
+                           force=None, fold_out=None, stream=None):
+        """Windows of different lengths: row r's tokens are
+        [cu_seqlens[r], cu_seqlens[r+1]) of the packed inputs (int32, B + 1)."""
+        _lib.rssm_verify_ragged(self.handle, layer, q, k, v, beta, g, cu_seqlens, slot, force,
+                                slot.numel(), max_T, o, fold_out, stream)
+
     def rssm_native_decode(self, layer, q, k, v, beta, g, slot, o, stream=None):
         """The per-token state read/write path ReplaySSM replaces (comparison
         point): the checkpoint is the live state; ring and cursor untouched."""
@@ -74,6 +81,10 @@ class ReplayStore:
 
     def rssm_commit(self, slot, accept_len, T, force=None, stream=None):
         _lib.rssm_commit(self.handle, slot, force, accept_len, slot.numel(), T, stream)
+
+    def rssm_commit_ragged(self, slot, accept_len, cu_seqlens, max_T, force=None, stream=None):
+        _lib.rssm_commit_ragged(self.handle, slot, force, accept_len, cu_seqlens, slot.numel(),
+                                max_T, stream)
 
     def rssm_fold(self, slot, stream=None):
         _lib.rssm_fold(self.handle, slot, slot.numel(), stream)

@@ -124,6 +124,24 @@ def accept_lengths(seed: int, B: int, T: int) -> np.ndarray:
     return rng.integers(0, T + 1, size=B).astype(np.int32)
 
 
+def ragged_lengths(seed: int, B: int, max_T: int) -> np.ndarray:
+    """Window length per row, uniform in [0, max_T], with at least one idle
+    row (0) and one full row (max_T) when B >= 2; returns cu_seqlens [B + 1]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n = rng.integers(0, max_T + 1, size=B)
+    if B >= 2:
+        i, j = rng.choice(B, size=2, replace=False)
+        n[i], n[j] = 0, max_T
+    return np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+
+
+def ragged_accept(seed: int, cu_seqlens: np.ndarray) -> np.ndarray:
+    """Accepted length per row, uniform in [0, T_r] for row r's window."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n = np.diff(np.asarray(cu_seqlens, dtype=np.int64))
+    return np.array([rng.integers(0, t + 1) for t in n], dtype=np.int32)
+
+
 def force_flags(seed: int, B: int, p: float) -> np.ndarray:
     """Per-row forced-fold flags, each set with probability p."""
     rng = np.random.Generator(np.random.PCG64(seed))

@@ -116,6 +116,36 @@ class Run:
         if self.orc_r is not None:
             self.orc_r.commit(self.orc_slots, np.asarray(accept)[self.sample], T, fsub, mode)
 
+    # ----------------------------------------------------------- ragged steps
+    def window_ragged(self, layer, inp, cu, max_T, force=None):
+        """Ragged verify of one layer on both sides (every row is sampled).
+        ``inp`` holds the packed tokens (at least cu[-1] of them). Returns
+        (o_gpu, o_orc, fold_gpu, fold_orc) over all packed tokens / rows."""
+        assert self.sample.size == self.B
+        q, k, v, beta, g = self._gpu_inputs(inp)
+        n_tok = inp["q"].shape[0]
+        o = torch.full((n_tok, self.HV, self.dv), SENTINEL, dtype=TORCH[self.in_dtype],
+                       device="cuda")
+        fold_out = torch.full((self.B,), 7, dtype=torch.uint8, device="cuda")
+        force_t = None if force is None else torch.from_numpy(np.asarray(force, np.uint8)).cuda()
+        cu_t = torch.from_numpy(np.asarray(cu, np.int32)).cuda()
+        self.store.rssm_verify_ragged(layer, q, k, v, beta, g, cu_t, self.slot_t, max_T, o,
+                                      force=force_t, fold_out=fold_out)
+        o_orc, f_orc = self.orc.window_ragged(layer, self.orc_slots, inp, cu, force)
+        if self.orc_r is not None:
+            self.orc_r.window_ragged(layer, self.orc_slots, inp, cu, force)
+        return o.double().cpu().numpy(), o_orc, fold_out.cpu().numpy(), f_orc
+
+    def commit_ragged(self, accept, cu, max_T, force=None):
+        acc_t = torch.from_numpy(np.asarray(accept, np.int32)).cuda()
+        force_t = None if force is None else torch.from_numpy(np.asarray(force, np.uint8)).cuda()
+        cu_t = torch.from_numpy(np.asarray(cu, np.int32)).cuda()
+        self.store.rssm_commit_ragged(self.slot_t, acc_t, cu_t, max_T, force=force_t)
+        mode = ring.FOLD_EVERY if self.commit_mode == "fold_every" else ring.LAZY
+        self.orc.commit_ragged(self.orc_slots, accept, cu, force, mode)
+        if self.orc_r is not None:
+            self.orc_r.commit_ragged(self.orc_slots, accept, cu, force, mode)
+
     # ------------------------------------------------------------- inspection
     def cursor_gpu(self):
         return self.store.cursor.cpu().numpy()
