@@ -307,6 +307,44 @@ class ReplayOracle:
             self.cursor[s] = ring.cursor_after_commit(c, int(lens[r]), self.L,
                                                       bool(force[r]), int(accept[r]), mode)
 
+    def prefill(self, layer, slots, inp, cu_seqlens):
+        """Replay prefill of one layer (LightLLM PR #1690, commit messages:
+        prefill writes the canonical state directly and leaves the cursor at
+        zero). Row r's prompt is tokens [cu_seqlens[r], cu_seqlens[r+1]) of
+        the packed inputs; it runs token by token from the row's committed
+        state (checkpoint plus ring history), and the checkpoint then takes
+        the result. Rows with a null slot or no tokens are left as they are.
+        The cursor moves in ``prefill_done``, after the last layer.
+
+        Returns o [N, HV, dv] (NaN where no row wrote), N = cu_seqlens[-1].
+        """
+        slots = np.asarray(slots, dtype=np.int64)
+        cu = np.asarray(cu_seqlens, dtype=np.int64)
+        lens = np.diff(cu)
+        if cu.shape[0] != slots.shape[0] + 1 or np.any(lens < 0) or cu[0] < 0:
+            raise ValueError("cu_seqlens must be non-negative and non-decreasing")
+        o = np.full((int(cu[-1]), self.HV, self.dv), np.nan)
+        with np.errstate(all="ignore"):
+            for r, s in enumerate(slots):
+                if s < 0 or lens[r] == 0:
+                    continue
+                S = self.S[layer, s][None]
+                for t in range(int(cu[r]), int(cu[r + 1])):
+                    q, k, v, beta, g = self._token_inputs(inp, np.array([t]))
+                    S, _, o[t:t + 1] = token_step(S, q, k, v, beta, g, self.scale, self.algo)
+                self.S[layer, s] = S[0]
+                self._checkpoint(layer, [s])
+                self.written[layer, s] = False
+        return o
+
+    def prefill_done(self, slots, cu_seqlens):
+        """After the last layer's prefill: cursor <- 0 for every row that had
+        prompt tokens (its history now lives in the checkpoint)."""
+        lens = np.diff(np.asarray(cu_seqlens, dtype=np.int64))
+        for r, s in enumerate(np.asarray(slots)):
+            if s >= 0 and lens[r] > 0:
+                self.cursor[s] = 0
+
     def fold(self, slots):
         """Explicit fold: checkpoint <- committed state, cursor <- 0."""
         for s in np.asarray(slots):
