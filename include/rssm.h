@@ -212,6 +212,29 @@ rssm_status rssm_verify_ragged(rssm_handle *h, int32_t layer, const void *q,
                                uint8_t *fold_out, void *stream);
 
 /*
+ * Replay prefill of one layer (LightLLM PR #1690, commit messages: prefill
+ * writes the canonical state directly and leaves the cursor at zero). Row r's
+ * prompt is tokens [cu_seqlens[r], cu_seqlens[r+1]) of q, k [N, HK, dk],
+ * v [N, HV, dv], beta [N, HV], g [N, HV] (GDN) or [N, HV, dk] (KDA), any
+ * length >= 0. For each row with s = slot[r] >= 0 and at least one token, the
+ * prompt runs through the gated delta rule from the row's committed state
+ * (checkpoint plus its c = cursor[s] ring records), o [N, HV, dv] (input
+ * dtype) takes every token's output, and the checkpoint of (layer, s) takes
+ * the final state (rounded to the state dtype); the ring is not written. When
+ * reset_cursor is non-zero (the last layer of the step) the cursor of every
+ * such row is then set to 0, so every layer reads the same history before.
+ * Rows with a null slot or no tokens are left untouched (outputs included).
+ * cu_seqlens is a device int32[B + 1], 4-byte aligned; offsets that are
+ * negative or decreasing set RSSM_DEVERR_SEQLEN and skip the row. Input
+ * alignment and other error rules as rssm_decode.
+ */
+rssm_status rssm_prefill(rssm_handle *h, int32_t layer, const void *q,
+                         const void *k, const void *v, const float *beta,
+                         const float *g, const int32_t *cu_seqlens,
+                         const int32_t *slot, int32_t B, void *o,
+                         int32_t reset_cursor, void *stream);
+
+/*
  * Native fused-recurrent decode of one layer, the path ReplaySSM replaces
  * (LightLLM PR #1690, PR description: the native mode writes the recurrent
  * state back every step). It is here as a comparison point: for each row r

@@ -23,8 +23,8 @@ DEVERR = {"slot": 1, "cursor": 2, "accept": 4, "timeout": 8, "seqlen": 16}
 
 # Every entry point declared in include/rssm.h.
 SYMBOLS = ("rssm_required_bytes", "rssm_alloc", "rssm_free", "rssm_decode", "rssm_verify",
-           "rssm_verify_ragged", "rssm_native_decode", "rssm_commit", "rssm_commit_ragged",
-           "rssm_fold", "rssm_reset_slots",
+           "rssm_verify_ragged", "rssm_prefill", "rssm_native_decode", "rssm_commit",
+           "rssm_commit_ragged", "rssm_fold", "rssm_reset_slots",
            "rssm_get_device_error", "rssm_status_string", "rssm_version")
 
 
@@ -80,6 +80,7 @@ def load() -> ctypes.CDLL:
         "rssm_verify": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P], _I),
         "rssm_verify_ragged": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P],
                                _I),
+        "rssm_prefill": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _P], _I),
         "rssm_native_decode": ([_P, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P], _I),
         "rssm_commit": ([_P, _P, _P, _P, _I, _I, _P], _I),
         "rssm_commit_ragged": ([_P, _P, _P, _P, _P, _I, _I, _P], _I),
@@ -168,6 +169,13 @@ def rssm_verify_ragged(handle, layer, q, k, v, beta, g, cu_seqlens, slot, force,
                                      _ptr(g), _ptr(cu_seqlens), _ptr(slot), _ptr(force), B,
                                      max_T, _ptr(o), _ptr(fold_out), _stream(stream)),
            "rssm_verify_ragged")
+
+
+def rssm_prefill(handle, layer, q, k, v, beta, g, cu_seqlens, slot, B, o, reset_cursor,
+                 stream=None):
+    _check(load().rssm_prefill(handle, layer, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                               _ptr(cu_seqlens), _ptr(slot), B, _ptr(o),
+                               int(bool(reset_cursor)), _stream(stream)), "rssm_prefill")
 
 
 def rssm_native_decode(handle, layer, q, k, v, beta, g, slot, B, o, stream=None):

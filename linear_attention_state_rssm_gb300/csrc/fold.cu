@@ -133,6 +133,15 @@ __global__ void cursor_kernel(int32_t* cursor, const int32_t* slot, const uint8_
     cursor[s] = 0;
     return;
   }
+  if (mode == CURSOR_PREFILL) {
+    const int a0 = cu[r], a1 = cu[r + 1];
+    if (a0 < 0 || a1 < a0) {
+      atomicOr(err, DEVERR_SEQLEN);
+      return;
+    }
+    if (a1 > a0 && c >= 0 && c <= L) cursor[s] = 0;
+    return;
+  }
   if (c < 0 || c > L) {
     atomicOr(err, DEVERR_CURSOR);
     return;

@@ -304,6 +304,9 @@ rssm_status rssm_alloc(const rssm_config* cfg, const rssm_buffers* buf, rssm_han
   if ((int)native_layout_for(*cfg).total <= max_smem &&
       native_prepare(cfg->algo, state_dt(*cfg), max_smem) != cudaSuccess)
     return RSSM_ERR_CUDA;
+  if ((int)prefill_layout(cfg->algo, cfg->dk, cfg->dv).total <= max_smem &&
+      prefill_prepare(cfg->algo, state_dt(*cfg), max_smem) != cudaSuccess)
+    return RSSM_ERR_CUDA;
 
   rssm_handle* h = new (std::nothrow) rssm_handle;
   if (h == nullptr) return RSSM_ERR_INVALID_ARG;
@@ -353,6 +356,55 @@ rssm_status rssm_verify_ragged(rssm_handle* h, int32_t layer, const void* q, con
   if (B > 0 && (cu_seqlens == nullptr || !aligned4(cu_seqlens))) return RSSM_ERR_INVALID_ARG;
   return window(h, layer, q, k, v, beta, g, slot, force, B, max_T, o, fold_out, stream,
                 cu_seqlens);
+}
+
+rssm_status rssm_prefill(rssm_handle* h, int32_t layer, const void* q, const void* k,
+                         const void* v, const float* beta, const float* g,
+                         const int32_t* cu_seqlens, const int32_t* slot, int32_t B, void* o,
+                         int32_t reset_cursor, void* stream) {
+  // the window rules of a one-token window cover the pointers and alignment
+  ReplayParams w;
+  const rssm_status st = window_params(h, layer, q, k, v, beta, g, slot, nullptr, B, 1, o,
+                                       nullptr, &w);
+  if (st != RSSM_OK || B == 0) return st;
+  if (cu_seqlens == nullptr || !aligned4(cu_seqlens)) return RSSM_ERR_INVALID_ARG;
+  const rssm_config& c = h->cfg;
+  PrefillParams p{};
+  p.state = w.state;
+  p.ring_k = w.ring_k;
+  p.ring_d = w.ring_d;
+  p.ring_g = w.ring_g;
+  p.cursor = w.cursor;
+  p.err = w.err;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.beta = beta;
+  p.g = g;
+  p.cu = cu_seqlens;
+  p.slot = slot;
+  p.o = o;
+  p.B = B;
+  p.L = c.L;
+  p.n_slots = c.n_slots;
+  p.HK = c.HK;
+  p.HV = c.HV;
+  p.G = h->G;
+  p.dk = c.dk;
+  p.dv = c.dv;
+  p.CB = prefill_cb(c.dv);
+  p.in_dt = w.in_dt;
+  p.rk_dt = w.rk_dt;
+  p.rd_dt = w.rd_dt;
+  p.scale = c.scale;
+  p.sm = prefill_layout(c.algo, c.dk, c.dv);
+  if ((int)p.sm.total > h->max_smem) return RSSM_ERR_UNSUPPORTED;
+  if ((long long)c.HV * (c.dv / p.CB) > kMaxGrid) return RSSM_ERR_UNSUPPORTED;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = prefill_launch(c.algo, state_dt(c), p, s);
+  if (e != cudaSuccess || !reset_cursor) return from_cuda(e);
+  return from_cuda(cursor_launch(h->buf.cursor, slot, nullptr, nullptr, cu_seqlens, B, 1, c.L,
+                                 c.n_slots, CURSOR_PREFILL, h->buf.err_word, s));
 }
 
 rssm_status rssm_native_decode(rssm_handle* h, int32_t layer, const void* q, const void* k,

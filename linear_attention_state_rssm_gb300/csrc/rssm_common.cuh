@@ -21,7 +21,13 @@ enum : uint32_t {
   DEVERR_TIMEOUT = 8u,
   DEVERR_SEQLEN = 16u,
 };
-enum : int { CURSOR_DECODE = 0, CURSOR_COMMIT_LAZY = 1, CURSOR_ZERO = 2, CURSOR_COMMIT_FOLD = 3 };
+enum : int {
+  CURSOR_DECODE = 0,
+  CURSOR_COMMIT_LAZY = 1,
+  CURSOR_ZERO = 2,
+  CURSOR_COMMIT_FOLD = 3,
+  CURSOR_PREFILL = 4  // cursor <- 0 for rows with prompt tokens (cu)
+};
 enum : int { FOLD_ALL = 0, FOLD_COMMIT = 1 };
 
 constexpr int kThreads = 128;  // 4 warps per CTA, one CTA per (row, value head)
@@ -192,6 +198,83 @@ __device__ __forceinline__ bool row_window(const int32_t* cu, int r, int T, size
   tok0 = (size_t)(a < 0 ? 0 : a);
   n = b - a;
   return a >= 0 && n >= 0 && n <= T;
+}
+
+// ------------------------------------------------------------------ prefill
+constexpr int kPrefillChunk = 16;     // prompt tokens per step of the prefill scan
+constexpr int kPrefillThreads = 256;  // threads of a prefill CTA
+
+struct PrefillSmem {
+  uint32_t S;     // [dk][CB]  fp32 state columns of this CTA
+  uint32_t wq;    // [C][dk]   fp32 chunk q
+  uint32_t wk;    // [C][dk]   fp32 chunk k (history replay: ring keys)
+  uint32_t wv;    // [C][CB]   fp32 chunk v columns
+  uint32_t xT;    // [dk][kPrefillXS] mat-vec inputs per key channel; then the update's
+                  // decayed keys [dk][kPrefillKS]
+  uint32_t y;     // [2C][CB]  S^T k_i, S^T q_i (decay applied); first the GDN pair sums
+  uint32_t dch;   // [C][CB]   chunk deltas (history replay: ring deltas)
+  uint32_t am;    // [C][C]
+  uint32_t fm;    // [C][C]
+  uint32_t G;     // GDN [C] / KDA [C][dk] in-chunk inclusive gate prefixes
+  uint32_t eG;    // GDN [C] e^{G_i}
+  uint32_t ekd;   // GDN [C] e^{G_last - G_i}
+  uint32_t wb;    // [C] betas
+  uint32_t decr;  // KDA [dk] e^{G_last} per key channel
+  uint32_t total;
+};
+
+struct PrefillParams {
+  void* state;
+  const void* ring_k;
+  const void* ring_d;
+  const float* ring_g;
+  const int32_t* cursor;
+  uint32_t* err;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* beta;
+  const float* g;
+  const int32_t* cu;
+  const int32_t* slot;
+  void* o;
+  int B, L, n_slots, HK, HV, G, dk, dv, CB;
+  int in_dt, rk_dt, rd_dt;
+  float scale;
+  PrefillSmem sm;
+};
+
+// Value columns per prefill CTA (the columns of the delta rule are independent).
+__host__ __device__ constexpr int prefill_cb(int dv) { return dv < 64 ? dv : 64; }
+
+// Row strides (floats) of the transposed per-channel arrays: four floats of
+// padding keep the 16-byte stores of consecutive channels on distinct banks.
+constexpr int kPrefillXS = 2 * kPrefillChunk + 4;
+constexpr int kPrefillKS = kPrefillChunk + 4;
+
+__host__ __device__ inline PrefillSmem prefill_layout(int algo, int dk, int dv) {
+  constexpr int C = kPrefillChunk;
+  const int CB = prefill_cb(dv);
+  const bool kda = algo == ALGO_KDA;
+  PrefillSmem m{};
+  uint32_t off = 0;
+  m.S = off;     off = align16(off + 4u * dk * CB);
+  m.wq = off;    off = align16(off + 4u * C * dk);
+  m.wk = off;    off = align16(off + 4u * C * dk);
+  m.wv = off;    off = align16(off + 4u * C * CB);
+  m.xT = off;    off = align16(off + 4u * dk * kPrefillXS);
+  // y also holds the GDN pair partial sums [4][C][2C] before the mat-vec
+  m.y = off;     off = align16(off + 4u * (2 * C * CB > 8 * C * C ? 2 * C * CB : 8 * C * C));
+  m.dch = off;   off = align16(off + 4u * C * CB);
+  m.am = off;    off = align16(off + 4u * C * C);
+  m.fm = off;    off = align16(off + 4u * C * C);
+  m.G = off;     off = align16(off + 4u * (kda ? C * dk : C));
+  m.eG = off;    off = align16(off + 4u * C);
+  m.ekd = off;   off = align16(off + 4u * C);
+  m.wb = off;    off = align16(off + 4u * C);
+  m.decr = off;  off = align16(off + 4u * dk);
+  m.total = off;
+  return m;
 }
 
 constexpr uint32_t kRankBytes = 8u * kThreads + 4u * kWarps;

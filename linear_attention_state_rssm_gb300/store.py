@@ -73,6 +73,13 @@ class ReplayStore:
         _lib.rssm_verify_ragged(self.handle, layer, q, k, v, beta, g, cu_seqlens, slot, force,
                                 slot.numel(), max_T, o, fold_out, stream)
 
+    def rssm_prefill(self, layer, q, k, v, beta, g, cu_seqlens, slot, o, reset_cursor=False,
+                     stream=None):
+        """Prompt of row r = tokens [cu_seqlens[r], cu_seqlens[r+1]); the
+        checkpoint takes the state; the cursor clears on the last layer."""
+        _lib.rssm_prefill(self.handle, layer, q, k, v, beta, g, cu_seqlens, slot, slot.numel(),
+                          o, reset_cursor, stream)
+
     def rssm_native_decode(self, layer, q, k, v, beta, g, slot, o, stream=None):
         """The per-token state read/write path ReplaySSM replaces (comparison
         point): the checkpoint is the live state; ring and cursor untouched."""

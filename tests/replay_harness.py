@@ -146,6 +146,28 @@ class Run:
         if self.orc_r is not None:
             self.orc_r.commit_ragged(self.orc_slots, accept, cu, force, mode)
 
+    # ---------------------------------------------------------------- prefill
+    def prefill(self, layer, inp, cu, reset_cursor):
+        """Replay prefill of one layer on both sides (every row sampled);
+        returns (o_gpu, o_orc) over the packed tokens (the GPU buffer may hold
+        spare tokens past cu[-1])."""
+        assert self.sample.size == self.B
+        q, k, v, beta, g = self._gpu_inputs(inp)
+        n_tok = inp["q"].shape[0]
+        o = torch.full((n_tok, self.HV, self.dv), SENTINEL, dtype=TORCH[self.in_dtype],
+                       device="cuda")
+        cu_t = torch.from_numpy(np.asarray(cu, np.int32)).cuda()
+        self.store.rssm_prefill(layer, q, k, v, beta, g, cu_t, self.slot_t, o,
+                                reset_cursor=reset_cursor)
+        o_orc = self.orc.prefill(layer, self.orc_slots, inp, cu)
+        if self.orc_r is not None:
+            self.orc_r.prefill(layer, self.orc_slots, inp, cu)
+        if reset_cursor:
+            self.orc.prefill_done(self.orc_slots, cu)
+            if self.orc_r is not None:
+                self.orc_r.prefill_done(self.orc_slots, cu)
+        return o.double().cpu().numpy(), o_orc
+
     # ------------------------------------------------------------- inspection
     def cursor_gpu(self):
         return self.store.cursor.cpu().numpy()
