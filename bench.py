@@ -12,7 +12,10 @@ Rows join a few steps apart before timing, so their cursors are staggered and
 every step folds about one row in sixteen, as in steady serving.
 
 A second workload, reported under "verify", times speculative verify + commit
-(batch 128, T = 8, L = 16, random accept lengths) on the same head shapes.
+(batch 128, T = 8, L = 16, random accept lengths) on the same head shapes; a
+third, under "prefill", times the replay prefill of 8 prompts of 4096 tokens
+(one layer per launch, checkpoint written, ALU-bound: reported against the
+fp32 FMA peak derived from the SM count and clock).
 
 --impl reference times the fp64 oracle (CPU) on a bounded sample of the same
 workload. Under torchrun each rank runs an independent replica (no
@@ -41,6 +44,9 @@ WL = dict(workload="Qwen3.5-4B-shaped GDN decode layer", algo="gdn", HK=16, HV=3
 VERIFY = dict(workload="GDN speculative verify+commit", batch=128, T=8, L=16,
               state_dtype="f32", commit_mode="lazy", layers=48)
 ESZ = {"f32": 4, "bf16": 2, "f16": 2}
+PREFILL = dict(workload="Qwen3.5-4B-shaped GDN replay prefill", prompts=8, tokens=4096,
+               in_dtype="bf16", state_dtype="f32")
+FP32_LANES_PER_SM = 128  # fp32 FMA lanes per SM (4 sub-partitions x 32)
 
 
 # --------------------------------------------------------------- accounting
@@ -386,6 +392,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.empty_cache()
 
     ver = run_verify(args, torch, dev, rank) if not args.no_verify else None
+    pre = run_prefill(args, torch, dev, rank) if not args.no_prefill else None
 
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -412,7 +419,72 @@ def run_ours(args, rank, world, local_rank):
         res["native_decode"] = native
     if ver is not None:
         res["verify"] = ver
+    if pre is not None:
+        res["prefill"] = pre
     return res
+
+
+def run_prefill(args, torch, dev, rank):
+    """Replay prefill of PREFILL's prompts into one layer's checkpoints; the
+    prefill kernel is ALU-bound (fp32 FMA on CUDA cores)."""
+    from linear_attention_state_rssm_gb300.store import ReplayStore
+    w, pf = WL, PREFILL
+    B, N = pf["prompts"], pf["tokens"]
+    HK, HV, dk, dv = w["HK"], w["HV"], w["dk"], w["dv"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3000 + rank)
+    st = ReplayStore("gdn", 1, B, HK, HV, dk, dv, w["L"], 1, pf["in_dtype"], pf["state_dtype"],
+                     "f16", "f32", "lazy", device=dev)
+    st.state.normal_(0.0, 0.1, generator=gen)
+    tot = B * N
+    nrm = torch.nn.functional.normalize
+    q = nrm(torch.randn(tot, HK, dk, device=dev, generator=gen), dim=-1).to(torch.bfloat16)
+    k = nrm(torch.randn(tot, HK, dk, device=dev, generator=gen), dim=-1).to(torch.bfloat16)
+    v = torch.randn(tot, HV, dv, device=dev, generator=gen).to(torch.bfloat16)
+    beta = torch.sigmoid(torch.randn(tot, HV, device=dev, generator=gen))
+    g = -torch.nn.functional.softplus(torch.randn(tot, HV, device=dev, generator=gen))
+    cu = torch.arange(B + 1, dtype=torch.int32, device=dev) * N
+    slot = torch.arange(B, dtype=torch.int32, device=dev)
+    o = torch.empty(tot, HV, dv, dtype=torch.bfloat16, device=dev)
+    for _ in range(args.warmup):
+        st.rssm_prefill(0, q, k, v, beta, g, cu, slot, o, reset_cursor=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        st.rssm_prefill(0, q, k, v, beta, g, cu, slot, o, reset_cursor=True)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    err = st.rssm_get_device_error()
+    props = torch.cuda.get_device_properties(dev)
+    sm_mhz = max_sm_mhz(dev.index if dev.index is not None else 0)
+    peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    flops = 6.0 * dk * dv * HV * tot  # the token recurrence: S^T k, rank-1 update, S^T q
+    achieved = flops / (ms / 1e3) / 1e12
+    del st, q, k, v, beta, g, o
+    torch.cuda.empty_cache()
+    return {"workload": pf["workload"], "prompts": B, "tokens_per_prompt": N,
+            "in_dtype": pf["in_dtype"], "state_dtype": pf["state_dtype"],
+            "tokens_per_s_per_layer": tot / (ms / 1e3), "launch_ms": ms,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak,
+                         "peak_kind": f"derived: {props.multi_processor_count} SMs x "
+                                      f"{FP32_LANES_PER_SM} fp32 lanes x 2 flop x {sm_mhz} MHz",
+                         "flops_per_launch": flops,
+                         "kernel": "prefill_kernel<GDN, f32, 64, bf16>"},
+            "gpu_launches_per_step": 2, "device_error_word": err}
+
+
+def max_sm_mhz(index):
+    """Maximum SM clock of the GPU (nvidia-smi), 2070 MHz if it cannot be read."""
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(index), "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                             timeout=30).stdout.strip()
+        return int(float(out.splitlines()[0]))
+    except (OSError, ValueError, IndexError, subprocess.TimeoutExpired):
+        return 2070
 
 
 def run_verify(args, torch, dev, rank):
@@ -525,6 +597,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-native", action="store_true",
                     help="skip the native fused-recurrent decode comparison line")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the replay prefill line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

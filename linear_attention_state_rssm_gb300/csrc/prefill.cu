@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
   float* xT = reinterpret_cast<float*>(smem + p.sm.xT);
   float* kdT = xT;  // the update's decayed keys replace the mat-vec inputs
   float* y = reinterpret_cast<float*>(smem + p.sm.y);
-  float* part = y;  // GDN pair partial sums [4][C][2C], before y is written
+  float* part = y;  // GDN pair partial sums [PW][2C][C], before y is written
   float* dch = reinterpret_cast<float*>(smem + p.sm.dch);
   float* am = reinterpret_cast<float*>(smem + p.sm.am);
   float* fm = reinterpret_cast<float*>(smem + p.sm.fm);
@@ -334,15 +334,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
     //      and q_i.k_j for every i over its channels (raw vectors; the
     //      in-window decay and beta go on when the partial sums are combined)
     if (ALGO == ALGO_GDN) {
-      if (tid < 128) {
-        const int j = tid & 15, cgrp = tid >> 4;  // 8 channel groups
+      {
+        const int j = tid & 15, cgrp = tid >> 4;  // 16 channel groups
         float kk[C], qk[C];
 #pragma unroll
         for (int i = 0; i < C; ++i) {
           kk[i] = 0.f;
           qk[i] = 0.f;
         }
-        for (int ch = cgrp; ch < dk; ch += 8) {
+        for (int ch = cgrp; ch < dk; ch += PT / 16) {
           const float* xr = xT + ch * XS;
           const float kj = xr[j];
 #pragma unroll
@@ -363,13 +363,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
           kk[i] += __shfl_xor_sync(kFull, kk[i], 16);
           qk[i] += __shfl_xor_sync(kFull, qk[i], 16);
         }
+        // partial sums [warp][2C][C]: lane j of the lower half stores column j
         if (lane < 16) {
-          float* pw = part + (warp * C + j) * 2 * C;
+          float* pw = part + warp * 2 * C * C + j;
 #pragma unroll
-          for (int i4 = 0; i4 < C; i4 += 4) {
-            *reinterpret_cast<float4*>(pw + i4) = make_float4(kk[i4], kk[i4 + 1], kk[i4 + 2], kk[i4 + 3]);
-            *reinterpret_cast<float4*>(pw + C + i4) =
-                make_float4(qk[i4], qk[i4 + 1], qk[i4 + 2], qk[i4 + 3]);
+          for (int i = 0; i < C; ++i) {
+            pw[i * C] = kk[i];
+            pw[(C + i) * C] = qk[i];
           }
         }
       }
@@ -379,9 +379,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
         const int i = tid >> 4, j = tid & 15;
         float skk = 0.f, sqk = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          skk += part[(w * C + j) * 2 * C + i];
-          sqk += part[(w * C + j) * 2 * C + C + i];
+        for (int w = 0; w < PW; ++w) {
+          skk += part[(w * 2 * C + i) * C + j];
+          sqk += part[(w * 2 * C + C + i) * C + j];
         }
         const bool on = i < cn && j <= i;
         const float wgt = on ? __expf(G[i] - G[j]) : 0.f;
@@ -391,8 +391,55 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
       __syncthreads();
     }
 
-    // ---- y_v = S^T x_v: four columns and VT vectors per thread
-    {
+    // ---- y_v = S^T x_v
+    if (CB == 64) {
+      // four columns x eight vectors per thread over a quarter of the rows
+      // (rows kq, kq + 4, ...: the four quarters of a step read four
+      // consecutive rows, on distinct banks), summed over the quarters by
+      // shuffles; lane = column quad (low 3 bits) + 8 quarter, warp = column
+      // half + 2 vector octet
+      const int cqm = (warp & 1) * 8 + (lane & 7), kq = lane >> 3, vo = warp >> 1;
+      float acc[8][4];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[u][q] = 0.f;
+      }
+      const float* sp = S + 4 * cqm;
+      const float* xp = xT + 8 * vo;
+#pragma unroll 2
+      for (int row = kq; row < dk; row += 4) {
+        const float4 s4 = ld4(sp + row * CB);
+        const float4 xa = ld4(xp + row * XS), xb = ld4(xp + row * XS + 4);
+        const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          acc[u][0] = fmaf(s4.x, xv[u], acc[u][0]);
+          acc[u][1] = fmaf(s4.y, xv[u], acc[u][1]);
+          acc[u][2] = fmaf(s4.z, xv[u], acc[u][2]);
+          acc[u][3] = fmaf(s4.w, xv[u], acc[u][3]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[u][q] += __shfl_xor_sync(kFull, acc[u][q], 8);
+          acc[u][q] += __shfl_xor_sync(kFull, acc[u][q], 16);
+        }
+      }
+      // quarter kq stores vectors 2kq, 2kq + 1 of the octet
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if ((u >> 1) == kq) {
+          const int vv = 8 * vo + u;
+          const float f = ALGO == ALGO_GDN ? eG[vv < C ? vv : vv - C] : 1.f;
+          *reinterpret_cast<float4*>(y + vv * CB + 4 * cqm) =
+              make_float4(f * acc[u][0], f * acc[u][1], f * acc[u][2], f * acc[u][3]);
+        }
+      }
+    } else {
+      // four columns and VT vectors per thread over all rows
       float acc[VT][4];
 #pragma unroll
       for (int u = 0; u < VT; ++u) {

@@ -263,8 +263,8 @@ __host__ __device__ inline PrefillSmem prefill_layout(int algo, int dk, int dv) 
   m.wk = off;    off = align16(off + 4u * C * dk);
   m.wv = off;    off = align16(off + 4u * C * CB);
   m.xT = off;    off = align16(off + 4u * dk * kPrefillXS);
-  // y also holds the GDN pair partial sums [4][C][2C] before the mat-vec
-  m.y = off;     off = align16(off + 4u * (2 * C * CB > 8 * C * C ? 2 * C * CB : 8 * C * C));
+  // y also holds the GDN pair partial sums [8][2C][C] before the mat-vec
+  m.y = off;     off = align16(off + 4u * (2 * C * CB > 16 * C * C ? 2 * C * CB : 16 * C * C));
   m.dch = off;   off = align16(off + 4u * C * CB);
   m.am = off;    off = align16(off + 4u * C * C);
   m.fm = off;    off = align16(off + 4u * C * C);
