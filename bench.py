@@ -429,7 +429,7 @@ def run_prefill(args, torch, dev, rank):
     prefill kernel is ALU-bound (fp32 FMA on CUDA cores)."""
     from linear_attention_state_rssm_gb300.store import ReplayStore
     w, pf = WL, PREFILL
-    B, N = pf["prompts"], pf["tokens"]
+    B, N = args.prefill_prompts, args.prefill_tokens
     HK, HV, dk, dv = w["HK"], w["HV"], w["dk"], w["dv"]
     gen = torch.Generator(device=dev)
     gen.manual_seed(3000 + rank)
@@ -598,6 +598,8 @@ def main():
     ap.add_argument("--no-native", action="store_true",
                     help="skip the native fused-recurrent decode comparison line")
     ap.add_argument("--no-prefill", action="store_true", help="skip the replay prefill line")
+    ap.add_argument("--prefill-prompts", type=int, default=PREFILL["prompts"])
+    ap.add_argument("--prefill-tokens", type=int, default=PREFILL["tokens"])
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
