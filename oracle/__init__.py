@@ -8,9 +8,11 @@ never calls it; there is no CPU fallback anywhere in the product.
   carrying the exact committed state, the checkpoint the GPU must hold and the
   ring records it must write.
 * ``oracle.ring``: the integer ring/cursor/fold rules.
+* ``oracle.conv``: the short causal convolution's window and its rollback.
 
 Pins (tests that check the oracle against something other than itself) live
-in ``tests/test_oracle_pins.py`` and ``tests/test_ring_rules.py``.
+in ``tests/test_oracle_pins.py``, ``tests/test_ring_rules.py`` and the other
+``tests/test_oracle_*.py`` files.
 """
 from .recurrence import ReplayOracle, round_bf16, token_step  # noqa: F401
-from . import ring  # noqa: F401
+from . import conv, ring  # noqa: F401
