@@ -75,6 +75,9 @@ typedef enum rssm_status {
 
 enum { RSSM_ALGO_GDN = 0, RSSM_ALGO_KDA = 1 };
 enum { RSSM_F32 = 0, RSSM_BF16 = 1, RSSM_F16 = 2 };
+
+/* Activation of the short causal convolution (rssm_conv_window). */
+enum { RSSM_CONV_ACT_NONE = 0, RSSM_CONV_ACT_SILU = 1 };
 enum { RSSM_COMMIT_LAZY = 0, RSSM_COMMIT_FOLD_EVERY = 1 };
 
 /* Bits of the device error word. */
@@ -271,6 +274,45 @@ rssm_status rssm_commit_ragged(rssm_handle *h, const int32_t *slot,
                                const uint8_t *force, const int32_t *accept_len,
                                const int32_t *cu_seqlens, int32_t B,
                                int32_t max_T, void *stream);
+
+/*
+ * Conv-state window of a layer's short causal convolution, the second
+ * per-request state beside the SSM (LightLLM PR #1690, commit messages: page
+ * save, PD and DP copy the accepted conv window; SGLang fork PR
+ * jianc99/sglang#2, fifth commit: the ring commit rolls the conv back). The
+ * pages do not print the convolution; it is read as depthwise and causal of
+ * width K: per live row r (slot[r] >= 0) and channel c,
+ *     y_t[c] = act(bias[c] + sum_{i<K} w[c][i] * xp[t + i][c]),
+ *     xp = [window[s] (K-1 rows), x_{r,0}, ..., x_{r,T-1}],
+ * act = identity (RSSM_CONV_ACT_NONE) or SiLU (RSSM_CONV_ACT_SILU).
+ * Layouts (device pointers, no alignment beyond the element size):
+ * x, y [B*T][D] and window [n_slots][K-1][D] in dtype (RSSM_F32 or RSSM_BF16),
+ * draft [n_slots][T][D] in dtype, w [D][K] fp32, bias [D] fp32 or null.
+ * With commit_now (decode) the window moves on by the T tokens at once and
+ * draft is not used (may be null); otherwise the window is left as it is and
+ * the T inputs are kept in draft[s] for rssm_conv_commit. 2 <= K <= 8. Null
+ * rows are skipped; a slot >= n_slots sets RSSM_DEVERR_SLOT in err_word (may
+ * be null) and skips the row. The caller owns every buffer; nothing is
+ * allocated and the call is capturable.
+ */
+rssm_status rssm_conv_window(const void *x, const float *w, const float *bias,
+                             void *window, void *draft, const int32_t *slot,
+                             int32_t B, int32_t T, int32_t D, int32_t K,
+                             int32_t n_slots, int32_t dtype, int32_t act,
+                             int32_t commit_now, void *y, uint32_t *err_word,
+                             void *stream);
+
+/*
+ * Conv rollback on commit: window[s] <- the last K-1 rows of
+ * [window[s], draft[s][0 .. a)], a = accept_len[r] in [0, T] (outside:
+ * RSSM_DEVERR_ACCEPT, row skipped). T, D, K, dtype and the slots must be those
+ * of the rssm_conv_window call that filled draft.
+ */
+rssm_status rssm_conv_commit(void *window, const void *draft,
+                             const int32_t *slot, const int32_t *accept_len,
+                             int32_t B, int32_t T, int32_t D, int32_t K,
+                             int32_t n_slots, int32_t dtype, uint32_t *err_word,
+                             void *stream);
 
 /* Explicit fold of every layer's history into its checkpoint, then cursor <- 0
  * (LightLLM PR #1690: materialise the canonical state). */

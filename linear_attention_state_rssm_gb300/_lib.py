@@ -24,7 +24,8 @@ DEVERR = {"slot": 1, "cursor": 2, "accept": 4, "timeout": 8, "seqlen": 16}
 # Every entry point declared in include/rssm.h.
 SYMBOLS = ("rssm_required_bytes", "rssm_alloc", "rssm_free", "rssm_decode", "rssm_verify",
            "rssm_verify_ragged", "rssm_prefill", "rssm_native_decode", "rssm_commit",
-           "rssm_commit_ragged", "rssm_fold", "rssm_reset_slots",
+           "rssm_commit_ragged", "rssm_fold", "rssm_reset_slots", "rssm_conv_window",
+           "rssm_conv_commit",
            "rssm_get_device_error", "rssm_status_string", "rssm_version")
 
 
@@ -85,6 +86,9 @@ def load() -> ctypes.CDLL:
         "rssm_commit": ([_P, _P, _P, _P, _I, _I, _P], _I),
         "rssm_commit_ragged": ([_P, _P, _P, _P, _P, _I, _I, _P], _I),
         "rssm_fold": ([_P, _P, _I, _P], _I),
+        "rssm_conv_window": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
+                              _P], _I),
+        "rssm_conv_commit": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
         "rssm_reset_slots": ([_P, _P, _I, _P], _I),
         "rssm_get_device_error": ([_P, ctypes.POINTER(ctypes.c_uint32), _I, _P], _I),
         "rssm_status_string": ([_I], ctypes.c_char_p),
@@ -193,6 +197,21 @@ def rssm_commit_ragged(handle, slot, force, accept_len, cu_seqlens, B, max_T, st
     _check(load().rssm_commit_ragged(handle, _ptr(slot), _ptr(force), _ptr(accept_len),
                                      _ptr(cu_seqlens), B, max_T, _stream(stream)),
            "rssm_commit_ragged")
+
+
+def rssm_conv_window(x, w, bias, window, draft, slot, B, T, D, K, n_slots, dtype, act,
+                     commit_now, y, err_word=None, stream=None):
+    _check(load().rssm_conv_window(_ptr(x), _ptr(w), _ptr(bias), _ptr(window), _ptr(draft),
+                                   _ptr(slot), B, T, D, K, n_slots, DTYPE[dtype], act,
+                                   int(bool(commit_now)), _ptr(y), _ptr(err_word),
+                                   _stream(stream)), "rssm_conv_window")
+
+
+def rssm_conv_commit(window, draft, slot, accept_len, B, T, D, K, n_slots, dtype, err_word=None,
+                     stream=None):
+    _check(load().rssm_conv_commit(_ptr(window), _ptr(draft), _ptr(slot), _ptr(accept_len), B, T,
+                                   D, K, n_slots, DTYPE[dtype], _ptr(err_word), _stream(stream)),
+           "rssm_conv_commit")
 
 
 def rssm_fold(handle, slot, B, stream=None):

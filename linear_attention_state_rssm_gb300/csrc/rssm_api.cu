@@ -407,6 +407,67 @@ rssm_status rssm_prefill(rssm_handle* h, int32_t layer, const void* q, const voi
                                  c.n_slots, CURSOR_PREFILL, h->buf.err_word, s));
 }
 
+static rssm_status conv_params(const void* x, const float* w, void* window, void* draft,
+                               const int32_t* slot, int32_t B, int32_t T, int32_t D, int32_t K,
+                               int32_t n_slots, int32_t dtype, ConvParams* out) {
+  if (B < 0 || B > kMaxGrid || T < 1 || D < 1 || n_slots < 1) return RSSM_ERR_INVALID_ARG;
+  if (K < 2 || K > kConvMaxK) return RSSM_ERR_UNSUPPORTED;
+  if (dtype != RSSM_F32 && dtype != RSSM_BF16) return RSSM_ERR_UNSUPPORTED;
+  if (!window || !slot) return RSSM_ERR_INVALID_ARG;
+  if (!aligned4(slot)) return RSSM_ERR_INVALID_ARG;
+  (void)x;
+  (void)w;
+  (void)draft;
+  ConvParams& p = *out;
+  p = ConvParams{};
+  p.window = window;
+  p.slot = slot;
+  p.B = B;
+  p.T = T;
+  p.D = D;
+  p.K = K;
+  p.n_slots = n_slots;
+  p.dt = dtype == RSSM_F32 ? DT_F32 : DT_BF16;
+  return RSSM_OK;
+}
+
+rssm_status rssm_conv_window(const void* x, const float* w, const float* bias, void* window,
+                             void* draft, const int32_t* slot, int32_t B, int32_t T, int32_t D,
+                             int32_t K, int32_t n_slots, int32_t dtype, int32_t act,
+                             int32_t commit_now, void* y, uint32_t* err_word, void* stream) {
+  ConvParams p;
+  const rssm_status st = conv_params(x, w, window, draft, slot, B, T, D, K, n_slots, dtype, &p);
+  if (st != RSSM_OK) return st;
+  if (act != RSSM_CONV_ACT_NONE && act != RSSM_CONV_ACT_SILU) return RSSM_ERR_INVALID_ARG;
+  if (B == 0) return RSSM_OK;
+  if (!x || !w || !y || (!commit_now && !draft)) return RSSM_ERR_INVALID_ARG;
+  p.x = x;
+  p.w = w;
+  p.bias = bias;
+  p.draft = draft;
+  p.y = y;
+  p.err = err_word;
+  p.act = act;
+  p.commit_now = commit_now ? 1 : 0;
+  return from_cuda(conv_launch(p, false, static_cast<cudaStream_t>(stream)));
+}
+
+rssm_status rssm_conv_commit(void* window, const void* draft, const int32_t* slot,
+                             const int32_t* accept_len, int32_t B, int32_t T, int32_t D,
+                             int32_t K, int32_t n_slots, int32_t dtype, uint32_t* err_word,
+                             void* stream) {
+  ConvParams p;
+  const rssm_status st = conv_params(nullptr, nullptr, window, nullptr, slot, B, T, D, K, n_slots,
+                                     dtype, &p);
+  if (st != RSSM_OK) return st;
+  if (B == 0) return RSSM_OK;
+  if (!draft || !accept_len || !aligned4(accept_len)) return RSSM_ERR_INVALID_ARG;
+  p.draft = const_cast<void*>(draft);
+  p.accept = accept_len;
+  p.err = err_word;
+  return from_cuda(conv_launch(p, true, static_cast<cudaStream_t>(stream)));
+}
+
 rssm_status rssm_native_decode(rssm_handle* h, int32_t layer, const void* q, const void* k,
                                const void* v, const float* beta, const float* g,
                                const int32_t* slot, int32_t B, void* o, void* stream) {

@@ -200,6 +200,23 @@ __device__ __forceinline__ bool row_window(const int32_t* cu, int r, int T, size
   return a >= 0 && n >= 0 && n <= T;
 }
 
+// --------------------------------------------------------------- conv window
+enum : int { CONV_ACT_NONE = 0, CONV_ACT_SILU = 1 };
+constexpr int kConvMaxK = 8;  // widest causal convolution built
+
+struct ConvParams {
+  const void* x;       // [B*T][D]
+  const float* w;      // [D][K]
+  const float* bias;   // [D] or null
+  void* window;        // [n_slots][K-1][D]
+  void* draft;         // [n_slots][T][D]
+  const int32_t* slot;
+  const int32_t* accept;
+  void* y;             // [B*T][D]
+  uint32_t* err;       // may be null
+  int B, T, D, K, n_slots, dt, act, commit_now;
+};
+
 // ------------------------------------------------------------------ prefill
 constexpr int kPrefillChunk = 16;     // prompt tokens per step of the prefill scan
 constexpr int kPrefillThreads = 256;  // threads of a prefill CTA

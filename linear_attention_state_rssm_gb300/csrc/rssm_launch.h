@@ -35,6 +35,7 @@ cudaError_t native_launch(int algo, int state_dt, const ReplayParams& p, const N
 cudaError_t native_prepare(int algo, int state_dt, int max_smem);
 cudaError_t prefill_launch(int algo, int state_dt, const PrefillParams& p, cudaStream_t st);
 cudaError_t prefill_prepare(int algo, int state_dt, int max_smem);
+cudaError_t conv_launch(const ConvParams& p, bool commit, cudaStream_t st);
 cudaError_t cursor_launch(int32_t* cursor, const int32_t* slot, const uint8_t* force,
                           const int32_t* accept, const int32_t* cu, int B, int T, int L,
                           int n_slots, int mode, uint32_t* err, cudaStream_t st);

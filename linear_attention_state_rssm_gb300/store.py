@@ -120,3 +120,33 @@ class ReplayStore:
 
     def state_bytes_per_row_layer(self) -> int:
         return self.HV * self.dk * self.dv * (4 if self.state_dtype == "f32" else 2)
+
+
+class ConvWindows:
+    """Conv-state windows of ``n_slots`` requests for one convolution of width K
+    over D channels, and the draft inputs of the last verify window.
+
+    Buffers: window [n_slots, K-1, D], draft [n_slots, max_T, D] (dtype),
+    err_word [1]. Taps w [D, K] and bias [D] are fp32 and passed per call.
+    """
+
+    ACT = {"none": 0, "silu": 1}
+
+    def __init__(self, n_slots, D, K, max_T=1, dtype="bf16", device="cuda"):
+        self.n_slots, self.D, self.K, self.max_T, self.dtype = n_slots, D, K, max_T, dtype
+        dev = torch.device(device)
+        self.window = torch.zeros((n_slots, K - 1, D), dtype=_TORCH[dtype], device=dev)
+        self.draft = torch.zeros((n_slots, max_T, D), dtype=_TORCH[dtype], device=dev)
+        self.err_word = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def rssm_conv_window(self, x, w, bias, slot, T, y, act="silu", commit_now=False,
+                         stream=None):
+        if T > self.max_T:
+            raise ValueError("window wider than the draft buffer")
+        _lib.rssm_conv_window(x, w, bias, self.window, self.draft, slot, slot.numel(), T, self.D,
+                              self.K, self.n_slots, self.dtype, self.ACT[act], commit_now, y,
+                              self.err_word, stream)
+
+    def rssm_conv_commit(self, slot, accept_len, T, stream=None):
+        _lib.rssm_conv_commit(self.window, self.draft, slot, accept_len, slot.numel(), T, self.D,
+                              self.K, self.n_slots, self.dtype, self.err_word, stream)
