@@ -47,6 +47,8 @@ ESZ = {"f32": 4, "bf16": 2, "f16": 2}
 PREFILL = dict(workload="Qwen3.5-4B-shaped GDN replay prefill", prompts=8, tokens=4096,
                in_dtype="bf16", state_dtype="f32")
 FP32_LANES_PER_SM = 128  # fp32 FMA lanes per SM (4 sub-partitions x 32)
+CONV = dict(workload="Qwen3.5-4B-shaped conv window (q, k, v channels) for verify + commit",
+            batch=128, T=8, K=4, layers=8, dtype="bf16")
 
 
 # --------------------------------------------------------------- accounting
@@ -393,6 +395,7 @@ def run_ours(args, rank, world, local_rank):
 
     ver = run_verify(args, torch, dev, rank) if not args.no_verify else None
     pre = run_prefill(args, torch, dev, rank) if not args.no_prefill else None
+    conv = run_conv(args, torch, dev, rank, peak) if not args.no_conv else None
 
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -421,7 +424,63 @@ def run_ours(args, rank, world, local_rank):
         res["verify"] = ver
     if pre is not None:
         res["prefill"] = pre
+    if conv is not None:
+        res["conv"] = conv
     return res
+
+
+def run_conv(args, torch, dev, rank, peak):
+    """Conv window (verify width, drafts kept) and its commit over distinct
+    per-layer buffers; HBM-bound."""
+    from linear_attention_state_rssm_gb300.store import ConvWindows
+    w_, c = WL, CONV
+    B, T, K, nl = c["batch"], c["T"], c["K"], c["layers"]
+    D = 2 * w_["HK"] * w_["dk"] + w_["HV"] * w_["dv"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4000 + rank)
+    cws = [ConvWindows(B, D, K, T, c["dtype"], device=dev) for _ in range(nl)]
+    for cw in cws:
+        cw.window.normal_(generator=gen)
+    x = torch.randn(nl, B * T, D, generator=gen, device=dev).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    w = torch.randn(nl, D, K, generator=gen, device=dev)
+    bias = torch.randn(nl, D, generator=gen, device=dev)
+    slot = torch.arange(B, dtype=torch.int32, device=dev)
+    acc = torch.randint(0, T + 1, (B,), generator=gen, device=dev, dtype=torch.int32)
+    ew = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ec = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    t_win = t_com = 0.0
+    for it in range(args.warmup + args.steps):
+        timed = it >= args.warmup
+        if timed:
+            ew[0].record()
+        for l in range(nl):
+            cws[l].rssm_conv_window(x[l], w[l], bias[l], slot, T, y[l], act="silu")
+        if timed:
+            ew[1].record()
+            ec[0].record()
+        for l in range(nl):
+            cws[l].rssm_conv_commit(slot, acc, T)
+        if timed:
+            ec[1].record()
+            torch.cuda.synchronize()
+            t_win += ew[0].elapsed_time(ew[1])
+            t_com += ec[0].elapsed_time(ec[1])
+    err = sum(int(cw.err_word.item()) for cw in cws)
+    n = args.steps * nl
+    ms_win, ms_com = t_win / n, t_com / n
+    # window: read the kept window, x and the taps, write y and the drafts
+    bytes_win = B * ((K - 1) * D * 2 + 3 * T * D * 2) + D * (K + 1) * 4
+    achieved = bytes_win / (ms_win / 1e3) / 1e9
+    del cws, x, y
+    torch.cuda.empty_cache()
+    return {"workload": c["workload"], "batch": B, "T": T, "K": K, "channels": D,
+            "layers": nl, "dtype": c["dtype"], "window_launch_ms": ms_win,
+            "commit_launch_ms": ms_com,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "bytes_per_launch": bytes_win,
+                         "kernel": "conv_window_kernel<4>"},
+            "device_error_word": err}
 
 
 def run_prefill(args, torch, dev, rank):
@@ -598,6 +657,7 @@ def main():
     ap.add_argument("--no-native", action="store_true",
                     help="skip the native fused-recurrent decode comparison line")
     ap.add_argument("--no-prefill", action="store_true", help="skip the replay prefill line")
+    ap.add_argument("--no-conv", action="store_true", help="skip the conv window line")
     ap.add_argument("--prefill-prompts", type=int, default=PREFILL["prompts"])
     ap.add_argument("--prefill-tokens", type=int, default=PREFILL["tokens"])
     args = ap.parse_args()

@@ -11,92 +11,162 @@
 // the commit makes the window the last K-1 rows of [window, x_0 .. x_{a-1}].
 // Decode commits its token at once.
 //
-// One thread per (row, channel): consecutive channels are consecutive
-// addresses in every buffer, so each access of a warp is one coalesced line;
-// the window and the taps stay in registers across the tokens. The work is a
-// few flops per byte: HBM-bound.
+// One thread per (row, 16 bytes of consecutive channels): every access is a
+// 16-byte vector and a warp's accesses are consecutive; a thread issues the
+// loads of up to eight tokens before it uses them, and keeps the window, the
+// taps and the bias in registers across the tokens. The work is a few flops
+// per byte: HBM-bound.
 #include "rssm_common.cuh"
 #include "rssm_launch.h"
 
 namespace rssm {
 
 constexpr int kConvThreads = 128;
+constexpr int kConvTok = 8;  // tokens whose loads are in flight together
 
-template <int K>
-__global__ void __launch_bounds__(kConvThreads) conv_window_kernel(const ConvParams p) {
-  const int c = blockIdx.x * kConvThreads + threadIdx.x, r = blockIdx.y;
-  if (c >= p.D) return;
-  const int s = p.slot[r];
-  if (s < 0) return;
-  if (s >= p.n_slots) {
-    if (c == 0 && p.err != nullptr) atomicOr(p.err, DEVERR_SLOT);
-    return;
-  }
-  const int D = p.D, T = p.T;
-  float taps[K], win[K - 1];
+// 16 bytes of EPV values (bf16 when EPV = 8, fp32 when EPV = 4) <-> fp32
+template <int EPV>
+__device__ __forceinline__ void unpack16(const uint4& u, float (&v)[EPV]) {
+  if (EPV == 4) {
+    v[0] = __uint_as_float(u.x);
+    v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z);
+    v[EPV - 1] = __uint_as_float(u.w);
+  } else {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-  for (int i = 0; i < K; ++i) taps[i] = p.w[(size_t)c * K + i];
-  const size_t wbase = (size_t)s * (K - 1) * D + c;
-#pragma unroll
-  for (int i = 0; i < K - 1; ++i) win[i] = ld_f32(p.window, wbase + (size_t)i * D, p.dt);
-  const float b = p.bias != nullptr ? p.bias[c] : 0.f;
-  for (int t = 0; t < T; ++t) {
-    const size_t xi = ((size_t)r * T + t) * D + c;
-    const float xt = ld_f32(p.x, xi, p.dt);
-    float acc = b;
-#pragma unroll
-    for (int i = 0; i < K - 1; ++i) acc = fmaf(taps[i], win[i], acc);
-    acc = fmaf(taps[K - 1], xt, acc);
-    if (p.act == CONV_ACT_SILU) acc = acc / (1.f + __expf(-acc));
-    st_f32(p.y, xi, p.dt, acc);
-    if (!p.commit_now) st_f32(p.draft, ((size_t)s * T + t) * D + c, p.dt, xt);
-#pragma unroll
-    for (int i = 0; i < K - 2; ++i) win[i] = win[i + 1];
-    win[K - 2] = xt;
-  }
-  if (p.commit_now) {
-#pragma unroll
-    for (int i = 0; i < K - 1; ++i) st_f32(p.window, wbase + (size_t)i * D, p.dt, win[i]);
+    for (int t = 0; t < 4; ++t) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[t]));
+      v[(2 * t) % EPV] = f.x;
+      v[(2 * t + 1) % EPV] = f.y;
+    }
   }
 }
 
-// window <- the last K-1 rows of [window, draft_0 .. draft_{a-1}]
-template <int K>
-__global__ void __launch_bounds__(kConvThreads) conv_commit_kernel(const ConvParams p) {
-  const int c = blockIdx.x * kConvThreads + threadIdx.x, r = blockIdx.y;
-  if (c >= p.D) return;
+template <int EPV>
+__device__ __forceinline__ uint4 pack16(const float (&v)[EPV]) {
+  if (EPV == 4) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                      __float_as_uint(v[EPV - 1]));
+  }
+  uint32_t w[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v[(2 * t) % EPV], v[(2 * t + 1) % EPV]);
+    w[t] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One thread per (row, group of EPV consecutive channels).
+template <int K, int EPV>
+__global__ void __launch_bounds__(kConvThreads) conv_window_kernel(const ConvParams p) {
+  const int D = p.D, T = p.T;
+  const int g = blockIdx.x * kConvThreads + threadIdx.x, r = blockIdx.y;
+  if (g * EPV >= D) return;
   const int s = p.slot[r];
   if (s < 0) return;
   if (s >= p.n_slots) {
-    if (c == 0 && p.err != nullptr) atomicOr(p.err, DEVERR_SLOT);
+    if (g == 0 && p.err != nullptr) atomicOr(p.err, DEVERR_SLOT);
+    return;
+  }
+  const int c0 = g * EPV, nv = D / EPV;  // 16-byte vectors per row of D channels
+  const uint4* x = static_cast<const uint4*>(p.x);
+  uint4* y = static_cast<uint4*>(p.y);
+  uint4* win_g = static_cast<uint4*>(p.window) + (size_t)s * (K - 1) * nv + g;
+  uint4* draft = static_cast<uint4*>(p.draft);
+
+  float taps[EPV][K], b[EPV], win[K - 1][EPV];
+#pragma unroll
+  for (int e = 0; e < EPV; ++e) {
+#pragma unroll
+    for (int i = 0; i < K; ++i) taps[e][i] = p.w[(size_t)(c0 + e) * K + i];
+    b[e] = p.bias != nullptr ? p.bias[c0 + e] : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < K - 1; ++i) unpack16<EPV>(win_g[(size_t)i * nv], win[i]);
+
+  for (int t0 = 0; t0 < T; t0 += kConvTok) {
+    uint4 xr[kConvTok];
+#pragma unroll
+    for (int u = 0; u < kConvTok; ++u) {
+      if (t0 + u < T) xr[u] = __ldg(x + ((size_t)r * T + t0 + u) * nv + g);
+    }
+#pragma unroll
+    for (int u = 0; u < kConvTok; ++u) {
+      if (t0 + u < T) {
+        const size_t xi = ((size_t)r * T + t0 + u) * nv + g;
+        float xv[EPV], yv[EPV];
+        unpack16<EPV>(xr[u], xv);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          float acc = b[e];
+#pragma unroll
+          for (int i = 0; i < K - 1; ++i) acc = fmaf(taps[e][i], win[i][e], acc);
+          acc = fmaf(taps[e][K - 1], xv[e], acc);
+          if (p.act == CONV_ACT_SILU) acc = acc / (1.f + __expf(-acc));
+          yv[e] = acc;
+        }
+        y[xi] = pack16<EPV>(yv);
+        if (!p.commit_now) draft[((size_t)s * T + t0 + u) * nv + g] = xr[u];
+#pragma unroll
+        for (int i = 0; i < K - 2; ++i) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) win[i][e] = win[i + 1][e];
+        }
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) win[K - 2][e] = xv[e];
+      }
+    }
+  }
+  if (p.commit_now) {
+#pragma unroll
+    for (int i = 0; i < K - 1; ++i) win_g[(size_t)i * nv] = pack16<EPV>(win[i]);
+  }
+}
+
+// window <- the last K-1 rows of [window, draft_0 .. draft_{a-1}] (raw copies)
+template <int K>
+__global__ void __launch_bounds__(kConvThreads) conv_commit_kernel(const ConvParams p) {
+  const int nv = p.D * dtype_bytes(p.dt) / 16;
+  const int g = blockIdx.x * kConvThreads + threadIdx.x, r = blockIdx.y;
+  if (g >= nv) return;
+  const int s = p.slot[r];
+  if (s < 0) return;
+  if (s >= p.n_slots) {
+    if (g == 0 && p.err != nullptr) atomicOr(p.err, DEVERR_SLOT);
     return;
   }
   const int a = p.accept[r];
   if (a < 0 || a > p.T) {
-    if (c == 0 && p.err != nullptr) atomicOr(p.err, DEVERR_ACCEPT);
+    if (g == 0 && p.err != nullptr) atomicOr(p.err, DEVERR_ACCEPT);
     return;
   }
-  const int D = p.D;
-  const size_t wbase = (size_t)s * (K - 1) * D + c;
-  float nw[K - 1];
+  uint4* win_g = static_cast<uint4*>(p.window) + (size_t)s * (K - 1) * nv + g;
+  const uint4* draft = static_cast<const uint4*>(p.draft);
+  uint4 nw[K - 1];
 #pragma unroll
   for (int i = 0; i < K - 1; ++i) {
     const int idx = a + i;  // position in [window (K-1 rows), drafts]
-    nw[i] = idx < K - 1 ? ld_f32(p.window, wbase + (size_t)idx * D, p.dt)
-                        : ld_f32(p.draft, ((size_t)s * p.T + idx - (K - 1)) * D + c, p.dt);
+    nw[i] = idx < K - 1 ? win_g[(size_t)idx * nv]
+                        : draft[((size_t)s * p.T + idx - (K - 1)) * nv + g];
   }
 #pragma unroll
-  for (int i = 0; i < K - 1; ++i) st_f32(p.window, wbase + (size_t)i * D, p.dt, nw[i]);
+  for (int i = 0; i < K - 1; ++i) win_g[(size_t)i * nv] = nw[i];
 }
 
 cudaError_t conv_launch(const ConvParams& p, bool commit, cudaStream_t st) {
-  const dim3 grid((unsigned)((p.D + kConvThreads - 1) / kConvThreads), (unsigned)p.B, 1);
+  const bool f32 = p.dt == DT_F32;
+  const int nv = p.D * (f32 ? 4 : 2) / 16;
+  const dim3 grid((unsigned)((nv + kConvThreads - 1) / kConvThreads), (unsigned)p.B, 1);
 #define RSSM_CONV_CASE(KV)                                                        \
   case KV:                                                                        \
     if (commit) {                                                                 \
       conv_commit_kernel<KV><<<grid, kConvThreads, 0, st>>>(p);                   \
+    } else if (f32) {                                                             \
+      conv_window_kernel<KV, 4><<<grid, kConvThreads, 0, st>>>(p);                \
     } else {                                                                      \
-      conv_window_kernel<KV><<<grid, kConvThreads, 0, st>>>(p);                   \
+      conv_window_kernel<KV, 8><<<grid, kConvThreads, 0, st>>>(p);                \
     }                                                                             \
     break;
   switch (p.K) {

@@ -415,9 +415,11 @@ static rssm_status conv_params(const void* x, const float* w, void* window, void
   if (dtype != RSSM_F32 && dtype != RSSM_BF16) return RSSM_ERR_UNSUPPORTED;
   if (!window || !slot) return RSSM_ERR_INVALID_ARG;
   if (!aligned4(slot)) return RSSM_ERR_INVALID_ARG;
-  (void)x;
+  // 16-byte vectors of channels: D a multiple of 16 bytes, buffers 16-byte aligned
+  if ((D * (dtype == RSSM_F32 ? 4 : 2)) % 16 != 0) return RSSM_ERR_UNSUPPORTED;
+  if (!aligned16(window) || (x && !aligned16(x)) || (draft && !aligned16(draft)))
+    return RSSM_ERR_INVALID_ARG;
   (void)w;
-  (void)draft;
   ConvParams& p = *out;
   p = ConvParams{};
   p.window = window;
@@ -441,6 +443,7 @@ rssm_status rssm_conv_window(const void* x, const float* w, const float* bias, v
   if (act != RSSM_CONV_ACT_NONE && act != RSSM_CONV_ACT_SILU) return RSSM_ERR_INVALID_ARG;
   if (B == 0) return RSSM_OK;
   if (!x || !w || !y || (!commit_now && !draft)) return RSSM_ERR_INVALID_ARG;
+  if (!aligned16(y)) return RSSM_ERR_INVALID_ARG;
   p.x = x;
   p.w = w;
   p.bias = bias;
