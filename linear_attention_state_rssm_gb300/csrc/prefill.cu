@@ -53,21 +53,63 @@ __device__ __forceinline__ void widen_store(float* dst, const uint4& u, int in_d
   }
 }
 
+// ---- warp-level tensor-core products (mma m16n8k8, tf32 in, fp32 accumulate).
+// Fragments, g = lane / 4, t = lane % 4: A (16 x 8) a0 (g, t), a1 (g + 8, t),
+// a2 (g, t + 4), a3 (g + 8, t + 4); B (8 x 8) b0 (t, g), b1 (t + 4, g);
+// C (16 x 8) c0 (g, 2t), c1 (g, 2t + 1), c2 (g + 8, 2t), c3 (g + 8, 2t + 1).
+// fp32 operands are split into a tf32 head and a tf32 tail, x = hi + lo, and a
+// product takes hi*hi + hi*lo + lo*hi, which keeps it at fp32 accuracy; an
+// operand that is exact in tf32 (bf16 values) has no tail.
+__device__ __forceinline__ uint32_t tf32_bits(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+struct Tf32 {
+  uint32_t hi, lo;
+};
+
+template <bool EXACT>
+__device__ __forceinline__ Tf32 tf32_split(float x) {
+  if (EXACT) return Tf32{__float_as_uint(x), 0u};
+  const uint32_t hi = tf32_bits(x);
+  return Tf32{hi, tf32_bits(x - __uint_as_float(hi))};
+}
+
+__device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// c += A B for split operands (the tail products first)
+template <bool EXACT_A, bool EXACT_B>
+__device__ __forceinline__ void mma_split(float (&c)[4], const Tf32 (&a)[4], const Tf32 (&b)[2]) {
+  if (!EXACT_A) mma_tf32(c, a[0].lo, a[1].lo, a[2].lo, a[3].lo, b[0].hi, b[1].hi);
+  if (!EXACT_B) mma_tf32(c, a[0].hi, a[1].hi, a[2].hi, a[3].hi, b[0].lo, b[1].lo);
+  mma_tf32(c, a[0].hi, a[1].hi, a[2].hi, a[3].hi, b[0].hi, b[1].hi);
+}
+
 template <int ALGO, typename ST, int CB, int INB>
 __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const PrefillParams p) {
   constexpr int PT = kPrefillThreads, PW = PT / 32;
   constexpr int C = kPrefillChunk;
-  constexpr int CQ = CB / 4;                  // column quads
-  constexpr int VT = 2 * C * CQ / PT;         // mat-vec vectors per thread (4 columns each)
-  constexpr int NRG = PT / CQ;                // row groups of the update
+  constexpr int CQ = CB / 4;                  // column quads of the state slice
   constexpr int XS = kPrefillXS, KS = kPrefillKS;
+  constexpr int SS = CB + 8, DS = CB + 8;     // row strides of S and of the deltas
+  constexpr int NTN = CB / 8;                 // 8-column tiles of a CB-wide product
+  // GDN mat-vec and pair inputs are the raw bf16 k, q: exact in tf32
+  constexpr bool EXACT_X = ALGO == ALGO_GDN && INB == 2;
   constexpr int EPU = 16 / INB;               // input values per 16-byte unit
   // 16-byte units of one chunk per thread (dk <= 128): q and k rows, v
   // columns, KDA gates
   constexpr int MQ = (C * 128 / EPU + PT - 1) / PT;
   constexpr int MV = (C * CB / EPU + PT - 1) / PT;
   constexpr int MG = ALGO == ALGO_KDA ? (C * 128 / 4 + PT - 1) / PT : 0;
-  static_assert((VT == 1 || VT == 2) && PT % CQ == 0, "prefill lane layout");
+  static_assert(PW == 8 && CB % 8 == 0, "prefill warp layout");
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int nb = p.dv / CB;
@@ -102,7 +144,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
   float* xT = reinterpret_cast<float*>(smem + p.sm.xT);
   float* kdT = xT;  // the update's decayed keys replace the mat-vec inputs
   float* y = reinterpret_cast<float*>(smem + p.sm.y);
-  float* part = y;  // GDN pair partial sums [PW][2C][C], before y is written
+  float* part = y;  // GDN pair partial sums [2][2C][C], before y is written
   float* dch = reinterpret_cast<float*>(smem + p.sm.dch);
   float* am = reinterpret_cast<float*>(smem + p.sm.am);
   float* fm = reinterpret_cast<float*>(smem + p.sm.fm);
@@ -229,33 +271,37 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
       }
     }
   };
-  // S <- e^{G_last} S + sum_j kd_j d_j^T (dch rows past the chunk are zero)
+  // S <- e^{G_last} S + sum_j kd_j d_j^T (dch rows past the chunk are zero):
+  // a [dk x C] x [C x CB] product on the tensor cores, the S tile as the fp32
+  // accumulator; warp w takes 8-column tile w % NTN of every 16-row tile
+  const int fg = lane >> 2, ft = lane & 3;  // fragment row group, thread in group
   auto update = [&](float dec) {
-    const int q4 = tid % CQ, rg0 = tid / CQ;
-    float4 dq[C];
+    const int ntiles = (dk / 16) * NTN;
+    const int nt = warp % NTN;
+    Tf32 bf[2][2];  // deltas: k-steps j0 = 0, 8
 #pragma unroll
-    for (int j = 0; j < C; ++j) dq[j] = ld4(dch + j * CB + 4 * q4);
-#pragma unroll 2
-    for (int row = rg0; row < dk; row += NRG) {
-      float4 s4 = ld4(S + row * CB + 4 * q4);
-      const float f = ALGO == ALGO_KDA ? decr[row] : dec;
-      s4.x *= f;
-      s4.y *= f;
-      s4.z *= f;
-      s4.w *= f;
+    for (int ks = 0; ks < 2; ++ks) {
+      bf[ks][0] = tf32_split<false>(dch[(8 * ks + ft) * DS + nt * 8 + fg]);
+      bf[ks][1] = tf32_split<false>(dch[(8 * ks + ft + 4) * DS + nt * 8 + fg]);
+    }
+    for (int id = warp; id < ntiles; id += PW) {
+      const int m0 = (id / NTN) * 16;
+      float* s0 = S + (m0 + fg) * SS + nt * 8 + 2 * ft;
+      float* s1 = s0 + 8 * SS;
+      const float2 u0 = *reinterpret_cast<const float2*>(s0);
+      const float2 u1 = *reinterpret_cast<const float2*>(s1);
+      const float f0 = ALGO == ALGO_KDA ? decr[m0 + fg] : dec;
+      const float f1 = ALGO == ALGO_KDA ? decr[m0 + fg + 8] : dec;
+      float acc[4] = {f0 * u0.x, f0 * u0.y, f1 * u1.x, f1 * u1.y};
 #pragma unroll
-      for (int j4 = 0; j4 < C; j4 += 4) {
-        const float4 kd = ld4(kdT + row * KS + j4);
-        const float kv[4] = {kd.x, kd.y, kd.z, kd.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          s4.x = fmaf(kv[u], dq[j4 + u].x, s4.x);
-          s4.y = fmaf(kv[u], dq[j4 + u].y, s4.y);
-          s4.z = fmaf(kv[u], dq[j4 + u].z, s4.z);
-          s4.w = fmaf(kv[u], dq[j4 + u].w, s4.w);
-        }
+      for (int ks = 0; ks < 2; ++ks) {
+        const float* kr = kdT + (m0 + fg) * KS + 8 * ks + ft;
+        const Tf32 af[4] = {tf32_split<false>(kr[0]), tf32_split<false>(kr[8 * KS]),
+                            tf32_split<false>(kr[4]), tf32_split<false>(kr[8 * KS + 4])};
+        mma_split<false, false>(acc, af, bf[ks]);
       }
-      *reinterpret_cast<float4*>(S + row * CB + 4 * q4) = s4;
+      *reinterpret_cast<float2*>(s0) = make_float2(acc[0], acc[1]);
+      *reinterpret_cast<float2*>(s1) = make_float2(acc[2], acc[3]);
     }
   };
 
@@ -267,7 +313,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
     const int row = e / CQ, q4 = e - row * CQ;
     float v4[4];
     ld_cols<ST, 4>(gtile + (size_t)row * dv + 4 * q4, v4);
-    *reinterpret_cast<float4*>(S + row * CB + 4 * q4) = make_float4(v4[0], v4[1], v4[2], v4[3]);
+    *reinterpret_cast<float4*>(S + row * SS + 4 * q4) = make_float4(v4[0], v4[1], v4[2], v4[3]);
   }
 
   // ---- committed state: replay the c ring records into S, 16 at a time
@@ -281,7 +327,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
     }
     for (int e = tid; e < C * CB; e += PT) {
       const int j = e / CB, col = e - j * CB;
-      dch[e] = j < nm ? ld_f32(p.ring_d, (sh * L + m0 + j) * dv + cb0 + col, p.rd_dt) : 0.f;
+      dch[j * DS + col] =
+          j < nm ? ld_f32(p.ring_d, (sh * L + m0 + j) * dv + cb0 + col, p.rd_dt) : 0.f;
     }
     if (ALGO == ALGO_GDN && warp == 0) gdn_scan(lane < nm ? p.ring_g[sh * L + m0 + lane] : 0.f, nm);
     __syncthreads();
@@ -296,7 +343,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
   }
 
   // ---- the prompt, chunk by chunk
-  const int cq = tid % CQ, vg = tid / CQ;  // mat-vec: columns 4cq.., vectors vg*VT..
   for (int ch = 0; ch < nchunks; ++ch) {
     const int t0 = ch * C, cn = min(C, n - t0);
     stage();
@@ -330,48 +376,28 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
     }
     __syncthreads();
 
-    // ---- GDN window coefficients: lane j of a half warp accumulates k_i.k_j
-    //      and q_i.k_j for every i over its channels (raw vectors; the
-    //      in-window decay and beta go on when the partial sums are combined)
+    // ---- GDN window coefficients: [K; Q] K^T over the key channels on the
+    //      tensor cores (raw vectors; the in-window decay and beta go on when
+    //      the two halves of the channels are combined). Warp w: 16-row block
+    //      (K or Q) and 8-column block of tile w % 4, channel half w / 4.
     if (ALGO == ALGO_GDN) {
       {
-        const int j = tid & 15, cgrp = tid >> 4;  // 16 channel groups
-        float kk[C], qk[C];
-#pragma unroll
-        for (int i = 0; i < C; ++i) {
-          kk[i] = 0.f;
-          qk[i] = 0.f;
+        const int tile = warp & 3, half = warp >> 2;
+        const int mq = (tile >> 1) * C, n8 = (tile & 1) * 8;
+        const int kspan = dk / 2;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k0 = half * kspan; k0 < (half + 1) * kspan; k0 += 8) {
+          const float* x0 = xT + (k0 + ft) * XS;
+          const float* x4 = x0 + 4 * XS;
+          const Tf32 af[4] = {tf32_split<EXACT_X>(x0[mq + fg]), tf32_split<EXACT_X>(x0[mq + fg + 8]),
+                              tf32_split<EXACT_X>(x4[mq + fg]), tf32_split<EXACT_X>(x4[mq + fg + 8])};
+          const Tf32 bf[2] = {tf32_split<EXACT_X>(x0[n8 + fg]), tf32_split<EXACT_X>(x4[n8 + fg])};
+          mma_split<EXACT_X, EXACT_X>(acc, af, bf);
         }
-        for (int ch = cgrp; ch < dk; ch += PT / 16) {
-          const float* xr = xT + ch * XS;
-          const float kj = xr[j];
-#pragma unroll
-          for (int i4 = 0; i4 < C; i4 += 4) {
-            const float4 k4 = ld4(xr + i4), q4v = ld4(xr + C + i4);
-            kk[i4] = fmaf(k4.x, kj, kk[i4]);
-            kk[i4 + 1] = fmaf(k4.y, kj, kk[i4 + 1]);
-            kk[i4 + 2] = fmaf(k4.z, kj, kk[i4 + 2]);
-            kk[i4 + 3] = fmaf(k4.w, kj, kk[i4 + 3]);
-            qk[i4] = fmaf(q4v.x, kj, qk[i4]);
-            qk[i4 + 1] = fmaf(q4v.y, kj, qk[i4 + 1]);
-            qk[i4 + 2] = fmaf(q4v.z, kj, qk[i4 + 2]);
-            qk[i4 + 3] = fmaf(q4v.w, kj, qk[i4 + 3]);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < C; ++i) {
-          kk[i] += __shfl_xor_sync(kFull, kk[i], 16);
-          qk[i] += __shfl_xor_sync(kFull, qk[i], 16);
-        }
-        // partial sums [warp][2C][C]: lane j of the lower half stores column j
-        if (lane < 16) {
-          float* pw = part + warp * 2 * C * C + j;
-#pragma unroll
-          for (int i = 0; i < C; ++i) {
-            pw[i * C] = kk[i];
-            pw[(C + i) * C] = qk[i];
-          }
-        }
+        // partial sums [half][2C][C]
+        float* pw = part + (half * 2 * C + mq + fg) * C + n8 + 2 * ft;
+        *reinterpret_cast<float2*>(pw) = make_float2(acc[0], acc[1]);
+        *reinterpret_cast<float2*>(pw + 8 * C) = make_float2(acc[2], acc[3]);
       }
       __syncthreads();
       // A_ij = beta_i e^{G_i - G_j} k_i.k_j (j < i), F_ij = e^{G_i - G_j} q_i.k_j (j <= i)
@@ -379,9 +405,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
         const int i = tid >> 4, j = tid & 15;
         float skk = 0.f, sqk = 0.f;
 #pragma unroll
-        for (int w = 0; w < PW; ++w) {
-          skk += part[(w * 2 * C + i) * C + j];
-          sqk += part[(w * 2 * C + C + i) * C + j];
+        for (int half = 0; half < 2; ++half) {
+          skk += part[(half * 2 * C + i) * C + j];
+          sqk += part[(half * 2 * C + C + i) * C + j];
         }
         const bool on = i < cn && j <= i;
         const float wgt = on ? __expf(G[i] - G[j]) : 0.f;
@@ -391,88 +417,42 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
       __syncthreads();
     }
 
-    // ---- y_v = S^T x_v
-    if (CB == 64) {
-      // four columns x eight vectors per thread over a quarter of the rows
-      // (rows kq, kq + 4, ...: the four quarters of a step read four
-      // consecutive rows, on distinct banks), summed over the quarters by
-      // shuffles; lane = column quad (low 3 bits) + 8 quarter, warp = column
-      // half + 2 vector octet
-      const int cqm = (warp & 1) * 8 + (lane & 7), kq = lane >> 3, vo = warp >> 1;
-      float acc[8][4];
+    // ---- y_v = S^T x_v for the 2C vectors: Y [2C x CB] = X^T S on the tensor
+    //      cores; warp w takes 16-vector block and 8-column blocks
+    //      TPW w, TPW w + 1, ...
+    {
+      constexpr int TPW = 2 * NTN / PW > 0 ? 2 * NTN / PW : 1;
+      const int id0 = warp * TPW;
+      const int v0 = (id0 / NTN) * 16;
+      float acc[TPW][4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[u][q] = 0.f;
-      }
-      const float* sp = S + 4 * cqm;
-      const float* xp = xT + 8 * vo;
-#pragma unroll 2
-      for (int row = kq; row < dk; row += 4) {
-        const float4 s4 = ld4(sp + row * CB);
-        const float4 xa = ld4(xp + row * XS), xb = ld4(xp + row * XS + 4);
-        const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          acc[u][0] = fmaf(s4.x, xv[u], acc[u][0]);
-          acc[u][1] = fmaf(s4.y, xv[u], acc[u][1]);
-          acc[u][2] = fmaf(s4.z, xv[u], acc[u][2]);
-          acc[u][3] = fmaf(s4.w, xv[u], acc[u][3]);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[u][q] += __shfl_xor_sync(kFull, acc[u][q], 8);
-          acc[u][q] += __shfl_xor_sync(kFull, acc[u][q], 16);
-        }
-      }
-      // quarter kq stores vectors 2kq, 2kq + 1 of the octet
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if ((u >> 1) == kq) {
-          const int vv = 8 * vo + u;
-          const float f = ALGO == ALGO_GDN ? eG[vv < C ? vv : vv - C] : 1.f;
-          *reinterpret_cast<float4*>(y + vv * CB + 4 * cqm) =
-              make_float4(f * acc[u][0], f * acc[u][1], f * acc[u][2], f * acc[u][3]);
-        }
-      }
-    } else {
-      // four columns and VT vectors per thread over all rows
-      float acc[VT][4];
-#pragma unroll
-      for (int u = 0; u < VT; ++u) {
+      for (int u = 0; u < TPW; ++u) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[u][q] = 0.f;
       }
-      const float* sp = S + 4 * cq;
-      const float* xp = xT + vg * VT;
-#pragma unroll 4
-      for (int row = 0; row < dk; ++row) {
-        const float4 s4 = ld4(sp + row * CB);
-        float xv[VT];
-        if (VT == 2) {
-          const float2 x2 = *reinterpret_cast<const float2*>(xp + row * XS);
-          xv[0] = x2.x;
-          xv[VT - 1] = x2.y;
-        } else {
-          xv[0] = xp[row * XS];
+      if (id0 < 2 * NTN) {
+        for (int k0 = 0; k0 < dk; k0 += 8) {
+          const float* x0 = xT + (k0 + ft) * XS + v0 + fg;
+          const float* x4 = x0 + 4 * XS;
+          const Tf32 af[4] = {tf32_split<EXACT_X>(x0[0]), tf32_split<EXACT_X>(x0[8]),
+                              tf32_split<EXACT_X>(x4[0]), tf32_split<EXACT_X>(x4[8])};
+#pragma unroll
+          for (int u = 0; u < TPW; ++u) {
+            const int n0 = ((id0 + u) % NTN) * 8;
+            const float* s0 = S + (k0 + ft) * SS + n0 + fg;
+            const Tf32 bf[2] = {tf32_split<false>(s0[0]), tf32_split<false>(s0[4 * SS])};
+            mma_split<EXACT_X, false>(acc[u], af, bf);
+          }
         }
 #pragma unroll
-        for (int u = 0; u < VT; ++u) {
-          acc[u][0] = fmaf(s4.x, xv[u], acc[u][0]);
-          acc[u][1] = fmaf(s4.y, xv[u], acc[u][1]);
-          acc[u][2] = fmaf(s4.z, xv[u], acc[u][2]);
-          acc[u][3] = fmaf(s4.w, xv[u], acc[u][3]);
+        for (int u = 0; u < TPW; ++u) {
+          const int n0 = ((id0 + u) % NTN) * 8 + 2 * ft;
+          const int va = v0 + fg, vb = va + 8;
+          const float fa = ALGO == ALGO_GDN ? eG[va < C ? va : va - C] : 1.f;
+          const float fb = ALGO == ALGO_GDN ? eG[vb < C ? vb : vb - C] : 1.f;
+          *reinterpret_cast<float2*>(y + va * CB + n0) = make_float2(fa * acc[u][0], fa * acc[u][1]);
+          *reinterpret_cast<float2*>(y + vb * CB + n0) = make_float2(fb * acc[u][2], fb * acc[u][3]);
         }
-      }
-#pragma unroll
-      for (int u = 0; u < VT; ++u) {
-        const int vv = vg * VT + u;
-        const float f = ALGO == ALGO_GDN ? eG[vv < C ? vv : vv - C] : 1.f;
-        *reinterpret_cast<float4*>(y + vv * CB + 4 * cq) =
-            make_float4(f * acc[u][0], f * acc[u][1], f * acc[u][2], f * acc[u][3]);
       }
     }
     __syncthreads();
@@ -494,7 +474,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
           for (int j = 0; j <= i; ++j) oi = fmaf(fm[i * C + j], d[j], oi);
           st_f32(p.o, (((size_t)a0 + t0 + i) * HV + h) * dv + cb0 + tid, p.in_dt, p.scale * oi);
         }
-        dch[i * CB + tid] = d[i];
+        dch[i * DS + tid] = d[i];
       }
     } else {
       build_kd(cn, tid - CB, PT - CB);
@@ -510,7 +490,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
   // ---- the checkpoint takes the state (rounded to its dtype)
   for (int e = tid; e < dk * CQ; e += PT) {
     const int row = e / CQ, q4 = e - row * CQ;
-    const float4 s4 = ld4(S + row * CB + 4 * q4);
+    const float4 s4 = ld4(S + row * SS + 4 * q4);
     float v4[4] = {s4.x, s4.y, s4.z, s4.w};
     st_cols<ST, 4>(gtile + (size_t)row * dv + 4 * q4, v4);
   }

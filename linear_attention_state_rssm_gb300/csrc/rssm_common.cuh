@@ -222,14 +222,14 @@ constexpr int kPrefillChunk = 16;     // prompt tokens per step of the prefill s
 constexpr int kPrefillThreads = 256;  // threads of a prefill CTA
 
 struct PrefillSmem {
-  uint32_t S;     // [dk][CB]  fp32 state columns of this CTA
+  uint32_t S;     // [dk][CB + 8]  fp32 state columns of this CTA (row stride CB + 8)
   uint32_t wq;    // [C][dk]   fp32 chunk q
   uint32_t wk;    // [C][dk]   fp32 chunk k (history replay: ring keys)
   uint32_t wv;    // [C][CB]   fp32 chunk v columns
   uint32_t xT;    // [dk][kPrefillXS] mat-vec inputs per key channel; then the update's
                   // decayed keys [dk][kPrefillKS]
   uint32_t y;     // [2C][CB]  S^T k_i, S^T q_i (decay applied); first the GDN pair sums
-  uint32_t dch;   // [C][CB]   chunk deltas (history replay: ring deltas)
+  uint32_t dch;   // [C][CB + 8]  chunk deltas (history replay: ring deltas)
   uint32_t am;    // [C][C]
   uint32_t fm;    // [C][C]
   uint32_t G;     // GDN [C] / KDA [C][dk] in-chunk inclusive gate prefixes
@@ -264,9 +264,11 @@ struct PrefillParams {
 // Value columns per prefill CTA (the columns of the delta rule are independent).
 __host__ __device__ constexpr int prefill_cb(int dv) { return dv < 64 ? dv : 64; }
 
-// Row strides (floats) of the transposed per-channel arrays: four floats of
-// padding keep the 16-byte stores of consecutive channels on distinct banks.
-constexpr int kPrefillXS = 2 * kPrefillChunk + 4;
+// Row strides (floats) of the per-channel arrays. The padding puts the
+// tensor-core fragment loads (lanes over 4 rows x 8 columns) on 32 distinct
+// banks: row strides of 8 (mod 32) floats for the mat-vec and pair inputs,
+// of 20 for the update's keys, and CB + 8 for the state and the deltas.
+constexpr int kPrefillXS = 2 * kPrefillChunk + 8;
 constexpr int kPrefillKS = kPrefillChunk + 4;
 
 __host__ __device__ inline PrefillSmem prefill_layout(int algo, int dk, int dv) {
@@ -275,14 +277,14 @@ __host__ __device__ inline PrefillSmem prefill_layout(int algo, int dk, int dv) 
   const bool kda = algo == ALGO_KDA;
   PrefillSmem m{};
   uint32_t off = 0;
-  m.S = off;     off = align16(off + 4u * dk * CB);
+  m.S = off;     off = align16(off + 4u * dk * (CB + 8));
   m.wq = off;    off = align16(off + 4u * C * dk);
   m.wk = off;    off = align16(off + 4u * C * dk);
   m.wv = off;    off = align16(off + 4u * C * CB);
   m.xT = off;    off = align16(off + 4u * dk * kPrefillXS);
-  // y also holds the GDN pair partial sums [8][2C][C] before the mat-vec
-  m.y = off;     off = align16(off + 4u * (2 * C * CB > 16 * C * C ? 2 * C * CB : 16 * C * C));
-  m.dch = off;   off = align16(off + 4u * C * CB);
+  // y also holds the GDN pair partial sums [2][2C][C] before the mat-vec
+  m.y = off;     off = align16(off + 4u * (2 * C * CB > 4 * C * C ? 2 * C * CB : 4 * C * C));
+  m.dch = off;   off = align16(off + 4u * C * (CB + 8));
   m.am = off;    off = align16(off + 4u * C * C);
   m.fm = off;    off = align16(off + 4u * C * C);
   m.G = off;     off = align16(off + 4u * (kda ? C * dk : C));
