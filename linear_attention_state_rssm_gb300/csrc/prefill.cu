@@ -103,12 +103,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
   constexpr int NTN = CB / 8;                 // 8-column tiles of a CB-wide product
   // GDN mat-vec and pair inputs are the raw bf16 k, q: exact in tf32
   constexpr bool EXACT_X = ALGO == ALGO_GDN && INB == 2;
+  // Warps 0-1 solve a chunk while warps 2-7 (the preparing warps) stage the
+  // next one and build its mat-vec inputs and window coefficients.
+  constexpr int PREP0 = 2 * 32, NP = PT - PREP0;
   constexpr int EPU = 16 / INB;               // input values per 16-byte unit
-  // 16-byte units of one chunk per thread (dk <= 128): q and k rows, v
-  // columns, KDA gates
-  constexpr int MQ = (C * 128 / EPU + PT - 1) / PT;
-  constexpr int MV = (C * CB / EPU + PT - 1) / PT;
-  constexpr int MG = ALGO == ALGO_KDA ? (C * 128 / 4 + PT - 1) / PT : 0;
+  // 16-byte units of one chunk per preparing thread (dk <= 128): q and k
+  // rows, v columns, KDA gates
+  constexpr int MQ = (C * 128 / EPU + NP - 1) / NP;
+  constexpr int MV = (C * CB / EPU + NP - 1) / NP;
+  constexpr int MG = ALGO == ALGO_KDA ? (C * 128 / 4 + NP - 1) / NP : 0;
   static_assert(PW == 8 && CB % 8 == 0, "prefill warp layout");
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -117,6 +120,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int dk = p.dk, dv = p.dv, L = p.L, HV = p.HV, HK = p.HK, kh = h / p.G;
   const bool reporter = tid == 0 && blockIdx.x == 0;
+  const bool prep = tid >= PREP0;
+  const int lt = tid - PREP0;  // index among the preparing threads
 
   const int s = p.slot[r];
   if (s < 0) return;
@@ -140,32 +145,34 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
   float* S = reinterpret_cast<float*>(smem + p.sm.S);
   float* wq = reinterpret_cast<float*>(smem + p.sm.wq);
   float* wk = reinterpret_cast<float*>(smem + p.sm.wk);
-  float* wv = reinterpret_cast<float*>(smem + p.sm.wv);
+  float* wv2 = reinterpret_cast<float*>(smem + p.sm.wv);
   float* xT = reinterpret_cast<float*>(smem + p.sm.xT);
-  float* kdT = xT;  // the update's decayed keys replace the mat-vec inputs
+  float* kdT = reinterpret_cast<float*>(smem + p.sm.kdT);
   float* y = reinterpret_cast<float*>(smem + p.sm.y);
-  float* part = y;  // GDN pair partial sums [2][2C][C], before y is written
+  float* part = reinterpret_cast<float*>(smem + p.sm.part);
   float* dch = reinterpret_cast<float*>(smem + p.sm.dch);
-  float* am = reinterpret_cast<float*>(smem + p.sm.am);
-  float* fm = reinterpret_cast<float*>(smem + p.sm.fm);
+  float* am2 = reinterpret_cast<float*>(smem + p.sm.am);
+  float* fm2 = reinterpret_cast<float*>(smem + p.sm.fm);
   float* G = reinterpret_cast<float*>(smem + p.sm.G);
   float* eG = reinterpret_cast<float*>(smem + p.sm.eG);
   float* ekd = reinterpret_cast<float*>(smem + p.sm.ekd);
-  float* wb = reinterpret_cast<float*>(smem + p.sm.wb);
-  float* decr = reinterpret_cast<float*>(smem + p.sm.decr);
+  float* wb2 = reinterpret_cast<float*>(smem + p.sm.wb);
+  float* decr2 = reinterpret_cast<float*>(smem + p.sm.decr);
 
   const int uq = dk / EPU, uv = CB / EPU, ug = dk / 4;  // 16-byte units per row
   const int nchunks = (n + C - 1) / C;
+  const int fg = lane >> 2, ft = lane & 3;  // fragment row group, thread in group
 
-  // ---- the next chunk's inputs, loaded into registers one chunk ahead
+  // ---- a chunk's inputs, loaded into registers of the preparing threads
+  //      one chunk ahead
   uint4 rq[MQ], rk[MQ], rv[MV], rg[MG > 0 ? MG : 1];
-  float rb = 0.f, rgg = 0.f;  // beta and GDN gate of token tid of the chunk
+  float rb = 0.f, rgg = 0.f;  // beta and GDN gate of token lt of the chunk
   auto prefetch = [&](int ch) {
     const int t0 = ch * C, cn = min(C, n - t0);
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int m = 0; m < MQ; ++m) {
-      const int u = tid + m * PT, i = u / uq, pu = u - i * uq;
+      const int u = lt + m * NP, i = u / uq, pu = u - i * uq;
       rq[m] = z;
       rk[m] = z;
       if (u < C * uq && i < cn) {
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
     }
 #pragma unroll
     for (int m = 0; m < MV; ++m) {
-      const int u = tid + m * PT, i = u / uv, pu = u - i * uv;
+      const int u = lt + m * NP, i = u / uv, pu = u - i * uv;
       rv[m] = z;
       if (u < C * uv && i < cn) {
         const size_t off = ((((size_t)a0 + t0 + i) * HV + h) * dv + cb0) * INB;
@@ -187,7 +194,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
     }
 #pragma unroll
     for (int m = 0; m < MG; ++m) {
-      const int u = tid + m * PT, i = u / ug, pu = u - i * ug;
+      const int u = lt + m * NP, i = u / ug, pu = u - i * ug;
       rg[m] = z;
       if (u < C * ug && i < cn) {
         const size_t off = (((size_t)a0 + t0 + i) * HV + h) * dk;
@@ -196,17 +203,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
     }
     rb = 0.f;
     rgg = 0.f;
-    if (tid < cn) {
-      const size_t tok = (size_t)a0 + t0 + tid;
+    if (lt < cn) {
+      const size_t tok = (size_t)a0 + t0 + lt;
       rb = __ldg(p.beta + tok * HV + h);
       if (ALGO == ALGO_GDN) rgg = __ldg(p.g + tok * HV + h);
     }
   };
   // registers -> fp32 chunk arrays (rows past the chunk are zero)
-  auto stage = [&]() {
+  auto stage = [&](float* wv, float* wb) {
 #pragma unroll
     for (int m = 0; m < MQ; ++m) {
-      const int u = tid + m * PT, i = u / uq, pu = u - i * uq;
+      const int u = lt + m * NP, i = u / uq, pu = u - i * uq;
       if (u < C * uq) {
         widen_store<INB>(wq + i * dk + pu * EPU, rq[m], p.in_dt);
         widen_store<INB>(wk + i * dk + pu * EPU, rk[m], p.in_dt);
@@ -214,17 +221,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
     }
 #pragma unroll
     for (int m = 0; m < MV; ++m) {
-      const int u = tid + m * PT, i = u / uv, pu = u - i * uv;
+      const int u = lt + m * NP, i = u / uv, pu = u - i * uv;
       if (u < C * uv) widen_store<INB>(wv + i * CB + pu * EPU, rv[m], p.in_dt);
     }
 #pragma unroll
     for (int m = 0; m < MG; ++m) {
-      const int u = tid + m * PT, i = u / ug, pu = u - i * ug;
+      const int u = lt + m * NP, i = u / ug, pu = u - i * ug;
       if (u < C * ug) widen_store<4>(G + i * dk + pu * 4, rg[m], DT_F32);
     }
-    if (tid < C) wb[tid] = rb;
+    if (lt < C) wb[lt] = rb;
   };
-  // GDN, warp 0: inclusive prefix of the nm gates x (lane i holds gate i),
+  // GDN, one warp: inclusive prefix of the nm gates x (lane i holds gate i),
   // G[i], eG[i] = e^{G_i}, ekd[i] = e^{G_last - G_i}
   auto gdn_scan = [&](float x, int nm) {
 #pragma unroll
@@ -241,8 +248,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
   };
   // KDA, one thread per key channel: in-place inclusive prefix of G rows
   // [0, nm) and the channel's total decay
-  auto kda_scan = [&](int nm) {
-    for (int ch = tid; ch < dk; ch += PT) {
+  auto kda_scan = [&](int nm, float* decr, int t, int nt) {
+    for (int ch = t; ch < dk; ch += nt) {
       float acc = 0.f;
       for (int i = 0; i < nm; ++i) {
         acc += G[i * dk + ch];
@@ -274,8 +281,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
   // S <- e^{G_last} S + sum_j kd_j d_j^T (dch rows past the chunk are zero):
   // a [dk x C] x [C x CB] product on the tensor cores, the S tile as the fp32
   // accumulator; warp w takes 8-column tile w % NTN of every 16-row tile
-  const int fg = lane >> 2, ft = lane & 3;  // fragment row group, thread in group
-  auto update = [&](float dec) {
+  auto update = [&](float dec, const float* decr) {
     const int ntiles = (dk / 16) * NTN;
     const int nt = warp % NTN;
     Tf32 bf[2][2];  // deltas: k-steps j0 = 0, 8
@@ -304,8 +310,72 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
       *reinterpret_cast<float2*>(s1) = make_float2(acc[2], acc[3]);
     }
   };
+  // The next chunk on the preparing warps (named barrier 1): stage it, its gate
+  // prefixes, mat-vec inputs per key channel (k_i at [0, C), q_i at [C, 2C);
+  // KDA: decayed by e^{G_i}), and its window coefficients
+  //     A_ij = beta_i e^{G_i - G_j} k_i.k_j (j < i), F_ij = e^{G_i - G_j} q_i.k_j (j <= i)
+  auto prepare = [&](int ch) {
+    const int b = ch & 1, cn = min(C, n - ch * C);
+    float* am = am2 + b * C * C;
+    float* fm = fm2 + b * C * C;
+    float* wb = wb2 + b * C;
+    stage(wv2 + b * C * CB, wb);
+    if (ALGO == ALGO_GDN && warp == 2) gdn_scan(rgg, cn);
+    if (ch + 1 < nchunks) prefetch(ch + 1);  // after the scan has read this chunk's gates
+    named_sync(1, NP);
+    if (ALGO == ALGO_KDA) {
+      kda_scan(cn, decr2 + b * dk, lt, NP);
+      named_sync(1, NP);
+    }
+    for (int e = lt; e < 2 * dk; e += NP) {
+      const int row = e >> 1, half = e & 1;
+      const float* src = half ? wq : wk;
+      float x[C];
+#pragma unroll
+      for (int i = 0; i < C; ++i) {
+        const float f = (ALGO == ALGO_KDA && i < cn) ? __expf(G[i * dk + row]) : 1.f;
+        x[i] = f * src[i * dk + row];
+      }
+#pragma unroll
+      for (int i4 = 0; i4 < C; i4 += 4) {
+        *reinterpret_cast<float4*>(xT + row * XS + half * C + i4) =
+            make_float4(x[i4], x[i4 + 1], x[i4 + 2], x[i4 + 3]);
+      }
+    }
+    if (ALGO == ALGO_KDA) {
+      window_pairs<ALGO, C>(cn, dk, wk, wq, G, wb, am, fm, warp - 2, PW - 2, lane);
+      return;
+    }
+    named_sync(1, NP);
+    // [K; Q] K^T over the key channels on the tensor cores (raw vectors):
+    // warps 2-5, one 16 x 8 tile each
+    if (warp < 6) {
+      const int tile = warp - 2;
+      const int mq = (tile >> 1) * C, n8 = (tile & 1) * 8;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int k0 = 0; k0 < dk; k0 += 8) {
+        const float* x0 = xT + (k0 + ft) * XS;
+        const float* x4 = x0 + 4 * XS;
+        const Tf32 af[4] = {tf32_split<EXACT_X>(x0[mq + fg]), tf32_split<EXACT_X>(x0[mq + fg + 8]),
+                            tf32_split<EXACT_X>(x4[mq + fg]), tf32_split<EXACT_X>(x4[mq + fg + 8])};
+        const Tf32 bf[2] = {tf32_split<EXACT_X>(x0[n8 + fg]), tf32_split<EXACT_X>(x4[n8 + fg])};
+        mma_split<EXACT_X, EXACT_X>(acc, af, bf);
+      }
+      float* pw = part + (mq + fg) * C + n8 + 2 * ft;
+      *reinterpret_cast<float2*>(pw) = make_float2(acc[0], acc[1]);
+      *reinterpret_cast<float2*>(pw + 8 * C) = make_float2(acc[2], acc[3]);
+    }
+    named_sync(1, NP);
+    for (int e = lt; e < C * C; e += NP) {
+      const int i = e >> 4, j = e & 15;
+      const bool on = i < cn && j <= i;
+      const float wgt = on ? __expf(G[i] - G[j]) : 0.f;
+      fm[e] = on ? wgt * part[(C + i) * C + j] : 0.f;
+      am[e] = (on && j < i) ? wb[i] * wgt * part[i * C + j] : 0.f;
+    }
+  };
 
-  prefetch(0);
+  if (prep) prefetch(0);
 
   // ---- the checkpoint slice -> fp32 S [dk][CB]
   ST* gtile = static_cast<ST*>(p.state) + ((size_t)s * HV + h) * dk * dv + cb0;
@@ -333,93 +403,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
     if (ALGO == ALGO_GDN && warp == 0) gdn_scan(lane < nm ? p.ring_g[sh * L + m0 + lane] : 0.f, nm);
     __syncthreads();
     if (ALGO == ALGO_KDA) {
-      kda_scan(nm);
+      kda_scan(nm, decr2, tid, PT);
       __syncthreads();
     }
     build_kd(nm, tid, PT);
     __syncthreads();
-    update(ALGO == ALGO_GDN ? __expf(G[nm - 1]) : 1.f);
+    update(ALGO == ALGO_GDN ? __expf(G[nm - 1]) : 1.f, decr2);
     __syncthreads();
   }
 
-  // ---- the prompt, chunk by chunk
+  // ---- the prompt, chunk by chunk: (A) mat-vec, (B) solve || prepare the
+  //      next chunk, (C) update
+  if (prep) prepare(0);
+  __syncthreads();
   for (int ch = 0; ch < nchunks; ++ch) {
-    const int t0 = ch * C, cn = min(C, n - t0);
-    stage();
-    if (ALGO == ALGO_GDN && warp == 0) gdn_scan(rgg, cn);
-    if (ch + 1 < nchunks) prefetch(ch + 1);
-    __syncthreads();
-    if (ALGO == ALGO_KDA) {
-      kda_scan(cn);
-      __syncthreads();
-    }
-
-    // ---- mat-vec inputs per key channel: k_i at [0, C), q_i at [C, 2C)
-    //      (KDA: decayed by e^{G_i} per channel); half the threads each
-    for (int e = tid; e < 2 * dk; e += PT) {
-      const int row = e >> 1, half = e & 1;
-      const float* src = half ? wq : wk;
-      float x[C];
-#pragma unroll
-      for (int i = 0; i < C; ++i) {
-        const float f = (ALGO == ALGO_KDA && i < cn) ? __expf(G[i * dk + row]) : 1.f;
-        x[i] = f * src[i * dk + row];
-      }
-#pragma unroll
-      for (int i4 = 0; i4 < C; i4 += 4) {
-        *reinterpret_cast<float4*>(xT + row * XS + half * C + i4) =
-            make_float4(x[i4], x[i4 + 1], x[i4 + 2], x[i4 + 3]);
-      }
-    }
-    if (ALGO == ALGO_KDA) {
-      window_pairs<ALGO, C>(cn, dk, wk, wq, G, wb, am, fm, warp, PW, lane);
-    }
-    __syncthreads();
-
-    // ---- GDN window coefficients: [K; Q] K^T over the key channels on the
-    //      tensor cores (raw vectors; the in-window decay and beta go on when
-    //      the two halves of the channels are combined). Warp w: 16-row block
-    //      (K or Q) and 8-column block of tile w % 4, channel half w / 4.
-    if (ALGO == ALGO_GDN) {
-      {
-        const int tile = warp & 3, half = warp >> 2;
-        const int mq = (tile >> 1) * C, n8 = (tile & 1) * 8;
-        const int kspan = dk / 2;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int k0 = half * kspan; k0 < (half + 1) * kspan; k0 += 8) {
-          const float* x0 = xT + (k0 + ft) * XS;
-          const float* x4 = x0 + 4 * XS;
-          const Tf32 af[4] = {tf32_split<EXACT_X>(x0[mq + fg]), tf32_split<EXACT_X>(x0[mq + fg + 8]),
-                              tf32_split<EXACT_X>(x4[mq + fg]), tf32_split<EXACT_X>(x4[mq + fg + 8])};
-          const Tf32 bf[2] = {tf32_split<EXACT_X>(x0[n8 + fg]), tf32_split<EXACT_X>(x4[n8 + fg])};
-          mma_split<EXACT_X, EXACT_X>(acc, af, bf);
-        }
-        // partial sums [half][2C][C]
-        float* pw = part + (half * 2 * C + mq + fg) * C + n8 + 2 * ft;
-        *reinterpret_cast<float2*>(pw) = make_float2(acc[0], acc[1]);
-        *reinterpret_cast<float2*>(pw + 8 * C) = make_float2(acc[2], acc[3]);
-      }
-      __syncthreads();
-      // A_ij = beta_i e^{G_i - G_j} k_i.k_j (j < i), F_ij = e^{G_i - G_j} q_i.k_j (j <= i)
-      {
-        const int i = tid >> 4, j = tid & 15;
-        float skk = 0.f, sqk = 0.f;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          skk += part[(half * 2 * C + i) * C + j];
-          sqk += part[(half * 2 * C + C + i) * C + j];
-        }
-        const bool on = i < cn && j <= i;
-        const float wgt = on ? __expf(G[i] - G[j]) : 0.f;
-        fm[i * C + j] = on ? wgt * sqk : 0.f;
-        am[i * C + j] = (on && j < i) ? wb[i] * wgt * skk : 0.f;
-      }
-      __syncthreads();
-    }
-
-    // ---- y_v = S^T x_v for the 2C vectors: Y [2C x CB] = X^T S on the tensor
-    //      cores; warp w takes 16-vector block and 8-column blocks
-    //      TPW w, TPW w + 1, ...
+    const int b = ch & 1, t0 = ch * C, cn = min(C, n - t0);
+    // ---- (A) y_v = S^T x_v for the 2C vectors: Y [2C x CB] = X^T S on the
+    //      tensor cores; warp w takes the 16-vector block and the 8-column
+    //      blocks TPW w, TPW w + 1, ...
     {
       constexpr int TPW = 2 * NTN / PW > 0 ? 2 * NTN / PW : 1;
       const int id0 = warp * TPW;
@@ -455,11 +456,18 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
         }
       }
     }
+    // the chunk's decay, read before the next chunk's gate scan
+    const float dec = ALGO == ALGO_GDN ? eG[cn - 1] : 1.f;
     __syncthreads();
 
-    // ---- per column: triangular solve and outputs; meanwhile the other
-    //      threads build the update's decayed keys (over xT, now free)
+    // ---- (B) per column: triangular solve and outputs, on warps 0-1; the
+    //      preparing warps build this chunk's decayed keys, then prepare the
+    //      next chunk
     if (tid < CB) {
+      const float* am = am2 + b * C * C;
+      const float* fm = fm2 + b * C * C;
+      const float* wv = wv2 + b * C * CB;
+      const float* wb = wb2 + b * C;
       float d[C];
 #pragma unroll
       for (int i = 0; i < C; ++i) {
@@ -476,16 +484,18 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
         }
         dch[i * DS + tid] = d[i];
       }
-    } else {
-      build_kd(cn, tid - CB, PT - CB);
+    } else if (prep) {
+      build_kd(cn, lt, NP);
+      if (ch + 1 < nchunks) {
+        named_sync(1, NP);  // the keys of this chunk are read before the next lands
+        prepare(ch + 1);
+      }
     }
-    // the chunk's decay, read before warp 0 may scan the next chunk's gates
-    const float dec = ALGO == ALGO_GDN ? eG[cn - 1] : 1.f;
     __syncthreads();
-    // (the next chunk's staging writes none of what the update reads)
-    update(dec);
+    // ---- (C) rank-16 update of the state slice
+    update(dec, decr2 + b * dk);
+    __syncthreads();
   }
-  __syncthreads();
 
   // ---- the checkpoint takes the state (rounded to its dtype)
   for (int e = tid; e < dk * CQ; e += PT) {

@@ -221,22 +221,25 @@ struct ConvParams {
 constexpr int kPrefillChunk = 16;     // prompt tokens per step of the prefill scan
 constexpr int kPrefillThreads = 256;  // threads of a prefill CTA
 
+// Chunk arrays marked x2 have one copy per chunk parity: the next chunk is
+// prepared while the current one is solved.
 struct PrefillSmem {
   uint32_t S;     // [dk][CB + 8]  fp32 state columns of this CTA (row stride CB + 8)
   uint32_t wq;    // [C][dk]   fp32 chunk q
   uint32_t wk;    // [C][dk]   fp32 chunk k (history replay: ring keys)
-  uint32_t wv;    // [C][CB]   fp32 chunk v columns
-  uint32_t xT;    // [dk][kPrefillXS] mat-vec inputs per key channel; then the update's
-                  // decayed keys [dk][kPrefillKS]
-  uint32_t y;     // [2C][CB]  S^T k_i, S^T q_i (decay applied); first the GDN pair sums
+  uint32_t wv;    // x2 [C][CB]  fp32 chunk v columns
+  uint32_t xT;    // [dk][kPrefillXS] mat-vec and pair inputs per key channel
+  uint32_t kdT;   // [dk][kPrefillKS] the update's decayed keys
+  uint32_t y;     // [2C][CB]  S^T k_i, S^T q_i (decay applied)
+  uint32_t part;  // [2C][C]   GDN pair sums k_i.k_j, q_i.k_j
   uint32_t dch;   // [C][CB + 8]  chunk deltas (history replay: ring deltas)
-  uint32_t am;    // [C][C]
-  uint32_t fm;    // [C][C]
+  uint32_t am;    // x2 [C][C]
+  uint32_t fm;    // x2 [C][C]
   uint32_t G;     // GDN [C] / KDA [C][dk] in-chunk inclusive gate prefixes
   uint32_t eG;    // GDN [C] e^{G_i}
   uint32_t ekd;   // GDN [C] e^{G_last - G_i}
-  uint32_t wb;    // [C] betas
-  uint32_t decr;  // KDA [dk] e^{G_last} per key channel
+  uint32_t wb;    // x2 [C] betas
+  uint32_t decr;  // KDA x2 [dk] e^{G_last} per key channel
   uint32_t total;
 };
 
@@ -280,18 +283,19 @@ __host__ __device__ inline PrefillSmem prefill_layout(int algo, int dk, int dv) 
   m.S = off;     off = align16(off + 4u * dk * (CB + 8));
   m.wq = off;    off = align16(off + 4u * C * dk);
   m.wk = off;    off = align16(off + 4u * C * dk);
-  m.wv = off;    off = align16(off + 4u * C * CB);
+  m.wv = off;    off = align16(off + 2u * 4u * C * CB);
   m.xT = off;    off = align16(off + 4u * dk * kPrefillXS);
-  // y also holds the GDN pair partial sums [2][2C][C] before the mat-vec
-  m.y = off;     off = align16(off + 4u * (2 * C * CB > 4 * C * C ? 2 * C * CB : 4 * C * C));
+  m.kdT = off;   off = align16(off + 4u * dk * kPrefillKS);
+  m.y = off;     off = align16(off + 4u * 2 * C * CB);
+  m.part = off;  off = align16(off + 4u * 2 * C * C);
   m.dch = off;   off = align16(off + 4u * C * (CB + 8));
-  m.am = off;    off = align16(off + 4u * C * C);
-  m.fm = off;    off = align16(off + 4u * C * C);
+  m.am = off;    off = align16(off + 2u * 4u * C * C);
+  m.fm = off;    off = align16(off + 2u * 4u * C * C);
   m.G = off;     off = align16(off + 4u * (kda ? C * dk : C));
   m.eG = off;    off = align16(off + 4u * C);
   m.ekd = off;   off = align16(off + 4u * C);
-  m.wb = off;    off = align16(off + 4u * C);
-  m.decr = off;  off = align16(off + 4u * dk);
+  m.wb = off;    off = align16(off + 2u * 4u * C);
+  m.decr = off;  off = align16(off + 2u * 4u * dk);
   m.total = off;
   return m;
 }
