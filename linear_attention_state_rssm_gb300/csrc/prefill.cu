@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
   constexpr int C = kPrefillChunk;
   constexpr int CQ = CB / 4;                  // column quads of the state slice
   constexpr int XS = kPrefillXS, KS = kPrefillKS;
-  constexpr int SS = CB + 8, DS = CB + 8;     // row strides of S and of the deltas
+  constexpr int SS = CB + 8, DS = CB + 8, YS = CB + 8;  // row strides: S, deltas, y
+  constexpr int FS = kPrefillKS;              // row stride of the coefficients A, F
   constexpr int NTN = CB / 8;                 // 8-column tiles of a CB-wide product
   // GDN mat-vec and pair inputs are the raw bf16 k, q: exact in tf32
   constexpr bool EXACT_X = ALGO == ALGO_GDN && INB == 2;
@@ -316,8 +317,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
   //     A_ij = beta_i e^{G_i - G_j} k_i.k_j (j < i), F_ij = e^{G_i - G_j} q_i.k_j (j <= i)
   auto prepare = [&](int ch) {
     const int b = ch & 1, cn = min(C, n - ch * C);
-    float* am = am2 + b * C * C;
-    float* fm = fm2 + b * C * C;
+    float* am = am2 + b * C * FS;
+    float* fm = fm2 + b * C * FS;
     float* wb = wb2 + b * C;
     stage(wv2 + b * C * CB, wb);
     if (ALGO == ALGO_GDN && warp == 2) gdn_scan(rgg, cn);
@@ -343,7 +344,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
       }
     }
     if (ALGO == ALGO_KDA) {
-      window_pairs<ALGO, C>(cn, dk, wk, wq, G, wb, am, fm, warp - 2, PW - 2, lane);
+      // (writes rows i < cn, entries j <= i; F's other entries stay zero)
+      for (int e = lt; e < C * FS; e += NP) {
+        const int i = e / FS, j = e - i * FS;
+        if (i >= cn || j > i) fm[e] = 0.f;
+      }
+      window_pairs<ALGO, FS>(cn, dk, wk, wq, G, wb, am, fm, warp - 2, PW - 2, lane);
       return;
     }
     named_sync(1, NP);
@@ -370,8 +376,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
       const int i = e >> 4, j = e & 15;
       const bool on = i < cn && j <= i;
       const float wgt = on ? __expf(G[i] - G[j]) : 0.f;
-      fm[e] = on ? wgt * part[(C + i) * C + j] : 0.f;
-      am[e] = (on && j < i) ? wb[i] * wgt * part[i * C + j] : 0.f;
+      fm[i * FS + j] = on ? wgt * part[(C + i) * C + j] : 0.f;
+      am[i * FS + j] = (on && j < i) ? wb[i] * wgt * part[i * C + j] : 0.f;
     }
   };
 
@@ -451,8 +457,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
           const int va = v0 + fg, vb = va + 8;
           const float fa = ALGO == ALGO_GDN ? eG[va < C ? va : va - C] : 1.f;
           const float fb = ALGO == ALGO_GDN ? eG[vb < C ? vb : vb - C] : 1.f;
-          *reinterpret_cast<float2*>(y + va * CB + n0) = make_float2(fa * acc[u][0], fa * acc[u][1]);
-          *reinterpret_cast<float2*>(y + vb * CB + n0) = make_float2(fb * acc[u][2], fb * acc[u][3]);
+          *reinterpret_cast<float2*>(y + va * YS + n0) = make_float2(fa * acc[u][0], fa * acc[u][1]);
+          *reinterpret_cast<float2*>(y + vb * YS + n0) = make_float2(fb * acc[u][2], fb * acc[u][3]);
         }
       }
     }
@@ -460,12 +466,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
     const float dec = ALGO == ALGO_GDN ? eG[cn - 1] : 1.f;
     __syncthreads();
 
-    // ---- (B) per column: triangular solve and outputs, on warps 0-1; the
-    //      preparing warps build this chunk's decayed keys, then prepare the
-    //      next chunk
+    // ---- (B) per column: the deltas by forward substitution, on warps 0-1
+    //      (four partial sums per step); the preparing warps build this
+    //      chunk's decayed keys, then prepare the next chunk
     if (tid < CB) {
-      const float* am = am2 + b * C * C;
-      const float* fm = fm2 + b * C * C;
+      const float* am = am2 + b * C * FS;
       const float* wv = wv2 + b * C * CB;
       const float* wb = wb2 + b * C;
       float d[C];
@@ -473,14 +478,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
       for (int i = 0; i < C; ++i) {
         d[i] = 0.f;
         if (i < cn) {
-          float di = wb[i] * (wv[i * CB + tid] - y[i * CB + tid]);
+          float sj[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < i; ++j) di = fmaf(-am[i * C + j], d[j], di);
-          d[i] = di;
-          float oi = y[(C + i) * CB + tid];
-#pragma unroll
-          for (int j = 0; j <= i; ++j) oi = fmaf(fm[i * C + j], d[j], oi);
-          st_f32(p.o, (((size_t)a0 + t0 + i) * HV + h) * dv + cb0 + tid, p.in_dt, p.scale * oi);
+          for (int j = 0; j < i; ++j) sj[j & 3] = fmaf(am[i * FS + j], d[j], sj[j & 3]);
+          d[i] = wb[i] * (wv[i * CB + tid] - y[i * YS + tid]) - ((sj[0] + sj[1]) + (sj[2] + sj[3]));
         }
         dch[i * DS + tid] = d[i];
       }
@@ -492,7 +493,36 @@ __global__ void __launch_bounds__(kPrefillThreads, 2) prefill_kernel(const Prefi
       }
     }
     __syncthreads();
-    // ---- (C) rank-16 update of the state slice
+    // ---- (C) outputs O = Y_q + F D on the tensor cores (warp w < NTN: the
+    //      8 columns of tile w), then the rank-16 update of the state slice
+    if (warp < NTN) {
+      const float* fm = fm2 + b * C * FS;
+      const int n0 = warp * 8;
+      const float* yq = y + (C + fg) * YS + n0 + 2 * ft;
+      const float2 q0 = *reinterpret_cast<const float2*>(yq);
+      const float2 q1 = *reinterpret_cast<const float2*>(yq + 8 * YS);
+      float acc[4] = {q0.x, q0.y, q1.x, q1.y};
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        const float* fr = fm + fg * FS + 8 * ks + ft;
+        const Tf32 af[4] = {tf32_split<false>(fr[0]), tf32_split<false>(fr[8 * FS]),
+                            tf32_split<false>(fr[4]), tf32_split<false>(fr[8 * FS + 4])};
+        const Tf32 bf[2] = {tf32_split<false>(dch[(8 * ks + ft) * DS + n0 + fg]),
+                            tf32_split<false>(dch[(8 * ks + ft + 4) * DS + n0 + fg])};
+        mma_split<false, false>(acc, af, bf);
+      }
+      const size_t col = (size_t)cb0 + n0 + 2 * ft;
+      if (fg < cn) {
+        const size_t ob = (((size_t)a0 + t0 + fg) * HV + h) * dv + col;
+        st_f32(p.o, ob, p.in_dt, p.scale * acc[0]);
+        st_f32(p.o, ob + 1, p.in_dt, p.scale * acc[1]);
+      }
+      if (fg + 8 < cn) {
+        const size_t ob = (((size_t)a0 + t0 + fg + 8) * HV + h) * dv + col;
+        st_f32(p.o, ob, p.in_dt, p.scale * acc[2]);
+        st_f32(p.o, ob + 1, p.in_dt, p.scale * acc[3]);
+      }
+    }
     update(dec, decr2 + b * dk);
     __syncthreads();
   }

@@ -230,11 +230,11 @@ struct PrefillSmem {
   uint32_t wv;    // x2 [C][CB]  fp32 chunk v columns
   uint32_t xT;    // [dk][kPrefillXS] mat-vec and pair inputs per key channel
   uint32_t kdT;   // [dk][kPrefillKS] the update's decayed keys
-  uint32_t y;     // [2C][CB]  S^T k_i, S^T q_i (decay applied)
+  uint32_t y;     // [2C][CB + 8]  S^T k_i, S^T q_i (decay applied)
   uint32_t part;  // [2C][C]   GDN pair sums k_i.k_j, q_i.k_j
   uint32_t dch;   // [C][CB + 8]  chunk deltas (history replay: ring deltas)
-  uint32_t am;    // x2 [C][C]
-  uint32_t fm;    // x2 [C][C]
+  uint32_t am;    // x2 [C][kPrefillKS]  window coefficients A (row stride kPrefillKS)
+  uint32_t fm;    // x2 [C][kPrefillKS]  window coefficients F
   uint32_t G;     // GDN [C] / KDA [C][dk] in-chunk inclusive gate prefixes
   uint32_t eG;    // GDN [C] e^{G_i}
   uint32_t ekd;   // GDN [C] e^{G_last - G_i}
@@ -270,7 +270,8 @@ __host__ __device__ constexpr int prefill_cb(int dv) { return dv < 64 ? dv : 64;
 // Row strides (floats) of the per-channel arrays. The padding puts the
 // tensor-core fragment loads (lanes over 4 rows x 8 columns) on 32 distinct
 // banks: row strides of 8 (mod 32) floats for the mat-vec and pair inputs,
-// of 20 for the update's keys, and CB + 8 for the state and the deltas.
+// of 20 for the update's keys and the coefficients F, and CB + 8 for the
+// state, the deltas and the mat-vec results.
 constexpr int kPrefillXS = 2 * kPrefillChunk + 8;
 constexpr int kPrefillKS = kPrefillChunk + 4;
 
@@ -286,11 +287,11 @@ __host__ __device__ inline PrefillSmem prefill_layout(int algo, int dk, int dv) 
   m.wv = off;    off = align16(off + 2u * 4u * C * CB);
   m.xT = off;    off = align16(off + 4u * dk * kPrefillXS);
   m.kdT = off;   off = align16(off + 4u * dk * kPrefillKS);
-  m.y = off;     off = align16(off + 4u * 2 * C * CB);
+  m.y = off;     off = align16(off + 4u * 2 * C * (CB + 8));
   m.part = off;  off = align16(off + 4u * 2 * C * C);
   m.dch = off;   off = align16(off + 4u * C * (CB + 8));
-  m.am = off;    off = align16(off + 2u * 4u * C * C);
-  m.fm = off;    off = align16(off + 2u * 4u * C * C);
+  m.am = off;    off = align16(off + 2u * 4u * C * kPrefillKS);
+  m.fm = off;    off = align16(off + 2u * 4u * C * kPrefillKS);
   m.G = off;     off = align16(off + 4u * (kda ? C * dk : C));
   m.eG = off;    off = align16(off + 4u * C);
   m.ekd = off;   off = align16(off + 4u * C);
