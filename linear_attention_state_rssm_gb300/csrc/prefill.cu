@@ -57,24 +57,22 @@ __device__ __forceinline__ void widen_store(float* dst, const uint4& u, int in_d
 // Fragments, g = lane / 4, t = lane % 4: A (16 x 8) a0 (g, t), a1 (g + 8, t),
 // a2 (g, t + 4), a3 (g + 8, t + 4); B (8 x 8) b0 (t, g), b1 (t + 4, g);
 // C (16 x 8) c0 (g, 2t), c1 (g, 2t + 1), c2 (g + 8, 2t), c3 (g + 8, 2t + 1).
-// fp32 operands are split into a tf32 head and a tf32 tail, x = hi + lo, and a
-// product takes hi*hi + hi*lo + lo*hi, which keeps it at fp32 accuracy; an
+// fp32 operands are split into a tf32 head and tail, x = hi + lo, and a
+// product takes hi*hi + hi*lo + lo*hi, which keeps it near fp32 accuracy; an
 // operand that is exact in tf32 (bf16 values) has no tail.
-__device__ __forceinline__ uint32_t tf32_bits(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
 
 struct Tf32 {
   uint32_t hi, lo;
 };
 
+// The head is the operand truncated to tf32 (its low 13 bits cleared), the
+// tail the exact fp32 remainder truncated to tf32 in the same way: the pair
+// carries about 21 significant bits of the operand.
 template <bool EXACT>
 __device__ __forceinline__ Tf32 tf32_split(float x) {
   if (EXACT) return Tf32{__float_as_uint(x), 0u};
-  const uint32_t hi = tf32_bits(x);
-  return Tf32{hi, tf32_bits(x - __uint_as_float(hi))};
+  const uint32_t hi = __float_as_uint(x) & 0xffffe000u;
+  return Tf32{hi, __float_as_uint(x - __uint_as_float(hi)) & 0xffffe000u};
 }
 
 __device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
