@@ -11,56 +11,62 @@
 // the commit makes the window the last K-1 rows of [window, x_0 .. x_{a-1}].
 // Decode commits its token at once.
 //
-// One thread per (row, 16 bytes of consecutive channels): every access is a
-// 16-byte vector and a warp's accesses are consecutive; a thread issues the
-// loads of up to eight tokens before it uses them, and keeps the window, the
-// taps and the bias in registers across the tokens. The work is a few flops
-// per byte: HBM-bound.
+// One thread per (row, four consecutive channels): every access is one vector
+// (8 bytes of bf16, 16 of fp32) and a warp's accesses are consecutive; a
+// thread issues the loads of up to eight tokens before it uses them and keeps
+// the window, the taps and the bias in registers across the tokens, few
+// enough that many threads, and their loads, are in flight. The work is a few
+// flops per byte: HBM-bound.
 #include "rssm_common.cuh"
 #include "rssm_launch.h"
+
+#include <type_traits>
 
 namespace rssm {
 
 constexpr int kConvThreads = 128;
 constexpr int kConvTok = 8;  // tokens whose loads are in flight together
 
-// 16 bytes of EPV values (bf16 when EPV = 8, fp32 when EPV = 4) <-> fp32
-template <int EPV>
-__device__ __forceinline__ void unpack16(const uint4& u, float (&v)[EPV]) {
-  if (EPV == 4) {
-    v[0] = __uint_as_float(u.x);
-    v[1] = __uint_as_float(u.y);
-    v[2] = __uint_as_float(u.z);
-    v[EPV - 1] = __uint_as_float(u.w);
-  } else {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+// VW 32-bit words of values (bf16 pairs or fp32) <-> fp32
+template <int VW, bool BF>
+struct ConvVec {
+  static constexpr int kVals = BF ? 2 * VW : VW;
+  using T = typename std::conditional<VW == 4, uint4, uint2>::type;
+  static __device__ __forceinline__ void unpack(const T& u, float (&v)[kVals]) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(&u);
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[t]));
-      v[(2 * t) % EPV] = f.x;
-      v[(2 * t + 1) % EPV] = f.y;
+    for (int t = 0; t < VW; ++t) {
+      if (BF) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[t]));
+        v[(2 * t) % kVals] = f.x;
+        v[(2 * t + 1) % kVals] = f.y;
+      } else {
+        v[t % kVals] = __uint_as_float(w[t]);
+      }
     }
   }
-}
-
-template <int EPV>
-__device__ __forceinline__ uint4 pack16(const float (&v)[EPV]) {
-  if (EPV == 4) {
-    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
-                      __float_as_uint(v[EPV - 1]));
-  }
-  uint32_t w[4];
+  static __device__ __forceinline__ T pack(const float (&v)[kVals]) {
+    T u;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(v[(2 * t) % EPV], v[(2 * t + 1) % EPV]);
-    w[t] = *reinterpret_cast<const uint32_t*>(&h);
+    for (int t = 0; t < VW; ++t) {
+      if (BF) {
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(v[(2 * t) % kVals], v[(2 * t + 1) % kVals]);
+        w[t] = *reinterpret_cast<const uint32_t*>(&hh);
+      } else {
+        w[t] = __float_as_uint(v[t % kVals]);
+      }
+    }
+    return u;
   }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
+};
 
-// One thread per (row, group of EPV consecutive channels).
-template <int K, int EPV>
+// One thread per (row, group of EPV consecutive channels) in VW-word vectors.
+template <int K, int VW, bool BF>
 __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(const ConvParams p) {
+  using Vec = ConvVec<VW, BF>;
+  using VT = typename Vec::T;
+  constexpr int EPV = Vec::kVals;
   const int D = p.D, T = p.T;
   const int g = blockIdx.x * kConvThreads + threadIdx.x, r = blockIdx.y;
   if (g * EPV >= D) return;
@@ -70,11 +76,11 @@ __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(const ConvPar
     if (g == 0 && p.err != nullptr) atomicOr(p.err, DEVERR_SLOT);
     return;
   }
-  const int c0 = g * EPV, nv = D / EPV;  // 16-byte vectors per row of D channels
-  const uint4* x = static_cast<const uint4*>(p.x);
-  uint4* y = static_cast<uint4*>(p.y);
-  uint4* win_g = static_cast<uint4*>(p.window) + (size_t)s * (K - 1) * nv + g;
-  uint4* draft = static_cast<uint4*>(p.draft);
+  const int c0 = g * EPV, nv = D / EPV;  // vectors per row of D channels
+  const VT* x = static_cast<const VT*>(p.x);
+  VT* y = static_cast<VT*>(p.y);
+  VT* win_g = static_cast<VT*>(p.window) + (size_t)s * (K - 1) * nv + g;
+  VT* draft = static_cast<VT*>(p.draft);
 
   float taps[EPV][K], b[EPV], win[K - 1][EPV];
 #pragma unroll
@@ -84,10 +90,10 @@ __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(const ConvPar
     b[e] = p.bias != nullptr ? p.bias[c0 + e] : 0.f;
   }
 #pragma unroll
-  for (int i = 0; i < K - 1; ++i) unpack16<EPV>(win_g[(size_t)i * nv], win[i]);
+  for (int i = 0; i < K - 1; ++i) Vec::unpack(win_g[(size_t)i * nv], win[i]);
 
   for (int t0 = 0; t0 < T; t0 += kConvTok) {
-    uint4 xr[kConvTok];
+    VT xr[kConvTok];
 #pragma unroll
     for (int u = 0; u < kConvTok; ++u) {
       if (t0 + u < T) xr[u] = __ldg(x + ((size_t)r * T + t0 + u) * nv + g);
@@ -97,7 +103,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(const ConvPar
       if (t0 + u < T) {
         const size_t xi = ((size_t)r * T + t0 + u) * nv + g;
         float xv[EPV], yv[EPV];
-        unpack16<EPV>(xr[u], xv);
+        Vec::unpack(xr[u], xv);
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
           float acc = b[e];
@@ -107,7 +113,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(const ConvPar
           if (p.act == CONV_ACT_SILU) acc = acc / (1.f + __expf(-acc));
           yv[e] = acc;
         }
-        y[xi] = pack16<EPV>(yv);
+        y[xi] = Vec::pack(yv);
         if (!p.commit_now) draft[((size_t)s * T + t0 + u) * nv + g] = xr[u];
 #pragma unroll
         for (int i = 0; i < K - 2; ++i) {
@@ -121,7 +127,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(const ConvPar
   }
   if (p.commit_now) {
 #pragma unroll
-    for (int i = 0; i < K - 1; ++i) win_g[(size_t)i * nv] = pack16<EPV>(win[i]);
+    for (int i = 0; i < K - 1; ++i) win_g[(size_t)i * nv] = Vec::pack(win[i]);
   }
 }
 
@@ -159,14 +165,16 @@ cudaError_t conv_launch(const ConvParams& p, bool commit, cudaStream_t st) {
   const bool f32 = p.dt == DT_F32;
   const int nv = p.D * (f32 ? 4 : 2) / 16;
   const dim3 grid((unsigned)((nv + kConvThreads - 1) / kConvThreads), (unsigned)p.B, 1);
+  const int nw = p.D / 4;  // four channels per window thread
+  const dim3 wgrid((unsigned)((nw + kConvThreads - 1) / kConvThreads), (unsigned)p.B, 1);
 #define RSSM_CONV_CASE(KV)                                                        \
   case KV:                                                                        \
     if (commit) {                                                                 \
       conv_commit_kernel<KV><<<grid, kConvThreads, 0, st>>>(p);                   \
     } else if (f32) {                                                             \
-      conv_window_kernel<KV, 4><<<grid, kConvThreads, 0, st>>>(p);                \
+      conv_window_kernel<KV, 4, false><<<wgrid, kConvThreads, 0, st>>>(p);        \
     } else {                                                                      \
-      conv_window_kernel<KV, 8><<<grid, kConvThreads, 0, st>>>(p);                \
+      conv_window_kernel<KV, 2, true><<<wgrid, kConvThreads, 0, st>>>(p);         \
     }                                                                             \
     break;
   switch (p.K) {
