@@ -13,7 +13,7 @@
 //
 // One thread per (row, four consecutive channels): every access is one vector
 // (8 bytes of bf16, 16 of fp32) and a warp's accesses are consecutive; a
-// thread issues the loads of up to eight tokens before it uses them and keeps
+// thread issues the loads of up to four tokens before it uses them and keeps
 // the window, the taps and the bias in registers across the tokens, few
 // enough that many threads, and their loads, are in flight. The work is a few
 // flops per byte: HBM-bound.
@@ -25,7 +25,7 @@
 namespace rssm {
 
 constexpr int kConvThreads = 128;
-constexpr int kConvTok = 8;  // tokens whose loads are in flight together
+constexpr int kConvTok = 4;  // tokens whose loads are in flight together
 
 // VW 32-bit words of values (bf16 pairs or fp32) <-> fp32
 template <int VW, bool BF>
