@@ -528,8 +528,10 @@ def run_prefill(args, torch, dev, rank):
             "tokens_per_s_per_layer": tot / (ms / 1e3), "launch_ms": ms,
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
-                         "peak_kind": f"derived: {props.multi_processor_count} SMs x "
-                                      f"{FP32_LANES_PER_SM} fp32 lanes x 2 flop x {sm_mhz} MHz",
+                         "peak_kind": f"derived fp32 FMA peak: {props.multi_processor_count} SMs"
+                                      f" x {FP32_LANES_PER_SM} lanes x 2 flop x {sm_mhz} MHz "
+                                      "(the scan runs on CUDA cores, the chunk products on "
+                                      "the tensor cores)",
                          "flops_per_launch": flops,
                          "kernel": "prefill_kernel<GDN, f32, 64, bf16>"},
             "gpu_launches_per_step": 2, "device_error_word": err}
