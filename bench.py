@@ -647,6 +647,121 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+# ----------------------------------------------------------------- sweep
+SWEEP = [  # (algo, B, L, T, state dtype, commit mode); decode when T == 1
+    ("gdn", 1, 16, 1, "f32", "lazy"), ("gdn", 8, 16, 1, "f32", "lazy"),
+    ("gdn", 64, 16, 1, "f32", "lazy"), ("gdn", 128, 16, 1, "f32", "lazy"),
+    ("gdn", 256, 16, 1, "f32", "lazy"), ("gdn", 64, 32, 1, "f32", "lazy"),
+    ("gdn", 64, 64, 1, "f32", "lazy"), ("gdn", 64, 16, 1, "bf16", "lazy"),
+    ("gdn", 64, 16, 3, "f32", "lazy"), ("gdn", 128, 16, 8, "f32", "lazy"),
+    ("gdn", 128, 16, 8, "bf16", "fold_every"),
+    ("kda", 64, 32, 1, "f32", "lazy"), ("kda", 64, 32, 1, "bf16", "lazy"),
+    ("kda", 64, 32, 3, "f32", "lazy"),
+]
+
+
+def sweep_point(torch, dev, algo, B, L, T, state_dtype, mode, steps, warmup, peak):
+    """Steady-state decode (T = 1) or verify + commit (T > 1) over enough
+    stacked layers that the checkpoints exceed L2; per-layer time from CUDA
+    events around CUDA-graph replays, algorithmic bytes of the replay launches
+    from the rows' cursor trajectory (the commit's own work is timed with them)."""
+    from linear_attention_state_rssm_gb300.store import ReplayStore
+    HK, HV, dk, dv = (16, 32, 128, 128) if algo == "gdn" else (32, 32, 128, 128)
+    n_g = 1 if algo == "gdn" else dk
+    s_state = ESZ[state_dtype]
+    layer_state = B * HV * dk * dv * s_state
+    nl = int(min(256, max(4, -(-(512 << 20) // layer_state))))
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5000 + B + 7 * T + L)
+    st = ReplayStore(algo, nl, B, HK, HV, dk, dv, L, T, "bf16", state_dtype, "f16", "f32", mode,
+                     device=dev)
+    for layer in range(nl):
+        st.state[layer].normal_(0.0, 0.1, generator=gen)
+    cur0 = [r % L for r in range(B)]  # staggered rows, as in steady serving
+    st.cursor.copy_(torch.tensor(cur0, dtype=torch.int32))
+    n = nl * B * T
+    nrm = torch.nn.functional.normalize
+    q = nrm(torch.randn(n, HK, dk, generator=gen, device=dev), dim=-1).to(torch.bfloat16)
+    k = nrm(torch.randn(n, HK, dk, generator=gen, device=dev), dim=-1).to(torch.bfloat16)
+    v = torch.randn(n, HV, dv, generator=gen, device=dev).to(torch.bfloat16)
+    beta = torch.sigmoid(torch.randn(n, HV, generator=gen, device=dev))
+    gshape = (n, HV) if algo == "gdn" else (n, HV, dk)
+    g = -torch.nn.functional.softplus(torch.randn(gshape, generator=gen, device=dev))
+    out = torch.empty(n, HV, dv, dtype=torch.bfloat16, device=dev)
+    slot = torch.arange(B, dtype=torch.int32, device=dev)
+    per = B * T
+    acc_all = torch.randint(0, T + 1, (warmup + steps, B), generator=gen, device=dev,
+                            dtype=torch.int32)
+    acc_cur = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def lv(layer):
+        a, b = layer * per, (layer + 1) * per
+        return q[a:b], k[a:b], v[a:b], beta[a:b], g[a:b]
+
+    def step():
+        for layer in range(nl):
+            if T == 1:
+                st.rssm_decode(layer, *lv(layer), slot, out[layer * per:(layer + 1) * per],
+                               advance_cursor=layer == nl - 1)
+            else:
+                st.rssm_verify(layer, *lv(layer), slot, T, out[layer * per:(layer + 1) * per])
+        if T > 1:
+            st.rssm_commit(slot, acc_cur, T)
+
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            step()
+    torch.cuda.current_stream().wait_stream(cap)
+    # host copy of the cursor trajectory for the byte count (capture ran nothing)
+    cur = list(cur0)
+    acc_h = acc_all.cpu().tolist()
+    total_bytes = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(warmup + steps):
+        if i == warmup:
+            torch.cuda.synchronize()
+            e0.record()
+        acc_cur.copy_(acc_all[i])
+        graph.replay()
+        a_row = [1] * B if T == 1 else acc_h[i]
+        for r in range(B):
+            c = cur[r]
+            nxt, fold = advance(c, T, L, a_row[r])
+            if i >= warmup:
+                total_bytes += nl * row_bytes(c, T, fold, HK, HV, dk, dv, s_state, 2, 2, 4, n_g)
+            cur[r] = 0 if (T > 1 and mode == "fold_every") else nxt
+    e1.record()
+    torch.cuda.synchronize()
+    ms_layer = e0.elapsed_time(e1) / (steps * nl)
+    gbs = total_bytes / (steps * nl) / (ms_layer / 1e3) / 1e9
+    err = st.rssm_get_device_error()
+    del graph, st, q, k, v, beta, g, out
+    torch.cuda.empty_cache()
+    return {"algo": algo, "batch": B, "L": L, "T": T, "state_dtype": state_dtype,
+            "commit_mode": mode, "layers": nl, "ms_per_layer": ms_layer,
+            "replayed_tokens_per_s_per_layer": B * T / (ms_layer / 1e3),
+            "replay_gbs": gbs, "frac_of_hbm_peak": gbs / peak, "device_error_word": err}
+
+
+def run_sweep(args):
+    """--sweep: the steady-state grid of the survey's measurement workload
+    (batch, ring length, window width, state dtype, GDN and KDA heads)."""
+    import torch
+    from linear_attention_state_rssm_gb300 import build as _build
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = peaks()
+    pts = [sweep_point(torch, dev, *pt, steps=args.steps, warmup=args.warmup, peak=peak)
+           for pt in SWEEP]
+    return {"sweep": pts, "peak_gbs": peak, "peak_kind": peak_kind,
+            "note": "per-layer time includes the step's cursor advance (decode) or commit "
+                    "(verify); bytes count the replay launches only"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -660,6 +775,8 @@ def main():
                     help="skip the native fused-recurrent decode comparison line")
     ap.add_argument("--no-prefill", action="store_true", help="skip the replay prefill line")
     ap.add_argument("--no-conv", action="store_true", help="skip the conv window line")
+    ap.add_argument("--sweep", action="store_true",
+                    help="print the steady-state grid (batch, L, T, state dtype, GDN/KDA)")
     ap.add_argument("--prefill-prompts", type=int, default=PREFILL["prompts"])
     ap.add_argument("--prefill-tokens", type=int, default=PREFILL["tokens"])
     args = ap.parse_args()
@@ -668,6 +785,10 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.sweep:
+        print(json.dumps(run_sweep(args)), flush=True)
+        return
 
     if args.impl == "reference":
         if rank == 0:
