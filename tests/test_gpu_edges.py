@@ -276,3 +276,25 @@ def test_decode_row_order_either_side_of_the_ranked_batch_limit(B):
     assert run.state_err() <= TOL32
     assert run.ring_d_err() <= TOL32
     assert run.store.rssm_get_device_error() == 0
+
+
+@pytest.mark.parametrize("algo,HK,HV", [("gdn", 2, 4), ("kda", 2, 2)])
+def test_decode_on_a_long_ring(algo, HK, HV):
+    """Decode with 128-wide heads on an L = 64 ring (the largest shared-memory
+    plan, long histories, the fold at c = 64): staggered cursors from forced
+    folds, bf16 inputs, fp32 state; outputs every step, then the checkpoint."""
+    B, L = 10, 64
+    slots = np.arange(B, dtype=np.int32)[::-1].copy()
+    run = Run(algo=algo, HK=HK, HV=HV, dk=128, dv=128, L=L, max_T=1, slots=slots,
+              n_slots=B, in_dtype="bf16", config_id=29)
+    for step in range(80):
+        inp = run.inputs(step, 0, 1)
+        force = np.array([1 if step == 5 * r + 3 else 0 for r in range(B)], dtype=np.uint8)
+        _, o_gpu, o_orc, f_gpu, f_orc = run.window(0, inp, 1, force=force, decode=True,
+                                                   advance=True)
+        assert rel_err(o_gpu, o_orc) <= TOL16, step
+        np.testing.assert_array_equal(f_gpu, f_orc)
+        run.check_cursors()
+    assert run.state_err() <= TOL16
+    assert run.ring_d_err() <= TOL16
+    assert run.store.rssm_get_device_error() == 0
