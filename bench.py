@@ -118,10 +118,17 @@ def ncu_traffic():
     return per_launch if want == sources_hash() else None
 
 
+# The files that define the decode launch the ncu summary describes (kernel,
+# shared-memory plan, launch); a change to any of them invalidates the traffic.
+DECODE_SOURCES = ("replay_impl.cuh", "rssm_history.cuh", "rssm_common.cuh", "replay_launch.cuh",
+                  "replay_gdn_f32.cu")
+
+
 def sources_hash():
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "linear_attention_state_rssm_gb300", "csrc", "*"))):
-        h.update(os.path.basename(f).encode())
+    for name in DECODE_SOURCES:
+        f = os.path.join(ROOT, "linear_attention_state_rssm_gb300", "csrc", name)
+        h.update(name.encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -407,9 +407,9 @@ rssm_status rssm_prefill(rssm_handle* h, int32_t layer, const void* q, const voi
                                  c.n_slots, CURSOR_PREFILL, h->buf.err_word, s));
 }
 
-static rssm_status conv_params(const void* x, const float* w, void* window, void* draft,
-                               const int32_t* slot, int32_t B, int32_t T, int32_t D, int32_t K,
-                               int32_t n_slots, int32_t dtype, ConvParams* out) {
+static rssm_status conv_params(const void* x, void* window, void* draft, const int32_t* slot,
+                               int32_t B, int32_t T, int32_t D, int32_t K, int32_t n_slots,
+                               int32_t dtype, ConvParams* out) {
   if (B < 0 || B > kMaxGrid || T < 1 || D < 1 || n_slots < 1) return RSSM_ERR_INVALID_ARG;
   if (K < 2 || K > kConvMaxK) return RSSM_ERR_UNSUPPORTED;
   if (dtype != RSSM_F32 && dtype != RSSM_BF16) return RSSM_ERR_UNSUPPORTED;
@@ -419,7 +419,6 @@ static rssm_status conv_params(const void* x, const float* w, void* window, void
   if ((D * (dtype == RSSM_F32 ? 4 : 2)) % 16 != 0) return RSSM_ERR_UNSUPPORTED;
   if (!aligned16(window) || (x && !aligned16(x)) || (draft && !aligned16(draft)))
     return RSSM_ERR_INVALID_ARG;
-  (void)w;
   ConvParams& p = *out;
   p = ConvParams{};
   p.window = window;
@@ -438,7 +437,7 @@ rssm_status rssm_conv_window(const void* x, const float* w, const float* bias, v
                              int32_t K, int32_t n_slots, int32_t dtype, int32_t act,
                              int32_t commit_now, void* y, uint32_t* err_word, void* stream) {
   ConvParams p;
-  const rssm_status st = conv_params(x, w, window, draft, slot, B, T, D, K, n_slots, dtype, &p);
+  const rssm_status st = conv_params(x, window, draft, slot, B, T, D, K, n_slots, dtype, &p);
   if (st != RSSM_OK) return st;
   if (act != RSSM_CONV_ACT_NONE && act != RSSM_CONV_ACT_SILU) return RSSM_ERR_INVALID_ARG;
   if (B == 0) return RSSM_OK;
@@ -460,8 +459,8 @@ rssm_status rssm_conv_commit(void* window, const void* draft, const int32_t* slo
                              int32_t K, int32_t n_slots, int32_t dtype, uint32_t* err_word,
                              void* stream) {
   ConvParams p;
-  const rssm_status st = conv_params(nullptr, nullptr, window, nullptr, slot, B, T, D, K, n_slots,
-                                     dtype, &p);
+  const rssm_status st = conv_params(nullptr, window, nullptr, slot, B, T, D, K, n_slots, dtype,
+                                     &p);
   if (st != RSSM_OK) return st;
   if (B == 0) return RSSM_OK;
   if (!draft || !accept_len || !aligned4(accept_len)) return RSSM_ERR_INVALID_ARG;
