@@ -285,12 +285,14 @@ __device__ __forceinline__ int swap_rank(const unsigned* fmask, int y) {
   return y;
 }
 
-// Narrow windows keep four CTAs per SM (at most 128 registers per thread);
-// wide verify windows trade occupancy for their larger accumulator tiles.
+// Narrow windows keep four CTAs per SM (at most 128 registers per thread),
+// eight-token windows three (two value columns per lane, a three-stage ring);
+// the widest trade occupancy for their larger accumulator tiles.
 // RAGGED: windows of different lengths from p.cu (verify widths only); the
 // uniform kernels keep the window length a launch constant.
 template <int ALGO, typename ST, int NT, bool RAGGED>
-__global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const ReplayParams p) {
+__global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
+    replay_kernel(const ReplayParams p) {
   constexpr int NV = 2 * NT;             // mat-vec vectors: k_i at [0, NT), q_i at [NT, 2NT)
   constexpr int CW = quad_width(NT);     // value columns per lane in the tile stream
   constexpr int MR = fold_reg_records(NT);
@@ -435,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : 2) replay_kernel(const
     return;
   }
   ST* gtile = tile_of(s);
-  const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv);
+  const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv,
+                          ring_stages(NT));
   if (tid == 0) pipe.prime();
   if (!have_c) c = p.cursor[s];
   if (c < 0 || c > L) {

@@ -235,9 +235,10 @@ struct TilePipe {
   const ST* gtile;
   int dv;
   TileRing tr;
-  __device__ __forceinline__ TilePipe(ST* ring_, uint64_t* mbar, const ST* gtile_, int dk, int dv_)
+  __device__ __forceinline__ TilePipe(ST* ring_, uint64_t* mbar, const ST* gtile_, int dk, int dv_,
+                                      int stages = kStages)
       : ring(ring_), full(mbar + kMbarFull), empty(mbar + kMbarEmpty), gtile(gtile_), dv(dv_),
-        tr(dk, dv_, (int)sizeof(ST)) {}
+        tr(dk, dv_, (int)sizeof(ST), stages) {}
   // mbarrier set-up (one thread): "full" before the first copy (and the fence
   // that makes initialisation visible to the copies), "empty" with the number
   // of consuming warps before the CTA barrier that precedes the stream.
