@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   }
   ST* gtile = tile_of(s);
   const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv,
-                          ring_stages(NT));
+                          ring_stages(NT, L));
   if (tid == 0) pipe.prime();
   if (!have_c) c = p.cursor[s];
   if (c < 0 || c > L) {

@@ -118,12 +118,15 @@ struct QuadLayout {
 // Columns per lane in the tile stream for a window width.
 __host__ __device__ constexpr int quad_width(int NT) { return NT <= 4 ? 4 : 2; }
 
-// Stages of the tile ring for a window width: decode keeps four (a 64 KB fp32
-// tile in two round trips); verify windows take three, which with their
-// larger window arrays keeps more CTAs per SM (the width-16 window keeps four:
+// Stages of the tile ring for a window width and ring length: decode on rings
+// of up to 16 records keeps four (a 64 KB fp32 tile in two round trips);
+// verify windows and longer rings take three, which with their larger window
+// or history arrays keeps more CTAs per SM (the width-16 window keeps four:
 // its partial sums fill the drained ring). Measured on 128-row verify: T = 8
 // 219 -> 173 us, T = 3 127 -> 101 us per launch.
-__host__ __device__ constexpr int ring_stages(int NT) { return NT == 1 || NT == 16 ? 4 : 3; }
+__host__ __device__ constexpr int ring_stages(int NT, int L) {
+  return (NT == 1 && L <= 16) || NT == 16 ? 4 : 3;
+}
 
 // Narrow GDN windows without a fold split the CTA: kSplitWarps warps stream
 // the checkpoint tile while the others stage the history and compute the
@@ -318,7 +321,7 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
   ReplaySmem m{};
   const int NV = 2 * NT;
   const bool kda = algo == ALGO_KDA;
-  const TileRing tr(dk, dv, state_bytes, ring_stages(NT));
+  const TileRing tr(dk, dv, state_bytes, ring_stages(NT, L));
   const QuadLayout ql(dv, quad_width(NT), kWarps);
   uint32_t off = 0;
   m.ring = off;  off = align16(off + tr.ns * tr.chunk_bytes);
