@@ -798,8 +798,8 @@ def sweep_point(torch, dev, algo, B, L, T, state_dtype, mode, steps, warmup, pea
 
 
 def run_sweep(args):
-    """--sweep: the steady-state grid of the survey's measurement workload
-    (batch, ring length, window width, state dtype, GDN and KDA heads)."""
+    """--sweep: a steady-state grid of decode and verify launches over batch,
+    ring length, window width, state dtype, and GDN and KDA heads."""
     import torch
     from linear_attention_state_rssm_gb300 import build as _build
     _build.build()
