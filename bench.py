@@ -454,12 +454,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded torch RNG on device; distributions of the pages' tiny "
                 "GDN workload)",
-        "config": {"workload": w["workload"], "algo": "gdn", "HK": HK, "HV": HV, "dk": dk,
-                   "dv": dv, "batch": B, "live_rows": B_live, "L": L, "T": T,
-                   "layers": nl, "in_dtype": w["in_dtype"], "state_dtype": w["state_dtype"],
-                   "ring_k_dtype": w["ring_k_dtype"], "ring_d_dtype": w["ring_d_dtype"],
-                   "cuda_graph": True, "replicas": world,
-                   "l2": "inputs larger than L2 (48 distinct layers, 6 GiB of checkpoints)"},
+        "config": bench_config(nl, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} (hbm_gbs, burst)",
                      "traffic": traffic, "kernel": "replay_kernel<GDN, f32, 1>",
@@ -675,8 +670,21 @@ def oracle_sample(rows, steps):
     return rows * steps / wall, wall, max(1, round(cpu / wall))
 
 
+def bench_config(nl, world):
+    """The decode workload both arms report (the reference arm times a bounded
+    sample of it, described in its cpu_baseline)."""
+    w = WL
+    return {"workload": w["workload"], "algo": "gdn", "HK": w["HK"], "HV": w["HV"],
+            "dk": w["dk"], "dv": w["dv"], "batch": w["batch"],
+            "live_rows": w["batch"] - w["null_slots"], "L": w["L"], "T": w["T"], "layers": nl,
+            "in_dtype": w["in_dtype"], "state_dtype": w["state_dtype"],
+            "ring_k_dtype": w["ring_k_dtype"], "ring_d_dtype": w["ring_d_dtype"],
+            "cuda_graph": True, "replicas": world,
+            "l2": f"inputs larger than L2 ({nl} distinct layers of checkpoints)"}
+
+
 def run_reference(args):
-    rows, per_step = 8, 1
+    rows, per_step = 8, 10
     t_total, toks = 0.0, 0
     for _ in range(args.warmup):
         oracle_sample(rows, per_step)
@@ -686,12 +694,12 @@ def run_reference(args):
         t_total += wall
         toks += rows * per_step
     value = toks / t_total
-    sample = f"{rows} rows x 1 layer x 1 decode step per bench step, fp64 numpy oracle"
+    sample = f"{rows} rows x 1 layer x {per_step} decode steps per bench step, fp64 numpy oracle"
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": WL["workload"], "batch": rows, "L": WL["L"], "T": 1},
+            "config": bench_config(args.layers, 1),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
