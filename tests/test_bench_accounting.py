@@ -1,0 +1,47 @@
+"""The byte accounting behind the bench's roofline (CPU only).
+
+The algorithmic bytes of one live row in one replay launch are the method's:
+the checkpoint tile once, c history records, the window's inputs, the outputs,
+the T new records and, on a fold, the checkpoint written back. Checked against
+the per-term sizes written out for the Qwen3.5-4B-shaped decode layer
+(HK 16, HV 32, dk = dv = 128, fp32 state, bf16 inputs, fp16 keys, fp32 deltas).
+"""
+import pytest
+
+import bench
+
+
+def _terms(c, T, fold):
+    state = 32 * 128 * 128 * 4                       # 2,097,152
+    record = 16 * 128 * 2 + 32 * 128 * 4 + 32 * 4    # key per key head, delta, gate: 20,608
+    window = T * (2 * 16 * 128 * 2 + 32 * 128 * 2 + 32 * 2 * 4)   # q, k, v, beta, g: 16,640
+    out = T * 32 * 128 * 2                           # 8,192
+    written = T * (record + 32 * 128 * 2 + 32 * 4)   # record + v + beta: 28,928
+    return state + c * record + window + out + written + (state if fold else 0)
+
+
+@pytest.mark.parametrize("c,T,fold", [(0, 1, False), (8, 1, False), (15, 1, False),
+                                      (16, 1, True), (5, 8, False), (12, 8, True)])
+def test_row_bytes_match_the_per_term_sizes(c, T, fold):
+    assert bench.row_bytes(c, T, fold, 16, 32, 128, 128, 4, 2, 2, 4) == _terms(c, T, fold)
+
+
+def test_decode_row_bytes_worked_example():
+    # 2,097,152 + 20,608 c + 16,640 + 8,192 + 28,928 (+ 2,097,152 on a fold)
+    assert bench.row_bytes(0, 1, False, 16, 32, 128, 128, 4, 2, 2, 4) == 2150912
+    assert bench.row_bytes(8, 1, False, 16, 32, 128, 128, 4, 2, 2, 4) == 2150912 + 8 * 20608
+    assert bench.row_bytes(16, 1, True, 16, 32, 128, 128, 4, 2, 2, 4) == \
+        2150912 + 16 * 20608 + 2097152
+
+
+@pytest.mark.parametrize("c,T,L,a,want", [(0, 1, 16, 1, (1, False)), (15, 1, 16, 1, (16, False)),
+                                          (16, 1, 16, 1, (1, True)), (8, 8, 16, 3, (11, False)),
+                                          (8, 8, 16, 0, (8, False)), (9, 8, 16, 5, (5, True))])
+def test_cursor_trajectory_rule(c, T, L, a, want):
+    """The bench's host copy of the cursor rule: fold when c + T > L, then the
+    accepted tokens go after base = fold ? 0 : c."""
+    assert bench.advance(c, T, L, a) == want
+
+
+def test_job_throughput_is_whole_job():
+    assert bench.job_throughput(1000.0, 4, 2.0) == 2000.0
