@@ -120,7 +120,8 @@ def ncu_traffic():
 
 # The files that define the decode launch the ncu summary describes (kernel,
 # shared-memory plan, launch); a change to any of them invalidates the traffic.
-DECODE_SOURCES = ("replay_impl.cuh", "rssm_history.cuh", "rssm_common.cuh", "replay_launch.cuh",
+DECODE_SOURCES = ("replay_impl.cuh", "rssm_history.cuh", "rssm_common.cuh", "rssm_mma.cuh",
+                  "replay_launch.cuh",
                   "replay_gdn_f32.cu")
 
 

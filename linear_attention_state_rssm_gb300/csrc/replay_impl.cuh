@@ -43,6 +43,7 @@
 
 #include "rssm_common.cuh"
 #include "rssm_history.cuh"
+#include "rssm_mma.cuh"
 
 namespace rssm {
 
@@ -285,6 +286,101 @@ __device__ __forceinline__ int swap_rank(const unsigned* fmask, int y) {
   return y;
 }
 
+// Decode fold of a GDN window with at most 16 history records and 128 value
+// columns on the tensor cores: each 16-row tile of the checkpoint is folded as
+//     S <- e^Gam S + K~^T D~,   K~^T [16 rows x 16 records], D~ [16 records x 128]
+// with the keys transposed in hkt (row stride round4(n); records >= n read as
+// zero), D~ = f_m d_m held as tensor-core fragments for the whole tile (f_m =
+// hf[m], the decay from record m to the end of the history), the tile rows
+// from the ring stage as the fp32 accumulator, the folded rows stored back to
+// the checkpoint and fed to the mat-vec y_v = S^T x_v (x from xh [dk][2]). Warp w owns value columns
+// [32w, 32w + 32); y[nt][c][v] ends as the column sums of its columns
+// 32w + 8nt + 2t + c in the lanes with g = 0. Keys from a 16-bit ring are
+// exact in tf32 (EXACT_K).
+template <typename ST, bool EXACT_K>
+__device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const float* hkt,
+                                                const float* hd, const float* hf, int n,
+                                                float decay, const float* xh, ST* gtile, int tid,
+                                                int warp, int lane, float (&y)[4][2][2]) {
+  constexpr int DV = 128, NV = 2;
+  const int g = lane >> 2, t = lane & 3, c0 = warp * 32, ks = round4(n);
+  Tf32 bf[2][4][2];
+#pragma unroll
+  for (int kq = 0; kq < 2; ++kq) {
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int m = 8 * kq + t + 4 * hh;
+        bf[kq][nt][hh] = tf32_split<false>(m < n ? hf[m] * hd[m * DV + c0 + 8 * nt + g] : 0.f);
+      }
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      y[nt][c][0] = 0.f;
+      y[nt][c][1] = 0.f;
+    }
+  }
+  bool ok = true;
+  const int cr = pipe.tr.cr;
+  for (int j = 0; j < pipe.tr.nchunk; ++j) {
+    ok = pipe.wait(j) && ok;
+    const ST* stg = pipe.stage(j);
+    for (int m0 = 0; m0 < cr; m0 += 16) {
+      const int ra = j * cr + m0 + g, rb = ra + 8;  // this lane's two tile rows
+      Tf32 af[2][4];
+#pragma unroll
+      for (int kq = 0; kq < 2; ++kq) {
+        const int ma = 8 * kq + t, mb = ma + 4;
+        af[kq][0] = tf32_split<EXACT_K>(ma < n ? hkt[ra * ks + ma] : 0.f);
+        af[kq][1] = tf32_split<EXACT_K>(ma < n ? hkt[rb * ks + ma] : 0.f);
+        af[kq][2] = tf32_split<EXACT_K>(mb < n ? hkt[ra * ks + mb] : 0.f);
+        af[kq][3] = tf32_split<EXACT_K>(mb < n ? hkt[rb * ks + mb] : 0.f);
+      }
+      const float xa0 = xh[ra * NV], xa1 = xh[ra * NV + 1];
+      const float xb0 = xh[rb * NV], xb1 = xh[rb * NV + 1];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int col = c0 + 8 * nt + 2 * t;
+        float sa[2], sb[2];
+        ld_cols<ST, 2>(stg + (size_t)(m0 + g) * DV + col, sa);
+        ld_cols<ST, 2>(stg + (size_t)(m0 + g + 8) * DV + col, sb);
+        float acc[4] = {decay * sa[0], decay * sa[1], decay * sb[0], decay * sb[1]};
+        mma_split<EXACT_K, false>(acc, af[0], bf[0][nt]);
+        if (n > 8) mma_split<EXACT_K, false>(acc, af[1], bf[1][nt]);
+        float wa[2] = {acc[0], acc[1]}, wb[2] = {acc[2], acc[3]};
+        st_cols<ST, 2>(gtile + (size_t)ra * DV + col, wa);
+        st_cols<ST, 2>(gtile + (size_t)rb * DV + col, wb);
+        // the mat-vec takes the stored (rounded) checkpoint values
+        y[nt][0][0] = fmaf(wa[0], xa0, fmaf(wb[0], xb0, y[nt][0][0]));
+        y[nt][0][1] = fmaf(wa[0], xa1, fmaf(wb[0], xb1, y[nt][0][1]));
+        y[nt][1][0] = fmaf(wa[1], xa0, fmaf(wb[1], xb0, y[nt][1][0]));
+        y[nt][1][1] = fmaf(wa[1], xa1, fmaf(wb[1], xb1, y[nt][1][1]));
+      }
+    }
+    ok = pipe.done(j, tid, lane) && ok;
+  }
+  // sum over the eight row groups (lanes with the same t)
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        float s = y[nt][c][v];
+        s += __shfl_xor_sync(kFull, s, 4);
+        s += __shfl_xor_sync(kFull, s, 8);
+        s += __shfl_xor_sync(kFull, s, 16);
+        y[nt][c][v] = s;
+      }
+    }
+  }
+  return ok;
+}
+
 // Narrow windows keep four CTAs per SM (at most 128 registers per thread),
 // eight-token windows three (two value columns per lane, a three-stage ring);
 // the widest trade occupancy for their larger accumulator tiles.
@@ -512,6 +608,8 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
 
   const QuadLayout qlay(dv, CW, sw);
   const QuadLane qlane(qlay, CW, warp, lane);
+  bool mma_fold = false;     // decode fold on the tensor cores (column sums in ymma)
+  float ymma[4][2][2];
   float acc[NV][CW];
 #pragma unroll
   for (int vv = 0; vv < NV; ++vv) {
@@ -676,10 +774,24 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     if (!early) {
       __syncthreads();
       if (fold && nh > 0) {
-        copies_ok = stream_quads<ALGO, ST, NV, CW, MR, true>(pipe, qlane, acc, gtile, dk, dv, nh,
-                                                             ALGO == ALGO_KDA ? hg : hk, hd, hf,
-                                                             hscal[1], egam, xh, tid, lane) &&
-                    copies_ok;
+        if constexpr (NT == 1 && ALGO == ALGO_GDN) {
+          mma_fold = nh <= 16 && dv == 128 && pipe.tr.cr % 16 == 0;
+        }
+        if (mma_fold) {
+          if constexpr (NT == 1 && ALGO == ALGO_GDN) {
+            copies_ok = (p.rk_dt == DT_F32
+                             ? fold_stream_mma<ST, false>(pipe, hk, hd, hf, nh, hscal[1], xh, gtile,
+                                                          tid, warp, lane, ymma)
+                             : fold_stream_mma<ST, true>(pipe, hk, hd, hf, nh, hscal[1], xh, gtile,
+                                                         tid, warp, lane, ymma)) &&
+                        copies_ok;
+          }
+        } else {
+          copies_ok = stream_quads<ALGO, ST, NV, CW, MR, true>(pipe, qlane, acc, gtile, dk, dv,
+                                                               nh, ALGO == ALGO_KDA ? hg : hk, hd,
+                                                               hf, hscal[1], egam, xh, tid, lane) &&
+                      copies_ok;
+        }
       } else {
         copies_ok = stream_quads<ALGO, ST, NV, CW, MR, false>(pipe, qlane, acc, gtile, dk, dv, 0,
                                                               hk, hd, hf, 1.f, egam, xh, tid,
@@ -695,9 +807,25 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     }
   }
   // partial column sums of the warp row groups -> shared memory (the ring is
-  // free once every warp has consumed the last chunk)
+  // free once every warp has consumed the last chunk); a tensor-core fold
+  // leaves whole column sums, in the first row-group slot
   __syncthreads();
-  if (warp < sw && qlane.first) {
+  if (mma_fold) {
+    if constexpr (NT == 1) {
+      if (lane < 4) {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int col = warp * 32 + 8 * nt + 2 * lane + cc;
+            red[0 * dv + col] = ymma[nt][cc][0];
+            red[1 * dv + col] = ymma[nt][cc][1];
+          }
+        }
+      }
+      for (int e = tid; e < (qlay.rgw - 1) * NV * dv; e += kThreads) red[NV * dv + e] = 0.f;
+    }
+  } else if (warp < sw && qlane.first) {
 #pragma unroll
     for (int vv = 0; vv < NV; ++vv) {
 #pragma unroll

@@ -298,3 +298,26 @@ def test_decode_on_a_long_ring(algo, HK, HV):
     assert run.state_err() <= TOL16
     assert run.ring_d_err() <= TOL16
     assert run.store.rssm_get_device_error() == 0
+
+
+@pytest.mark.parametrize("state,ring_k", [("f32", "f32"), ("bf16", "f16"), ("f32", "bf16")])
+def test_decode_fold_of_every_history_length(state, ring_k):
+    """GDN decode with 128-wide heads on an L = 16 ring: row r is forced to fold
+    at step r, so one launch folds histories of every length 0..16 (then each
+    row folds a full ring every 16 steps), for fp32 and bf16 checkpoints and
+    fp32, fp16 and bf16 ring keys."""
+    B, L = 17, 16
+    slots = np.arange(B, dtype=np.int32)
+    tol = TOL32 if state == "f32" and ring_k == "f32" else TOL16
+    run = Run(algo="gdn", HK=1, HV=2, dk=128, dv=128, L=L, max_T=1, slots=slots, n_slots=B,
+              state_dtype=state, ring_k_dtype=ring_k, config_id=33)
+    for step in range(36):
+        force = (np.arange(B) == step).astype(np.uint8)
+        _, o_gpu, o_orc, f_gpu, f_orc = run.window(0, run.inputs(step, 0, 1), 1, force=force,
+                                                   decode=True, advance=True)
+        assert rel_err(o_gpu, o_orc) <= tol, step
+        np.testing.assert_array_equal(f_gpu, f_orc)
+        run.check_cursors()
+        assert run.state_err() <= tol, step
+    assert run.ring_d_err() <= tol
+    assert run.store.rssm_get_device_error() == 0
