@@ -19,10 +19,12 @@
 // (G_i the in-chunk inclusive gate prefix; per key channel for KDA). Each
 // chunk's inputs are loaded into registers (16-byte coalesced loads) while the
 // chunk before is computed, and widened to fp32 as they are stored to shared
-// memory. The O(dk CB) work per token runs on CUDA cores in fp32: the
-// two mat-vec passes (one column and 16 vectors per thread, inputs broadcast
-// from a per-channel row) and the rank-16 update (four columns and sixteen
-// rows per step of a thread).
+// memory. The chunk's dense products run on the tensor cores (warp-level
+// mma.sync m16n8k8, tf32 head/tail operand splits, fp32 accumulation): the
+// mat-vecs Y = X^T S for its 2C vectors, the GDN pair dots [K; Q] K^T, the
+// outputs O = Y_q + F D and the rank-16 update of the state slice. The forward
+// substitution for the deltas (one column per thread, on warps 0-1) and the
+// gate scans run on CUDA cores while warps 2-7 prepare the next chunk.
 #include "replay_impl.cuh"
 #include "rssm_mma.cuh"
 #include "rssm_launch.h"
