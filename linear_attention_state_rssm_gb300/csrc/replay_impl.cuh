@@ -45,6 +45,8 @@
 #include "rssm_history.cuh"
 #include "rssm_mma.cuh"
 
+#include <type_traits>
+
 namespace rssm {
 
 __device__ __forceinline__ float4 ld4(const float* p) {
@@ -381,6 +383,107 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
   return ok;
 }
 
+// Tile stream of a GDN window of eight tokens (16 mat-vec vectors) with 128
+// value columns on the tensor cores, with the fold of a history of at most 16
+// records when FOLD. Both products take the value columns as the m index and
+// the checkpoint rows as the reduction or n index, so the fold's accumulator
+// fragment is the mat-vec's A fragment as it stands:
+//     fold     S^T <- e^Gam S^T + D~^T K~     D~^T [128 x n records], K~ [n x rows]
+//     mat-vec  Y^T += S^T X                   X [rows x 16] (xh, [dk][16])
+// with D~ = f_m d_m (f_m = hf[m]) and the raw keys K~ transposed in hkt (row
+// stride round4(n); records >= n read as zero). Warp w owns the columns
+// [32w, 32w + 32): lane (g, t) reads the four columns 32w + 4g .. 32w + 4g + 3
+// of rows 2t and 2t + 1 of each eight-row step (one 16-byte load per row, the
+// 32 lanes cover four whole rows); in m-tile mt, m = g is column 32w + 4g + 2mt
+// and m = g + 8 the column after it; the step's reduction index k = t is row
+// 2t and k = t + 4 row 2t + 1. Folded rows are stored back (rounded to the
+// checkpoint dtype) and the mat-vec takes the stored values. y[mt][nt] ends as
+// the fragment of Y^T: c0 (column 32w + 4g + 2mt, vector 8nt + 2t), c1 (same
+// column, vector + 1), c2 and c3 (the next column). 16-bit checkpoint values,
+// 16-bit inputs (EXACT_X) and 16-bit ring keys (EXACT_K) are exact in tf32.
+template <typename ST, bool FOLD, bool EXACT_X, bool EXACT_K>
+__device__ __forceinline__ bool stream_mma16(const TilePipe<ST>& pipe, const float* hkt,
+                                             const float* hd, const float* hf, int n, float decay,
+                                             const float* xh, ST* gtile, int tid, int warp,
+                                             int lane, float (&y)[2][2][4]) {
+  constexpr int DV = 128, NV = 16;
+  constexpr bool EXACT_S = !std::is_same<ST, float>::value;
+  const int g = lane >> 2, t = lane & 3, col = warp * 32 + 4 * g, ks = round4(n);
+  Tf32 df[2][2][4];  // fold A fragments: [m-tile][record step][4]
+  if (FOLD) {
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int kq = 0; kq < 2; ++kq) {
+        const int m0 = 8 * kq + t, m1 = m0 + 4, c0 = col + 2 * mt;
+        const float f0 = m0 < n ? hf[m0] : 0.f, f1 = m1 < n ? hf[m1] : 0.f;
+        df[mt][kq][0] = tf32_split<false>(m0 < n ? f0 * hd[m0 * DV + c0] : 0.f);
+        df[mt][kq][1] = tf32_split<false>(m0 < n ? f0 * hd[m0 * DV + c0 + 1] : 0.f);
+        df[mt][kq][2] = tf32_split<false>(m1 < n ? f1 * hd[m1 * DV + c0] : 0.f);
+        df[mt][kq][3] = tf32_split<false>(m1 < n ? f1 * hd[m1 * DV + c0 + 1] : 0.f);
+      }
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) y[mt][nt][e] = 0.f;
+    }
+  }
+  bool ok = true;
+  const int cr = pipe.tr.cr;
+  for (int j = 0; j < pipe.tr.nchunk; ++j) {
+    ok = pipe.wait(j) && ok;
+    const ST* stg = pipe.stage(j);
+    for (int kb = 0; kb < cr; kb += 8) {
+      const int r0 = j * cr + kb + 2 * t, r1 = r0 + 1;  // this lane's two tile rows
+      float s0[4], s1[4];
+      ld_cols<ST, 4>(stg + (size_t)(kb + 2 * t) * DV + col, s0);
+      ld_cols<ST, 4>(stg + (size_t)(kb + 2 * t + 1) * DV + col, s1);
+      if (FOLD) {
+        const int rn = j * cr + kb + g;  // the fold's B column: row kb + g
+        Tf32 kf[2][2];
+#pragma unroll
+        for (int kq = 0; kq < 2; ++kq) {
+          const int ma = 8 * kq + t, mb = ma + 4;
+          kf[kq][0] = tf32_split<EXACT_K>(ma < n ? hkt[rn * ks + ma] : 0.f);
+          kf[kq][1] = tf32_split<EXACT_K>(mb < n ? hkt[rn * ks + mb] : 0.f);
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          float c[4] = {decay * s0[2 * mt], decay * s1[2 * mt], decay * s0[2 * mt + 1],
+                        decay * s1[2 * mt + 1]};
+          mma_split<false, EXACT_K>(c, df[mt][0], kf[0]);
+          if (n > 8) mma_split<false, EXACT_K>(c, df[mt][1], kf[1]);
+          s0[2 * mt] = c[0];
+          s1[2 * mt] = c[1];
+          s0[2 * mt + 1] = c[2];
+          s1[2 * mt + 1] = c[3];
+        }
+        st_cols<ST, 4>(gtile + (size_t)r0 * DV + col, s0);
+        st_cols<ST, 4>(gtile + (size_t)r1 * DV + col, s1);
+      }
+      Tf32 xf[2][2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        xf[nt][0] = tf32_split<EXACT_X>(xh[r0 * NV + 8 * nt + g]);
+        xf[nt][1] = tf32_split<EXACT_X>(xh[r1 * NV + 8 * nt + g]);
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const Tf32 af[4] = {tf32_split<EXACT_S>(s0[2 * mt]), tf32_split<EXACT_S>(s0[2 * mt + 1]),
+                            tf32_split<EXACT_S>(s1[2 * mt]), tf32_split<EXACT_S>(s1[2 * mt + 1])};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) mma_split<EXACT_S, EXACT_X>(y[mt][nt], af, xf[nt]);
+      }
+    }
+    ok = pipe.done(j, tid, lane) && ok;
+  }
+  return ok;
+}
+
 // Narrow windows keep four CTAs per SM (at most 128 registers per thread),
 // eight-token windows three (two value columns per lane, a three-stage ring);
 // the widest trade occupancy for their larger accumulator tiles.
@@ -610,6 +713,8 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   const QuadLane qlane(qlay, CW, warp, lane);
   bool mma_fold = false;     // decode fold on the tensor cores (column sums in ymma)
   float ymma[4][2][2];
+  bool mma16 = false;        // eight-token tile stream on the tensor cores (sums in y16)
+  float y16[2][2][4];
   float acc[NV][CW];
 #pragma unroll
   for (int vv = 0; vv < NV; ++vv) {
@@ -680,11 +785,25 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   } else {
     // A wide GDN window without a fold streams first, while its history lands.
     const bool early = ALGO == ALGO_GDN && !fold;
+    if constexpr (NT == 8 && ALGO == ALGO_GDN) {
+      mma16 = dv == 128 && pipe.tr.cr % 8 == 0 && (!fold || nh <= 16);
+    }
     if (early) {
-      copies_ok = stream_quads<ALGO, ST, NV, CW, MR, false>(pipe, qlane, acc, gtile, dk, dv, 0,
-                                                            hk, hd, hf, 1.f, egam, xh, tid,
-                                                            lane) &&
-                  copies_ok;
+      if (mma16) {
+        if constexpr (NT == 8 && ALGO == ALGO_GDN) {
+          copies_ok = (p.in_dt == DT_F32
+                           ? stream_mma16<ST, false, false, false>(pipe, hk, hd, hf, 0, 1.f, xh,
+                                                                   gtile, tid, warp, lane, y16)
+                           : stream_mma16<ST, false, true, false>(pipe, hk, hd, hf, 0, 1.f, xh,
+                                                                  gtile, tid, warp, lane, y16)) &&
+                      copies_ok;
+        }
+      } else {
+        copies_ok = stream_quads<ALGO, ST, NV, CW, MR, false>(pipe, qlane, acc, gtile, dk, dv, 0,
+                                                              hk, hd, hf, 1.f, egam, xh, tid,
+                                                              lane) &&
+                    copies_ok;
+      }
     }
     if (nh > 0 && !fold) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
     if (nh > 0) {
@@ -777,7 +896,22 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
         if constexpr (NT == 1 && ALGO == ALGO_GDN) {
           mma_fold = nh <= 16 && dv == 128 && pipe.tr.cr % 16 == 0;
         }
-        if (mma_fold) {
+        if (mma16) {
+          if constexpr (NT == 8 && ALGO == ALGO_GDN) {
+            const bool xk = p.in_dt != DT_F32, kk = p.rk_dt != DT_F32;
+            copies_ok =
+                (xk ? (kk ? stream_mma16<ST, true, true, true>(pipe, hk, hd, hf, nh, hscal[1], xh,
+                                                               gtile, tid, warp, lane, y16)
+                          : stream_mma16<ST, true, true, false>(pipe, hk, hd, hf, nh, hscal[1],
+                                                                xh, gtile, tid, warp, lane, y16))
+                    : (kk ? stream_mma16<ST, true, false, true>(pipe, hk, hd, hf, nh, hscal[1],
+                                                                xh, gtile, tid, warp, lane, y16)
+                          : stream_mma16<ST, true, false, false>(pipe, hk, hd, hf, nh, hscal[1],
+                                                                 xh, gtile, tid, warp, lane,
+                                                                 y16))) &&
+                copies_ok;
+          }
+        } else if (mma_fold) {
           if constexpr (NT == 1 && ALGO == ALGO_GDN) {
             copies_ok = (p.rk_dt == DT_F32
                              ? fold_stream_mma<ST, false>(pipe, hk, hd, hf, nh, hscal[1], xh, gtile,
@@ -790,6 +924,15 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
           copies_ok = stream_quads<ALGO, ST, NV, CW, MR, true>(pipe, qlane, acc, gtile, dk, dv,
                                                                nh, ALGO == ALGO_KDA ? hg : hk, hd,
                                                                hf, hscal[1], egam, xh, tid, lane) &&
+                      copies_ok;
+        }
+      } else if (mma16) {
+        if constexpr (NT == 8 && ALGO == ALGO_GDN) {
+          copies_ok = (p.in_dt == DT_F32
+                           ? stream_mma16<ST, false, false, false>(pipe, hk, hd, hf, 0, 1.f, xh,
+                                                                   gtile, tid, warp, lane, y16)
+                           : stream_mma16<ST, false, true, false>(pipe, hk, hd, hf, 0, 1.f, xh,
+                                                                  gtile, tid, warp, lane, y16)) &&
                       copies_ok;
         }
       } else {
@@ -821,6 +964,22 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
             red[0 * dv + col] = ymma[nt][cc][0];
             red[1 * dv + col] = ymma[nt][cc][1];
           }
+        }
+      }
+      for (int e = tid; e < (qlay.rgw - 1) * NV * dv; e += kThreads) red[NV * dv + e] = 0.f;
+    }
+  } else if (mma16) {
+    if constexpr (NT == 8) {
+      const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int col = warp * 32 + 4 * g + 2 * mt, v = 8 * nt + 2 * t;
+          red[v * dv + col] = y16[mt][nt][0];
+          red[(v + 1) * dv + col] = y16[mt][nt][1];
+          red[v * dv + col + 1] = y16[mt][nt][2];
+          red[(v + 1) * dv + col + 1] = y16[mt][nt][3];
         }
       }
       for (int e = tid; e < (qlay.rgw - 1) * NV * dv; e += kThreads) red[NV * dv + e] = 0.f;

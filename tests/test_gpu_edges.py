@@ -321,3 +321,29 @@ def test_decode_fold_of_every_history_length(state, ring_k):
         assert run.state_err() <= tol, step
     assert run.ring_d_err() <= tol
     assert run.store.rssm_get_device_error() == 0
+
+
+@pytest.mark.parametrize("in_dt,ring_k,state", [("f32", "f32", "f32"), ("f32", "bf16", "f32"),
+                                                ("bf16", "f32", "bf16"), ("bf16", "f16", "f32")])
+def test_eight_token_verify_across_input_key_and_state_dtypes(in_dt, ring_k, state):
+    """Eight-token verify + commit with 128-wide heads (fp32 and 16-bit inputs,
+    ring keys and checkpoints), forced folds on top of the ring's own, accept
+    lengths U[0, 8]: outputs, fold flags, cursors and checkpoints vs the oracle."""
+    B, L, T = 12, 16, 8
+    tol = TOL32 if (in_dt, ring_k, state) == ("f32", "f32", "f32") else TOL16
+    run = Run(algo="gdn", HK=1, HV=2, dk=128, dv=128, L=L, max_T=T,
+              slots=np.arange(B, dtype=np.int32), n_slots=B, in_dtype=in_dt, state_dtype=state,
+              ring_k_dtype=ring_k, config_id=34)
+    for step in range(14):
+        inp = run.inputs(step, 0, T)
+        force = synth.force_flags(3400 + step, B, 0.15)
+        acc = synth.accept_lengths(3500 + step, B, T)
+        _, o_gpu, o_orc, f_gpu, f_orc = run.window(0, inp, T, force=force)
+        mask = (np.arange(T)[None, :] < acc[:, None]).reshape(-1)
+        assert rel_err(o_gpu[mask], o_orc[mask]) <= tol, step
+        np.testing.assert_array_equal(f_gpu, f_orc)
+        run.commit(acc, T, force=force)
+        run.check_cursors()
+        assert run.state_err() <= tol, step
+    assert run.ring_d_err() <= tol
+    assert run.store.rssm_get_device_error() == 0
