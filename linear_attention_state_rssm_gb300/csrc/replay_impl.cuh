@@ -383,6 +383,15 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
   return ok;
 }
 
+// Slot of mat-vec input (row ch, vector v) of a 16-vector window in fragment
+// order: for rows [8s, 8s + 8) lane (g, t) finds vectors g and 8 + g of rows
+// 8s + 2t and 8s + 2t + 1 at [4 (32 s + 4 g + t)], as (v = g, row 2t),
+// (v = g, row 2t + 1), (v = 8 + g, row 2t), (v = 8 + g, row 2t + 1).
+__device__ __forceinline__ int x_frag16(int ch, int v) {
+  const int s8 = ch >> 3, r = ch & 7;
+  return 4 * (32 * s8 + 4 * (v & 7) + (r >> 1)) + 2 * (v >> 3) + (r & 1);
+}
+
 // Tile stream of a GDN window of eight tokens (16 mat-vec vectors) with 128
 // value columns on the tensor cores, with the fold of a history of at most 16
 // records when FOLD. Both products take the value columns as the m index and
@@ -390,8 +399,10 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
 // fragment is the mat-vec's A fragment as it stands:
 //     fold     S^T <- e^Gam S^T + D~^T K~     D~^T [128 x n records], K~ [n x rows]
 //     mat-vec  Y^T += S^T X                   X [rows x 16] (xh, [dk][16])
-// with D~ = f_m d_m (f_m = hf[m]) and the raw keys K~ transposed in hkt (row
-// stride round4(n); records >= n read as zero). Warp w owns the columns
+// with D~ = f_m d_m (f_m = hf[m]). The raw keys (hkf, from frag_keys16) and
+// the window vectors X (xf, from x_frag16) are stored in fragment order: one
+// 16-byte load per lane and step gives both of the step's fragments of each.
+// Warp w owns the columns
 // [32w, 32w + 32): lane (g, t) reads the four columns 32w + 4g .. 32w + 4g + 3
 // of rows 2t and 2t + 1 of each eight-row step (one 16-byte load per row, the
 // 32 lanes cover four whole rows); in m-tile mt, m = g is column 32w + 4g + 2mt
@@ -402,13 +413,15 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
 // column, vector + 1), c2 and c3 (the next column). 16-bit checkpoint values,
 // 16-bit inputs (EXACT_X) and 16-bit ring keys (EXACT_K) are exact in tf32.
 template <typename ST, bool FOLD, bool EXACT_X, bool EXACT_K>
-__device__ __forceinline__ bool stream_mma16(const TilePipe<ST>& pipe, const float* hkt,
+__device__ __forceinline__ bool stream_mma16(const TilePipe<ST>& pipe, const float* hkf,
                                              const float* hd, const float* hf, int n, float decay,
-                                             const float* xh, ST* gtile, int tid, int warp,
+                                             const float* xf, ST* gtile, int tid, int warp,
                                              int lane, float (&y)[2][2][4]) {
-  constexpr int DV = 128, NV = 16;
+  constexpr int DV = 128;
   constexpr bool EXACT_S = !std::is_same<ST, float>::value;
-  const int g = lane >> 2, t = lane & 3, col = warp * 32 + 4 * g, ks = round4(n);
+  const int g = lane >> 2, t = lane & 3, col = warp * 32 + 4 * g;
+  const float4* xf4 = reinterpret_cast<const float4*>(xf);
+  const float4* kf4 = reinterpret_cast<const float4*>(hkf);
   Tf32 df[2][2][4];  // fold A fragments: [m-tile][record step][4]
   if (FOLD) {
 #pragma unroll
@@ -439,18 +452,14 @@ __device__ __forceinline__ bool stream_mma16(const TilePipe<ST>& pipe, const flo
     const ST* stg = pipe.stage(j);
     for (int kb = 0; kb < cr; kb += 8) {
       const int r0 = j * cr + kb + 2 * t, r1 = r0 + 1;  // this lane's two tile rows
+      const int fi = ((j * cr + kb) >> 3) * 32 + lane;   // fragment slot of this step
       float s0[4], s1[4];
       ld_cols<ST, 4>(stg + (size_t)(kb + 2 * t) * DV + col, s0);
       ld_cols<ST, 4>(stg + (size_t)(kb + 2 * t + 1) * DV + col, s1);
       if (FOLD) {
-        const int rn = j * cr + kb + g;  // the fold's B column: row kb + g
-        Tf32 kf[2][2];
-#pragma unroll
-        for (int kq = 0; kq < 2; ++kq) {
-          const int ma = 8 * kq + t, mb = ma + 4;
-          kf[kq][0] = tf32_split<EXACT_K>(ma < n ? hkt[rn * ks + ma] : 0.f);
-          kf[kq][1] = tf32_split<EXACT_K>(mb < n ? hkt[rn * ks + mb] : 0.f);
-        }
+        const float4 k4 = kf4[fi];  // row kb + g: records t, t + 4, 8 + t, 12 + t
+        const Tf32 kf[2][2] = {{tf32_split<EXACT_K>(k4.x), tf32_split<EXACT_K>(k4.y)},
+                               {tf32_split<EXACT_K>(k4.z), tf32_split<EXACT_K>(k4.w)}};
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
           float c[4] = {decay * s0[2 * mt], decay * s1[2 * mt], decay * s0[2 * mt + 1],
@@ -465,18 +474,15 @@ __device__ __forceinline__ bool stream_mma16(const TilePipe<ST>& pipe, const flo
         st_cols<ST, 4>(gtile + (size_t)r0 * DV + col, s0);
         st_cols<ST, 4>(gtile + (size_t)r1 * DV + col, s1);
       }
-      Tf32 xf[2][2];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        xf[nt][0] = tf32_split<EXACT_X>(xh[r0 * NV + 8 * nt + g]);
-        xf[nt][1] = tf32_split<EXACT_X>(xh[r1 * NV + 8 * nt + g]);
-      }
+      const float4 x4 = xf4[fi];  // vectors g and 8 + g of rows 2t, 2t + 1
+      const Tf32 xb[2][2] = {{tf32_split<EXACT_X>(x4.x), tf32_split<EXACT_X>(x4.y)},
+                             {tf32_split<EXACT_X>(x4.z), tf32_split<EXACT_X>(x4.w)}};
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const Tf32 af[4] = {tf32_split<EXACT_S>(s0[2 * mt]), tf32_split<EXACT_S>(s0[2 * mt + 1]),
                             tf32_split<EXACT_S>(s1[2 * mt]), tf32_split<EXACT_S>(s1[2 * mt + 1])};
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) mma_split<EXACT_S, EXACT_X>(y[mt][nt], af, xf[nt]);
+        for (int nt = 0; nt < 2; ++nt) mma_split<EXACT_S, EXACT_X>(y[mt][nt], af, xb[nt]);
       }
     }
     ok = pipe.done(j, tid, lane) && ok;
@@ -654,6 +660,11 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   const int nh = c;
   const bool split = can_split(ALGO, NT) && !fold;
   const int sw = split ? kSplitWarps : kWarps;  // warps that stream the tile
+  // Eight-token GDN windows with 128 value columns stream on the tensor cores
+  // (mat-vec inputs and fold keys in fragment order, column sums in y16); a
+  // fold there takes at most 16 records and a ring of at least 16.
+  const bool mma16 = NT == 8 && ALGO == ALGO_GDN && dv == 128 && pipe.tr.cr % 8 == 0 &&
+                     (!fold || (nh <= 16 && L >= 16));
   const size_t kbase = ((size_t)s * HV + h) * L * dk;
   const size_t dbase = ((size_t)s * HV + h) * L * dv;
   const size_t gbase = ((size_t)s * HV + h) * L * (ALGO == ALGO_GDN ? 1 : dk);
@@ -680,7 +691,8 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     for (int e = tid; e < dk * NV; e += kThreads) {
       const int ch = e / NV, vv = e - ch * NV;
       const int i = vv < NT ? vv : vv - NT;
-      xh[e] = i < T ? ld_f32(vv < NT ? ksrc : qsrc, (size_t)i * dk + ch, p.in_dt) : 0.f;
+      const float x = i < T ? ld_f32(vv < NT ? ksrc : qsrc, (size_t)i * dk + ch, p.in_dt) : 0.f;
+      xh[mma16 ? x_frag16(ch, vv) : e] = x;
     }
   }
   if (tid < T) {
@@ -713,8 +725,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   const QuadLane qlane(qlay, CW, warp, lane);
   bool mma_fold = false;     // decode fold on the tensor cores (column sums in ymma)
   float ymma[4][2][2];
-  bool mma16 = false;        // eight-token tile stream on the tensor cores (sums in y16)
-  float y16[2][2][4];
+  float y16[2][2][4];        // column sums of the eight-token tensor-core stream
   float acc[NV][CW];
 #pragma unroll
   for (int vv = 0; vv < NV; ++vv) {
@@ -785,9 +796,6 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   } else {
     // A wide GDN window without a fold streams first, while its history lands.
     const bool early = ALGO == ALGO_GDN && !fold;
-    if constexpr (NT == 8 && ALGO == ALGO_GDN) {
-      mma16 = dv == 128 && pipe.tr.cr % 8 == 0 && (!fold || nh <= 16);
-    }
     if (early) {
       if (mma16) {
         if constexpr (NT == 8 && ALGO == ALGO_GDN) {
@@ -809,7 +817,9 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     if (nh > 0) {
       if (p.rd_dt != DT_F32) widen16(hd, hdraw, nh * dv, p.rd_dt, tid, kThreads);
       if (ALGO == ALGO_GDN) {
-        if (fold) {
+        if (fold && mma16) {
+          frag_keys16(hk, hkraw, nh, dk, p.rk_dt, tid, kThreads);
+        } else if (fold) {
           transpose_keys(hk, hkraw, nh, dk, p.rk_dt, tid, kThreads);
         } else {
           widen_keys(hk, hkraw, nh * dk, p.rk_dt, tid, kThreads);

@@ -87,6 +87,25 @@ __device__ __forceinline__ void transpose_keys(float* hkt, const void* raw, int 
   }
 }
 
+// The raw keys of n <= 16 records in the order of the B fragments of an
+// m16n8k8 product with the records as k and eight rows as n: for rows
+// [8s, 8s + 8) lane (g, t) finds at hkf[4 (32 s + 4 g + t)] the keys of row
+// 8s + g from records t, t + 4, 8 + t and 12 + t (zero for records >= n).
+// hkf holds dk * 16 floats.
+__device__ __forceinline__ void frag_keys16(float* hkf, const void* raw, int n, int dk, int dt,
+                                            int t, int nt) {
+  for (int e = t; e < dk * 4; e += nt) {
+    const int s8 = e >> 5, ln = e & 31, row = 8 * s8 + (ln >> 2), m0 = ln & 3;
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int m = m0 + 4 * j;
+      v[j] = m < n ? ld_f32(raw, (size_t)m * dk + row, dt) : 0.f;
+    }
+    *reinterpret_cast<float4*>(hkf + 4 * e) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
 // GDN, warp 0: hf[m] holds the raw record gates g_m; replaces them with
 // exp(sum_{m' > m} g_m') and writes Gam, exp(Gam) to scal[0], scal[1].
 __device__ __forceinline__ void gdn_history_scan(int n, float* hf, float* scal, int lane) {
