@@ -383,44 +383,50 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
   return ok;
 }
 
-// Slot of mat-vec input (row ch, vector v) of a 16-vector window in fragment
-// order: for rows [8s, 8s + 8) lane (g, t) finds vectors g and 8 + g of rows
-// 8s + 2t and 8s + 2t + 1 at [4 (32 s + 4 g + t)], as (v = g, row 2t),
-// (v = g, row 2t + 1), (v = 8 + g, row 2t), (v = 8 + g, row 2t + 1).
-__device__ __forceinline__ int x_frag16(int ch, int v) {
-  const int s8 = ch >> 3, r = ch & 7;
-  return 4 * (32 * s8 + 4 * (v & 7) + (r >> 1)) + 2 * (v >> 3) + (r & 1);
+// Fragment order of the mat-vec inputs of a window with 8 NTN vectors (NTN
+// n-tiles of eight): for rows [8s, 8s + 8) lane (g, t) finds at
+// [2 NTN (32 s + 4 g + t) + 2 nt + h] vector 8 nt + g of row 8s + 2t + h.
+// x_slot maps slot e back to its (row ch, vector v).
+template <int NTN>
+__device__ __forceinline__ void x_slot(int e, int& ch, int& v) {
+  constexpr int CPL = 2 * NTN;  // values per lane and step
+  const int s8 = e / (32 * CPL), ln = (e / CPL) & 31, comp = e % CPL;
+  ch = 8 * s8 + 2 * (ln & 3) + (comp & 1);
+  v = 8 * (comp >> 1) + (ln >> 2);
 }
 
-// Tile stream of a GDN window of eight tokens (16 mat-vec vectors) with 128
-// value columns on the tensor cores, with the fold of a history of at most 16
-// records when FOLD. Both products take the value columns as the m index and
-// the checkpoint rows as the reduction or n index, so the fold's accumulator
-// fragment is the mat-vec's A fragment as it stands:
+// Tile stream of a GDN window with 8 NTN mat-vec vectors (four or eight
+// tokens) and 128 value columns on the tensor cores, with the fold of a
+// history of at most 16 records when FOLD. Both products take the value
+// columns as the m index and the checkpoint rows as the reduction or n index,
+// so the fold's accumulator fragment is the mat-vec's A fragment as it stands:
 //     fold     S^T <- e^Gam S^T + D~^T K~     D~^T [128 x n records], K~ [n x rows]
-//     mat-vec  Y^T += S^T X                   X [rows x 16] (xh, [dk][16])
+//     mat-vec  Y^T += S^T X                   X [rows x 8 NTN]
 // with D~ = f_m d_m (f_m = hf[m]). The raw keys (hkf, from frag_keys16) and
-// the window vectors X (xf, from x_frag16) are stored in fragment order: one
-// 16-byte load per lane and step gives both of the step's fragments of each.
-// Warp w owns the columns
-// [32w, 32w + 32): lane (g, t) reads the four columns 32w + 4g .. 32w + 4g + 3
-// of rows 2t and 2t + 1 of each eight-row step (one 16-byte load per row, the
-// 32 lanes cover four whole rows); in m-tile mt, m = g is column 32w + 4g + 2mt
-// and m = g + 8 the column after it; the step's reduction index k = t is row
-// 2t and k = t + 4 row 2t + 1. Folded rows are stored back (rounded to the
-// checkpoint dtype) and the mat-vec takes the stored values. y[mt][nt] ends as
-// the fragment of Y^T: c0 (column 32w + 4g + 2mt, vector 8nt + 2t), c1 (same
-// column, vector + 1), c2 and c3 (the next column). 16-bit checkpoint values,
-// 16-bit inputs (EXACT_X) and 16-bit ring keys (EXACT_K) are exact in tf32.
-template <typename ST, bool FOLD, bool EXACT_X, bool EXACT_K>
-__device__ __forceinline__ bool stream_mma16(const TilePipe<ST>& pipe, const float* hkf,
-                                             const float* hd, const float* hf, int n, float decay,
-                                             const float* xf, ST* gtile, int tid, int warp,
-                                             int lane, float (&y)[2][2][4]) {
-  constexpr int DV = 128;
+// the window vectors X (xf, see x_slot) are stored in fragment order: one
+// load per lane and step gives all of the step's fragments of each.
+// The 128 / (16 MT) streaming warps own 16 MT columns each; lane (g, t) of warp
+// w reads, for each of its MT / 2 column quads q, the four columns
+// 16 MT w + 32 q + 4g .. + 3 of rows 2t and 2t + 1 of each eight-row step (one
+// 16-byte load per row and quad; eight lanes cover 128 contiguous bytes); in
+// m-tile mt (quad mt / 2), m = g is column 16 MT w + 32 (mt / 2) + 4g +
+// 2 (mt % 2) and m = g + 8 the column after it; the step's reduction index
+// k = t is row 2t and k = t + 4 row 2t + 1. Folded rows are stored back
+// (rounded to the checkpoint dtype) and the mat-vec takes the stored values.
+// y[4 (NTN mt + nt) + e] ends as the fragment of Y^T: e = 0 (column of m = g,
+// vector 8 nt + 2t), 1 (same column, next vector), 2 and 3 (the next column).
+// 16-bit checkpoint values, 16-bit inputs (EXACT_X) and 16-bit ring keys
+// (EXACT_K) are exact in tf32. A fold runs on four warps (MT = 2).
+template <typename ST, int NTN, int MT, bool FOLD, bool EXACT_X, bool EXACT_K>
+__device__ __forceinline__ bool stream_mma(const TilePipe<ST>& pipe, const float* hkf,
+                                           const float* hd, const float* hf, int n, float decay,
+                                           const float* xf, ST* gtile, int tid, int warp,
+                                           int lane, float (&y)[16]) {
+  static_assert(NTN * MT * 4 <= 16 && (MT == 2 || MT == 4) && (!FOLD || MT == 2),
+                "tensor-core stream shape");
+  constexpr int DV = 128, NQ = MT / 2;
   constexpr bool EXACT_S = !std::is_same<ST, float>::value;
-  const int g = lane >> 2, t = lane & 3, col = warp * 32 + 4 * g;
-  const float4* xf4 = reinterpret_cast<const float4*>(xf);
+  const int g = lane >> 2, t = lane & 3, col = warp * 16 * MT + 4 * g;
   const float4* kf4 = reinterpret_cast<const float4*>(hkf);
   Tf32 df[2][2][4];  // fold A fragments: [m-tile][record step][4]
   if (FOLD) {
@@ -438,13 +444,7 @@ __device__ __forceinline__ bool stream_mma16(const TilePipe<ST>& pipe, const flo
     }
   }
 #pragma unroll
-  for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) y[mt][nt][e] = 0.f;
-    }
-  }
+  for (int e = 0; e < 16; ++e) y[e] = 0.f;
   bool ok = true;
   const int cr = pipe.tr.cr;
   for (int j = 0; j < pipe.tr.nchunk; ++j) {
@@ -453,36 +453,52 @@ __device__ __forceinline__ bool stream_mma16(const TilePipe<ST>& pipe, const flo
     for (int kb = 0; kb < cr; kb += 8) {
       const int r0 = j * cr + kb + 2 * t, r1 = r0 + 1;  // this lane's two tile rows
       const int fi = ((j * cr + kb) >> 3) * 32 + lane;   // fragment slot of this step
-      float s0[4], s1[4];
-      ld_cols<ST, 4>(stg + (size_t)(kb + 2 * t) * DV + col, s0);
-      ld_cols<ST, 4>(stg + (size_t)(kb + 2 * t + 1) * DV + col, s1);
-      if (FOLD) {
+      float s0[NQ][4], s1[NQ][4];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        ld_cols<ST, 4>(stg + (size_t)(kb + 2 * t) * DV + col + 32 * q, s0[q]);
+        ld_cols<ST, 4>(stg + (size_t)(kb + 2 * t + 1) * DV + col + 32 * q, s1[q]);
+      }
+      if constexpr (FOLD) {
         const float4 k4 = kf4[fi];  // row kb + g: records t, t + 4, 8 + t, 12 + t
         const Tf32 kf[2][2] = {{tf32_split<EXACT_K>(k4.x), tf32_split<EXACT_K>(k4.y)},
                                {tf32_split<EXACT_K>(k4.z), tf32_split<EXACT_K>(k4.w)}};
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
-          float c[4] = {decay * s0[2 * mt], decay * s1[2 * mt], decay * s0[2 * mt + 1],
-                        decay * s1[2 * mt + 1]};
+          float c[4] = {decay * s0[0][2 * mt], decay * s1[0][2 * mt], decay * s0[0][2 * mt + 1],
+                        decay * s1[0][2 * mt + 1]};
           mma_split<false, EXACT_K>(c, df[mt][0], kf[0]);
           if (n > 8) mma_split<false, EXACT_K>(c, df[mt][1], kf[1]);
-          s0[2 * mt] = c[0];
-          s1[2 * mt] = c[1];
-          s0[2 * mt + 1] = c[2];
-          s1[2 * mt + 1] = c[3];
+          s0[0][2 * mt] = c[0];
+          s1[0][2 * mt] = c[1];
+          s0[0][2 * mt + 1] = c[2];
+          s1[0][2 * mt + 1] = c[3];
         }
-        st_cols<ST, 4>(gtile + (size_t)r0 * DV + col, s0);
-        st_cols<ST, 4>(gtile + (size_t)r1 * DV + col, s1);
+        st_cols<ST, 4>(gtile + (size_t)r0 * DV + col, s0[0]);
+        st_cols<ST, 4>(gtile + (size_t)r1 * DV + col, s1[0]);
       }
-      const float4 x4 = xf4[fi];  // vectors g and 8 + g of rows 2t, 2t + 1
-      const Tf32 xb[2][2] = {{tf32_split<EXACT_X>(x4.x), tf32_split<EXACT_X>(x4.y)},
-                             {tf32_split<EXACT_X>(x4.z), tf32_split<EXACT_X>(x4.w)}};
+      Tf32 xb[NTN][2];  // vectors 8 nt + g of rows 2t, 2t + 1
+      if constexpr (NTN == 2) {
+        const float4 x4 = reinterpret_cast<const float4*>(xf)[fi];
+        xb[0][0] = tf32_split<EXACT_X>(x4.x);
+        xb[0][1] = tf32_split<EXACT_X>(x4.y);
+        xb[NTN - 1][0] = tf32_split<EXACT_X>(x4.z);
+        xb[NTN - 1][1] = tf32_split<EXACT_X>(x4.w);
+      } else {
+        const float2 x2 = reinterpret_cast<const float2*>(xf)[fi];
+        xb[0][0] = tf32_split<EXACT_X>(x2.x);
+        xb[0][1] = tf32_split<EXACT_X>(x2.y);
+      }
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const Tf32 af[4] = {tf32_split<EXACT_S>(s0[2 * mt]), tf32_split<EXACT_S>(s0[2 * mt + 1]),
-                            tf32_split<EXACT_S>(s1[2 * mt]), tf32_split<EXACT_S>(s1[2 * mt + 1])};
+      for (int mt = 0; mt < MT; ++mt) {
+        const int q = mt >> 1, h = 2 * (mt & 1);
+        const Tf32 af[4] = {tf32_split<EXACT_S>(s0[q][h]), tf32_split<EXACT_S>(s0[q][h + 1]),
+                            tf32_split<EXACT_S>(s1[q][h]), tf32_split<EXACT_S>(s1[q][h + 1])};
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) mma_split<EXACT_S, EXACT_X>(y[mt][nt], af, xb[nt]);
+        for (int nt = 0; nt < NTN; ++nt) {
+          float(&c)[4] = *reinterpret_cast<float(*)[4]>(&y[4 * (NTN * mt + nt)]);
+          mma_split<EXACT_S, EXACT_X>(c, af, xb[nt]);
+        }
       }
     }
     ok = pipe.done(j, tid, lane) && ok;
@@ -490,12 +506,55 @@ __device__ __forceinline__ bool stream_mma16(const TilePipe<ST>& pipe, const flo
   return ok;
 }
 
+// The column sums of stream_mma -> red[v][col] (dv = 128), each (column,
+// vector) from the one lane that holds it.
+template <int NTN, int MT>
+__device__ __forceinline__ void red_mma(float* red, const float (&y)[16], int warp, int lane) {
+  constexpr int DV = 128;
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt) {
+      const int col = warp * 16 * MT + 32 * (mt >> 1) + 4 * g + 2 * (mt & 1), v = 8 * nt + 2 * t;
+      const float* c = &y[4 * (NTN * mt + nt)];
+      red[v * DV + col] = c[0];
+      red[(v + 1) * DV + col] = c[1];
+      red[v * DV + col + 1] = c[2];
+      red[(v + 1) * DV + col + 1] = c[3];
+    }
+  }
+}
+
+// stream_mma with the exact-operand variants chosen by the input and ring-key
+// dtypes.
+template <typename ST, int NTN, int MT, bool FOLD>
+__device__ __forceinline__ bool stream_mma_dt(const TilePipe<ST>& pipe, int in_dt, int rk_dt,
+                                              const float* hkf, const float* hd, const float* hf,
+                                              int n, float decay, const float* xf, ST* gtile,
+                                              int tid, int warp, int lane, float (&y)[16]) {
+  const bool xk = in_dt != DT_F32, kk = FOLD && rk_dt != DT_F32;
+  if (xk) {
+    return kk ? stream_mma<ST, NTN, MT, FOLD, true, true>(pipe, hkf, hd, hf, n, decay, xf, gtile,
+                                                          tid, warp, lane, y)
+              : stream_mma<ST, NTN, MT, FOLD, true, false>(pipe, hkf, hd, hf, n, decay, xf, gtile,
+                                                           tid, warp, lane, y);
+  }
+  return kk ? stream_mma<ST, NTN, MT, FOLD, false, true>(pipe, hkf, hd, hf, n, decay, xf, gtile,
+                                                         tid, warp, lane, y)
+            : stream_mma<ST, NTN, MT, FOLD, false, false>(pipe, hkf, hd, hf, n, decay, xf, gtile,
+                                                          tid, warp, lane, y);
+}
+
 // Narrow windows keep four CTAs per SM (at most 128 registers per thread),
 // eight-token windows three (two value columns per lane, a three-stage ring);
 // the widest trade occupancy for their larger accumulator tiles.
 // RAGGED: windows of different lengths from p.cu (verify widths only); the
 // uniform kernels keep the window length a launch constant.
-template <int ALGO, typename ST, int NT, bool RAGGED>
+// LONG: GDN decode on a ring longer than 16 records, whose own folds carry
+// more than 16 records; it leaves out the tensor-core fold (up to 16 records),
+// whose code slows the general fold when both are compiled into one kernel.
+template <int ALGO, typename ST, int NT, bool RAGGED, bool LONG = false>
 __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     replay_kernel(const ReplayParams p) {
   constexpr int NV = 2 * NT;             // mat-vec vectors: k_i at [0, NT), q_i at [NT, 2NT)
@@ -660,11 +719,13 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   const int nh = c;
   const bool split = can_split(ALGO, NT) && !fold;
   const int sw = split ? kSplitWarps : kWarps;  // warps that stream the tile
-  // Eight-token GDN windows with 128 value columns stream on the tensor cores
-  // (mat-vec inputs and fold keys in fragment order, column sums in y16); a
-  // fold there takes at most 16 records and a ring of at least 16.
-  const bool mma16 = NT == 8 && ALGO == ALGO_GDN && dv == 128 && pipe.tr.cr % 8 == 0 &&
-                     (!fold || (nh <= 16 && L >= 16));
+  // Four- and eight-token GDN windows with 128 value columns stream on the
+  // tensor cores (mat-vec inputs and fold keys in fragment order, column sums
+  // in ymm); a fold there takes at most 16 records and a ring of at least 16.
+  constexpr bool kMmaNT = ALGO == ALGO_GDN && (NT == 4 || NT == 8);
+  constexpr int NTN = NV >= 8 ? NV / 8 : 1;  // n-tiles of eight vectors
+  const bool mmas = kMmaNT && dv == 128 && pipe.tr.cr % 8 == 0 &&
+                    (!fold || (nh <= 16 && L >= 16));
   const size_t kbase = ((size_t)s * HV + h) * L * dk;
   const size_t dbase = ((size_t)s * HV + h) * L * dv;
   const size_t gbase = ((size_t)s * HV + h) * L * (ALGO == ALGO_GDN ? 1 : dk);
@@ -689,10 +750,16 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     const void* qsrc = f32in ? static_cast<const void*>(wq) : wraw;
     const void* ksrc = f32in ? static_cast<const void*>(wk) : wraw + T * qrow;
     for (int e = tid; e < dk * NV; e += kThreads) {
-      const int ch = e / NV, vv = e - ch * NV;
+      // slot e holds (row ch, vector vv): row-major, or in fragment order
+      int ch, vv;
+      if (mmas) {
+        x_slot<NTN>(e, ch, vv);
+      } else {
+        ch = e / NV;
+        vv = e - ch * NV;
+      }
       const int i = vv < NT ? vv : vv - NT;
-      const float x = i < T ? ld_f32(vv < NT ? ksrc : qsrc, (size_t)i * dk + ch, p.in_dt) : 0.f;
-      xh[mma16 ? x_frag16(ch, vv) : e] = x;
+      xh[e] = i < T ? ld_f32(vv < NT ? ksrc : qsrc, (size_t)i * dk + ch, p.in_dt) : 0.f;
     }
   }
   if (tid < T) {
@@ -725,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   const QuadLane qlane(qlay, CW, warp, lane);
   bool mma_fold = false;     // decode fold on the tensor cores (column sums in ymma)
   float ymma[4][2][2];
-  float y16[2][2][4];        // column sums of the eight-token tensor-core stream
+  float ymm[16];             // column sums of the tensor-core stream (stream_mma)
   float acc[NV][CW];
 #pragma unroll
   for (int vv = 0; vv < NV; ++vv) {
@@ -743,6 +810,12 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
         copies_ok = stream_fixed<ST, NV, CW, kFixedRpl, kSplitWarps, 128>(pipe, qlane, acc, xh,
                                                                          tid, lane) &&
                     copies_ok;
+      } else if (mmas) {
+        if constexpr (kMmaNT && NT == 4) {
+          copies_ok = stream_mma_dt<ST, NTN, 4, false>(pipe, p.in_dt, p.rk_dt, hk, hd, hf, 0, 1.f,
+                                                       xh, gtile, tid, warp, lane, ymm) &&
+                      copies_ok;
+        }
       } else {
         copies_ok = stream_quads<ALGO, ST, NV, CW, MR, false>(pipe, qlane, acc, gtile, dk, dv, 0,
                                                               hk, hd, hf, 1.f, egam, xh, tid,
@@ -797,13 +870,10 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     // A wide GDN window without a fold streams first, while its history lands.
     const bool early = ALGO == ALGO_GDN && !fold;
     if (early) {
-      if (mma16) {
-        if constexpr (NT == 8 && ALGO == ALGO_GDN) {
-          copies_ok = (p.in_dt == DT_F32
-                           ? stream_mma16<ST, false, false, false>(pipe, hk, hd, hf, 0, 1.f, xh,
-                                                                   gtile, tid, warp, lane, y16)
-                           : stream_mma16<ST, false, true, false>(pipe, hk, hd, hf, 0, 1.f, xh,
-                                                                  gtile, tid, warp, lane, y16)) &&
+      if (mmas) {
+        if constexpr (kMmaNT) {
+          copies_ok = stream_mma_dt<ST, NTN, 2, false>(pipe, p.in_dt, p.rk_dt, hk, hd, hf, 0, 1.f,
+                                                       xh, gtile, tid, warp, lane, ymm) &&
                       copies_ok;
         }
       } else {
@@ -817,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     if (nh > 0) {
       if (p.rd_dt != DT_F32) widen16(hd, hdraw, nh * dv, p.rd_dt, tid, kThreads);
       if (ALGO == ALGO_GDN) {
-        if (fold && mma16) {
+        if (fold && mmas) {
           frag_keys16(hk, hkraw, nh, dk, p.rk_dt, tid, kThreads);
         } else if (fold) {
           transpose_keys(hk, hkraw, nh, dk, p.rk_dt, tid, kThreads);
@@ -903,26 +973,18 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     if (!early) {
       __syncthreads();
       if (fold && nh > 0) {
-        if constexpr (NT == 1 && ALGO == ALGO_GDN) {
+        if constexpr (NT == 1 && ALGO == ALGO_GDN && !LONG) {
           mma_fold = nh <= 16 && dv == 128 && pipe.tr.cr % 16 == 0;
         }
-        if (mma16) {
-          if constexpr (NT == 8 && ALGO == ALGO_GDN) {
-            const bool xk = p.in_dt != DT_F32, kk = p.rk_dt != DT_F32;
-            copies_ok =
-                (xk ? (kk ? stream_mma16<ST, true, true, true>(pipe, hk, hd, hf, nh, hscal[1], xh,
-                                                               gtile, tid, warp, lane, y16)
-                          : stream_mma16<ST, true, true, false>(pipe, hk, hd, hf, nh, hscal[1],
-                                                                xh, gtile, tid, warp, lane, y16))
-                    : (kk ? stream_mma16<ST, true, false, true>(pipe, hk, hd, hf, nh, hscal[1],
-                                                                xh, gtile, tid, warp, lane, y16)
-                          : stream_mma16<ST, true, false, false>(pipe, hk, hd, hf, nh, hscal[1],
-                                                                 xh, gtile, tid, warp, lane,
-                                                                 y16))) &&
-                copies_ok;
+        if (mmas) {
+          if constexpr (kMmaNT) {
+            copies_ok = stream_mma_dt<ST, NTN, 2, true>(pipe, p.in_dt, p.rk_dt, hk, hd, hf, nh,
+                                                        hscal[1], xh, gtile, tid, warp, lane,
+                                                        ymm) &&
+                        copies_ok;
           }
         } else if (mma_fold) {
-          if constexpr (NT == 1 && ALGO == ALGO_GDN) {
+          if constexpr (NT == 1 && ALGO == ALGO_GDN && !LONG) {
             copies_ok = (p.rk_dt == DT_F32
                              ? fold_stream_mma<ST, false>(pipe, hk, hd, hf, nh, hscal[1], xh, gtile,
                                                           tid, warp, lane, ymma)
@@ -936,13 +998,10 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
                                                                hf, hscal[1], egam, xh, tid, lane) &&
                       copies_ok;
         }
-      } else if (mma16) {
-        if constexpr (NT == 8 && ALGO == ALGO_GDN) {
-          copies_ok = (p.in_dt == DT_F32
-                           ? stream_mma16<ST, false, false, false>(pipe, hk, hd, hf, 0, 1.f, xh,
-                                                                   gtile, tid, warp, lane, y16)
-                           : stream_mma16<ST, false, true, false>(pipe, hk, hd, hf, 0, 1.f, xh,
-                                                                  gtile, tid, warp, lane, y16)) &&
+      } else if (mmas) {
+        if constexpr (kMmaNT) {
+          copies_ok = stream_mma_dt<ST, NTN, 2, false>(pipe, p.in_dt, p.rk_dt, hk, hd, hf, 0, 1.f,
+                                                       xh, gtile, tid, warp, lane, ymm) &&
                       copies_ok;
         }
       } else {
@@ -978,19 +1037,16 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
       }
       for (int e = tid; e < (qlay.rgw - 1) * NV * dv; e += kThreads) red[NV * dv + e] = 0.f;
     }
-  } else if (mma16) {
-    if constexpr (NT == 8) {
-      const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int col = warp * 32 + 4 * g + 2 * mt, v = 8 * nt + 2 * t;
-          red[v * dv + col] = y16[mt][nt][0];
-          red[(v + 1) * dv + col] = y16[mt][nt][1];
-          red[v * dv + col + 1] = y16[mt][nt][2];
-          red[(v + 1) * dv + col + 1] = y16[mt][nt][3];
+  } else if (mmas) {
+    if constexpr (kMmaNT) {
+      if constexpr (can_split(ALGO, NT)) {
+        if (!split) {
+          red_mma<NTN, 2>(red, ymm, warp, lane);
+        } else if (warp < sw) {
+          red_mma<NTN, 4>(red, ymm, warp, lane);
         }
+      } else {
+        red_mma<NTN, 2>(red, ymm, warp, lane);
       }
       for (int e = tid; e < (qlay.rgw - 1) * NV * dv; e += kThreads) red[NV * dv + e] = 0.f;
     }

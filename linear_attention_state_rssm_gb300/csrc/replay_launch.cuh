@@ -9,20 +9,39 @@
 namespace rssm {
 
 // One CTA per (value head, request row).
-template <int ALGO, typename ST, int NT, bool RAGGED>
+template <int ALGO, typename ST, int NT, bool RAGGED, bool LONG = false>
 static cudaError_t replay_launch_one(const ReplayParams& p, cudaStream_t st) {
   const dim3 grid((unsigned)p.HV, (unsigned)p.B, 1);
-  replay_kernel<ALGO, ST, NT, RAGGED><<<grid, kThreads, p.sm.total, st>>>(p);
+  replay_kernel<ALGO, ST, NT, RAGGED, LONG><<<grid, kThreads, p.sm.total, st>>>(p);
   return cudaGetLastError();
 }
 
-template <int ALGO, typename ST, int NT, bool RAGGED>
+template <int ALGO, typename ST, int NT, bool RAGGED, bool LONG = false>
 static cudaError_t replay_prepare_one(int max_smem) {
-  cudaError_t e = cudaFuncSetAttribute(replay_kernel<ALGO, ST, NT, RAGGED>,
+  cudaError_t e = cudaFuncSetAttribute(replay_kernel<ALGO, ST, NT, RAGGED, LONG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(replay_kernel<ALGO, ST, NT, RAGGED>,
+  return cudaFuncSetAttribute(replay_kernel<ALGO, ST, NT, RAGGED, LONG>,
                               cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+}
+
+// Decode: GDN rings longer than 16 records take the kernel without the
+// tensor-core fold (their folds carry more than 16 records).
+template <int ALGO, typename ST>
+static cudaError_t replay_launch_decode(const ReplayParams& p, cudaStream_t st) {
+  if constexpr (ALGO == ALGO_GDN) {
+    if (p.L > 16) return replay_launch_one<ALGO, ST, 1, false, true>(p, st);
+  }
+  return replay_launch_one<ALGO, ST, 1, false>(p, st);
+}
+
+template <int ALGO, typename ST>
+static cudaError_t replay_prepare_decode(int max_smem) {
+  if constexpr (ALGO == ALGO_GDN) {
+    const cudaError_t e = replay_prepare_one<ALGO, ST, 1, false, true>(max_smem);
+    if (e != cudaSuccess) return e;
+  }
+  return replay_prepare_one<ALGO, ST, 1, false>(max_smem);
 }
 
 }  // namespace rssm
@@ -31,7 +50,7 @@ static cudaError_t replay_prepare_one(int max_smem) {
   namespace rssm {                                                                          \
   cudaError_t NAME##_launch(const ReplayParams& p, int NT, cudaStream_t st) {             \
     switch (NT) {                                                                           \
-      case 1: return replay_launch_one<ALGO, ST, 1, false>(p, st);                          \
+      case 1: return replay_launch_decode<ALGO, ST>(p, st);                                 \
       case 2: return replay_launch_one<ALGO, ST, 2, false>(p, st);                          \
       case 4: return replay_launch_one<ALGO, ST, 4, false>(p, st);                          \
       case 8: return replay_launch_one<ALGO, ST, 8, false>(p, st);                          \
@@ -41,7 +60,7 @@ static cudaError_t replay_prepare_one(int max_smem) {
   }                                                                                         \
   cudaError_t NAME##_prepare(int max_smem) {                                                \
     cudaError_t e;                                                                          \
-    if ((e = replay_prepare_one<ALGO, ST, 1, false>(max_smem)) != cudaSuccess) return e;    \
+    if ((e = replay_prepare_decode<ALGO, ST>(max_smem)) != cudaSuccess) return e;           \
     if ((e = replay_prepare_one<ALGO, ST, 2, false>(max_smem)) != cudaSuccess) return e;    \
     if ((e = replay_prepare_one<ALGO, ST, 4, false>(max_smem)) != cudaSuccess) return e;    \
     if ((e = replay_prepare_one<ALGO, ST, 8, false>(max_smem)) != cudaSuccess) return e;    \
