@@ -323,17 +323,18 @@ def test_decode_fold_of_every_history_length(state, ring_k):
     assert run.store.rssm_get_device_error() == 0
 
 
+@pytest.mark.parametrize("algo", ["gdn", "kda"])
 @pytest.mark.parametrize("T", [3, 8])
 @pytest.mark.parametrize("in_dt,ring_k,state", [("f32", "f32", "f32"), ("f32", "bf16", "f32"),
                                                 ("bf16", "f32", "bf16"), ("bf16", "f16", "f32")])
-def test_verify_across_input_key_and_state_dtypes(in_dt, ring_k, state, T):
-    """Three- and eight-token verify + commit with 128-wide heads (fp32 and
-    16-bit inputs, ring keys and checkpoints), forced folds on top of the ring's
-    own, accept lengths U[0, T]: outputs, fold flags, cursors and checkpoints vs
-    the oracle."""
+def test_verify_across_input_key_and_state_dtypes(in_dt, ring_k, state, T, algo):
+    """Three- and eight-token GDN and KDA verify + commit with 128-wide heads
+    (fp32 and 16-bit inputs, ring keys and checkpoints), forced folds on top of
+    the ring's own, accept lengths U[0, T]: outputs, fold flags, cursors and
+    checkpoints vs the oracle."""
     B, L = 12, 16
     tol = TOL32 if (in_dt, ring_k, state) == ("f32", "f32", "f32") else TOL16
-    run = Run(algo="gdn", HK=1, HV=2, dk=128, dv=128, L=L, max_T=T,
+    run = Run(algo=algo, HK=1, HV=2, dk=128, dv=128, L=L, max_T=T,
               slots=np.arange(B, dtype=np.int32), n_slots=B, in_dtype=in_dt, state_dtype=state,
               ring_k_dtype=ring_k, config_id=34)
     for step in range(14):
