@@ -93,3 +93,58 @@ def test_null_handle_is_refused(lib):
         _lib.rssm_commit(None, None, None, None, 1, 1, stream=0)
     with pytest.raises(_lib.RssmError):
         _lib.rssm_fold(None, None, 1, stream=0)
+
+
+# Stand-in addresses, 16-byte aligned unless a case offsets one: every case
+# below is refused (or is an empty batch) before any CUDA call, so nothing is
+# dereferenced and no device is needed. They run only where no GPU is visible,
+# so a stand-in address can never reach a kernel.
+def _cuda_visible():
+    import torch
+    return torch.cuda.is_available()
+
+
+_NO_GPU = pytest.mark.skipif(_cuda_visible(), reason="stand-in addresses: CPU-only hosts")
+_A = 0x100000
+_CONV = dict(x=_A, w=_A + 0x1000, bias=_A + 0x2000, window=_A + 0x3000, draft=_A + 0x4000,
+             slot=_A + 0x5000, B=2, T=4, D=64, K=4, n_slots=3, dtype=1, act=1, commit_now=0,
+             y=_A + 0x6000)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=1), 2), (dict(K=9), 2),      # convolution width outside 2..8
+    (dict(dtype=2), 2),                  # fp16 channels not built
+    (dict(D=4), 2),                      # bf16 rows of 8 bytes: not whole 16-byte vectors
+    (dict(D=0), 1), (dict(T=0), 1), (dict(n_slots=0), 1), (dict(B=-1), 1),
+    (dict(window=_A + 8), 1),            # window not 16-byte aligned
+    (dict(x=_A + 4), 1),                 # inputs not 16-byte aligned
+    (dict(slot=_A + 2), 1),              # slots not 4-byte aligned
+    (dict(act=7), 1),                    # unknown activation
+    (dict(y=None), 1),                   # no output buffer
+    (dict(draft=None), 1),               # a verify window without a draft buffer
+    (dict(y=_A + 8), 1),                 # outputs not 16-byte aligned
+    (dict(B=0), 0),                      # an empty batch is a no-op
+])
+@_NO_GPU
+def test_conv_window_host_refusals(lib, kw, status):
+    a = {**_CONV, **kw}
+    st = lib.rssm_conv_window(a["x"], a["w"], a["bias"], a["window"], a["draft"], a["slot"],
+                              a["B"], a["T"], a["D"], a["K"], a["n_slots"], a["dtype"], a["act"],
+                              a["commit_now"], a["y"], None, None)
+    assert st == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(accept=None), 1),              # no accepted lengths
+    (dict(accept=_A + 0x7002), 1),       # accepted lengths not 4-byte aligned
+    (dict(draft=None), 1),               # nothing to roll the window onto
+    (dict(K=9), 2), (dict(dtype=2), 2),
+    (dict(window=_A + 4), 1),
+    (dict(B=0), 0),                      # an empty batch is a no-op
+])
+@_NO_GPU
+def test_conv_commit_host_refusals(lib, kw, status):
+    a = {**_CONV, "accept": _A + 0x7000, **kw}
+    st = lib.rssm_conv_commit(a["window"], a["draft"], a["slot"], a["accept"], a["B"], a["T"],
+                              a["D"], a["K"], a["n_slots"], a["dtype"], None, None)
+    assert st == status
