@@ -43,7 +43,9 @@ import numpy as np
 
 from . import ring
 
-__all__ = ["token_step", "ReplayOracle", "round_bf16"]
+__all__ = ["token_step", "ReplayOracle", "round_bf16", "FP16_MAX"]
+
+FP16_MAX = 65504.0  # largest finite IEEE half-precision value
 
 
 def round_bf16(x):
@@ -90,11 +92,18 @@ class ReplayOracle:
     """
 
     def __init__(self, algo, n_layers, n_slots, HK, HV, dk, dv, L, scale, S0,
-                 ckpt_round=None):
+                 ckpt_round=None, ring_d_dtype="f32"):
         """``ckpt_round="bf16"`` models a bf16 checkpoint: at every fold the
         committed state is rounded to bf16 and the chain continues from the
         rounded value, as the GPU does (vLLM PR #64699, commit message on
-        accounting for BF16 state rounding between flushes)."""
+        accounting for BF16 state rounding between flushes).
+
+        ``ring_d_dtype="f16"`` models a store that keeps its deltas in fp16,
+        against LightLLM PR #1690 (PR description: deltas are kept in fp32
+        because fp16 deltas overflow). The recurrence stays fp64; the oracle
+        only flags, per (layer, slot), every accepted delta whose magnitude
+        exceeds 65504, the largest finite fp16 value (``d_overflow``), so a
+        run in that configuration can show it stayed inside the fp16 range."""
         if HV % HK:
             raise ValueError("HV must be a multiple of HK")
         self.algo, self.n_layers, self.n_slots = algo, n_layers, n_slots
@@ -104,6 +113,9 @@ class ReplayOracle:
         if ckpt_round not in (None, "bf16"):
             raise ValueError(ckpt_round)
         self.ckpt_round = ckpt_round
+        if ring_d_dtype not in ("f32", "f16"):
+            raise ValueError(ring_d_dtype)
+        self.ring_d_dtype = ring_d_dtype
         S0 = np.asarray(S0, dtype=np.float64)
         if S0.shape == (n_slots, HV, dk, dv):
             S0 = np.broadcast_to(S0, (n_layers,) + S0.shape)
@@ -120,6 +132,8 @@ class ReplayOracle:
         self.ring_beta = np.full((n_layers, n_slots, HV, L), nan)
         # positions [base, base+T) written by the last window of each layer
         self.written = np.zeros((n_layers, n_slots, L), dtype=bool)
+        # accepted deltas outside the fp16 range (only tracked for an fp16 delta ring)
+        self.d_overflow = np.zeros((n_layers, n_slots), dtype=bool)
         self._pending: dict[int, dict] = {}
         # rows per batch of work: keeps each temporary near 16 MB
         self._chunk = max(1, (16 << 20) // (HV * dk * dv * 8))
@@ -191,6 +205,7 @@ class ReplayOracle:
         active = (slots >= 0) & (lens > 0)
         live = np.nonzero(active)[0]
         o = np.full((n_tok, self.HV, self.dv), np.nan)
+        over = np.zeros((B, int(lens.max()) if B else 0), dtype=bool)
         flags = np.where(active, fold.astype(np.int8), np.int8(-1))
         if live.size:
             sl = slots[live]
@@ -203,17 +218,18 @@ class ReplayOracle:
                 for c0 in range(0, live.size, self._chunk):
                     rows = live[c0:c0 + self._chunk]
                     final[c0:c0 + rows.size] = self._run_window(layer, rows, slots, inp, starts,
-                                                                lens, base, o)
+                                                                lens, base, o, over)
         else:
             final = None
         self._pending[layer] = {"slots": slots.copy(), "inp": inp, "T": T, "starts": starts,
                                 "lens": lens, "force": np.asarray(force).copy(), "base": base,
-                                "final": final}
+                                "final": final, "over": over}
         return o, flags
 
-    def _run_window(self, layer, rows, slots, inp, starts, lens, base, o):
+    def _run_window(self, layer, rows, slots, inp, starts, lens, base, o, over):
         """Run the window tokens of some live rows; record outputs and ring
-        records; return the rows' states after their windows."""
+        records (and, for an fp16 delta ring, which tokens' deltas leave the
+        fp16 range in ``over``); return the rows' states after their windows."""
         sl = slots[rows]
         S = self.S[layer, sl]                     # fancy indexing: a copy
         for i in range(int(lens[rows].max())):
@@ -223,6 +239,8 @@ class ReplayOracle:
             q, k, v, beta, g = self._token_inputs(inp, idx)
             S[on], d, oi = token_step(S[on], q, k, v, beta, g, self.scale, self.algo)
             o[idx] = oi
+            if self.ring_d_dtype == "f16":
+                over[r_i, i] = np.any(np.abs(d) > FP16_MAX, axis=(1, 2))
             pos = base[r_i] + i
             self.ring_k[layer, s_i, :, pos] = inp["k"][idx]
             self.ring_d[layer, s_i, :, pos] = d
@@ -239,6 +257,11 @@ class ReplayOracle:
         starts, lens = pend["starts"], pend["lens"]
         live = np.nonzero((slots >= 0) & (lens > 0))[0]
         a_live = np.asarray(accept)[live]
+        # an fp16 delta ring keeps the accepted records: flag the ones out of range
+        over = pend["over"]
+        for r, a in zip(live, a_live):
+            if over[r, :int(a)].any():
+                self.d_overflow[layer, slots[r]] = True
         for c0 in range(0, live.size, self._chunk):
             rows = live[c0:c0 + self._chunk]
             a = a_live[c0:c0 + rows.size]
@@ -362,6 +385,18 @@ class ReplayOracle:
             if s >= 0:
                 self.cursor[s] = 0
                 self.S[:, s] = self.ckpt[:, s]
+
+    def select_slots(self, idx):
+        """Keep only slots ``idx`` (renumbered 0 .. len(idx) - 1), between
+        steps; lets a test follow every row for a while and then a sample."""
+        if self._pending:
+            raise ValueError("select_slots between steps only (a window is pending)")
+        idx = np.asarray(idx, dtype=np.int64)
+        for name in ("S", "ckpt", "ring_k", "ring_d", "ring_g", "ring_v", "ring_beta",
+                     "written", "d_overflow"):
+            setattr(self, name, getattr(self, name)[:, idx].copy())
+        self.cursor = self.cursor[idx].copy()
+        self.n_slots = int(idx.size)
 
     def accepted_positions(self, slot):
         """Ring positions holding committed history: [0, cursor)."""

@@ -368,3 +368,48 @@ def test_bf16_checkpoint_mode_rounds_only_at_folds():
         np.testing.assert_array_equal(round_bf16(rounded.ckpt), rounded.ckpt)
         assert np.max(np.abs(o1 - o2)) <= 1e-2 * np.max(np.abs(o1))
     assert not np.array_equal(exact.ckpt, rounded.ckpt)
+
+
+# ------------------------------------------- fp16 delta ring: overflow flag
+def test_fp16_delta_overflow_flag_marks_accepted_deltas_beyond_half_range():
+    """With S0 = 0, g = 0 and a unit key, the first token's delta is exactly
+    beta * v, so the flag is pinned by hand: 65504 (the largest finite fp16
+    value) passes, anything beyond it is flagged, rejected drafts never
+    count, and an fp32 delta ring is never flagged."""
+    HK, HV, dk, dv, L = 1, 2, 4, 3, 4
+    S0 = np.zeros((1, HV, dk, dv))
+
+    def tokens(v_rows, beta=1.0):
+        n = len(v_rows)
+        k = np.zeros((n, HK, dk))
+        k[:, :, 0] = 1.0
+        v = np.zeros((n, HV, dv))
+        for t, val in enumerate(v_rows):
+            v[t, 0, 1] = val              # head 0, one value column
+        return {"q": k.copy(), "k": k, "v": v, "beta": np.full((n, HV), beta),
+                "g": np.zeros((n, HV))}
+
+    # decode, two slots: slot 0 at the bound, slot 1 just past it
+    orc = ReplayOracle("gdn", 1, 2, HK, HV, dk, dv, L, 1.0, np.concatenate([S0, S0]),
+                       ring_d_dtype="f16")
+    orc.decode(0, [0, 1], tokens([65504.0, 65504.5]), advance=True)
+    np.testing.assert_array_equal(orc.d_overflow[0], [False, True])
+    np.testing.assert_array_equal(orc.ring_d[0, :, 0, 0, 1], [65504.0, 65504.5])
+    # beta scales the delta: beta * v = 0.5 * 2e5 = 1e5 > 65504
+    orc = ReplayOracle("gdn", 1, 1, HK, HV, dk, dv, L, 1.0, S0, ring_d_dtype="f16")
+    orc.decode(0, [0], tokens([2e5], beta=0.5), advance=True)
+    assert orc.d_overflow[0, 0]
+    # ... and it is the delta, not the value, that is checked: 0.25 * 2e5 = 5e4
+    orc = ReplayOracle("gdn", 1, 1, HK, HV, dk, dv, L, 1.0, S0, ring_d_dtype="f16")
+    orc.decode(0, [0], tokens([2e5], beta=0.25), advance=True)
+    assert not orc.d_overflow[0, 0]
+    # verify: a huge delta at a rejected draft does not count, an accepted one does
+    for accept, want in ((1, False), (2, True)):
+        orc = ReplayOracle("gdn", 1, 1, HK, HV, dk, dv, L, 1.0, S0, ring_d_dtype="f16")
+        orc.window(0, [0], tokens([3.0, 1e6]), 2)
+        orc.commit([0], [accept], 2)
+        assert orc.d_overflow[0, 0] == want, accept
+    # an fp32 delta ring is never flagged
+    orc = ReplayOracle("gdn", 1, 1, HK, HV, dk, dv, L, 1.0, S0)
+    orc.decode(0, [0], tokens([1e6]), advance=True)
+    assert not orc.d_overflow.any()
