@@ -37,11 +37,27 @@
  * enqueued; a failed check returns RSSM_ERR_INVALID_ARG or
  * RSSM_ERR_UNSUPPORTED and launches nothing. Conditions only the device can see
  * (a slot index >= n_slots, a cursor outside [0, L], an accepted length outside
- * [0, T], a bounded wait that ran out) set bits in the device error word and the
- * affected row is skipped; the kernels never trap. A null slot (-1) is not an
- * error: its row is skipped and its outputs are left untouched. Two live rows
- * of one call must not name the same slot (the result is then undefined).
- * Launch failures return RSSM_ERR_CUDA. No C++ exception crosses this ABI.
+ * [0, T]) set bits in the device error word and the affected row is skipped;
+ * the kernels never trap. A null slot (-1) is not an error: its row is skipped
+ * and its outputs are left untouched. Two live rows of one call must not name
+ * the same slot (the result is then undefined). Launch failures return
+ * RSSM_ERR_CUDA. No C++ exception crosses this ABI.
+ *
+ * Bounded waits: every wait of a kernel for its own async copies gives up
+ * after 0.5 s and sets RSSM_DEVERR_TIMEOUT (a copy that never lands is a
+ * hardware fault; nothing in normal operation comes near the limit). What the
+ * affected row of a replay or fold launch then holds:
+ *  - a wait for the window rows or history records: nothing of the row is
+ *    written (outputs, records, fold_out, checkpoint);
+ *  - a wait for a checkpoint chunk: no output, record or fold_out is written,
+ *    and no checkpoint chunk from the failed one on is stored back; a row that
+ *    folds may have stored the chunks before it already folded, so its
+ *    checkpoint is then part old, part folded.
+ * The cursor kernels do not see the failure (decode's advance_cursor, commit
+ * and fold still move the cursor). A caller that finds the bit set must treat
+ * the step as failed and restore the slots it touched (write a checkpoint,
+ * rssm_reset_slots). Copies still in flight after a second bounded wait may
+ * land after the CTA has left.
  *
  * Layouts (row-major, element counts; "tok" = r*T + i for row r, token i):
  *   q, k : [B*T][HK][dk]  in_dtype          v, o : [B*T][HV][dv] in_dtype
@@ -79,6 +95,9 @@ enum { RSSM_F32 = 0, RSSM_BF16 = 1, RSSM_F16 = 2 };
 /* Activation of the short causal convolution (rssm_conv_window). */
 enum { RSSM_CONV_ACT_NONE = 0, RSSM_CONV_ACT_SILU = 1 };
 enum { RSSM_COMMIT_LAZY = 0, RSSM_COMMIT_FOLD_EVERY = 1 };
+
+/* Kernel family serving rssm_decode / rssm_verify (rssm_set_plan). */
+enum { RSSM_PLAN_AUTO = 0, RSSM_PLAN_ROWS = 1, RSSM_PLAN_PIPE = 2 };
 
 /* Bits of the device error word. */
 enum {
@@ -330,6 +349,36 @@ rssm_status rssm_reset_slots(rssm_handle *h, const int32_t *slot, int32_t B,
  * For tests and debugging; not capturable. */
 rssm_status rssm_get_device_error(rssm_handle *h, uint32_t *out, int32_t clear,
                                   void *stream);
+
+/*
+ * Which kernel serves rssm_decode and rssm_verify of this handle. Both compute
+ * the same replay (same inputs, outputs, records and fold decisions; sums may
+ * differ in rounding order):
+ *  - RSSM_PLAN_ROWS: one CTA per (request row, value head) for the launch;
+ *  - RSSM_PLAN_PIPE: the pipelined kernel, one persistent CTA per SM walking
+ *    the (row, value head) items, checkpoint chunks streamed continuously
+ *    across items while other warps prepare the next item and solve the last.
+ *    It serves GDN stores with dk = dv = 128, L <= 16 and L a multiple of 4,
+ *    fp32 or fp16 deltas, calls with T <= 8 and B <= 512 (uniform windows);
+ *    calls outside that run on the per-row kernel.
+ *  - RSSM_PLAN_AUTO (after rssm_alloc): the per-row kernel.
+ * RSSM_PLAN_PIPE on a store it cannot serve returns RSSM_ERR_UNSUPPORTED. Host
+ * state only; takes effect at the next launch.
+ */
+rssm_status rssm_set_plan(rssm_handle *h, int32_t plan);
+
+/*
+ * Test and debugging hook of the bounded waits (no counterpart in the pages:
+ * it exists so that the timeout path above can be exercised without a fault).
+ * barrier: -1 turns the hook off (the state after rssm_alloc); 0 the window
+ * rows' barrier, 1 the history records', 2 + j that of checkpoint chunk j.
+ * While the hook is on, every replay and fold launch of this handle registers
+ * 16 bytes more on that barrier than its copies carry, so every wait on it
+ * runs out, after wait_limit_us microseconds (1 .. 1000000) instead of the
+ * usual 0.5 s; the copies themselves all land. Host state only: takes effect
+ * at the next launch. Never on in production calls.
+ */
+rssm_status rssm_debug_withhold(rssm_handle *h, int32_t barrier, int32_t wait_limit_us);
 
 const char *rssm_status_string(rssm_status s);
 

@@ -26,7 +26,8 @@ SYMBOLS = ("rssm_required_bytes", "rssm_alloc", "rssm_free", "rssm_decode", "rss
            "rssm_verify_ragged", "rssm_prefill", "rssm_native_decode", "rssm_commit",
            "rssm_commit_ragged", "rssm_fold", "rssm_reset_slots", "rssm_conv_window",
            "rssm_conv_commit",
-           "rssm_get_device_error", "rssm_status_string", "rssm_version")
+           "rssm_get_device_error", "rssm_set_plan", "rssm_debug_withhold",
+           "rssm_status_string", "rssm_version")
 
 
 class RssmError(RuntimeError):
@@ -91,6 +92,8 @@ def load() -> ctypes.CDLL:
         "rssm_conv_commit": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
         "rssm_reset_slots": ([_P, _P, _I, _P], _I),
         "rssm_get_device_error": ([_P, ctypes.POINTER(ctypes.c_uint32), _I, _P], _I),
+        "rssm_set_plan": ([_P, _I], _I),
+        "rssm_debug_withhold": ([_P, _I, _I], _I),
         "rssm_status_string": ([_I], ctypes.c_char_p),
         "rssm_version": ([], _I),
     }
@@ -229,6 +232,31 @@ def rssm_get_device_error(handle, clear=True, stream=None) -> int:
     if st not in (RSSM_OK, 4):
         raise RssmError(st, "rssm_get_device_error")
     return int(word.value)
+
+
+PLAN = {"auto": 0, "rows": 1, "pipe": 2}
+
+
+def rssm_set_plan(handle, plan):
+    """Kernel family for decode and verify: "auto", "rows" or "pipe"."""
+    _check(load().rssm_set_plan(handle, PLAN[plan] if isinstance(plan, str) else int(plan)),
+           "rssm_set_plan")
+
+
+# barriers of the bounded-wait test hook (rssm_debug_withhold)
+WITHHOLD = {"off": -1, "window": 0, "history": 1}
+
+
+def withhold_chunk(j: int) -> int:
+    """Barrier index of checkpoint chunk j for rssm_debug_withhold."""
+    return 2 + int(j)
+
+
+def rssm_debug_withhold(handle, barrier, wait_limit_us=1000):
+    """Test hook: every later replay/fold launch of this handle short-changes
+    `barrier` (see include/rssm.h); barrier -1 turns it off."""
+    _check(load().rssm_debug_withhold(handle, int(barrier), int(wait_limit_us)),
+           "rssm_debug_withhold")
 
 
 def rssm_status_string(status: int) -> str:

@@ -75,7 +75,9 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
   const size_t dbase = layer * p.layer_d + ((size_t)s * HV + h) * L * dv;
   const size_t gbase = layer * p.layer_g + ((size_t)s * HV + h) * L * (ALGO == ALGO_GDN ? 1 : dk);
 
-  const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv);
+  const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv, kStages,
+                          p.hook);
+  const unsigned long long lim = p.hook.limit_ns;
   if (tid == 0) {
     mbar_init(&mbar[kMbarWin], 1);
     mbar_init(&mbar[kMbarHist], 1);
@@ -88,16 +90,18 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
     issue_history<ALGO>(n, dk, dv, p.ring_k, kbase, p.rk_dt,
                         p.rk_dt == DT_F32 ? static_cast<void*>(hk) : hkraw, p.ring_d, dbase,
                         p.rd_dt, p.rd_dt == DT_F32 ? static_cast<void*>(hd) : hdraw, p.ring_g,
-                        gbase, hg, &mbar[kMbarHist]);
+                        gbase, hg, &mbar[kMbarHist], p.hook.extra(WH_HIST));
   }
   if (ALGO == ALGO_GDN) {
     for (int m = tid; m < n; m += kThreads) hf[m] = p.ring_g[gbase + m];
   }
-  const bool ok = mbar_wait_bounded(&mbar[kMbarHist], 0);
-  if (!ok) {
-    if (tid == 0) atomicOr(p.err, DEVERR_TIMEOUT);
-    mbar_wait_bounded(&mbar[kMbarHist], 0);
-    pipe.drain();
+  // the history copy did not arrive in time: the checkpoint is left as it is
+  if (!__syncthreads_and(mbar_wait_bounded(&mbar[kMbarHist], 0, lim))) {
+    if (tid == 0) {
+      atomicOr(p.err, DEVERR_TIMEOUT);
+      mbar_wait_bounded(&mbar[kMbarHist], 0, lim);
+      pipe.drain();
+    }
     return;
   }
   widen_history(n, dk, dv, p.rk_dt, p.rd_dt, hk, hkraw, hd, hdraw, tid);
@@ -110,10 +114,14 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
     }
   }
   __syncthreads();
+  // a chunk that did not arrive in time: no chunk from there on is stored (the
+  // ones before it hold the folded state), and the copies issued are waited for
   float unused[1] = {0.f};
-  if (!stream_tile<ALGO, ST, 0, true>(pipe, unused, gcol, cm, dk, dv, n, hk, hd, hf, scal[1], egam,
-                                      nullptr, tid, lane)) {
-    if (tid == 0) atomicOr(p.err, DEVERR_TIMEOUT);
+  const bool ok = stream_tile<ALGO, ST, 0, true>(pipe, unused, gcol, cm, dk, dv, n, hk, hd, hf,
+                                                 scal[1], egam, nullptr, tid, lane);
+  if (!__syncthreads_and(ok) && tid == 0) {
+    atomicOr(p.err, DEVERR_TIMEOUT);
+    pipe.drain_tail();
   }
 }
 

@@ -35,7 +35,7 @@ struct WholeTile {
     return ring + (size_t)j * tr.cr * dv;
   }
   __device__ __forceinline__ bool wait(int j) const { return mbar_wait_bounded(&full[j], 0); }
-  __device__ __forceinline__ bool done(int, int, int) const { return true; }
+  __device__ __forceinline__ bool done(int, int, int, bool) const { return true; }
 };
 
 template <int ALGO, typename ST>

@@ -329,7 +329,7 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
   bool ok = true;
   const int cr = pipe.tr.cr;
   for (int j = 0; j < pipe.tr.nchunk; ++j) {
-    ok = pipe.wait(j) && ok;
+    ok = __all_sync(kFull, pipe.wait(j) && ok);  // no store-back once a wait has run out
     const ST* stg = pipe.stage(j);
     for (int m0 = 0; m0 < cr; m0 += 16) {
       const int ra = j * cr + m0 + g, rb = ra + 8;  // this lane's two tile rows
@@ -354,8 +354,10 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
         mma_split<EXACT_K, false>(acc, af[0], bf[0][nt]);
         if (n > 8) mma_split<EXACT_K, false>(acc, af[1], bf[1][nt]);
         float wa[2] = {acc[0], acc[1]}, wb[2] = {acc[2], acc[3]};
-        st_cols<ST, 2>(gtile + (size_t)ra * DV + col, wa);
-        st_cols<ST, 2>(gtile + (size_t)rb * DV + col, wb);
+        if (ok) {
+          st_cols<ST, 2>(gtile + (size_t)ra * DV + col, wa);
+          st_cols<ST, 2>(gtile + (size_t)rb * DV + col, wb);
+        }
         // the mat-vec takes the stored (rounded) checkpoint values
         y[nt][0][0] = fmaf(wa[0], xa0, fmaf(wb[0], xb0, y[nt][0][0]));
         y[nt][0][1] = fmaf(wa[0], xa1, fmaf(wb[0], xb1, y[nt][0][1]));
@@ -363,7 +365,7 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
         y[nt][1][1] = fmaf(wa[1], xa1, fmaf(wb[1], xb1, y[nt][1][1]));
       }
     }
-    ok = pipe.done(j, tid, lane) && ok;
+    ok = pipe.done(j, tid, lane, ok) && ok;
   }
   // sum over the eight row groups (lanes with the same t)
 #pragma unroll
@@ -381,18 +383,6 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
     }
   }
   return ok;
-}
-
-// Fragment order of the mat-vec inputs of a window with 8 NTN vectors (NTN
-// n-tiles of eight): for rows [8s, 8s + 8) lane (g, t) finds at
-// [2 NTN (32 s + 4 g + t) + 2 nt + h] vector 8 nt + g of row 8s + 2t + h.
-// x_slot maps slot e back to its (row ch, vector v).
-template <int NTN>
-__device__ __forceinline__ void x_slot(int e, int& ch, int& v) {
-  constexpr int CPL = 2 * NTN;  // values per lane and step
-  const int s8 = e / (32 * CPL), ln = (e / CPL) & 31, comp = e % CPL;
-  ch = 8 * s8 + 2 * (ln & 3) + (comp & 1);
-  v = 8 * (comp >> 1) + (ln >> 2);
 }
 
 // Tile stream of a GDN window with 8 NTN mat-vec vectors (four or eight
@@ -449,6 +439,7 @@ __device__ __forceinline__ bool stream_mma(const TilePipe<ST>& pipe, const float
   const int cr = pipe.tr.cr;
   for (int j = 0; j < pipe.tr.nchunk; ++j) {
     ok = pipe.wait(j) && ok;
+    if (FOLD) ok = __all_sync(kFull, ok);  // no store-back once a wait has run out
     const ST* stg = pipe.stage(j);
     for (int kb = 0; kb < cr; kb += 8) {
       const int r0 = j * cr + kb + 2 * t, r1 = r0 + 1;  // this lane's two tile rows
@@ -474,8 +465,10 @@ __device__ __forceinline__ bool stream_mma(const TilePipe<ST>& pipe, const float
           s0[0][2 * mt + 1] = c[2];
           s1[0][2 * mt + 1] = c[3];
         }
-        st_cols<ST, 4>(gtile + (size_t)r0 * DV + col, s0[0]);
-        st_cols<ST, 4>(gtile + (size_t)r1 * DV + col, s1[0]);
+        if (ok) {
+          st_cols<ST, 4>(gtile + (size_t)r0 * DV + col, s0[0]);
+          st_cols<ST, 4>(gtile + (size_t)r1 * DV + col, s1[0]);
+        }
       }
       Tf32 xb[NTN][2];  // vectors 8 nt + g of rows 2t, 2t + 1
       if constexpr (NTN == 2) {
@@ -501,7 +494,7 @@ __device__ __forceinline__ bool stream_mma(const TilePipe<ST>& pipe, const float
         }
       }
     }
-    ok = pipe.done(j, tid, lane) && ok;
+    ok = pipe.done(j, tid, lane, ok) && ok;
   }
   return ok;
 }
@@ -567,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   const int dk = p.dk, dv = p.dv, L = p.L, HV = p.HV, HK = p.HK;
   int T = p.T;  // this row's window (RAGGED: set once the row is known)
   const int kh = h / p.G;
+  const unsigned long long lim = p.hook.limit_ns;
 
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + p.sm.mbar);
   float* wq = reinterpret_cast<float*>(smem + p.sm.wq);
@@ -609,8 +603,9 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     return static_cast<ST*>(p.state) + ((size_t)slot * HV + h) * dk * dv;
   };
   auto issue_window = [&](size_t t0) {
-    mbar_expect_tx(&mbar[kMbarWin],
-                   T * (2 * qrow + vrow) + (ALGO == ALGO_KDA ? (uint32_t)(T * dk * 4) : 0u));
+    mbar_expect_tx(&mbar[kMbarWin], T * (2 * qrow + vrow) +
+                                        (ALGO == ALGO_KDA ? (uint32_t)(T * dk * 4) : 0u) +
+                                        p.hook.extra(WH_WINDOW));
     for (int i = 0; i < T; ++i) {
       const size_t tok = t0 + i;
       const size_t qoff = ((tok * HK + kh) * dk) * s_in;
@@ -631,7 +626,8 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     void* kdst = (ALGO == ALGO_KDA && p.rk_dt == DT_F32) ? static_cast<void*>(hk) : hkraw;
     issue_history<ALGO>(n, dk, dv, p.ring_k, sh * L * dk, p.rk_dt, kdst, p.ring_d, sh * L * dv,
                         p.rd_dt, p.rd_dt == DT_F32 ? static_cast<void*>(hd) : hdraw, p.ring_g,
-                        sh * L * (ALGO == ALGO_GDN ? 1 : dk), hg, &mbar[kMbarHist]);
+                        sh * L * (ALGO == ALGO_GDN ? 1 : dk), hg, &mbar[kMbarHist],
+                        p.hook.extra(WH_HIST));
   };
   // ---- row order. A folding row's CTAs live several times longer than the
   //      others; started last they would set the end of the launch. For
@@ -696,19 +692,19 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     // null row (or a slot out of range): let the window copies land, leave
     if (tid == 0) {
       if (s >= p.n_slots && h == 0) atomicOr(p.err, DEVERR_SLOT);
-      mbar_wait_bounded(&mbar[kMbarWin], 0);
+      mbar_wait_bounded(&mbar[kMbarWin], 0, lim);
     }
     return;
   }
   ST* gtile = tile_of(s);
   const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv,
-                          ring_stages(NT, L));
+                          ring_stages(NT, L), p.hook);
   if (tid == 0) pipe.prime();
   if (!have_c) c = p.cursor[s];
   if (c < 0 || c > L) {
     if (tid == 0) {
       if (h == 0) atomicOr(p.err, DEVERR_CURSOR);
-      mbar_wait_bounded(&mbar[kMbarWin], 0);
+      mbar_wait_bounded(&mbar[kMbarWin], 0, lim);
       pipe.drain();
     }
     return;
@@ -740,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
 
   // ---- window rows -> fp32; GDN mat-vec inputs xh[ch][v] are the raw window
   //      vectors (their scalar decay goes on the column results)
-  bool copies_ok = mbar_wait_bounded(&mbar[kMbarWin], 0);
+  bool copies_ok = mbar_wait_bounded(&mbar[kMbarWin], 0, lim);
   if (!f32in) {
     widen16(wq, wraw, T * dk, p.in_dt, tid, kThreads);
     widen16(wk, wraw + T * qrow, T * dk, p.in_dt, tid, kThreads);
@@ -770,22 +766,18 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     if (tid < nh) hf[tid] = hgate;
     for (int m = tid + kThreads; m < nh; m += kThreads) hf[m] = p.ring_g[gbase + m];
   }
-  // A folding window writes over positions [0, T) of the history it reads:
-  // its history copy must have landed before the records below.
-  if (fold && nh > 0) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
-  __syncthreads();
-
-  // ---- records that need no result of the window: keys, gates and betas at
-  //      ring positions base + i
-  for (int ch = tid; ch < dk; ch += kThreads) {
-    for (int i = 0; i < T; ++i) {
-      st_f32(p.ring_k, kbase + (size_t)(base + i) * dk + ch, p.rk_dt, wk[i * dk + ch]);
-      if (ALGO == ALGO_KDA) p.ring_g[gbase + (size_t)(base + i) * dk + ch] = wg[i * dk + ch];
+  // A folding window streams its fold right away: its history must be here.
+  if (fold && nh > 0) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0, lim) && copies_ok;
+  if (!__syncthreads_and(copies_ok)) {
+    // a copy of the window (or of a folding window's history) did not arrive
+    // in time: the row is left as it is
+    if (tid == 0) {
+      atomicOr(p.err, DEVERR_TIMEOUT);
+      mbar_wait_bounded(&mbar[kMbarWin], 0, lim);
+      if (nh > 0) mbar_wait_bounded(&mbar[kMbarHist], 0, lim);
+      pipe.drain();
     }
-  }
-  if (tid < T) {
-    p.ring_beta[((size_t)s * HV + h) * L + base + tid] = wb[tid];
-    if (ALGO == ALGO_GDN) p.ring_g[gbase + base + tid] = wg[tid];
+    return;
   }
 
   const QuadLayout qlay(dv, CW, sw);
@@ -831,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
       // column correction below)
       const bool decode1 = NT == 1 && nhw == 2;
       if (nh > 0) {
-        copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
+        copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0, lim) && copies_ok;
         if (!decode1) widen_keys(hk, hkraw, nh * dk, p.rk_dt, ht, nht);
         if (p.rd_dt != DT_F32) widen16(hd, hdraw, nh * dv, p.rd_dt, ht, nht);
       }
@@ -883,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
                     copies_ok;
       }
     }
-    if (nh > 0 && !fold) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0) && copies_ok;
+    if (nh > 0 && !fold) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0, lim) && copies_ok;
     if (nh > 0) {
       if (p.rd_dt != DT_F32) widen16(hd, hdraw, nh * dv, p.rd_dt, tid, kThreads);
       if (ALGO == ALGO_GDN) {
@@ -1057,10 +1049,31 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
       for (int cc = 0; cc < CW; ++cc) red[(qlane.rg * NV + vv) * dv + qlane.col0 + cc] = acc[vv][cc];
     }
   }
-  __syncthreads();
+  // every wait of the CTA succeeded, or the row's outputs and records are not
+  // written (a folding row may have stored back the chunks folded before the
+  // wait that failed)
+  const bool all_ok = __syncthreads_and(copies_ok);
+
+  // ---- records that need no result of the solve: keys, gates and betas at
+  //      ring positions base + i (KDA's raw gates were turned into prefixes in
+  //      shared memory: they are copied from the input)
+  if (all_ok) {
+    for (int ch = tid; ch < dk; ch += kThreads) {
+      for (int i = 0; i < T; ++i) {
+        st_f32(p.ring_k, kbase + (size_t)(base + i) * dk + ch, p.rk_dt, wk[i * dk + ch]);
+        if (ALGO == ALGO_KDA) {
+          p.ring_g[gbase + (size_t)(base + i) * dk + ch] = p.g[((tok0 + i) * HV + h) * dk + ch];
+        }
+      }
+    }
+    if (tid < T) {
+      p.ring_beta[((size_t)s * HV + h) * L + base + tid] = wb[tid];
+      if (ALGO == ALGO_GDN) p.ring_g[gbase + base + tid] = wg[tid];
+    }
+  }
 
   // ---- 4. per value column: corrections, triangular solve, outputs, deltas
-  if (tid < dv) {
+  if (tid < dv && all_ok) {
     const int col = tid;
     float y[NV];
 #pragma unroll
@@ -1110,13 +1123,14 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
       }
     }
   }
-  if (h == 0 && tid == 0 && p.fold_out != nullptr) p.fold_out[r] = fold ? 1 : 0;
-  if (!copies_ok) {
+  if (all_ok) {
+    if (h == 0 && tid == 0 && p.fold_out != nullptr) p.fold_out[r] = fold ? 1 : 0;
+  } else if (tid == 0) {
     atomicOr(p.err, DEVERR_TIMEOUT);
-    // give copies that did not arrive a second bounded chance before exit
-    mbar_wait_bounded(&mbar[kMbarWin], 0);
-    if (nh > 0) mbar_wait_bounded(&mbar[kMbarHist], 0);
-    pipe.drain();
+    // copies that did not arrive in time get a second bounded wait before the
+    // CTA leaves (the window's waited above, or the row would not be here)
+    if (nh > 0) mbar_wait_bounded(&mbar[kMbarHist], 0, lim);
+    pipe.drain_tail();
   }
 }
 

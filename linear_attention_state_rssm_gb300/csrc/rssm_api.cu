@@ -17,6 +17,9 @@ struct rssm_handle {
   int max_smem;
   int num_sms;
   size_t layer_state, layer_k, layer_d, layer_g, layer_v, layer_beta;  // elements
+  WaitHook hook;  // bounded-wait test hook (off unless rssm_debug_withhold set it)
+  bool pipe_cfg;  // the configuration is one the pipelined kernel serves
+  int plan;       // RSSM_PLAN_*
 };
 
 namespace {
@@ -181,7 +184,16 @@ rssm_status window_params(const rssm_handle* h, int32_t layer, const void* q, co
   p.rk_dt = c.ring_k_dtype;
   p.rd_dt = c.ring_d_dtype;
   p.scale = c.scale;
+  p.hook = h->hook;
   return RSSM_OK;
+}
+
+// Whether a store configuration is one the pipelined kernel serves: GDN heads
+// of 128 x 128, a ring of at most 16 records (multiple of 4), fp32 or fp16
+// deltas.
+bool pipe_config(const rssm_config& c) {
+  return c.algo == RSSM_ALGO_GDN && c.dk == 128 && c.dv == 128 && c.L <= kPipeHist &&
+         c.L % 4 == 0 && (c.ring_d_dtype == RSSM_F32 || c.ring_d_dtype == RSSM_F16);
 }
 
 rssm_status window(rssm_handle* h, int32_t layer, const void* q, const void* k, const void* v,
@@ -193,6 +205,18 @@ rssm_status window(rssm_handle* h, int32_t layer, const void* q, const void* k, 
                                        fold_out, &p);
   if (st != RSSM_OK || B == 0) return st;
   p.cu = cu;
+  const rssm_config& c = h->cfg;
+  if (cu == nullptr && h->plan == RSSM_PLAN_PIPE && h->pipe_cfg && T <= kPipeMaxNT &&
+      B <= kPipeMaxRows) {
+    const int NT = pipe_nt(T);
+    const PipeSmem sm = pipe_layout(NT, B, c.dk, c.dv, c.in_dtype, c.ring_k_dtype,
+                                    c.ring_d_dtype, h->max_smem);
+    if (sm.ns >= 4) {
+      const long long items = (long long)B * c.HV;
+      const int grid = (int)(items < h->num_sms ? items : h->num_sms);
+      return from_cuda(pipe_launch(state_dt(c), NT, p, sm, grid, static_cast<cudaStream_t>(stream)));
+    }
+  }
   const int NT = cu != nullptr ? nt_for_ragged(T) : nt_for(T);
   p.sm = layout_for(h->cfg, T, NT);
   if ((int)p.sm.total > h->max_smem) return RSSM_ERR_UNSUPPORTED;
@@ -232,6 +256,7 @@ FoldParams fold_params(const rssm_handle* h, const int32_t* slot, const uint8_t*
   p.rk_dt = c.ring_k_dtype;
   p.rd_dt = c.ring_d_dtype;
   p.mode = mode;
+  p.hook = h->hook;
   p.sm = fold_layout_for(c);
   return p;
 }
@@ -307,6 +332,8 @@ rssm_status rssm_alloc(const rssm_config* cfg, const rssm_buffers* buf, rssm_han
   if ((int)prefill_layout(cfg->algo, cfg->dk, cfg->dv).total <= max_smem &&
       prefill_prepare(cfg->algo, state_dt(*cfg), max_smem) != cudaSuccess)
     return RSSM_ERR_CUDA;
+  const bool pipe_cfg = pipe_config(*cfg);
+  if (pipe_cfg && pipe_prepare(state_dt(*cfg), max_smem) != cudaSuccess) return RSSM_ERR_CUDA;
 
   rssm_handle* h = new (std::nothrow) rssm_handle;
   if (h == nullptr) return RSSM_ERR_INVALID_ARG;
@@ -322,6 +349,9 @@ rssm_status rssm_alloc(const rssm_config* cfg, const rssm_buffers* buf, rssm_han
   h->layer_g = slots * cfg->HV * cfg->L * n_gate(*cfg);
   h->layer_v = slots * cfg->HV * cfg->L * cfg->dv;
   h->layer_beta = slots * cfg->HV * cfg->L;
+  h->hook = WaitHook{WH_OFF, kWaitLimitNs};
+  h->pipe_cfg = pipe_cfg;
+  h->plan = RSSM_PLAN_AUTO;
   *out = h;
   return RSSM_OK;
 }
@@ -534,6 +564,27 @@ rssm_status rssm_get_device_error(rssm_handle* h, uint32_t* out, int32_t clear, 
   }
   *out = word;
   return word == 0 ? RSSM_OK : RSSM_ERR_DEVICE;
+}
+
+rssm_status rssm_set_plan(rssm_handle* h, int32_t plan) {
+  if (h == nullptr) return RSSM_ERR_INVALID_ARG;
+  if (plan != RSSM_PLAN_AUTO && plan != RSSM_PLAN_ROWS && plan != RSSM_PLAN_PIPE)
+    return RSSM_ERR_INVALID_ARG;
+  if (plan == RSSM_PLAN_PIPE && !h->pipe_cfg) return RSSM_ERR_UNSUPPORTED;
+  h->plan = plan;
+  return RSSM_OK;
+}
+
+rssm_status rssm_debug_withhold(rssm_handle* h, int32_t barrier, int32_t wait_limit_us) {
+  if (h == nullptr) return RSSM_ERR_INVALID_ARG;
+  if (barrier < WH_OFF || barrier >= WH_CHUNK0 + 256) return RSSM_ERR_INVALID_ARG;
+  if (barrier == WH_OFF) {
+    h->hook = WaitHook{WH_OFF, kWaitLimitNs};
+    return RSSM_OK;
+  }
+  if (wait_limit_us < 1 || wait_limit_us > 1000000) return RSSM_ERR_INVALID_ARG;
+  h->hook = WaitHook{barrier, 1000ull * (unsigned long long)wait_limit_us};
+  return RSSM_OK;
 }
 
 const char* rssm_status_string(rssm_status s) {

@@ -33,8 +33,23 @@ enum : int { FOLD_ALL = 0, FOLD_COMMIT = 1 };
 constexpr int kThreads = 128;  // 4 warps per CTA, one CTA per (row, value head)
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
+// A bounded wait gives up after this many nanoseconds of %globaltimer (a
+// launch may ask for a shorter limit, see WaitHook).
 constexpr unsigned long long kWaitLimitNs = 500ull * 1000ull * 1000ull;
+
+// Test hook of the bounded waits, off (withhold < 0) in every ordinary call:
+// the copies that complete on barrier `withhold` (0 the window rows, 1 the
+// history records, 2 + j chunk j of the checkpoint tile) register 16 more
+// bytes than they carry, so no copy can complete that barrier and every wait
+// on it runs out after limit_ns. Nothing faults: the copies themselves all land.
+enum : int { WH_OFF = -1, WH_WINDOW = 0, WH_HIST = 1, WH_CHUNK0 = 2 };
+struct WaitHook {
+  int withhold;
+  unsigned long long limit_ns;
+  __host__ __device__ uint32_t extra(int barrier) const {
+    return withhold == barrier ? 16u : 0u;
+  }
+};
 
 __host__ __device__ constexpr int dtype_bytes(int dt) { return dt == DT_F32 ? 4 : 2; }
 __host__ __device__ constexpr uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -168,6 +183,7 @@ struct ReplayParams {
   int B, T, L, n_slots, HK, HV, G, dk, dv;  // T: the window (ragged: the widest allowed)
   int in_dt, rk_dt, rd_dt;
   float scale;
+  WaitHook hook;
   ReplaySmem sm;
 };
 
@@ -189,6 +205,7 @@ struct FoldParams {
   size_t layer_state, layer_k, layer_d, layer_g;  // per-layer strides (elements)
   int B, T, L, n_slots, HK, HV, G, dk, dv;
   int rk_dt, rd_dt, mode;
+  WaitHook hook;
   FoldSmem sm;
 };
 
@@ -371,6 +388,86 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
   return m;
 }
 
+// ----------------------------------------------------------- pipelined replay
+// Persistent replay kernel (pipe_impl.cuh): one CTA per SM walks a list of
+// (row, value head) items. Warps 0-3 stream the checkpoint tiles on the tensor
+// cores, warps 4-7 prepare the next item and solve the previous one, warp 8
+// issues the checkpoint chunks into a ring that runs across items.
+constexpr int kPipeMath = 4;                       // warps streaming the tile
+constexpr int kPipePrep = 4;                       // warps preparing / solving items
+constexpr int kPipeProd = kPipeMath + kPipePrep;   // warp issuing the chunk copies
+constexpr int kPipeThreads = 32 * (kPipeProd + 1);
+constexpr int kPipeMaxRows = 512;                  // request rows ranked in shared memory
+constexpr int kPipeMaxStages = 16;                 // chunk ring stages at most
+constexpr int kPipeHist = 16;                      // history records an item folds / corrects
+constexpr int kPipeMaxNT = 8;                      // widest window
+
+// barriers: window copies [2], item prepared [2], item streamed [2], column sums
+// read [2], then "full" and "empty" per ring stage
+enum : int { PB_WIN = 0, PB_PREP = 2, PB_MATH = 4, PB_YFREE = 6, PB_FULL = 8 };
+constexpr int kPipeMbars = PB_FULL + 2 * kPipeMaxStages;
+
+// Per-item scalars shared by the roles (one copy per item buffer).
+struct PipeItem {
+  int row, h, s, c, base, fold, n, pad;
+  float egam;                    // e^Gam of the history (the fold's decay, or the scale of
+                                 // the checkpoint term of a window that does not fold)
+  float beta[kPipeMaxNT], eG[kPipeMaxNT], G[kPipeMaxNT];
+  float hf[kPipeHist];           // e^{Gam - Gam_m}: decay of record m to the end of the history
+  float am[kPipeMaxNT * kPipeMaxNT], fm[kPipeMaxNT * kPipeMaxNT];
+};
+
+struct PipeSmem {
+  uint32_t ring;                 // ns stages of one 8 KB chunk
+  uint32_t mbar;                 // kPipeMbars barriers, then the abort word
+  uint32_t rows;                 // slot, cursor, order, flags [maxb] (int32), group counts
+  uint32_t item[2];              // PipeItem
+  uint32_t wraw[2];              // window q, k rows as stored [2][NT][dk]
+  uint32_t hkr[2];               // history keys as stored [16][dk]
+  uint32_t hdr[2];               // history deltas as stored [16][dv]
+  uint32_t hgr[2];               // history gates [16] fp32
+  uint32_t xf[2];                // mat-vec inputs in fragment order [dk][8 NTN]
+  uint32_t kf[2];                // fold keys in fragment order [dk][16]
+  uint32_t df[2];                // f_m d_m in A-fragment order [4 warps][32 lanes][16]
+  uint32_t hh[2];                // history dots k_m . x_v [16][16]
+  uint32_t y[2];                 // column sums [2 NT][dv]
+  uint32_t total;
+  int ns;                        // ring stages
+  int maxb;                      // rows the ranking tables hold (a multiple of 32, >= B)
+};
+
+__host__ __device__ constexpr int pipe_ntn(int NT) { return NT <= 4 ? 1 : 2; }
+
+// Layout for windows of up to NT tokens; the ring takes what is left of
+// max_smem (at most kPipeMaxStages stages). ns < 2 means it does not fit.
+__host__ __device__ inline PipeSmem pipe_layout(int NT, int B, int dk, int dv, int in_dt,
+                                                int rk_dt, int rd_dt, int max_smem) {
+  PipeSmem m{};
+  const int ntn = pipe_ntn(NT);
+  m.maxb = (B + 31) & ~31;
+  uint32_t off = 0;
+  m.mbar = off;  off = align16(off + 8u * kPipeMbars + 16u);
+  m.rows = off;  off = align16(off + 16u * m.maxb + 8u * (kPipeMaxRows / 32));
+  for (int b = 0; b < 2; ++b) {
+    m.item[b] = off;  off = align16(off + (uint32_t)sizeof(PipeItem));
+    m.wraw[b] = off;  off = align16(off + 2u * NT * dk * dtype_bytes(in_dt));
+    m.hkr[b] = off;   off = align16(off + (uint32_t)(kPipeHist * dk * dtype_bytes(rk_dt)));
+    m.hdr[b] = off;   off = align16(off + (uint32_t)(kPipeHist * dv * dtype_bytes(rd_dt)));
+    m.hgr[b] = off;   off = align16(off + 4u * kPipeHist);
+    m.xf[b] = off;    off = align16(off + 4u * dk * 8 * ntn);
+    m.kf[b] = off;    off = align16(off + 4u * dk * kPipeHist);
+    m.df[b] = off;    off = align16(off + 4u * kPipeMath * 32 * 16);
+    m.hh[b] = off;    off = align16(off + 4u * kPipeHist * kPipeHist);
+    m.y[b] = off;     off = align16(off + 4u * 2 * NT * dv);
+  }
+  off = (off + 127u) & ~127u;
+  m.ring = off;
+  const int room = (max_smem - (int)off) / kChunkBytes;
+  m.ns = room < kPipeMaxStages ? room : kPipeMaxStages;
+  m.total = off + (uint32_t)(m.ns > 0 ? m.ns : 0) * kChunkBytes;
+  return m;
+}
+
 // Native fused-recurrent decode: the whole tile, one mbarrier for the window
 // and one per chunk, the window, the mat-vec inputs and the partial sums.
 struct NativeSmem {
@@ -501,13 +598,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-// Wait for phase `parity` of `bar`, giving up after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of `bar`, giving up after limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -46,8 +46,8 @@ __device__ __forceinline__ void issue_history(int n, int dk, int dv, const void*
                                               size_t kbase, int rk_dt, void* kdst,
                                               const void* ring_d, size_t dbase, int rd_dt,
                                               void* ddst, const float* ring_g, size_t gbase,
-                                              float* hg, uint64_t* bar) {
-  mbar_expect_tx(bar, history_bytes<ALGO>(n, dk, dv, rk_dt, rd_dt));
+                                              float* hg, uint64_t* bar, uint32_t extra = 0u) {
+  mbar_expect_tx(bar, history_bytes<ALGO>(n, dk, dv, rk_dt, rd_dt) + extra);
   history_copies<ALGO>(n, dk, dv, ring_k, kbase, rk_dt, kdst, ring_d, dbase, rd_dt, ddst, ring_g,
                        gbase, hg, bar);
 }
@@ -254,10 +254,11 @@ struct TilePipe {
   const ST* gtile;
   int dv;
   TileRing tr;
+  WaitHook hook;
   __device__ __forceinline__ TilePipe(ST* ring_, uint64_t* mbar, const ST* gtile_, int dk, int dv_,
-                                      int stages = kStages)
+                                      int stages, const WaitHook& hook_)
       : ring(ring_), full(mbar + kMbarFull), empty(mbar + kMbarEmpty), gtile(gtile_), dv(dv_),
-        tr(dk, dv_, (int)sizeof(ST), stages) {}
+        tr(dk, dv_, (int)sizeof(ST), stages), hook(hook_) {}
   // mbarrier set-up (one thread): "full" before the first copy (and the fence
   // that makes initialisation visible to the copies), "empty" with the number
   // of consuming warps before the CTA barrier that precedes the stream.
@@ -273,7 +274,7 @@ struct TilePipe {
   }
   __device__ __forceinline__ void issue(int j) const {
     const int st = j % tr.ns;
-    mbar_expect_tx(&full[st], tr.chunk_bytes);
+    mbar_expect_tx(&full[st], tr.chunk_bytes + hook.extra(WH_CHUNK0 + j));
     bulk_g2s(ring + (size_t)st * tr.cr * dv, gtile + (size_t)j * tr.cr * dv, tr.chunk_bytes,
              &full[st]);
   }
@@ -282,7 +283,7 @@ struct TilePipe {
     for (int j = 0; j < tr.ns; ++j) issue(j);
   }
   __device__ __forceinline__ bool wait_full(int j) const {
-    return mbar_wait_bounded(&full[j % tr.ns], (uint32_t)((j / tr.ns) & 1));
+    return mbar_wait_bounded(&full[j % tr.ns], (uint32_t)((j / tr.ns) & 1), hook.limit_ns);
   }
   // every warp, once it has consumed chunk j
   __device__ __forceinline__ void release(int j, int lane) const {
@@ -292,22 +293,31 @@ struct TilePipe {
   // producer, after its own release of chunk j: refill that stage with chunk j + ns
   __device__ __forceinline__ bool refill(int j) const {
     if (j + tr.ns >= tr.nchunk) return true;
-    const bool ok = mbar_wait_bounded(&empty[j % tr.ns], (uint32_t)((j / tr.ns) & 1));
+    const bool ok = mbar_wait_bounded(&empty[j % tr.ns], (uint32_t)((j / tr.ns) & 1),
+                                      hook.limit_ns);
     if (ok) issue(j + tr.ns);
     return ok;
   }
   // a CTA that leaves early lets the primed chunks land first
   __device__ __forceinline__ void drain() const {
-    for (int j = 0; j < tr.ns; ++j) mbar_wait_bounded(&full[j], 0);
+    for (int j = 0; j < tr.ns; ++j) mbar_wait_bounded(&full[j], 0, hook.limit_ns);
+  }
+  // a CTA whose stream failed lets the chunks that may still be in flight (the
+  // last ns issued) land before it leaves; each wait is bounded again
+  __device__ __forceinline__ void drain_tail() const {
+    const int j0 = tr.nchunk > tr.ns ? tr.nchunk - tr.ns : 0;
+    for (int j = j0; j < tr.nchunk; ++j) wait_full(j);
   }
   // interface of stream_quads: stage data of chunk j, wait for it, hand it back
   __device__ __forceinline__ const ST* stage(int j) const {
     return ring + (size_t)(j % tr.ns) * tr.cr * dv;
   }
   __device__ __forceinline__ bool wait(int j) const { return wait_full(j); }
-  __device__ __forceinline__ bool done(int j, int tid, int lane) const {
+  // (the producer issues nothing more once one of its own waits has run out,
+  // so every copy it issued can be waited for before the CTA leaves)
+  __device__ __forceinline__ bool done(int j, int tid, int lane, bool ok) const {
     release(j, lane);
-    return tid == 0 ? refill(j) : true;
+    return tid == 0 && ok ? refill(j) : true;
   }
 };
 
@@ -324,10 +334,11 @@ __device__ __forceinline__ bool stream_tile(const TilePipe<ST>& pipe, float (&y)
   const int rpc = pipe.tr.cr / cm.RG;  // this thread's rows per chunk (a multiple of 8)
   bool ok = true;
   for (int j = 0; j < pipe.tr.nchunk; ++j) {
-    ok = pipe.wait_full(j) && ok;
+    // a warp stores no chunk once one of its waits has run out
+    ok = __all_sync(kFull, pipe.wait_full(j) && ok);
     const ST* stg = pipe.ring + (size_t)(j % pipe.tr.ns) * pipe.tr.cr * dv +
                     (size_t)cm.rg * dv + cm.col;
-    for (int u0 = 0; u0 < rpc; u0 += RB) {
+    for (int u0 = 0; ok && u0 < rpc; u0 += RB) {
       float buf[RB];
 #pragma unroll
       for (int u = 0; u < RB; ++u) buf[u] = st_load<ST>(stg + (size_t)cm.RG * (u0 + u) * dv);
@@ -335,7 +346,7 @@ __device__ __forceinline__ bool stream_tile(const TilePipe<ST>& pipe, float (&y)
                                            gdn_decay, egam, xh);
     }
     pipe.release(j, lane);
-    if (tid == 0) ok = pipe.refill(j) && ok;
+    if (tid == 0 && ok) ok = pipe.refill(j);
   }
   return ok;
 }
@@ -454,6 +465,7 @@ __device__ __forceinline__ bool stream_quads(const PIPE& pipe, const QuadLane& q
   bool ok = true;
   for (int j = 0; j < pipe.tr.nchunk; ++j) {
     ok = pipe.wait(j) && ok;
+    if (FOLD) ok = __all_sync(kFull, ok);  // no store-back once a wait has run out
     const ST* stg = pipe.stage(j) + ql.col0;
     const int row0 = j * pipe.tr.cr;
     for (int u0 = 0; u0 < rpl; u0 += RS) {
@@ -503,7 +515,7 @@ __device__ __forceinline__ bool stream_quads(const PIPE& pipe, const QuadLane& q
         }
 #pragma unroll
         for (int u = 0; u < RS; ++u) {
-          if (u0 + u < rpl) st_cols<ST, CW>(gtile + (size_t)rows[u] * dv + ql.col0, s[u]);
+          if (ok && u0 + u < rpl) st_cols<ST, CW>(gtile + (size_t)rows[u] * dv + ql.col0, s[u]);
         }
       }
 #pragma unroll
@@ -533,7 +545,7 @@ __device__ __forceinline__ bool stream_quads(const PIPE& pipe, const QuadLane& q
         }
       }
     }
-    ok = pipe.done(j, tid, lane) && ok;
+    ok = pipe.done(j, tid, lane, ok) && ok;
   }
   for (int off = ql.lanes; off < 32; off <<= 1) {
 #pragma unroll
@@ -585,7 +597,7 @@ __device__ __forceinline__ bool stream_fixed(const PIPE& pipe, const QuadLane& q
         }
       }
     }
-    ok = pipe.done(j, tid, lane) && ok;
+    ok = pipe.done(j, tid, lane, ok) && ok;
   }
   for (int off = ql.lanes; off < 32; off <<= 1) {
 #pragma unroll

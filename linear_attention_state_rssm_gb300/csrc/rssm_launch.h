@@ -27,6 +27,13 @@ RSSM_DECLARE_REPLAY(replay_kda_f32_ragged)
 RSSM_DECLARE_REPLAY(replay_kda_bf16_ragged)
 #undef RSSM_DECLARE_REPLAY
 
+// Pipelined replay kernel (GDN, dk = dv = 128, rings of at most 16 records,
+// windows of at most 8 tokens, uniform windows): NT in {1, 2, 4, 8}.
+cudaError_t pipe_launch(int state_dt, int NT, const ReplayParams& p, const PipeSmem& sm, int grid,
+                        cudaStream_t st);
+cudaError_t pipe_prepare(int state_dt, int max_smem);
+inline int pipe_nt(int T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8; }
+
 cudaError_t fold_launch(int algo, int state_dt, const FoldParams& p, int n_layers,
                         cudaStream_t st);
 cudaError_t fold_prepare(int algo, int state_dt, int max_smem);

@@ -45,4 +45,16 @@ __device__ __forceinline__ void mma_split(float (&c)[4], const Tf32 (&a)[4], con
   mma_tf32(c, a[0].hi, a[1].hi, a[2].hi, a[3].hi, b[0].hi, b[1].hi);
 }
 
+// Fragment order of the mat-vec inputs of a window with 8 NTN vectors (NTN
+// n-tiles of eight): for rows [8s, 8s + 8) lane (g, t) finds at
+// [2 NTN (32 s + 4 g + t) + 2 nt + h] vector 8 nt + g of row 8s + 2t + h.
+// x_slot maps slot e back to its (row ch, vector v).
+template <int NTN>
+__device__ __forceinline__ void x_slot(int e, int& ch, int& v) {
+  constexpr int CPL = 2 * NTN;  // values per lane and step
+  const int s8 = e / (32 * CPL), ln = (e / CPL) & 31, comp = e % CPL;
+  ch = 8 * s8 + 2 * (ln & 3) + (comp & 1);
+  v = 8 * (comp >> 1) + (ln >> 2);
+}
+
 }  // namespace rssm

@@ -102,6 +102,15 @@ class ReplayStore:
     def rssm_get_device_error(self, clear=True, stream=None) -> int:
         return _lib.rssm_get_device_error(self.handle, clear, stream)
 
+    def rssm_set_plan(self, plan):
+        """Kernel family for decode and verify: "auto", "rows" or "pipe"."""
+        _lib.rssm_set_plan(self.handle, plan)
+
+    def rssm_debug_withhold(self, barrier, wait_limit_us=1000):
+        """Test hook of the bounded waits (include/rssm.h): later launches of
+        this store short-change `barrier` (-1: off)."""
+        _lib.rssm_debug_withhold(self.handle, barrier, wait_limit_us)
+
     def close(self):
         if getattr(self, "handle", None):
             _lib.rssm_free(self.handle)

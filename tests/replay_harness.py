@@ -57,11 +57,29 @@ class Run:
         self.orc_gpu_slots = np.array(live_slots, dtype=np.int64)
         S0o = S0[:, live_slots] if live_slots else S0[:, :1]
         no = max(len(live_slots), 1)
-        self.orc = ReplayOracle(algo, n_layers, no, HK, HV, dk, dv, L, self.store.scale, S0o)
+        rd = "f16" if ring_d_dtype == "f16" else "f32"
+        self.orc = ReplayOracle(algo, n_layers, no, HK, HV, dk, dv, L, self.store.scale, S0o,
+                                ring_d_dtype=rd)
         # A bf16 checkpoint is also checked against a chain that rounds its
         # checkpoint to bf16 at the same folds (outputs use the exact chain).
         self.orc_r = (ReplayOracle(algo, n_layers, no, HK, HV, dk, dv, L, self.store.scale, S0o,
-                                   ckpt_round="bf16") if state_dtype == "bf16" else None)
+                                   ckpt_round="bf16", ring_d_dtype=rd)
+                      if state_dtype == "bf16" else None)
+
+    def narrow(self, sample):
+        """From now on the oracle follows (and the checks compare) only rows
+        ``sample``, which must be among the rows followed so far."""
+        sample = np.asarray(sample)
+        live_slots = sorted({int(self.slots[r]) for r in sample if self.slots[r] >= 0})
+        keep = [self.orc_index[s] for s in live_slots]
+        for orc in (self.orc, self.orc_r):
+            if orc is not None:
+                orc.select_slots(keep)
+        self.sample = sample
+        self.orc_index = {s: j for j, s in enumerate(live_slots)}
+        self.orc_slots = np.array([self.orc_index.get(int(self.slots[r]), -1)
+                                   for r in sample], dtype=np.int64)
+        self.orc_gpu_slots = np.array(live_slots, dtype=np.int64)
 
     # ------------------------------------------------------------------ inputs
     def inputs(self, step, layer, T):
@@ -192,6 +210,35 @@ class Run:
         ulp = np.ldexp(1.0, np.frexp(np.abs(ref))[1] - 8)
         excess = np.maximum(np.abs(S - ref) - ulp, 0.0)
         return float(np.max(excess) / np.max(np.abs(ref)))
+
+    def check_ring_records(self):
+        """Ring records k, g, v and beta of the oracle's slots equal the
+        oracle's bit for bit (keys after rounding to the ring-key dtype, each
+        value head holding its key head's key) at every position the last
+        window of each layer wrote and every committed position [0, cursor);
+        non-finite values of rejected drafts must match as well."""
+        sl = self.orc_gpu_slots
+        n = len(sl)
+        if n == 0:
+            return
+        orc, st, G = self.orc, self.store, self.HV // self.HK
+        pos = np.arange(self.L)
+        mask = orc.written[:, :n] | (pos[None, None, :] < orc.cursor[None, :n, None])
+        got = {"k": st.ring_k, "g": st.ring_g, "v": st.ring_v, "beta": st.ring_beta}
+        want = {"k": synth.quantize(np.repeat(orc.ring_k[:, :n], G, axis=2), st.ring_k_dtype),
+                "g": orc.ring_g[:, :n], "v": orc.ring_v[:, :n], "beta": orc.ring_beta[:, :n]}
+        for name in ("k", "g", "v", "beta"):
+            a = got[name].double().cpu().numpy()[:, sl]
+            b = want[name]
+            m = np.broadcast_to(mask[:, :, None, :].reshape(mask.shape[:2] + (1, self.L) +
+                                                            (1,) * (a.ndim - 4)), a.shape)
+            assert np.array_equal(a[m], b[m], equal_nan=True), (
+                f"ring_{name} differs at {np.count_nonzero(~np.isclose(a[m], b[m], equal_nan=True))}"
+                f" of {np.count_nonzero(m)} checked values")
+
+    def check_no_fp16_delta_overflow(self):
+        """An fp16 delta ring stayed inside the fp16 range (oracle flag)."""
+        assert not self.orc.d_overflow.any(), "an accepted delta exceeds the fp16 range"
 
     def ring_d_err(self):
         """Committed history records d[0, cursor) vs the oracle's."""

@@ -45,3 +45,13 @@ def test_cursor_trajectory_rule(c, T, L, a, want):
 
 def test_job_throughput_is_whole_job():
     assert bench.job_throughput(1000.0, 4, 2.0) == 2000.0
+
+
+def test_commit_bytes_fold_every():
+    """A fold-every commit reads and writes the checkpoint once and reads the
+    n committed records: 2 * 2,097,152 + n * 20,608 for the decode shapes."""
+    assert bench.commit_bytes(0, 16, 32, 128, 128, 4, 2, 4) == 2 * 2097152
+    assert bench.commit_bytes(5, 16, 32, 128, 128, 4, 2, 4) == 2 * 2097152 + 5 * 20608
+    # KDA: a gate per key channel, bf16 checkpoint, fp16 keys and deltas
+    assert bench.commit_bytes(3, 32, 32, 128, 128, 2, 2, 2, 128) == \
+        2 * 32 * 128 * 128 * 2 + 3 * (32 * 128 * 2 + 32 * 128 * 2 + 32 * 128 * 4)

@@ -34,6 +34,7 @@ def test_forced_folds_ragged_batch():
         np.testing.assert_array_equal(f_gpu, f_orc)
         run.commit(acc, T, force=force)
         run.check_cursors()
+        run.check_ring_records()
         assert run.state_err() <= TOL32
     assert run.ring_d_err() <= TOL32
 
@@ -69,6 +70,7 @@ def test_written_ring_positions_are_exact():
         assert not written[3].any()                  # slot 3 is never referenced
         run.commit(acc, T)
         run.check_cursors()
+        run.check_ring_records()
 
 
 def test_device_error_word_bad_slot_and_cursor():
@@ -138,6 +140,7 @@ def test_restore_copy_checkpoint_into_fresh_slot():
         np.testing.assert_array_equal(o_all[0], o_all[1])
         assert rel_err(o_gpu, o_orc) <= TOL32
         run.check_cursors()
+        run.check_ring_records()
 
 
 def test_runs_are_deterministic():
@@ -218,6 +221,7 @@ def test_head_sizes_and_groups(algo, dk, dv, G):
         np.testing.assert_array_equal(f_gpu, f_orc)
         run.commit(acc, T)
         run.check_cursors()
+        run.check_ring_records()
         assert run.state_err() <= TOL32
 
 
@@ -236,6 +240,7 @@ def test_widest_window_and_longest_ring(algo):
         np.testing.assert_array_equal(f_gpu, f_orc)
         run.commit(acc, T)
         run.check_cursors()
+        run.check_ring_records()
     assert run.ring_d_err() <= TOL32
 
 
@@ -249,6 +254,7 @@ def test_multi_layer_decode_moves_cursor_once_per_step():
             assert rel_err(o_gpu, o_orc) <= TOL32, (step, layer)
             np.testing.assert_array_equal(f_gpu, f_orc)
         run.check_cursors()
+        run.check_ring_records()
     assert run.state_err() <= TOL32
 
 
@@ -273,6 +279,7 @@ def test_decode_row_order_either_side_of_the_ranked_batch_limit(B):
         np.testing.assert_array_equal(f_gpu[live_rows], f_orc[live_rows])
         assert np.all(o_all[null] == SENTINEL), "null rows must be left untouched"
         run.check_cursors()
+        run.check_ring_records()
     assert run.state_err() <= TOL32
     assert run.ring_d_err() <= TOL32
     assert run.store.rssm_get_device_error() == 0
@@ -295,6 +302,7 @@ def test_decode_on_a_long_ring(algo, HK, HV):
         assert rel_err(o_gpu, o_orc) <= TOL16, step
         np.testing.assert_array_equal(f_gpu, f_orc)
         run.check_cursors()
+        run.check_ring_records()
     assert run.state_err() <= TOL16
     assert run.ring_d_err() <= TOL16
     assert run.store.rssm_get_device_error() == 0
@@ -318,6 +326,7 @@ def test_decode_fold_of_every_history_length(state, ring_k):
         assert rel_err(o_gpu, o_orc) <= tol, step
         np.testing.assert_array_equal(f_gpu, f_orc)
         run.check_cursors()
+        run.check_ring_records()
         assert run.state_err() <= tol, step
     assert run.ring_d_err() <= tol
     assert run.store.rssm_get_device_error() == 0
@@ -347,6 +356,7 @@ def test_verify_across_input_key_and_state_dtypes(in_dt, ring_k, state, T, algo)
         np.testing.assert_array_equal(f_gpu, f_orc)
         run.commit(acc, T, force=force)
         run.check_cursors()
+        run.check_ring_records()
         assert run.state_err() <= tol, step
     assert run.ring_d_err() <= tol
     assert run.store.rssm_get_device_error() == 0

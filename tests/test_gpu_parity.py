@@ -42,6 +42,7 @@ def test_tiny_gdn_decode_forty_steps_two_folds():
         assert rel_err(o_gpu, o_orc) <= TOL32, step
         np.testing.assert_array_equal(f_gpu, f_orc)
         run.check_cursors()
+        run.check_ring_records()
         if f_gpu[0]:
             fold_steps.append(step)
         assert run.state_err() <= TOL32
@@ -50,17 +51,19 @@ def test_tiny_gdn_decode_forty_steps_two_folds():
     assert run.store.rssm_get_device_error() == 0
 
 
-def test_qwen_shaped_gdn_decode_full_batch_sampled():
+def test_qwen_shaped_gdn_decode_full_batch():
     """HK=16, HV=32, dk=dv=128, batch 64 with 8 null slots, L=16, bf16 q/k/v,
-    fp32 state and deltas, fp16 ring keys; 34 steps (two folds). The GPU runs
-    the whole batch; the oracle checks a sample of rows."""
+    fp32 state and deltas, fp16 ring keys; 34 steps (two folds). Every live row
+    is compared with the oracle on every step (outputs, fold flags, cursors,
+    ring records; checkpoints after each fold), so the decode kernel's
+    reordering of folding rows is covered for every row."""
     B = 64
     slots = _null_slots(B, 8, 1001)
     null = np.nonzero(slots < 0)[0]
     live = np.nonzero(slots >= 0)[0]
-    sample = np.concatenate([live[[0, 7, 19, 33, 55]], null[:2]])
     run = Run(algo="gdn", HK=16, HV=32, dk=128, dv=128, L=16, max_T=1, slots=slots,
-              n_slots=B, in_dtype="bf16", config_id=1, sample=sample)
+              n_slots=B, in_dtype="bf16", config_id=1)
+    folds = 0
     for step in range(34):
         inp = run.inputs(step, 0, 1)
         o_all, o_gpu, o_orc, f_gpu, f_orc = run.window(0, inp, 1, decode=True, advance=True)
@@ -69,6 +72,11 @@ def test_qwen_shaped_gdn_decode_full_batch_sampled():
         assert np.all(o_all[null] == SENTINEL), "null rows must be left untouched"
         np.testing.assert_array_equal(f_gpu[live_tok], f_orc[live_tok])
         run.check_cursors()
+        run.check_ring_records()
+        if f_gpu[live_tok].any():
+            folds += 1
+            assert run.state_err() <= TOL16, step
+    assert folds == 2
     cur = run.cursor_gpu()
     assert np.all(cur[null] == 0)
     assert np.all(cur[live] == cur[live[0]])
@@ -78,10 +86,19 @@ def test_qwen_shaped_gdn_decode_full_batch_sampled():
 
 
 # --------------------------------------------------------------- verify
-def _verify_chain(run, T, steps, poison_frac, seed0, check_oracle=True):
-    """Chained verify + commit; returns accepted outputs per step (GPU)."""
+def _verify_chain(run, T, steps, poison_frac, seed0, check_oracle=True, narrow_to=None,
+                  full_steps=4):
+    """Chained verify + commit; returns accepted outputs per step (GPU).
+
+    With ``narrow_to``, the run starts on every row and keeps every row until
+    at least ``full_steps`` steps, one of them with ring-overflow folds, have
+    been compared; then it follows the rows ``narrow_to`` only."""
     accepted = []
+    fold_seen = False
     for step in range(steps):
+        if narrow_to is not None and step >= full_steps and fold_seen:
+            run.narrow(narrow_to)
+            narrow_to = None
         inp = run.inputs(step, 0, T)
         acc = synth.accept_lengths(seed0 + step, run.B, T)
         if poison_frac:
@@ -94,9 +111,12 @@ def _verify_chain(run, T, steps, poison_frac, seed0, check_oracle=True):
             assert rel_err(o_gpu[mask], o_orc[mask]) <= run.tol, (step, T)
             live = run.orc_slots >= 0
             np.testing.assert_array_equal(f_gpu[live], f_orc[live])
+            # a fold-every commit folds every step (its windows never overflow)
+            fold_seen |= bool(f_gpu[live].any()) or run.commit_mode == "fold_every"
         run.commit(acc, T)
         if check_oracle:
             run.check_cursors()
+            run.check_ring_records()
             assert run.state_err() <= run.tol
         amask = (np.arange(T)[None, :] < acc[:, None]).reshape(-1)
         amask &= np.repeat(run.slots >= 0, T)
@@ -108,14 +128,15 @@ def _verify_chain(run, T, steps, poison_frac, seed0, check_oracle=True):
 @pytest.mark.parametrize("state,mode", [("f32", "lazy"), ("bf16", "fold_every")])
 def test_gdn_verify_commit_with_poisoned_drafts(T, state, mode):
     """HK=16, HV=32, dk=dv=128, batch 128, L=16, accept ~ U[0, T], NaN/Inf at
-    rejected positions of 10% of the rows with rejections, 24 chained steps."""
+    rejected positions of 10% of the rows with rejections, 24 chained steps.
+    Every row is compared until at least four steps, one with ring-overflow
+    folds, have been; then a sample of rows for the rest of the chain."""
     B = 128
     sample = np.array([0, 5, 17, 42, 77, 101, 127])
     run = Run(algo="gdn", HK=16, HV=32, dk=128, dv=128, L=16, max_T=T, slots=np.arange(B),
-              in_dtype="bf16", state_dtype=state, commit_mode=mode, config_id=2,
-              sample=sample)
+              in_dtype="bf16", state_dtype=state, commit_mode=mode, config_id=2)
     run.tol = TOL16
-    _verify_chain(run, T, 24, 0.10, 7000 + T)
+    _verify_chain(run, T, 24, 0.10, 7000 + T, narrow_to=sample)
     assert run.ring_d_err() <= TOL16
     assert run.store.rssm_get_device_error() == 0
 
@@ -161,8 +182,10 @@ def test_kda_decode_and_verify_alternating(variant):
     B = 64
     sample = np.array([3, 31, 60])
     run = Run(algo="kda", HK=32, HV=32, dk=128, dv=128, L=32, max_T=3, slots=np.arange(B),
-              config_id=3, sample=sample, **kw)
+              config_id=3, **kw)
     for step in range(64):
+        if step == 8:
+            run.narrow(sample)   # every row for the first eight steps
         if step % 2 == 0:
             inp = run.inputs(step, 0, 1)
             _, o_gpu, o_orc, f_gpu, f_orc = run.window(0, inp, 1, decode=True, advance=True)
@@ -172,11 +195,14 @@ def test_kda_decode_and_verify_alternating(variant):
             inp = run.inputs(step, 0, T)
             acc = synth.accept_lengths(3300 + step, B, T)
             _, o_gpu, o_orc, f_gpu, f_orc = run.window(0, inp, T)
-            mask = (np.arange(T)[None, :] < acc[sample][:, None]).reshape(-1)
+            mask = (np.arange(T)[None, :] < acc[run.sample][:, None]).reshape(-1)
             assert rel_err(o_gpu[mask], o_orc[mask]) <= tol, step
             run.commit(acc, T)
         np.testing.assert_array_equal(f_gpu, f_orc)
         run.check_cursors()
+        run.check_ring_records()
         assert run.state_err() <= tol
     assert run.ring_d_err() <= tol
+    if variant != "fp32":
+        run.check_no_fp16_delta_overflow()
     assert run.store.rssm_get_device_error() == 0

@@ -70,6 +70,7 @@ def test_prefill_after_history_then_decode(algo, HK, HV, dk, dv, in_dt, state):
                 live = run.orc_slots >= 0
                 assert rel_err(o_gpu[live], o_orc[live]) <= tol, (step, layer)
             run.check_cursors()
+            run.check_ring_records()
 
     decode_steps(0, 3)
     lens = np.array([17, 0, 5, 1, 45, 16, 15])
@@ -79,6 +80,7 @@ def test_prefill_after_history_then_decode(algo, HK, HV, dk, dv, in_dt, state):
         o_gpu, o_orc = run.prefill(layer, inp, cu, reset_cursor=layer == n_layers - 1)
         _check_prefill(run, o_gpu, o_orc, cu, tol)
     run.check_cursors()
+    run.check_ring_records()
     cur = run.cursor_gpu()
     assert cur[slots[1]] == 3, "a row without prompt tokens keeps its history"
     assert all(cur[s] == 0 for r, s in enumerate(slots) if s >= 0 and lens[r] > 0)
@@ -100,6 +102,7 @@ def test_prefill_qwen_shapes():
     o_gpu, o_orc = run.prefill(0, inp, cu, reset_cursor=True)
     _check_prefill(run, o_gpu, o_orc, cu, TOL16)
     run.check_cursors()
+    run.check_ring_records()
     assert run.state_err() <= TOL16
     assert run.store.rssm_get_device_error() == 0
 

@@ -68,6 +68,7 @@ def test_ragged_verify_commit_chain(algo, HK, HV, max_T, in_dt, state, mode):
         acc = synth.ragged_accept(synth.seed_for(60, step, 3), cu)
         run.commit_ragged(acc, cu, max_T, force)
         run.check_cursors()
+        run.check_ring_records()
         idle_slots = slots[(slots >= 0) & (lens == 0)]
         np.testing.assert_array_equal(run.cursor_gpu()[idle_slots], cur0[idle_slots])
         assert run.state_err() <= tol, step
