@@ -259,6 +259,7 @@ def run_ours(args, rank, world, local_rank):
 
     st = ReplayStore("gdn", nl, B, HK, HV, dk, dv, L, 1, w["in_dtype"], w["state_dtype"],
                      w["ring_k_dtype"], w["ring_d_dtype"], "lazy", device=dev)
+    st.rssm_set_plan(args.plan)
     for layer in range(nl):
         st.state[layer].normal_(0.0, 0.1, generator=gen)
     null = torch.randperm(B, generator=torch.Generator().manual_seed(7))[:w["null_slots"]]
@@ -644,6 +645,7 @@ def run_verify(args, torch, dev, rank, peak, clk_index):
     gen.manual_seed(2000 + rank)
     st = ReplayStore("gdn", nl, B, HK, HV, dk, dv, L, T, "bf16", v["state_dtype"], "f16", "f32",
                      v["commit_mode"], device=dev)
+    st.rssm_set_plan(args.plan)
     for layer in range(nl):
         st.state[layer].normal_(0.0, 0.1, generator=gen)
     slot = torch.arange(B, dtype=torch.int32, device=dev)
@@ -1023,7 +1025,7 @@ SWEEP = [  # (algo, B, L, T, state dtype, commit mode); decode when T == 1
 ]
 
 
-def sweep_point(torch, dev, algo, B, L, T, state_dtype, mode, steps, warmup, peak):
+def sweep_point(torch, dev, algo, B, L, T, state_dtype, mode, steps, warmup, peak, plan="auto"):
     """Steady-state decode (T = 1) or verify + commit (T > 1) over enough
     stacked layers that the checkpoints exceed L2; per-layer time from CUDA
     events around CUDA-graph replays, algorithmic bytes of the replay launches
@@ -1038,6 +1040,8 @@ def sweep_point(torch, dev, algo, B, L, T, state_dtype, mode, steps, warmup, pea
     gen.manual_seed(5000 + B + 7 * T + L)
     st = ReplayStore(algo, nl, B, HK, HV, dk, dv, L, T, "bf16", state_dtype, "f16", "f32", mode,
                      device=dev)
+    if algo == "gdn" and L <= 16:
+        st.rssm_set_plan(plan)
     for layer in range(nl):
         st.state[layer].normal_(0.0, 0.1, generator=gen)
     cur0 = [r % L for r in range(B)]  # staggered rows, as in steady serving
@@ -1104,7 +1108,7 @@ def sweep_point(torch, dev, algo, B, L, T, state_dtype, mode, steps, warmup, pea
     del graph, st, q, k, v, beta, g, out
     torch.cuda.empty_cache()
     return {"algo": algo, "batch": B, "L": L, "T": T, "state_dtype": state_dtype,
-            "commit_mode": mode, "layers": nl, "ms_per_layer": ms_layer,
+            "commit_mode": mode, "layers": nl, "ms_per_layer": ms_layer, "plan": plan,
             "replayed_tokens_per_s_per_layer": B * T / (ms_layer / 1e3),
             "replay_gbs": gbs, "frac_of_hbm_peak": gbs / peak, "device_error_word": err}
 
@@ -1118,7 +1122,8 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     peak, peak_kind = peaks()
-    pts = [sweep_point(torch, dev, *pt, steps=args.steps, warmup=args.warmup, peak=peak)
+    pts = [sweep_point(torch, dev, *pt, steps=args.steps, warmup=args.warmup, peak=peak,
+                       plan=args.plan)
            for pt in SWEEP]
     return {"sweep": pts, "peak_gbs": peak, "peak_kind": peak_kind,
             "note": "per-layer time includes the step's cursor advance (decode) or commit "
@@ -1139,6 +1144,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the replay prefill line")
     ap.add_argument("--no-conv", action="store_true", help="skip the conv window line")
     ap.add_argument("--no-kda", action="store_true", help="skip the KDA decode+verify line")
+    ap.add_argument("--plan", default="auto", choices=["auto", "rows", "pipe"],
+                    help="kernel family for GDN decode/verify (rssm_set_plan)")
     ap.add_argument("--sweep", action="store_true",
                     help="print the steady-state grid (batch, L, T, state dtype, GDN/KDA)")
     ap.add_argument("--prefill-prompts", type=int, default=PREFILL["prompts"])

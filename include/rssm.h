@@ -358,6 +358,9 @@ rssm_status rssm_get_device_error(rssm_handle *h, uint32_t *out, int32_t clear,
  *  - RSSM_PLAN_PIPE: the pipelined kernel, one persistent CTA per SM walking
  *    the (row, value head) items, checkpoint chunks streamed continuously
  *    across items while other warps prepare the next item and solve the last.
+ *    A bounded wait that runs out there stops the CTA: the rows of the items
+ *    it had not finished are left untouched (as above for the item in
+ *    progress).
  *    It serves GDN stores with dk = dv = 128, L <= 16 and L a multiple of 4,
  *    fp32 or fp16 deltas, calls with T <= 8 and B <= 512 (uniform windows);
  *    calls outside that run on the per-row kernel.

@@ -15,24 +15,32 @@
 // How the work is laid out. A CTA of the per-row kernel spends most of its
 // life outside the checkpoint stream (window set-up, window solve), and with
 // three or four CTAs per SM the stream of one is not enough to keep HBM busy.
-// Here the three kinds of work run on separate warps, one item apart:
-//  - warp 8 (one thread) issues the 8 KB checkpoint chunks of item after item
-//    into a ring of up to 16 stages, so the SM's stream never stops at an item
-//    boundary;
-//  - warps 0-3 ("math") consume the chunks on the tensor cores: for a folding
-//    item S^T <- e^Gam S^T + D~^T K (D~ = f_m d_m, stored back), then the
-//    mat-vec Y^T = S^T X for the 2T window vectors (X = raw k_i, q_i); for an
-//    item with history that does not fold, Y^T <- e^Gam Y^T + D~^T H with
-//    H = K X the history dots (the correction term of the replayed state);
-//  - warps 4-7 ("prep") prepare item k + 1 (gate scans, X and D~ in fragment
-//    order, fold keys or H, the window coefficients A and F) while the math
-//    warps stream item k, then solve item k - 1 per value column (outputs and
-//    records), and issue the window and history copies of item k + 2.
+// Here the kinds of work run on separate warps, one item apart:
+//  - warps 8-11 issue every async copy as 16-byte cp.async pieces spread over
+//    their 128 threads: the 8 KB checkpoint chunks of item after item into a
+//    ring of up to 16 stages (each as soon as its stage is released), and the
+//    window and history rows of item k + 2 as soon as item k is prepared;
+//    each barrier counts one arrival per copying thread, made when that
+//    thread's copies have landed. They poll and wait, never release: a
+//    release waits for the issuing thread's copies in flight, and one thread
+//    issuing whole-chunk bulk copies reached one chunk per ~900 cycles, a
+//    fifth of an SM's share of HBM;
+//  - warps 0-3 ("math"), one value column per thread, consume the chunks: for
+//    a folding item S[row] <- e^Gam S[row] + sum_m k_m[row] f_m d_m (stored
+//    back), then y_v += x_v[row] S[row] for the 2T window vectors (raw k_i,
+//    q_i); for an item with history that does not fold, y_v <- e^Gam y_v +
+//    sum_m (k_m . x_v) f_m d_m (the correction term of the replayed state);
+//  - warps 4-7 ("prep") prepare item k + 1 (gate scans, the mat-vec inputs,
+//    transposed history keys, f_m d_m, the history dots k_m . x_v, the window
+//    coefficients A and F) while the math warps stream item k, then solve item
+//    k - 1 per value column (outputs and records).
+// All of it runs on the CUDA cores: every sum is short or split across
+// threads, so no thread waits on a long chain of dependent products (the
+// warp-level tensor-core product takes hundreds of cycles from operands to a
+// usable accumulator on this part, and a 128-row mat-vec made of them was
+// four times slower than the stream of its chunks).
 // Items are dealt round-robin from one order that every CTA computes alike:
 // folding rows first, so every CTA gets an equal share of the heavier items.
-// Each product uses warp-level mma.sync m16n8k8 with tf32 operands and fp32
-// accumulation; fp32 operands are split into tf32 head and tail (hi*hi +
-// hi*lo + lo*hi), 16-bit values are exact in tf32 and take one product.
 //
 // Waits: every mbarrier wait is bounded (the launch's limit) and also gives up
 // once another role has given up (abort word). A CTA whose wait ran out sets
@@ -42,11 +50,8 @@
 // leaves, every copy it issued is waited for again (bounded).
 #pragma once
 
-#include <type_traits>
-
 #include "rssm_common.cuh"
 #include "rssm_history.cuh"
-#include "rssm_mma.cuh"
 
 namespace rssm {
 
@@ -54,17 +59,24 @@ enum : int { PF_LIVE = 1, PF_FOLD = 2 };
 constexpr int kPipeDK = 128, kPipeDV = 128;
 constexpr int kPipeGroups = kPipeMaxRows / 32;
 
-// Bounded wait that also returns false once the CTA's abort word is set.
+// Bounded wait that also returns false once the CTA's abort word is set. The
+// thread is parked by the hardware between polls (a suspend-time hint), so a
+// waiting warp leaves the issue slots of its sub-partition to the warps that
+// have work: with short sleeps instead, the waiting and polling warps issued
+// most of a launch's instructions.
+constexpr uint32_t kPipeParkNs = 1000;
 __device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity,
                                           unsigned long long lim, const volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint(bar, parity, kPipeParkNs)) return true;
     if (*abort) return false;
     if (global_ns() - t0 > lim) return false;
   }
 }
+
+
 
 // AND of `pred` over the `count` threads that name barrier `id`.
 __device__ __forceinline__ bool named_and(int id, int count, bool pred) {
@@ -80,118 +92,103 @@ __device__ __forceinline__ bool named_and(int id, int count, bool pred) {
   return out != 0;
 }
 
-// Four consecutive values of a 16-bit or fp32 array in shared memory as fp32.
-__device__ __forceinline__ float4 ld4_as_f32(const void* base, int i, int dt) {
-  if (dt == DT_F32) return *reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
-  const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i);
-  float2 a, b;
-  if (dt == DT_BF16) {
-    a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-    b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-  } else {
-    a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-    b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+// Eight consecutive 16-bit values (bf16 or fp16) or fp32 values in shared
+// memory as fp32 (i a multiple of 8).
+__device__ __forceinline__ void ld8_as_f32(const void* base, int i, int dt, float (&v)[8]) {
+  if (dt == DT_F32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
+    const float4 a = p[0], b = p[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    return;
   }
-  return make_float4(a.x, a.y, b.x, b.y);
+  const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + i);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float2 f;
+    if (dt == DT_BF16) {
+      f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
+    } else {
+      f = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
+    }
+    v[2 * q] = f.x;
+    v[2 * q + 1] = f.y;
+  }
 }
 
-// Two consecutive values as fp32 (i even).
-__device__ __forceinline__ float2 ld2_as_f32(const void* base, int i, int dt) {
-  if (dt == DT_F32) return *reinterpret_cast<const float2*>(static_cast<const float*>(base) + i);
-  const uint32_t u = *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(base) + i);
-  if (dt == DT_BF16) return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-  return __half22float2(*reinterpret_cast<const __half2*>(&u));
+// y[v] += x_v[row] s over the NV mat-vec inputs of one row (xr: [NV] floats)
+template <int NV>
+__device__ __forceinline__ void matvec_row(const float* xr, float s, float (&y)[NV]) {
+  const float4* x4 = reinterpret_cast<const float4*>(xr);
+#pragma unroll
+  for (int v4 = 0; v4 < NV / 4; ++v4) {
+    const float4 x = x4[v4];
+    y[4 * v4] = fmaf(x.x, s, y[4 * v4]);
+    y[4 * v4 + 1] = fmaf(x.y, s, y[4 * v4 + 1]);
+    y[4 * v4 + 2] = fmaf(x.z, s, y[4 * v4 + 2]);
+    y[4 * v4 + 3] = fmaf(x.w, s, y[4 * v4 + 3]);
+  }
+  if constexpr (NV % 4 != 0) {
+    const float2 x = reinterpret_cast<const float2*>(xr)[NV / 2 - 1];
+    y[NV - 2] = fmaf(x.x, s, y[NV - 2]);
+    y[NV - 1] = fmaf(x.y, s, y[NV - 1]);
+  }
 }
 
 // ---------------------------------------------------------------- math warps
-// One item's stream on math warp `warp` (columns 32 warp + 4g .. + 3 of every
-// eight-row step, rows 2t and 2t + 1; see stream_mma in replay_impl.cuh for
-// the fragment relabelling this shares). q is the global index of the item's
-// first chunk. Returns false if a wait gave up (the item is then abandoned:
-// nothing more is stored, the stages it did not release stay held).
-template <typename ST, int NTN, bool EXACT_X, bool EXACT_K>
+// One item's stream, thread `col` owning value column col. q is the global
+// index of the item's first chunk. Returns false if a wait gave up (the item
+// is then abandoned: nothing more is stored, the stages it did not release
+// stay held).
+template <typename ST, int NV>
 __device__ __forceinline__ bool pipe_stream(const PipeItem& I, const ST* ring, uint64_t* mb, int NS,
-                                            int q, const float* xf, const float* kf,
-                                            const float* dfp, const float* hh, ST* gtile,
+                                            int q, const float* xh, const float* hkt,
+                                            const float* dtm, const float* hh, ST* gtile,
                                             unsigned long long lim, const volatile int* abort,
-                                            int warp, int lane, float (&y)[16]) {
+                                            int col, int lane, float (&y)[NV]) {
   constexpr int DV = kPipeDV, DK = kPipeDK;
   constexpr int CR = kChunkBytes / (DV * (int)sizeof(ST));  // rows per chunk
   constexpr int NCH = DK / CR;
-  constexpr bool EXACT_S = !std::is_same<ST, float>::value;
-  const int g = lane >> 2, t = lane & 3, col = 32 * warp + 4 * g;
   const bool fold = I.fold != 0;
-  const int n = I.n, nkq = n > 8 ? 2 : (n > 0 ? 1 : 0);
+  const int n = I.n;
   const float decay = I.egam;
-  // f_m d_m as A fragments [m-tile][record block][4] (zero past the history)
-  Tf32 df[2][2][4];
-  if (n > 0) {
-    const float4* d4 = reinterpret_cast<const float4*>(dfp) + (warp * 32 + lane) * 4;
+  // f_m d_m of this column (zero past the history)
+  float dm[kPipeHist];
 #pragma unroll
-    for (int mk = 0; mk < 4; ++mk) {
-      const float4 v = d4[mk];
-      df[mk >> 1][mk & 1][0] = tf32_split<false>(v.x);
-      df[mk >> 1][mk & 1][1] = tf32_split<false>(v.y);
-      df[mk >> 1][mk & 1][2] = tf32_split<false>(v.z);
-      df[mk >> 1][mk & 1][3] = tf32_split<false>(v.w);
-    }
-  }
+  for (int m = 0; m < kPipeHist; ++m) dm[m] = n > 0 ? dtm[m * DV + col] : 0.f;
 #pragma unroll
-  for (int e = 0; e < 16; ++e) y[e] = 0.f;
-  const float4* kf4 = reinterpret_cast<const float4*>(kf);
+  for (int v = 0; v < NV; ++v) y[v] = 0.f;
   for (int j = 0; j < NCH; ++j, ++q) {
     const int st = q % NS;
     if (!__all_sync(kFull, pipe_wait(&mb[PB_FULL + st], (uint32_t)((q / NS) & 1), lim, abort)))
       return false;
-    const ST* stg = ring + (size_t)st * CR * DV;
-#pragma unroll 2
-    for (int kb = 0; kb < CR; kb += 8) {
-      const int r0 = j * CR + kb + 2 * t;        // this lane's tile rows r0, r0 + 1
-      const int fi = ((j * CR + kb) >> 3) * 32 + lane;
-      float s0[4], s1[4];
-      ld_cols<ST, 4>(stg + (size_t)(kb + 2 * t) * DV + col, s0);
-      ld_cols<ST, 4>(stg + (size_t)(kb + 2 * t + 1) * DV + col, s1);
-      if (fold) {
-        const float4 k4 = kf4[fi];  // row j*CR + kb + g: records t, t + 4, 8 + t, 12 + t
-        const Tf32 kb0[2] = {tf32_split<EXACT_K>(k4.x), tf32_split<EXACT_K>(k4.y)};
-        const Tf32 kb1[2] = {tf32_split<EXACT_K>(k4.z), tf32_split<EXACT_K>(k4.w)};
+    const ST* stg = ring + (size_t)st * CR * DV + col;
+    if (fold) {
+#pragma unroll 4
+      for (int u = 0; u < CR; ++u) {
+        const int row = j * CR + u;
+        float s = decay * st_load<ST>(stg + (size_t)u * DV);
+        if (n > 0) {  // (an empty history folds to the checkpoint itself)
+          const float4* kr = reinterpret_cast<const float4*>(hkt + row * kPipeHist);
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          float c[4] = {decay * s0[2 * mt], decay * s1[2 * mt], decay * s0[2 * mt + 1],
-                        decay * s1[2 * mt + 1]};
-          if (nkq > 0) mma_split<false, EXACT_K>(c, df[mt][0], kb0);
-          if (nkq > 1) mma_split<false, EXACT_K>(c, df[mt][1], kb1);
-          s0[2 * mt] = c[0];
-          s1[2 * mt] = c[1];
-          s0[2 * mt + 1] = c[2];
-          s1[2 * mt + 1] = c[3];
+          for (int q4 = 0; q4 < kPipeHist / 4; ++q4) {
+            const float4 k4 = kr[q4];
+            s = fmaf(k4.x, dm[4 * q4], s);
+            s = fmaf(k4.y, dm[4 * q4 + 1], s);
+            s = fmaf(k4.z, dm[4 * q4 + 2], s);
+            s = fmaf(k4.w, dm[4 * q4 + 3], s);
+          }
         }
-        // the mat-vec takes the stored (rounded) checkpoint values
-        st_cols<ST, 4>(gtile + (size_t)r0 * DV + col, s0);
-        st_cols<ST, 4>(gtile + (size_t)(r0 + 1) * DV + col, s1);
+        // the mat-vec takes the stored (rounded) checkpoint value
+        s = st_store<ST>(gtile + (size_t)row * DV + col, s);
+        matvec_row<NV>(xh + row * NV, s, y);
       }
-      Tf32 xb[NTN][2];
-      if constexpr (NTN == 2) {
-        const float4 x4 = reinterpret_cast<const float4*>(xf)[fi];
-        xb[0][0] = tf32_split<EXACT_X>(x4.x);
-        xb[0][1] = tf32_split<EXACT_X>(x4.y);
-        xb[NTN - 1][0] = tf32_split<EXACT_X>(x4.z);
-        xb[NTN - 1][1] = tf32_split<EXACT_X>(x4.w);
-      } else {
-        const float2 x2 = reinterpret_cast<const float2*>(xf)[fi];
-        xb[0][0] = tf32_split<EXACT_X>(x2.x);
-        xb[0][1] = tf32_split<EXACT_X>(x2.y);
-      }
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const int h2 = 2 * mt;
-        const Tf32 af[4] = {tf32_split<EXACT_S>(s0[h2]), tf32_split<EXACT_S>(s0[h2 + 1]),
-                            tf32_split<EXACT_S>(s1[h2]), tf32_split<EXACT_S>(s1[h2 + 1])};
-#pragma unroll
-        for (int nt = 0; nt < NTN; ++nt) {
-          float(&c)[4] = *reinterpret_cast<float(*)[4]>(&y[4 * (NTN * mt + nt)]);
-          mma_split<EXACT_S, EXACT_X>(c, af, xb[nt]);
-        }
+    } else {
+#pragma unroll 8
+      for (int u = 0; u < CR; ++u) {
+        const int row = j * CR + u;
+        matvec_row<NV>(xh + row * NV, st_load<ST>(stg + (size_t)u * DV), y);
       }
     }
     __syncwarp();
@@ -200,24 +197,106 @@ __device__ __forceinline__ bool pipe_stream(const PipeItem& I, const ST* ring, u
   if (!fold && n > 0) {
     // replayed state of a window that does not fold: e^Gam S0^T x + sum_m f_m d_m (k_m . x)
 #pragma unroll
-    for (int e = 0; e < 16; ++e) y[e] *= decay;
+    for (int v = 0; v < NV; ++v) y[v] *= decay;
 #pragma unroll
-    for (int kq = 0; kq < 2; ++kq) {
-      if (kq < nkq) {
+    for (int m = 0; m < kPipeHist; ++m) {
+      if (m < n) {
 #pragma unroll
-        for (int nt = 0; nt < NTN; ++nt) {
-          const Tf32 hb[2] = {tf32_split<false>(hh[(8 * kq + t) * kPipeHist + 8 * nt + g]),
-                              tf32_split<false>(hh[(8 * kq + t + 4) * kPipeHist + 8 * nt + g])};
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            float(&c)[4] = *reinterpret_cast<float(*)[4]>(&y[4 * (NTN * mt + nt)]);
-            mma_split<false, false>(c, df[mt][kq], hb);
-          }
-        }
+        for (int v = 0; v < NV; ++v) y[v] = fmaf(hh[m * NV + v], dm[m], y[v]);
       }
     }
   }
   return true;
+}
+
+// The items of one CTA: item k is (row, value head) number b0 + k P of the
+// launch's order (rows as ranked, value heads fastest).
+struct PipeItems {
+  const int* order;
+  int b0, P, HV;
+  __device__ __forceinline__ void at(int k, int& row, int& h) const {
+    const int i = b0 + k * P;
+    row = order[i / HV];
+    h = i - (i / HV) * HV;
+  }
+};
+
+// Copies of item k's window into buffer k & 1: q, k, v rows, and the
+// history's keys, deltas and gates; copying thread pp of NP takes the 16-byte
+// pieces pp, pp + NP, ... of the whole list, then arrives on the buffer's
+// barrier once its copies have landed. The thread that withholds its arrival
+// (test hook) leaves the barrier one arrival short.
+template <int NP>
+__device__ __forceinline__ void pipe_copy_window(const ReplayParams& p, const PipeSmem& sm,
+                                                 unsigned char* smem, uint64_t* mb,
+                                                 const PipeItems& it, const int* r_slot,
+                                                 const int* r_cur, int k, int pp) {
+  constexpr int DK = kPipeDK, DV = kPipeDV;
+  int row, h;
+  it.at(k, row, h);
+  const int T = p.T, L = p.L, HV = p.HV;
+  const int b = k & 1, s = r_slot[row], n = r_cur[row];
+  const size_t tok0 = (size_t)row * T;
+  const int kh = h / p.G;
+  const uint32_t qrow = (uint32_t)(DK * dtype_bytes(p.in_dt));
+  unsigned char* wr = smem + sm.buf + b * sm.bufsz + sm.wraw;
+  const int sk = dtype_bytes(p.rk_dt), sd = dtype_bytes(p.rd_dt);
+  const int rowp = (int)(qrow / 16);  // pieces of one q, k or v row
+  const int nwin = 3 * T * rowp;
+  const int nkey = n * DK * sk / 16, ndel = n * DV * sd / 16, ngat = n > 0 ? round4(n) / 4 : 0;
+  const size_t sh = (size_t)s * HV + h;
+  const char* kbase = static_cast<const char*>(p.ring_k) + sh * L * DK * sk;
+  const char* dbase = static_cast<const char*>(p.ring_d) + sh * L * DV * sd;
+  const char* gbase = reinterpret_cast<const char*>(p.ring_g + sh * L);
+  for (int e = pp; e < nwin + nkey + ndel + ngat; e += NP) {
+    if (e < nwin) {
+      const int r3 = e / rowp, off = (e - r3 * rowp) * 16;  // row r3 of [q | k | v][T]
+      const int which = r3 / T, i = r3 - which * T;
+      const char* src;
+      if (which == 2) {
+        src = static_cast<const char*>(p.v) + ((tok0 + i) * HV + h) * (size_t)qrow;
+      } else {
+        src = static_cast<const char*>(which == 0 ? p.q : p.k) +
+              ((tok0 + i) * p.HK + kh) * (size_t)qrow;
+      }
+      cp_async16(wr + r3 * qrow + off, src + off);
+    } else if (e < nwin + nkey) {
+      const int off = (e - nwin) * 16;
+      cp_async16(smem + sm.buf + b * sm.bufsz + sm.hkr + off, kbase + off);
+    } else if (e < nwin + nkey + ndel) {
+      const int off = (e - nwin - nkey) * 16;
+      cp_async16(smem + sm.buf + b * sm.bufsz + sm.hdr + off, dbase + off);
+    } else {
+      const int off = (e - nwin - nkey - ndel) * 16;
+      cp_async16(smem + sm.buf + b * sm.bufsz + sm.hgr + off, gbase + off);
+    }
+  }
+  const bool held = k == 0 && pp == 0 &&
+                    (p.hook.withhold == WH_WINDOW || (n > 0 && p.hook.withhold == WH_HIST));
+  if (!held) cp_async_arrive(&mb[PB_WIN + b]);
+}
+
+// Chunk qq of the CTA's stream (chunk qq % NCH of item qq / NCH) into ring
+// stage qq % NS, copying thread pp's share of its 16-byte pieces.
+template <typename ST, int NP>
+__device__ __forceinline__ void pipe_copy_chunk(const ReplayParams& p, const PipeSmem& sm,
+                                                unsigned char* smem, uint64_t* mb,
+                                                const PipeItems& it, const int* r_slot, int qq,
+                                                int pp) {
+  constexpr int DK = kPipeDK, DV = kPipeDV;
+  constexpr int NCH = DK * DV * (int)sizeof(ST) / kChunkBytes;
+  const int k = qq / NCH, j = qq - k * NCH;
+  int row, h;
+  it.at(k, row, h);
+  const char* src = reinterpret_cast<const char*>(static_cast<const ST*>(p.state) +
+                                                  ((size_t)r_slot[row] * p.HV + h) * DK * DV) +
+                    (size_t)j * kChunkBytes;
+  const int st = qq % sm.ns;
+  unsigned char* dst = smem + sm.ring + (size_t)st * kChunkBytes;
+#pragma unroll
+  for (int e = pp; e < kChunkBytes / 16; e += NP) cp_async16(dst + e * 16, src + e * 16);
+  const bool held = k == 0 && pp == 0 && p.hook.withhold == WH_CHUNK0 + j;
+  if (!held) cp_async_arrive(&mb[PB_FULL + st]);
 }
 
 // ---------------------------------------------------------------- kernel
@@ -225,10 +304,10 @@ template <int ALGO, typename ST, int NT>
 __global__ void __launch_bounds__(kPipeThreads, 1)
     pipe_kernel(const ReplayParams p, const PipeSmem sm) {
   static_assert(ALGO == ALGO_GDN, "the pipelined kernel serves GDN heads");
-  constexpr int DK = kPipeDK, DV = kPipeDV, NTN = pipe_ntn(NT), NV = 2 * NT;
+  constexpr int DK = kPipeDK, DV = kPipeDV, NV = 2 * NT;
   constexpr int CR = kChunkBytes / (DV * (int)sizeof(ST));
   constexpr int NCH = DK / CR;
-  constexpr int PT = 32 * kPipePrep;       // prep threads
+  constexpr int PT = 32 * kPipePrep;       // prep threads (one per value column)
   constexpr int kPrepBar = 1;              // named barrier of the prep warps
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -244,15 +323,16 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   int* gcnt = r_flag + sm.maxb;  // [2][kPipeGroups]: folding / other live rows per group
   ST* ring = reinterpret_cast<ST*>(smem + sm.ring);
 
+  constexpr int NP = 32 * kPipeProdWarps;  // copying threads
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&mb[PB_WIN + b], 1);
+      mbar_init(&mb[PB_WIN + b], NP);
       mbar_init(&mb[PB_PREP + b], 1);
       mbar_init(&mb[PB_MATH + b], kPipeMath);
       mbar_init(&mb[PB_YFREE + b], 1);
     }
     for (int st = 0; st < NS; ++st) {
-      mbar_init(&mb[PB_FULL + st], 1);
+      mbar_init(&mb[PB_FULL + st], NP);
       mbar_init(&mb[PB_FULL + NS + st], kPipeMath);
     }
     *abort = 0;
@@ -315,53 +395,75 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   const int n_items = nlive * HV;
   const int P = gridDim.x, b0 = blockIdx.x;
   const int nk = b0 < n_items ? (n_items - b0 + P - 1) / P : 0;
-  auto item_of = [&](int k, int& row, int& h) {
-    const int i = b0 + k * P;
-    row = r_order[i / HV];
-    h = i - (i / HV) * HV;
-  };
+  const PipeItems items{r_order, b0, P, HV};
+  const int pt = tid - 32 * kPipeMath;  // prep thread (negative on the math warps)
+  const int s_in = dtype_bytes(p.in_dt);
+  const uint32_t qrow = (uint32_t)(DK * s_in);
+  const int nq = nk * NCH;  // chunks of this CTA's stream
+  // the window betas and gates of every item of this CTA, staged once: the
+  // prep warps then read no global memory on their critical path
+  float2* bgt = reinterpret_cast<float2*>(smem + sm.bg);
+  for (int e = tid; e < nk * T; e += kPipeThreads) {
+    const int k = e / T, i = e - k * T;
+    int row, h;
+    items.at(k, row, h);
+    const size_t ix = ((size_t)row * T + i) * HV + h;
+    bgt[k * NT + i] = make_float2(p.beta[ix], p.g[ix]);
+  }
+  __syncthreads();
 
-  if (warp == kPipeProd) {
-    // ================= producer: checkpoint chunks of every item, in order
-    int q = 0;
-    if (lane == 0) {
-      bool ok = true;
-      for (int k = 0; ok && k < nk; ++k) {
-        int row, h;
-        item_of(k, row, h);
-        const ST* tile = static_cast<const ST*>(p.state) + ((size_t)r_slot[row] * HV + h) * DK * DV;
-        for (int j = 0; j < NCH; ++j) {
-          const int st = q % NS;
-          if (q >= NS &&
-              !pipe_wait(&mb[PB_FULL + NS + st], (uint32_t)(((q / NS) - 1) & 1), lim, abort)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(&mb[PB_FULL + st],
-                         (uint32_t)kChunkBytes + (k == 0 ? p.hook.extra(WH_CHUNK0 + j) : 0u));
-          bulk_g2s(ring + (size_t)st * CR * DV, tile + (size_t)j * CR * DV, kChunkBytes,
-                   &mb[PB_FULL + st]);
-          ++q;
-        }
+  if (warp >= kPipeProd) {
+    // ================= copying threads: every async copy, as its buffer frees
+    const int pp = tid - 32 * kPipeProd;
+    int kw = 0, qq = 0;  // windows and chunks issued
+    unsigned long long t_last = global_ns();
+    while (kw < nk || qq < nq) {
+      bool progress = false;
+      // window and history rows of item kw into buffer kw & 1, once item kw - 2
+      // (the buffer's last user) is prepared
+      while (kw < nk && (kw < 2 || mbar_test(&mb[PB_PREP + (kw & 1)],
+                                             (uint32_t)(((kw - 2) >> 1) & 1)))) {
+        pipe_copy_window<NP>(p, sm, smem, mb, items, r_slot, r_cur, kw++, pp);
+        progress = true;
       }
-      if (!ok && !*abort) {
-        *abort = 1;
-        atomicOr(p.err, DEVERR_TIMEOUT);
+      // every chunk whose stage is free, each once the chunk NS before it is released
+      while (qq < nq && (qq < NS || mbar_test(&mb[PB_FULL + NS + qq % NS],
+                                              (uint32_t)(((qq / NS) - 1) & 1)))) {
+        pipe_copy_chunk<ST, NP>(p, sm, smem, mb, items, r_slot, qq++, pp);
+        progress = true;
+      }
+      if (progress) {
+        t_last = global_ns();
+        continue;
+      }
+      if (*abort) break;
+      if (global_ns() - t_last > lim) {
+        if (!*abort) {
+          *abort = 1;
+          atomicOr(p.err, DEVERR_TIMEOUT);
+        }
+        break;
+      }
+      // park until the next stage is released (or the window buffer frees, the
+      // next time round)
+      if (qq < nq) {
+        mbar_try_wait_hint(&mb[PB_FULL + NS + qq % NS], (uint32_t)(((qq / NS) - 1) & 1),
+                           kPipeParkNs);
+      } else {
+        mbar_try_wait_hint(&mb[PB_PREP + (kw & 1)], (uint32_t)(((kw - 2) >> 1) & 1),
+                           kPipeParkNs);
       }
     }
+    // every copy this thread issued has landed before the CTA leaves
+    cp_async_wait_all();
     __syncwarp();
     __syncthreads();
-    // every chunk issued has landed before the CTA leaves (bounded)
-    if (lane == 0) {
-      for (int qq = q > NS ? q - NS : 0; qq < q; ++qq)
-        mbar_wait_bounded(&mb[PB_FULL + qq % NS], (uint32_t)((qq / NS) & 1), lim);
-    }
     return;
   }
 
   if (warp < kPipeMath) {
-    // ================= math: stream every item's tile on the tensor cores
-    const bool xk = p.in_dt != DT_F32, kk = p.rk_dt != DT_F32;
+    // ================= math: stream every item's tile, one value column per thread
+    const int col = tid;
     int q = 0;
     for (int k = 0; k < nk; ++k) {
       const int b = k & 1;
@@ -372,25 +474,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         }
         break;
       }
-      const PipeItem& I = *reinterpret_cast<const PipeItem*>(smem + sm.item[b]);
+      const PipeItem& I = *reinterpret_cast<const PipeItem*>(smem + sm.buf + b * sm.bufsz + sm.item);
       ST* gtile = static_cast<ST*>(p.state) + ((size_t)I.s * HV + I.h) * DK * DV;
-      const float* xf = reinterpret_cast<const float*>(smem + sm.xf[b]);
-      const float* kf = reinterpret_cast<const float*>(smem + sm.kf[b]);
-      const float* dfp = reinterpret_cast<const float*>(smem + sm.df[b]);
-      const float* hh = reinterpret_cast<const float*>(smem + sm.hh[b]);
-      float y[16];
-      bool ok;
-      if (xk) {
-        ok = kk ? pipe_stream<ST, NTN, true, true>(I, ring, mb, NS, q, xf, kf, dfp, hh, gtile, lim,
-                                                   abort, warp, lane, y)
-                : pipe_stream<ST, NTN, true, false>(I, ring, mb, NS, q, xf, kf, dfp, hh, gtile,
-                                                    lim, abort, warp, lane, y);
-      } else {
-        ok = kk ? pipe_stream<ST, NTN, false, true>(I, ring, mb, NS, q, xf, kf, dfp, hh, gtile,
-                                                    lim, abort, warp, lane, y)
-                : pipe_stream<ST, NTN, false, false>(I, ring, mb, NS, q, xf, kf, dfp, hh, gtile,
-                                                     lim, abort, warp, lane, y);
-      }
+      float y[NV];
+      bool ok = pipe_stream<ST, NV>(
+          I, ring, mb, NS, q, reinterpret_cast<const float*>(smem + sm.buf + b * sm.bufsz + sm.xh),
+          reinterpret_cast<const float*>(smem + sm.buf + b * sm.bufsz + sm.hkt),
+          reinterpret_cast<const float*>(smem + sm.buf + b * sm.bufsz + sm.dt),
+          reinterpret_cast<const float*>(smem + sm.buf + b * sm.bufsz + sm.hh), gtile, lim, abort, col, lane, y);
       q += NCH;
       // the column sums of item k - 2 (same buffer) have been read
       if (ok && k >= 2)
@@ -403,67 +494,19 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         }
         break;
       }
-      float* yo = reinterpret_cast<float*>(smem + sm.y[b]);
-      const int g = lane >> 2, t = lane & 3;
+      float* yo = reinterpret_cast<float*>(smem + sm.buf + b * sm.bufsz + sm.y);
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-        for (int nt = 0; nt < NTN; ++nt) {
-          const int c0 = 32 * warp + 4 * g + 2 * mt, v = 8 * nt + 2 * t;
-          const float* c = &y[4 * (NTN * mt + nt)];
-          if (v < NV) {
-            yo[v * DV + c0] = c[0];
-            yo[v * DV + c0 + 1] = c[2];
-          }
-          if (v + 1 < NV) {
-            yo[(v + 1) * DV + c0] = c[1];
-            yo[(v + 1) * DV + c0 + 1] = c[3];
-          }
-        }
-      }
+      for (int v = 0; v < NV; ++v) yo[v * DV + col] = y[v];
       __syncwarp();
       if (lane == 0) mbar_arrive(&mb[PB_MATH + b]);
     }
+    __syncwarp();
     __syncthreads();
     return;
   }
 
   // ================= prep warps: prepare item k, solve item k - 1
-  const int pt = tid - 32 * kPipeMath, pw = pt >> 5;
-  const int s_in = dtype_bytes(p.in_dt);
-  const uint32_t qrow = (uint32_t)(DK * s_in);
-  int kw = 0;  // windows issued (by prep thread 0)
-  auto issue_window = [&](int k) {
-    int row, h;
-    item_of(k, row, h);
-    const int b = k & 1, s = r_slot[row], n = r_cur[row];
-    const size_t tok0 = (size_t)row * T;
-    const int kh = h / p.G;
-    unsigned char* wr = smem + sm.wraw[b];
-    const int sk = dtype_bytes(p.rk_dt), sd = dtype_bytes(p.rd_dt);
-    uint32_t bytes = 2u * T * qrow;
-    if (n > 0) bytes += (uint32_t)(n * (DK * sk + DV * sd) + 4 * round4(n));
-    const uint32_t extra =
-        k == 0 ? p.hook.extra(WH_WINDOW) + (n > 0 ? p.hook.extra(WH_HIST) : 0u) : 0u;
-    mbar_expect_tx(&mb[PB_WIN + b], bytes + extra);
-    for (int i = 0; i < T; ++i) {
-      const size_t off = ((tok0 + i) * p.HK + kh) * (size_t)qrow;
-      bulk_g2s(wr + i * qrow, static_cast<const char*>(p.q) + off, qrow, &mb[PB_WIN + b]);
-      bulk_g2s(wr + (T + i) * qrow, static_cast<const char*>(p.k) + off, qrow, &mb[PB_WIN + b]);
-    }
-    if (n > 0) {
-      const size_t sh = (size_t)s * HV + h;
-      bulk_g2s(smem + sm.hkr[b], static_cast<const char*>(p.ring_k) + sh * L * DK * sk,
-               (uint32_t)(n * DK * sk), &mb[PB_WIN + b]);
-      bulk_g2s(smem + sm.hdr[b], static_cast<const char*>(p.ring_d) + sh * L * DV * sd,
-               (uint32_t)(n * DV * sd), &mb[PB_WIN + b]);
-      bulk_g2s(smem + sm.hgr[b], p.ring_g + sh * L, (uint32_t)(4 * round4(n)), &mb[PB_WIN + b]);
-    }
-  };
-  if (pt == 0) {
-    for (; kw < 2 && kw < nk; ++kw) issue_window(kw);
-  }
-  __syncwarp();
+  const int pw = pt >> 5;
   bool alive = true;  // no wait of the prep warps has run out
   int nprep = 0;      // items prepared (handed to the math warps)
   for (int k = 0; k <= nk; ++k) {
@@ -471,16 +514,16 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     if (named_and(kPrepBar, PT, alive && k < nk && !*abort)) {
       const int b = k & 1;
       int row, h;
-      item_of(k, row, h);
+      items.at(k, row, h);
       const int s = r_slot[row], c = r_cur[row];
       const bool fold = (r_flag[row] & PF_FOLD) != 0;
       const int n = c;
-      const size_t tok0 = (size_t)row * T;
-      PipeItem& I = *reinterpret_cast<PipeItem*>(smem + sm.item[b]);
+      PipeItem& I = *reinterpret_cast<PipeItem*>(smem + sm.buf + b * sm.bufsz + sm.item);
       float bet = 0.f, gw = 0.f;
       if (pt < T) {
-        bet = p.beta[(tok0 + pt) * HV + h];
-        gw = p.g[(tok0 + pt) * HV + h];
+        const float2 e = bgt[k * NT + pt];
+        bet = e.x;
+        gw = e.y;
       }
       const bool landed = named_and(kPrepBar, PT,
                                     pipe_wait(&mb[PB_WIN + b], (uint32_t)((k >> 1) & 1), lim,
@@ -493,13 +536,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         __syncwarp();
         alive = false;
       } else {
-        const unsigned char* wr = smem + sm.wraw[b];
+        const unsigned char* wr = smem + sm.buf + b * sm.bufsz + sm.wraw;
         const void* wq = wr;                      // q rows [T][dk]
         const void* wkr = wr + T * qrow;          // k rows [T][dk]
-        float* xf = reinterpret_cast<float*>(smem + sm.xf[b]);
+        float* xh = reinterpret_cast<float*>(smem + sm.buf + b * sm.bufsz + sm.xh);
+        const int ch = pt;                        // key channel / value column of this thread
         // P1 (prep warp 0): gates, item scalars
         if (pw == 0) {
-          const float* hg = reinterpret_cast<const float*>(smem + sm.hgr[b]);
+          const float* hg = reinterpret_cast<const float*>(smem + sm.buf + b * sm.bufsz + sm.hgr);
           // history: hf[m] = e^{sum_{m' > m} g_m'} (n <= 16 records: one pass)
           const int m = n - 1 - lane;
           float incl = (m >= 0) ? hg[m] : 0.f;
@@ -537,116 +581,99 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             I.egam = __expf(gam);
           }
         }
-        // P2 (all prep threads): mat-vec inputs in fragment order
-        for (int e = pt; e < DK * 8 * NTN; e += PT) {
-          int ch, v;
-          x_slot<NTN>(e, ch, v);
-          const int i = v < NT ? v : v - NT;
-          float x = 0.f;
-          if (v < NV && i < T) x = ld_f32(v < NT ? wkr : wq, (size_t)i * DK + ch, p.in_dt);
-          xf[e] = x;
+        // P2 (thread = key channel): the window's k and v rows kept for the
+        // solve (the landing buffer takes item k + 2's copies), the mat-vec
+        // inputs of this channel, and its history keys transposed
+        {
+          const uint4* src = reinterpret_cast<const uint4*>(wkr);
+          uint4* dst = reinterpret_cast<uint4*>(smem + sm.buf + b * sm.bufsz + sm.ep);
+          for (int e = pt; e < (int)(2 * T * qrow / 16); e += PT) dst[e] = src[e];
+        }
+        {
+          float xv[NV];
+#pragma unroll
+          for (int i = 0; i < NT; ++i) {
+            xv[i] = i < T ? ld_f32(wkr, (size_t)i * DK + ch, p.in_dt) : 0.f;
+            xv[NT + i] = i < T ? ld_f32(wq, (size_t)i * DK + ch, p.in_dt) : 0.f;
+          }
+          float* xr = xh + ch * NV;
+#pragma unroll
+          for (int v = 0; v < NV; ++v) xr[v] = xv[v];
+        }
+        if (fold && n > 0) {
+          const void* hk = smem + sm.buf + b * sm.bufsz + sm.hkr;
+          float kt[kPipeHist];
+#pragma unroll
+          for (int m = 0; m < kPipeHist; ++m)
+            kt[m] = m < n ? ld_f32(hk, (size_t)m * DK + ch, p.rk_dt) : 0.f;
+          float4* kr = reinterpret_cast<float4*>(smem + sm.buf + b * sm.bufsz + sm.hkt) + ch * (kPipeHist / 4);
+#pragma unroll
+          for (int q4 = 0; q4 < kPipeHist / 4; ++q4)
+            kr[q4] = make_float4(kt[4 * q4], kt[4 * q4 + 1], kt[4 * q4 + 2], kt[4 * q4 + 3]);
         }
         named_sync(kPrepBar, PT);
-        // P3: window coefficients, one warp per pair (j <= i < T)
+        // P3: f_m d_m of this column (the fold's and the correction's deltas)
+        if (n > 0) {
+          const void* hd = smem + sm.buf + b * sm.bufsz + sm.hdr;
+          float* dtm = reinterpret_cast<float*>(smem + sm.buf + b * sm.bufsz + sm.dt);
+#pragma unroll
+          for (int m = 0; m < kPipeHist; ++m)
+            dtm[m * DV + ch] = m < n ? I.hf[m] * ld_f32(hd, (size_t)m * DV + ch, p.rd_dt) : 0.f;
+        }
+        // P4: window coefficients, two threads per pair (j <= i < T), half the
+        // key channels each
         {
-          int pi = 0;
-          for (int i = 0; i < T; ++i) {
-            for (int j = 0; j <= i; ++j, ++pi) {
-              if (pi % kPipePrep != pw) continue;
-              const float4 kj = ld4_as_f32(wkr, j * DK + 4 * lane, p.in_dt);
-              const float4 ki = ld4_as_f32(wkr, i * DK + 4 * lane, p.in_dt);
-              const float4 qi = ld4_as_f32(wq, i * DK + 4 * lane, p.in_dt);
-              float skk = fmaf(kj.x, ki.x, fmaf(kj.y, ki.y, fmaf(kj.z, ki.z, kj.w * ki.w)));
-              float skq = fmaf(kj.x, qi.x, fmaf(kj.y, qi.y, fmaf(kj.z, qi.z, kj.w * qi.w)));
-              skk = warp_sum(skk);
-              skq = warp_sum(skq);
-              if (lane == 0) {
-                const float wgt = __expf(I.G[i] - I.G[j]);
-                I.fm[i * kPipeMaxNT + j] = wgt * skq;
-                I.am[i * kPipeMaxNT + j] = j < i ? I.beta[i] * wgt * skk : 0.f;
+          const int pr2 = pt >> 1, half = pt & 1;
+          const int i = pr2 / kPipeMaxNT, j = pr2 - i * kPipeMaxNT;
+          float skk = 0.f, skq = 0.f;
+          if (i < T && j <= i) {
+            for (int c8 = 64 * half; c8 < 64 * half + 64; c8 += 8) {
+              float kj[8], ki[8], qi[8];
+              ld8_as_f32(wkr, j * DK + c8, p.in_dt, kj);
+              ld8_as_f32(wkr, i * DK + c8, p.in_dt, ki);
+              ld8_as_f32(wq, i * DK + c8, p.in_dt, qi);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                skk = fmaf(kj[e], ki[e], skk);
+                skq = fmaf(kj[e], qi[e], skq);
               }
             }
           }
-        }
-        // P4: history operands. f_m d_m in the math lanes' A-fragment order
-        if (n > 0) {
-          float* dfp = reinterpret_cast<float*>(smem + sm.df[b]);
-          const void* hd = smem + sm.hdr[b];
-          const int w = pt >> 5, l = pt & 31, g = l >> 2, t = l & 3;
-          float v16[16];
-#pragma unroll
-          for (int mk = 0; mk < 4; ++mk) {
-            const int mt = mk >> 1, kq = mk & 1, c0 = 32 * w + 4 * g + 2 * mt;
-            const int m0 = 8 * kq + t, m1 = m0 + 4;
-            float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
-            if (m0 < n) d0 = ld2_as_f32(hd, m0 * DV + c0, p.rd_dt);
-            if (m1 < n) d1 = ld2_as_f32(hd, m1 * DV + c0, p.rd_dt);
-            const float f0 = m0 < n ? I.hf[m0] : 0.f, f1 = m1 < n ? I.hf[m1] : 0.f;
-            v16[4 * mk + 0] = f0 * d0.x;
-            v16[4 * mk + 1] = f0 * d0.y;
-            v16[4 * mk + 2] = f1 * d1.x;
-            v16[4 * mk + 3] = f1 * d1.y;
+          skk += __shfl_xor_sync(kFull, skk, 1);
+          skq += __shfl_xor_sync(kFull, skq, 1);
+          if (half == 0 && i < T && j <= i) {
+            const float wgt = __expf(I.G[i] - I.G[j]);
+            I.fm[i * kPipeMaxNT + j] = wgt * skq;
+            I.am[i * kPipeMaxNT + j] = j < i ? I.beta[i] * wgt * skk : 0.f;
           }
-          float4* o4 = reinterpret_cast<float4*>(dfp) + pt * 4;
+        }
+        // P5: history dots k_m . x_v of a window that does not fold, one
+        // thread per (record, pair of vectors)
+        if (!fold && n > 0) {
+          const void* hk = smem + sm.buf + b * sm.bufsz + sm.hkr;
+          float* hh = reinterpret_cast<float*>(smem + sm.buf + b * sm.bufsz + sm.hh);
+          constexpr int VP = NV / 2;  // vector pairs
+          for (int o = pt; o < kPipeHist * VP; o += PT) {
+            const int m = o / VP, v0 = 2 * (o - m * VP);
+            float a0 = 0.f, a1 = 0.f;
+            if (m < n) {
+              for (int c8 = 0; c8 < DK; c8 += 8) {
+                float km[8];
+                ld8_as_f32(hk, m * DK + c8, p.rk_dt, km);
 #pragma unroll
-          for (int mk = 0; mk < 4; ++mk)
-            o4[mk] = make_float4(v16[4 * mk], v16[4 * mk + 1], v16[4 * mk + 2], v16[4 * mk + 3]);
-          if (fold) {
-            // fold keys in the B-fragment order of the tile rows
-            frag_keys16(reinterpret_cast<float*>(smem + sm.kf[b]), smem + sm.hkr[b], n, DK,
-                        p.rk_dt, pt, PT);
-          } else if (pw == kPipePrep - 1) {
-            // history dots H[m][v] = k_m . x_v on the tensor cores: records as m,
-            // window vectors as n, key channels as k (relabelled as in x_slot)
-            const void* hk = smem + sm.hkr[b];
-            const bool xk = p.in_dt != DT_F32, kk = p.rk_dt != DT_F32;
-            const int g = lane >> 2, t = lane & 3;
-            float hc[NTN][4];
-#pragma unroll
-            for (int nt = 0; nt < NTN; ++nt) hc[nt][0] = hc[nt][1] = hc[nt][2] = hc[nt][3] = 0.f;
-            for (int s8 = 0; s8 < DK / 8; ++s8) {
-              const int ch = 8 * s8 + 2 * t;
-              float2 ka = make_float2(0.f, 0.f), kb = make_float2(0.f, 0.f);
-              if (g < n) ka = ld2_as_f32(hk, g * DK + ch, p.rk_dt);
-              if (g + 8 < n) kb = ld2_as_f32(hk, (g + 8) * DK + ch, p.rk_dt);
-              const int fi = s8 * 32 + lane;
-#pragma unroll
-              for (int nt = 0; nt < NTN; ++nt) {
-                const float x0 = xf[2 * NTN * fi + 2 * nt], x1 = xf[2 * NTN * fi + 2 * nt + 1];
-                if (kk && xk) {
-                  const Tf32 a[4] = {tf32_split<true>(ka.x), tf32_split<true>(kb.x),
-                                     tf32_split<true>(ka.y), tf32_split<true>(kb.y)};
-                  const Tf32 bb[2] = {tf32_split<true>(x0), tf32_split<true>(x1)};
-                  mma_split<true, true>(hc[nt], a, bb);
-                } else {
-                  const Tf32 a[4] = {tf32_split<false>(ka.x), tf32_split<false>(kb.x),
-                                     tf32_split<false>(ka.y), tf32_split<false>(kb.y)};
-                  const Tf32 bb[2] = {tf32_split<false>(x0), tf32_split<false>(x1)};
-                  mma_split<false, false>(hc[nt], a, bb);
+                for (int e = 0; e < 8; ++e) {
+                  const float2 x = *reinterpret_cast<const float2*>(xh + (c8 + e) * NV + v0);
+                  a0 = fmaf(km[e], x.x, a0);
+                  a1 = fmaf(km[e], x.y, a1);
                 }
               }
             }
-            float* hh = reinterpret_cast<float*>(smem + sm.hh[b]);
-#pragma unroll
-            for (int nt = 0; nt < NTN; ++nt) {
-              hh[g * kPipeHist + 8 * nt + 2 * t] = hc[nt][0];
-              hh[g * kPipeHist + 8 * nt + 2 * t + 1] = hc[nt][1];
-              hh[(g + 8) * kPipeHist + 8 * nt + 2 * t] = hc[nt][2];
-              hh[(g + 8) * kPipeHist + 8 * nt + 2 * t + 1] = hc[nt][3];
-            }
-            if (NTN == 1) {
-              hh[g * kPipeHist + 8 + 2 * t] = 0.f;
-              hh[g * kPipeHist + 8 + 2 * t + 1] = 0.f;
-              hh[(g + 8) * kPipeHist + 8 + 2 * t] = 0.f;
-              hh[(g + 8) * kPipeHist + 8 + 2 * t + 1] = 0.f;
-            }
+            hh[m * NV + v0] = a0;
+            hh[m * NV + v0 + 1] = a1;
           }
         }
         named_sync(kPrepBar, PT);
-        if (pt == 0) {
-          if (kw < nk) issue_window(kw++);  // into the buffer item k's copies used
-          mbar_arrive(&mb[PB_PREP + b]);
-        }
+        if (pt == 0) mbar_arrive(&mb[PB_PREP + b]);  // (frees the landing buffer too)
         __syncwarp();
         nprep = k + 1;
       }
@@ -665,8 +692,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         alive = false;
         nprep = 0;
       } else {
-        const PipeItem& I = *reinterpret_cast<const PipeItem*>(smem + sm.item[b]);
-        const float* yo = reinterpret_cast<const float*>(smem + sm.y[b]);
+        const PipeItem& I = *reinterpret_cast<const PipeItem*>(smem + sm.buf + b * sm.bufsz + sm.item);
+        const float* yo = reinterpret_cast<const float*>(smem + sm.buf + b * sm.bufsz + sm.y);
+        const void* ek = smem + sm.buf + b * sm.bufsz + sm.ep;               // k rows [T][dk]
+        const void* ev = smem + sm.buf + b * sm.bufsz + sm.ep + T * qrow;    // v rows [T][dv]
         const int row = I.row, h = I.h, s = I.s, base = I.base;
         const size_t tok0 = (size_t)row * T;
         const size_t sh = (size_t)s * HV + h;
@@ -681,7 +710,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
           if (i < T) {
             const float eg = I.eG[i];
             const size_t tok = tok0 + i;
-            const float vi = ld_f32(p.v, (tok * HV + h) * DV + col, p.in_dt);
+            const float vi = ld_f32(ev, (size_t)i * DV + col, p.in_dt);
             float a = I.beta[i] * (vi - eg * y[i]);
 #pragma unroll
             for (int j = 0; j < i; ++j) a = fmaf(-I.am[i * kPipeMaxNT + j], d[j], a);
@@ -693,13 +722,13 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             const size_t rec = (sh * L + base + i) * DV + col;
             st_f32(p.ring_d, rec, p.rd_dt, a);
             st_f32(p.ring_v, rec, p.in_dt, vi);
-            const float kv = ld_f32(p.k, (tok * p.HK + h / p.G) * DK + col, p.in_dt);
+            const float kv = ld_f32(ek, (size_t)i * DK + col, p.in_dt);
             st_f32(p.ring_k, (sh * L + base + i) * DK + col, p.rk_dt, kv);
           }
         }
         if (pt < T) {
           p.ring_beta[sh * L + base + pt] = I.beta[pt];
-          p.ring_g[sh * L + base + pt] = p.g[(tok0 + pt) * HV + h];
+          p.ring_g[sh * L + base + pt] = bgt[kp * NT + pt].y;
         }
         if (pt == 0 && h == 0 && p.fold_out != nullptr) p.fold_out[row] = (uint8_t)I.fold;
         named_sync(kPrepBar, PT);  // the column sums are read
@@ -709,11 +738,6 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     }
   }
   __syncthreads();
-  // the window copies issued have landed before the CTA leaves (bounded)
-  if (pt == 0) {
-    for (int kk2 = kw > 2 ? kw - 2 : 0; kk2 < kw; ++kk2)
-      mbar_wait_bounded(&mb[PB_WIN + (kk2 & 1)], (uint32_t)((kk2 >> 1) & 1), lim);
-  }
 }
 
 }  // namespace rssm

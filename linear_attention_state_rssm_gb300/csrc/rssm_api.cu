@@ -209,11 +209,12 @@ rssm_status window(rssm_handle* h, int32_t layer, const void* q, const void* k, 
   if (cu == nullptr && h->plan == RSSM_PLAN_PIPE && h->pipe_cfg && T <= kPipeMaxNT &&
       B <= kPipeMaxRows) {
     const int NT = pipe_nt(T);
+    const long long items = (long long)B * c.HV;
+    const int grid = (int)(items < h->num_sms ? items : h->num_sms);
+    const int nkmax = (int)((items + grid - 1) / grid);
     const PipeSmem sm = pipe_layout(NT, B, c.dk, c.dv, c.in_dtype, c.ring_k_dtype,
-                                    c.ring_d_dtype, h->max_smem);
+                                    c.ring_d_dtype, h->max_smem, nkmax);
     if (sm.ns >= 4) {
-      const long long items = (long long)B * c.HV;
-      const int grid = (int)(items < h->num_sms ? items : h->num_sms);
       return from_cuda(pipe_launch(state_dt(c), NT, p, sm, grid, static_cast<cudaStream_t>(stream)));
     }
   }

@@ -390,13 +390,15 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
 
 // ----------------------------------------------------------- pipelined replay
 // Persistent replay kernel (pipe_impl.cuh): one CTA per SM walks a list of
-// (row, value head) items. Warps 0-3 stream the checkpoint tiles on the tensor
-// cores, warps 4-7 prepare the next item and solve the previous one, warp 8
-// issues the checkpoint chunks into a ring that runs across items.
+// (row, value head) items. Warps 0-3 stream the checkpoint tiles, warps 4-7
+// prepare the next item and solve the previous one, warps 8-11 issue every
+// async copy (checkpoint chunks into a ring that runs across items, window
+// and history rows into two item buffers).
 constexpr int kPipeMath = 4;                       // warps streaming the tile
 constexpr int kPipePrep = 4;                       // warps preparing / solving items
-constexpr int kPipeProd = kPipeMath + kPipePrep;   // warp issuing the chunk copies
-constexpr int kPipeThreads = 32 * (kPipeProd + 1);
+constexpr int kPipeProd = kPipeMath + kPipePrep;   // first copy-issuing warp
+constexpr int kPipeProdWarps = 4;                  // copy-issuing warps
+constexpr int kPipeThreads = 32 * (kPipeProd + kPipeProdWarps);
 constexpr int kPipeMaxRows = 512;                  // request rows ranked in shared memory
 constexpr int kPipeMaxStages = 16;                 // chunk ring stages at most
 constexpr int kPipeHist = 16;                      // history records an item folds / corrects
@@ -417,49 +419,60 @@ struct PipeItem {
   float am[kPipeMaxNT * kPipeMaxNT], fm[kPipeMaxNT * kPipeMaxNT];
 };
 
+// Shared memory of the pipelined kernel. The two item buffers have the same
+// layout: buffer b starts at buf + b * bufsz and its arrays sit at the offsets
+// below within it (so a buffer is chosen by arithmetic, not by indexing a
+// kernel parameter, which would put the parameter block in local memory).
 struct PipeSmem {
   uint32_t ring;                 // ns stages of one 8 KB chunk
   uint32_t mbar;                 // kPipeMbars barriers, then the abort word
   uint32_t rows;                 // slot, cursor, order, flags [maxb] (int32), group counts
-  uint32_t item[2];              // PipeItem
-  uint32_t wraw[2];              // window q, k rows as stored [2][NT][dk]
-  uint32_t hkr[2];               // history keys as stored [16][dk]
-  uint32_t hdr[2];               // history deltas as stored [16][dv]
-  uint32_t hgr[2];               // history gates [16] fp32
-  uint32_t xf[2];                // mat-vec inputs in fragment order [dk][8 NTN]
-  uint32_t kf[2];                // fold keys in fragment order [dk][16]
-  uint32_t df[2];                // f_m d_m in A-fragment order [4 warps][32 lanes][16]
-  uint32_t hh[2];                // history dots k_m . x_v [16][16]
-  uint32_t y[2];                 // column sums [2 NT][dv]
+  uint32_t bg;                   // window beta and gate of every item of the CTA [nkmax][NT][2]
+  uint32_t buf, bufsz;           // item buffer 0, size of one buffer
+  uint32_t item;                 // PipeItem
+  uint32_t wraw;                 // window q, k, v rows as stored [3][NT][dk]
+  uint32_t ep;                   // window k, v rows kept for the solve [2][NT][dk]
+  uint32_t hkr;                  // history keys as stored [16][dk]
+  uint32_t hdr;                  // history deltas as stored [16][dv]
+  uint32_t hgr;                  // history gates [16] fp32
+  uint32_t xh;                   // mat-vec inputs [dk][2 NT] fp32 (k_i at i, q_i at NT + i)
+  uint32_t hkt;                  // history keys transposed [dk][16] fp32 (a fold)
+  uint32_t dt;                   // f_m d_m [16][dv] fp32
+  uint32_t hh;                   // history dots k_m . x_v [16][2 NT] fp32
+  uint32_t y;                    // column sums [2 NT][dv]
   uint32_t total;
   int ns;                        // ring stages
   int maxb;                      // rows the ranking tables hold (a multiple of 32, >= B)
+  int nkmax;                     // items of one CTA at most
 };
-
-__host__ __device__ constexpr int pipe_ntn(int NT) { return NT <= 4 ? 1 : 2; }
 
 // Layout for windows of up to NT tokens; the ring takes what is left of
 // max_smem (at most kPipeMaxStages stages). ns < 2 means it does not fit.
 __host__ __device__ inline PipeSmem pipe_layout(int NT, int B, int dk, int dv, int in_dt,
-                                                int rk_dt, int rd_dt, int max_smem) {
+                                                int rk_dt, int rd_dt, int max_smem, int nkmax) {
   PipeSmem m{};
-  const int ntn = pipe_ntn(NT);
+  const int nv = 2 * NT;
   m.maxb = (B + 31) & ~31;
+  m.nkmax = nkmax;
   uint32_t off = 0;
   m.mbar = off;  off = align16(off + 8u * kPipeMbars + 16u);
   m.rows = off;  off = align16(off + 16u * m.maxb + 8u * (kPipeMaxRows / 32));
-  for (int b = 0; b < 2; ++b) {
-    m.item[b] = off;  off = align16(off + (uint32_t)sizeof(PipeItem));
-    m.wraw[b] = off;  off = align16(off + 2u * NT * dk * dtype_bytes(in_dt));
-    m.hkr[b] = off;   off = align16(off + (uint32_t)(kPipeHist * dk * dtype_bytes(rk_dt)));
-    m.hdr[b] = off;   off = align16(off + (uint32_t)(kPipeHist * dv * dtype_bytes(rd_dt)));
-    m.hgr[b] = off;   off = align16(off + 4u * kPipeHist);
-    m.xf[b] = off;    off = align16(off + 4u * dk * 8 * ntn);
-    m.kf[b] = off;    off = align16(off + 4u * dk * kPipeHist);
-    m.df[b] = off;    off = align16(off + 4u * kPipeMath * 32 * 16);
-    m.hh[b] = off;    off = align16(off + 4u * kPipeHist * kPipeHist);
-    m.y[b] = off;     off = align16(off + 4u * 2 * NT * dv);
-  }
+  m.bg = off;    off = align16(off + 8u * nkmax * NT);
+  m.buf = off;
+  uint32_t o = 0;  // within one buffer
+  m.item = o;  o = align16(o + (uint32_t)sizeof(PipeItem));
+  m.wraw = o;  o = align16(o + 3u * NT * dk * dtype_bytes(in_dt));
+  m.ep = o;    o = align16(o + 2u * NT * dk * dtype_bytes(in_dt));
+  m.hkr = o;   o = align16(o + (uint32_t)(kPipeHist * dk * dtype_bytes(rk_dt)));
+  m.hdr = o;   o = align16(o + (uint32_t)(kPipeHist * dv * dtype_bytes(rd_dt)));
+  m.hgr = o;   o = align16(o + 4u * kPipeHist);
+  m.xh = o;    o = align16(o + 4u * dk * nv);
+  m.hkt = o;   o = align16(o + 4u * dk * kPipeHist);
+  m.dt = o;    o = align16(o + 4u * kPipeHist * dv);
+  m.hh = o;    o = align16(o + 4u * kPipeHist * nv);
+  m.y = o;     o = align16(o + 4u * nv * dv);
+  m.bufsz = o;
+  off += 2u * o;
   off = (off + 127u) & ~127u;
   m.ring = off;
   const int room = (max_smem - (int)off) / kChunkBytes;
@@ -559,14 +572,75 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+// Arrive with an expected byte count, without release semantics: for a
+// thread that only issues async copies (a release would order it behind the
+// copies it already has in flight).
+__device__ __forceinline__ void mbar_expect_tx_relaxed(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_addr(bar)),
                "r"(bytes)
                : "memory");
+}
+
+// 16-byte async copy global -> shared (cache at L2 only), and an arrive on
+// `bar` once every such copy this thread has issued so far has completed
+// (the barrier's expected count includes the arrival).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Wait for phase `parity` of `bar` for up to about hint_ns, the thread parked
+// by the hardware meanwhile (it resumes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of phase `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The arrival that registers a copy's byte count is made by the thread that
+// issues the copies, and it carries no release semantics: nothing the thread
+// wrote before is published through it (the data comes with the copy), and on
+// this part a release by a thread waits for the copies that thread has in
+// flight, which serialised each refill of a tile ring behind the copy before.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  mbar_expect_tx_relaxed(bar, bytes);
 }
 
 // One bulk (non-tensor) async copy global -> shared, completing on `bar`.

@@ -285,10 +285,18 @@ struct TilePipe {
   __device__ __forceinline__ bool wait_full(int j) const {
     return mbar_wait_bounded(&full[j % tr.ns], (uint32_t)((j / tr.ns) & 1), hook.limit_ns);
   }
-  // every warp, once it has consumed chunk j
-  __device__ __forceinline__ void release(int j, int lane) const {
+  // every warp, once it has consumed chunk j (thread 0, the producer, whose own
+  // reads come before its refill in program order, arrives without release
+  // semantics, which would wait for its copies in flight)
+  __device__ __forceinline__ void release(int j, int tid, int lane) const {
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[j % tr.ns]);
+    if (lane == 0) {
+      if (tid == 0) {
+        mbar_arrive_relaxed(&empty[j % tr.ns]);
+      } else {
+        mbar_arrive(&empty[j % tr.ns]);
+      }
+    }
   }
   // producer, after its own release of chunk j: refill that stage with chunk j + ns
   __device__ __forceinline__ bool refill(int j) const {
@@ -316,7 +324,7 @@ struct TilePipe {
   // (the producer issues nothing more once one of its own waits has run out,
   // so every copy it issued can be waited for before the CTA leaves)
   __device__ __forceinline__ bool done(int j, int tid, int lane, bool ok) const {
-    release(j, lane);
+    release(j, tid, lane);
     return tid == 0 && ok ? refill(j) : true;
   }
 };
@@ -345,7 +353,7 @@ __device__ __forceinline__ bool stream_tile(const TilePipe<ST>& pipe, float (&y)
       consume_rows<ALGO, ST, RB, NV, FOLD>(buf, y, gcol, j * rpc + u0, cm, dk, dv, n, hk, hd, hf,
                                            gdn_decay, egam, xh);
     }
-    pipe.release(j, lane);
+    pipe.release(j, tid, lane);
     if (tid == 0 && ok) ok = pipe.refill(j);
   }
   return ok;

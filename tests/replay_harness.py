@@ -33,7 +33,8 @@ class Run:
 
     def __init__(self, *, algo="gdn", HK, HV, dk, dv, L, max_T, slots, n_slots=None,
                  n_layers=1, in_dtype="f32", state_dtype="f32", ring_k_dtype=None,
-                 ring_d_dtype="f32", commit_mode="lazy", config_id=0, sample=None):
+                 ring_d_dtype="f32", commit_mode="lazy", config_id=0, sample=None,
+                 plan="auto"):
         from linear_attention_state_rssm_gb300 import ReplayStore
         self.algo, self.HK, self.HV, self.dk, self.dv, self.L = algo, HK, HV, dk, dv, L
         self.in_dtype, self.state_dtype, self.config_id = in_dtype, state_dtype, config_id
@@ -44,6 +45,7 @@ class Run:
         self.n_layers = n_layers
         self.store = ReplayStore(algo, n_layers, self.n_slots, HK, HV, dk, dv, L, max_T,
                                  in_dtype, state_dtype, ring_k_dtype, ring_d_dtype, commit_mode)
+        self.store.rssm_set_plan(plan)   # which kernel serves decode and verify
         S0 = np.stack([synth.initial_state(synth.seed_for(config_id, 10_000, l), self.n_slots,
                                            HV, dk, dv, state_dtype) for l in range(n_layers)])
         self.store.state.copy_(dev(S0, state_dtype))

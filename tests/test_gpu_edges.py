@@ -308,8 +308,9 @@ def test_decode_on_a_long_ring(algo, HK, HV):
     assert run.store.rssm_get_device_error() == 0
 
 
+@pytest.mark.parametrize("plan", ["rows", "pipe"])
 @pytest.mark.parametrize("state,ring_k", [("f32", "f32"), ("bf16", "f16"), ("f32", "bf16")])
-def test_decode_fold_of_every_history_length(state, ring_k):
+def test_decode_fold_of_every_history_length(state, ring_k, plan):
     """GDN decode with 128-wide heads on an L = 16 ring: row r is forced to fold
     at step r, so one launch folds histories of every length 0..16 (then each
     row folds a full ring every 16 steps), for fp32 and bf16 checkpoints and
@@ -318,7 +319,7 @@ def test_decode_fold_of_every_history_length(state, ring_k):
     slots = np.arange(B, dtype=np.int32)
     tol = TOL32 if state == "f32" and ring_k == "f32" else TOL16
     run = Run(algo="gdn", HK=1, HV=2, dk=128, dv=128, L=L, max_T=1, slots=slots, n_slots=B,
-              state_dtype=state, ring_k_dtype=ring_k, config_id=33)
+              state_dtype=state, ring_k_dtype=ring_k, config_id=33, plan=plan)
     for step in range(36):
         force = (np.arange(B) == step).astype(np.uint8)
         _, o_gpu, o_orc, f_gpu, f_orc = run.window(0, run.inputs(step, 0, 1), 1, force=force,
@@ -332,11 +333,11 @@ def test_decode_fold_of_every_history_length(state, ring_k):
     assert run.store.rssm_get_device_error() == 0
 
 
-@pytest.mark.parametrize("algo", ["gdn", "kda"])
-@pytest.mark.parametrize("T", [3, 8])
+@pytest.mark.parametrize("algo,plan", [("gdn", "rows"), ("gdn", "pipe"), ("kda", "rows")])
+@pytest.mark.parametrize("T", [1, 2, 3, 8])
 @pytest.mark.parametrize("in_dt,ring_k,state", [("f32", "f32", "f32"), ("f32", "bf16", "f32"),
                                                 ("bf16", "f32", "bf16"), ("bf16", "f16", "f32")])
-def test_verify_across_input_key_and_state_dtypes(in_dt, ring_k, state, T, algo):
+def test_verify_across_input_key_and_state_dtypes(in_dt, ring_k, state, T, algo, plan):
     """Three- and eight-token GDN and KDA verify + commit with 128-wide heads
     (fp32 and 16-bit inputs, ring keys and checkpoints), forced folds on top of
     the ring's own, accept lengths U[0, T]: outputs, fold flags, cursors and
@@ -345,7 +346,7 @@ def test_verify_across_input_key_and_state_dtypes(in_dt, ring_k, state, T, algo)
     tol = TOL32 if (in_dt, ring_k, state) == ("f32", "f32", "f32") else TOL16
     run = Run(algo=algo, HK=1, HV=2, dk=128, dv=128, L=L, max_T=T,
               slots=np.arange(B, dtype=np.int32), n_slots=B, in_dtype=in_dt, state_dtype=state,
-              ring_k_dtype=ring_k, config_id=34)
+              ring_k_dtype=ring_k, config_id=34, plan=plan)
     for step in range(14):
         inp = run.inputs(step, 0, T)
         force = synth.force_flags(3400 + step, B, 0.15)

@@ -51,7 +51,8 @@ def test_tiny_gdn_decode_forty_steps_two_folds():
     assert run.store.rssm_get_device_error() == 0
 
 
-def test_qwen_shaped_gdn_decode_full_batch():
+@pytest.mark.parametrize("plan", ["rows", "pipe"])
+def test_qwen_shaped_gdn_decode_full_batch(plan):
     """HK=16, HV=32, dk=dv=128, batch 64 with 8 null slots, L=16, bf16 q/k/v,
     fp32 state and deltas, fp16 ring keys; 34 steps (two folds). Every live row
     is compared with the oracle on every step (outputs, fold flags, cursors,
@@ -62,7 +63,7 @@ def test_qwen_shaped_gdn_decode_full_batch():
     null = np.nonzero(slots < 0)[0]
     live = np.nonzero(slots >= 0)[0]
     run = Run(algo="gdn", HK=16, HV=32, dk=128, dv=128, L=16, max_T=1, slots=slots,
-              n_slots=B, in_dtype="bf16", config_id=1)
+              n_slots=B, in_dtype="bf16", config_id=1, plan=plan)
     folds = 0
     for step in range(34):
         inp = run.inputs(step, 0, 1)
@@ -124,9 +125,10 @@ def _verify_chain(run, T, steps, poison_frac, seed0, check_oracle=True, narrow_t
     return accepted
 
 
+@pytest.mark.parametrize("plan", ["rows", "pipe"])
 @pytest.mark.parametrize("T", [3, 8])
 @pytest.mark.parametrize("state,mode", [("f32", "lazy"), ("bf16", "fold_every")])
-def test_gdn_verify_commit_with_poisoned_drafts(T, state, mode):
+def test_gdn_verify_commit_with_poisoned_drafts(T, state, mode, plan):
     """HK=16, HV=32, dk=dv=128, batch 128, L=16, accept ~ U[0, T], NaN/Inf at
     rejected positions of 10% of the rows with rejections, 24 chained steps.
     Every row is compared until at least four steps, one with ring-overflow
@@ -134,15 +136,16 @@ def test_gdn_verify_commit_with_poisoned_drafts(T, state, mode):
     B = 128
     sample = np.array([0, 5, 17, 42, 77, 101, 127])
     run = Run(algo="gdn", HK=16, HV=32, dk=128, dv=128, L=16, max_T=T, slots=np.arange(B),
-              in_dtype="bf16", state_dtype=state, commit_mode=mode, config_id=2)
+              in_dtype="bf16", state_dtype=state, commit_mode=mode, config_id=2, plan=plan)
     run.tol = TOL16
     _verify_chain(run, T, 24, 0.10, 7000 + T, narrow_to=sample)
     assert run.ring_d_err() <= TOL16
     assert run.store.rssm_get_device_error() == 0
 
 
+@pytest.mark.parametrize("plan", ["rows", "pipe"])
 @pytest.mark.parametrize("state,mode", [("f32", "lazy"), ("bf16", "fold_every")])
-def test_poisoned_rejected_drafts_are_bitwise_inert(state, mode):
+def test_poisoned_rejected_drafts_are_bitwise_inert(state, mode, plan):
     """Poisoned vs clean rejected positions: accepted outputs, checkpoints,
     accepted ring records and cursors are bitwise identical."""
     B, T = 64, 4
@@ -150,7 +153,7 @@ def test_poisoned_rejected_drafts_are_bitwise_inert(state, mode):
     for poison in (0.0, 0.5):
         run = Run(algo="gdn", HK=4, HV=8, dk=128, dv=128, L=16, max_T=T, slots=np.arange(B),
                   in_dtype="bf16", state_dtype=state, commit_mode=mode, config_id=12,
-                  sample=np.array([0]))
+                  sample=np.array([0]), plan=plan)
         acc = _verify_chain(run, T, 10, poison, 900, check_oracle=False)
         runs.append((run, acc))
     (r0, a0), (r1, a1) = runs

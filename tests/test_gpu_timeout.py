@@ -77,15 +77,15 @@ def _clean_step(run, inp, T, step, force=None, decode=False):
     assert run.store.rssm_get_device_error() == 0
 
 
-@pytest.mark.parametrize("algo", ["gdn", "kda"])
+@pytest.mark.parametrize("algo,plan", [("gdn", "rows"), ("gdn", "pipe"), ("kda", "rows")])
 @pytest.mark.parametrize("where", ["window", "history", "chunk"])
-def test_wait_that_runs_out_leaves_the_row_untouched(algo, where):
+def test_wait_that_runs_out_leaves_the_row_untouched(algo, where, plan):
     """A verify window (no fold) whose window, history or checkpoint-chunk wait
     runs out writes nothing: outputs, fold flags, ring, checkpoint, cursor."""
     from linear_attention_state_rssm_gb300 import _lib as L_
     T = 3
     run = Run(algo=algo, HK=2, HV=4, dk=128, dv=128, L=8, max_T=T, slots=[0, 2, 1],
-              config_id=70)
+              config_id=70, plan=plan)
     _history(run, 2)                                   # cursor 2: 2 + 3 <= 8, no fold
     snap = _snap(run.store)
     barrier = {"window": L_.WITHHOLD["window"], "history": L_.WITHHOLD["history"],
@@ -101,8 +101,11 @@ def test_wait_that_runs_out_leaves_the_row_untouched(algo, where):
     _clean_step(run, inp, T, 10)
 
 
-@pytest.mark.parametrize("algo,T", [("gdn", 3), ("kda", 3), ("gdn", 1), ("gdn", 8)])
-def test_folding_row_stops_storing_at_the_failed_chunk(algo, T):
+@pytest.mark.parametrize("algo,T,plan", [("gdn", 3, "rows"), ("kda", 3, "rows"),
+                                         ("gdn", 1, "rows"), ("gdn", 8, "rows"),
+                                         ("gdn", 3, "pipe"), ("gdn", 1, "pipe"),
+                                         ("gdn", 8, "pipe")])
+def test_folding_row_stops_storing_at_the_failed_chunk(algo, T, plan):
     """A forced fold whose checkpoint chunk 5 never completes (verify, or decode
     for T = 1): no output, fold flag or ring record is written, the checkpoint
     rows from chunk 5 on are untouched (the chunks before it may hold the
@@ -110,7 +113,7 @@ def test_folding_row_stops_storing_at_the_failed_chunk(algo, T):
     clean call matches."""
     from linear_attention_state_rssm_gb300 import _lib as L_
     run = Run(algo=algo, HK=2, HV=4, dk=128, dv=128, L=16, max_T=T, slots=[0, 1],
-              config_id=71)
+              config_id=71, plan=plan)
     _history(run, 4)
     snap = _snap(run.store)
     run.store.rssm_debug_withhold(L_.withhold_chunk(5), 1000)
