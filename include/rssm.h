@@ -47,12 +47,16 @@
  * after 0.5 s and sets RSSM_DEVERR_TIMEOUT (a copy that never lands is a
  * hardware fault; nothing in normal operation comes near the limit). What the
  * affected row of a replay or fold launch then holds:
- *  - a wait for the window rows or history records: nothing of the row is
- *    written (outputs, records, fold_out, checkpoint);
- *  - a wait for a checkpoint chunk: no output, record or fold_out is written,
- *    and no checkpoint chunk from the failed one on is stored back; a row that
- *    folds may have stored the chunks before it already folded, so its
- *    checkpoint is then part old, part folded.
+ *  - a wait for the window rows, or for the history records of a window that
+ *    folds: nothing of the row is written (outputs, records, fold_out,
+ *    checkpoint);
+ *  - a later wait (the history of a window that does not fold, a checkpoint
+ *    chunk): no output, delta, value or fold_out is written and no checkpoint
+ *    chunk from the failed one on is stored back. A window that does not fold
+ *    may have written its keys, gates and betas at ring positions [c, c + T),
+ *    past the committed history (the row's committed state is untouched); a
+ *    row that folds may have stored the chunks before the failed one already
+ *    folded, so its checkpoint is then part old, part folded.
  * The cursor kernels do not see the failure (decode's advance_cursor, commit
  * and fold still move the cursor). A caller that finds the bit set must treat
  * the step as failed and restore the slots it touched (write a checkpoint,
@@ -374,14 +378,14 @@ rssm_status rssm_set_plan(rssm_handle *h, int32_t plan);
  * Test and debugging hook of the bounded waits (no counterpart in the pages:
  * it exists so that the timeout path above can be exercised without a fault).
  * barrier: -1 turns the hook off (the state after rssm_alloc); 0 the window
- * rows' barrier, 1 the history records', 2 + j that of checkpoint chunk j.
- * While the hook is on, every replay and fold launch of this handle registers
- * 16 bytes more on that barrier than its copies carry, so every wait on it
- * runs out, after wait_limit_us microseconds (1 .. 1000000) instead of the
- * usual 0.5 s; the copies themselves all land. Host state only: takes effect
- * at the next launch. Never on in production calls.
+ * rows' barrier, 1 the history records', 2 + j that of checkpoint chunk j of
+ * the launch's first item (every row for the per-row kernel). While the hook
+ * is on, every replay and fold launch of this handle leaves that barrier short
+ * of what its copies bring, so every wait on it runs out after the usual
+ * 0.5 s; the copies themselves all land. Host state only: takes effect at the
+ * next launch. Never on in production calls.
  */
-rssm_status rssm_debug_withhold(rssm_handle *h, int32_t barrier, int32_t wait_limit_us);
+rssm_status rssm_debug_withhold(rssm_handle *h, int32_t barrier);
 
 const char *rssm_status_string(rssm_status s);
 

@@ -93,7 +93,7 @@ def load() -> ctypes.CDLL:
         "rssm_reset_slots": ([_P, _P, _I, _P], _I),
         "rssm_get_device_error": ([_P, ctypes.POINTER(ctypes.c_uint32), _I, _P], _I),
         "rssm_set_plan": ([_P, _I], _I),
-        "rssm_debug_withhold": ([_P, _I, _I], _I),
+        "rssm_debug_withhold": ([_P, _I], _I),
         "rssm_status_string": ([_I], ctypes.c_char_p),
         "rssm_version": ([], _I),
     }
@@ -252,11 +252,10 @@ def withhold_chunk(j: int) -> int:
     return 2 + int(j)
 
 
-def rssm_debug_withhold(handle, barrier, wait_limit_us=1000):
+def rssm_debug_withhold(handle, barrier):
     """Test hook: every later replay/fold launch of this handle short-changes
     `barrier` (see include/rssm.h); barrier -1 turns it off."""
-    _check(load().rssm_debug_withhold(handle, int(barrier), int(wait_limit_us)),
-           "rssm_debug_withhold")
+    _check(load().rssm_debug_withhold(handle, int(barrier)), "rssm_debug_withhold")
 
 
 def rssm_status_string(status: int) -> str:

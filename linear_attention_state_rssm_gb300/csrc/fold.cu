@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
 
   const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv, kStages,
                           p.hook);
-  const unsigned long long lim = p.hook.limit_ns;
+  constexpr unsigned long long lim = kWaitLimitNs;
   if (tid == 0) {
     mbar_init(&mbar[kMbarWin], 1);
     mbar_init(&mbar[kMbarHist], 1);

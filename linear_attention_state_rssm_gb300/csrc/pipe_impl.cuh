@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.B, T = p.T, L = p.L, HV = p.HV, NS = sm.ns;
-  const unsigned long long lim = p.hook.limit_ns;
+  constexpr unsigned long long lim = kWaitLimitNs;
   uint64_t* mb = reinterpret_cast<uint64_t*>(smem + sm.mbar);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + sm.mbar + 8 * kPipeMbars);
   int* r_slot = reinterpret_cast<int*>(smem + sm.rows);

@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   const int dk = p.dk, dv = p.dv, L = p.L, HV = p.HV, HK = p.HK;
   int T = p.T;  // this row's window (RAGGED: set once the row is known)
   const int kh = h / p.G;
-  const unsigned long long lim = p.hook.limit_ns;
+  constexpr unsigned long long lim = kWaitLimitNs;
 
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + p.sm.mbar);
   float* wq = reinterpret_cast<float*>(smem + p.sm.wq);
@@ -779,6 +779,26 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     }
     return;
   }
+
+  // ---- records that need no result of the solve: keys, gates and betas at
+  //      ring positions base + i (KDA's raw gates were turned into prefixes in
+  //      shared memory: they are copied from the input). A window that does
+  //      not fold writes them now, past the history it reads ([0, c)).
+  auto write_kgb = [&]() {
+    for (int ch = tid; ch < dk; ch += kThreads) {
+      for (int i = 0; i < T; ++i) {
+        st_f32(p.ring_k, kbase + (size_t)(base + i) * dk + ch, p.rk_dt, wk[i * dk + ch]);
+        if (ALGO == ALGO_KDA) {
+          p.ring_g[gbase + (size_t)(base + i) * dk + ch] = p.g[((tok0 + i) * HV + h) * dk + ch];
+        }
+      }
+    }
+    if (tid < T) {
+      p.ring_beta[((size_t)s * HV + h) * L + base + tid] = wb[tid];
+      if (ALGO == ALGO_GDN) p.ring_g[gbase + base + tid] = wg[tid];
+    }
+  };
+  if (!fold) write_kgb();
 
   const QuadLayout qlay(dv, CW, sw);
   const QuadLane qlane(qlay, CW, warp, lane);
@@ -1054,23 +1074,9 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   // wait that failed)
   const bool all_ok = __syncthreads_and(copies_ok);
 
-  // ---- records that need no result of the solve: keys, gates and betas at
-  //      ring positions base + i (KDA's raw gates were turned into prefixes in
-  //      shared memory: they are copied from the input)
-  if (all_ok) {
-    for (int ch = tid; ch < dk; ch += kThreads) {
-      for (int i = 0; i < T; ++i) {
-        st_f32(p.ring_k, kbase + (size_t)(base + i) * dk + ch, p.rk_dt, wk[i * dk + ch]);
-        if (ALGO == ALGO_KDA) {
-          p.ring_g[gbase + (size_t)(base + i) * dk + ch] = p.g[((tok0 + i) * HV + h) * dk + ch];
-        }
-      }
-    }
-    if (tid < T) {
-      p.ring_beta[((size_t)s * HV + h) * L + base + tid] = wb[tid];
-      if (ALGO == ALGO_GDN) p.ring_g[gbase + base + tid] = wg[tid];
-    }
-  }
+  // a folding window writes its keys, gates and betas only now: positions
+  // [0, T) are the ones its history was read from
+  if (fold && all_ok) write_kgb();
 
   // ---- 4. per value column: corrections, triangular solve, outputs, deltas
   if (tid < dv && all_ok) {

@@ -350,7 +350,7 @@ rssm_status rssm_alloc(const rssm_config* cfg, const rssm_buffers* buf, rssm_han
   h->layer_g = slots * cfg->HV * cfg->L * n_gate(*cfg);
   h->layer_v = slots * cfg->HV * cfg->L * cfg->dv;
   h->layer_beta = slots * cfg->HV * cfg->L;
-  h->hook = WaitHook{WH_OFF, kWaitLimitNs};
+  h->hook = WaitHook{WH_OFF};
   h->pipe_cfg = pipe_cfg;
   h->plan = RSSM_PLAN_AUTO;
   *out = h;
@@ -576,15 +576,10 @@ rssm_status rssm_set_plan(rssm_handle* h, int32_t plan) {
   return RSSM_OK;
 }
 
-rssm_status rssm_debug_withhold(rssm_handle* h, int32_t barrier, int32_t wait_limit_us) {
+rssm_status rssm_debug_withhold(rssm_handle* h, int32_t barrier) {
   if (h == nullptr) return RSSM_ERR_INVALID_ARG;
   if (barrier < WH_OFF || barrier >= WH_CHUNK0 + 256) return RSSM_ERR_INVALID_ARG;
-  if (barrier == WH_OFF) {
-    h->hook = WaitHook{WH_OFF, kWaitLimitNs};
-    return RSSM_OK;
-  }
-  if (wait_limit_us < 1 || wait_limit_us > 1000000) return RSSM_ERR_INVALID_ARG;
-  h->hook = WaitHook{barrier, 1000ull * (unsigned long long)wait_limit_us};
+  h->hook = WaitHook{barrier};
   return RSSM_OK;
 }
 

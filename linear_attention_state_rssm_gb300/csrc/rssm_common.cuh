@@ -33,19 +33,17 @@ enum : int { FOLD_ALL = 0, FOLD_COMMIT = 1 };
 constexpr int kThreads = 128;  // 4 warps per CTA, one CTA per (row, value head)
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
-// A bounded wait gives up after this many nanoseconds of %globaltimer (a
-// launch may ask for a shorter limit, see WaitHook).
+// A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 500ull * 1000ull * 1000ull;
 
 // Test hook of the bounded waits, off (withhold < 0) in every ordinary call:
 // the copies that complete on barrier `withhold` (0 the window rows, 1 the
 // history records, 2 + j chunk j of the checkpoint tile) register 16 more
 // bytes than they carry, so no copy can complete that barrier and every wait
-// on it runs out after limit_ns. Nothing faults: the copies themselves all land.
+// on it runs out. Nothing faults: the copies themselves all land.
 enum : int { WH_OFF = -1, WH_WINDOW = 0, WH_HIST = 1, WH_CHUNK0 = 2 };
 struct WaitHook {
   int withhold;
-  unsigned long long limit_ns;
   __host__ __device__ uint32_t extra(int barrier) const {
     return withhold == barrier ? 16u : 0u;
   }

@@ -283,7 +283,7 @@ struct TilePipe {
     for (int j = 0; j < tr.ns; ++j) issue(j);
   }
   __device__ __forceinline__ bool wait_full(int j) const {
-    return mbar_wait_bounded(&full[j % tr.ns], (uint32_t)((j / tr.ns) & 1), hook.limit_ns);
+    return mbar_wait_bounded(&full[j % tr.ns], (uint32_t)((j / tr.ns) & 1));
   }
   // every warp, once it has consumed chunk j (thread 0, the producer, whose own
   // reads come before its refill in program order, arrives without release
@@ -301,14 +301,13 @@ struct TilePipe {
   // producer, after its own release of chunk j: refill that stage with chunk j + ns
   __device__ __forceinline__ bool refill(int j) const {
     if (j + tr.ns >= tr.nchunk) return true;
-    const bool ok = mbar_wait_bounded(&empty[j % tr.ns], (uint32_t)((j / tr.ns) & 1),
-                                      hook.limit_ns);
+    const bool ok = mbar_wait_bounded(&empty[j % tr.ns], (uint32_t)((j / tr.ns) & 1));
     if (ok) issue(j + tr.ns);
     return ok;
   }
   // a CTA that leaves early lets the primed chunks land first
   __device__ __forceinline__ void drain() const {
-    for (int j = 0; j < tr.ns; ++j) mbar_wait_bounded(&full[j], 0, hook.limit_ns);
+    for (int j = 0; j < tr.ns; ++j) mbar_wait_bounded(&full[j], 0);
   }
   // a CTA whose stream failed lets the chunks that may still be in flight (the
   // last ns issued) land before it leaves; each wait is bounded again

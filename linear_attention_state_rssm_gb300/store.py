@@ -106,10 +106,10 @@ class ReplayStore:
         """Kernel family for decode and verify: "auto", "rows" or "pipe"."""
         _lib.rssm_set_plan(self.handle, plan)
 
-    def rssm_debug_withhold(self, barrier, wait_limit_us=1000):
+    def rssm_debug_withhold(self, barrier):
         """Test hook of the bounded waits (include/rssm.h): later launches of
         this store short-change `barrier` (-1: off)."""
-        _lib.rssm_debug_withhold(self.handle, barrier, wait_limit_us)
+        _lib.rssm_debug_withhold(self.handle, barrier)
 
     def close(self):
         if getattr(self, "handle", None):

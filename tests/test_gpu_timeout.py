@@ -1,6 +1,7 @@
 """The bounded waits of the replay and fold kernels, made to run out on
 purpose through the test hook rssm_debug_withhold: one barrier is promised 16
-bytes more than its copies carry, so every wait on it gives up after 1 ms.
+bytes more than its copies carry, so every wait on it gives up after its
+usual 0.5 s.
 Nothing faults or hangs (every copy lands; only the count is short). Checked:
 the call returns, RSSM_DEVERR_TIMEOUT is set, the row's outputs, records and
 checkpoint are as include/rssm.h says, and with the hook off the next call is
@@ -81,7 +82,9 @@ def _clean_step(run, inp, T, step, force=None, decode=False):
 @pytest.mark.parametrize("where", ["window", "history", "chunk"])
 def test_wait_that_runs_out_leaves_the_row_untouched(algo, where, plan):
     """A verify window (no fold) whose window, history or checkpoint-chunk wait
-    runs out writes nothing: outputs, fold flags, ring, checkpoint, cursor."""
+    runs out writes no output, fold flag, delta, value, checkpoint or cursor;
+    keys, gates and betas may be written only at ring positions [c, c + T),
+    past the committed history (the window's own wait: nothing at all)."""
     from linear_attention_state_rssm_gb300 import _lib as L_
     T = 3
     run = Run(algo=algo, HK=2, HV=4, dk=128, dv=128, L=8, max_T=T, slots=[0, 2, 1],
@@ -90,14 +93,20 @@ def test_wait_that_runs_out_leaves_the_row_untouched(algo, where, plan):
     snap = _snap(run.store)
     barrier = {"window": L_.WITHHOLD["window"], "history": L_.WITHHOLD["history"],
                "chunk": L_.withhold_chunk(5)}[where]
-    run.store.rssm_debug_withhold(barrier, 1000)
+    run.store.rssm_debug_withhold(barrier)
     inp = run.inputs(10, 0, T)
     o, fold_out, err, secs = _timed_out_call(run, inp, T)
     assert err & L_.DEVERR["timeout"]
     assert secs < 30.0
     assert torch.all(o == SENTINEL)
     assert torch.all(fold_out == 7)
-    _same(run.store, snap)
+    kgb = ("ring_k", "ring_g", "ring_beta")
+    _same(run.store, snap, [n for n in BUFS if n not in kgb or where == "window"])
+    c = 2
+    for name in kgb:
+        now, was = getattr(run.store, name), snap[name]
+        assert torch.equal(now[:, :, :, :c], was[:, :, :, :c]), name
+        assert torch.equal(now[:, :, :, c + T:], was[:, :, :, c + T:]), name
     _clean_step(run, inp, T, 10)
 
 
@@ -116,7 +125,7 @@ def test_folding_row_stops_storing_at_the_failed_chunk(algo, T, plan):
               config_id=71, plan=plan)
     _history(run, 4)
     snap = _snap(run.store)
-    run.store.rssm_debug_withhold(L_.withhold_chunk(5), 1000)
+    run.store.rssm_debug_withhold(L_.withhold_chunk(5))
     inp = run.inputs(10, 0, T)
     force = np.ones(run.B, np.uint8)
     o, fold_out, err, secs = _timed_out_call(run, inp, T, force, decode=T == 1)
@@ -141,7 +150,7 @@ def test_fold_every_commit_stops_storing_at_the_failed_chunk():
     inp = run.inputs(0, 0, T)
     run.window(0, inp, T)
     before = run.store.state.clone()
-    run.store.rssm_debug_withhold(L_.withhold_chunk(3), 1000)
+    run.store.rssm_debug_withhold(L_.withhold_chunk(3))
     acc = torch.full((run.B,), T, dtype=torch.int32, device="cuda")
     run.store.rssm_commit(run.slot_t, acc, T)
     assert run.store.rssm_get_device_error() & L_.DEVERR["timeout"]
@@ -161,7 +170,7 @@ def test_hook_arguments_are_checked():
     from linear_attention_state_rssm_gb300 import RssmError
     run = Run(algo="gdn", HK=1, HV=1, dk=32, dv=32, L=4, max_T=1, slots=[0], config_id=73)
     with pytest.raises(RssmError):
-        run.store.rssm_debug_withhold(0, 0)            # limit below 1 us
+        run.store.rssm_debug_withhold(-2)              # no such barrier
     with pytest.raises(RssmError):
-        run.store.rssm_debug_withhold(-2, 1000)        # no such barrier
+        run.store.rssm_debug_withhold(2 + 256)         # beyond the last chunk
     run.store.rssm_debug_withhold(-1)                  # off is always accepted
