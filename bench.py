@@ -1144,7 +1144,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the replay prefill line")
     ap.add_argument("--no-conv", action="store_true", help="skip the conv window line")
     ap.add_argument("--no-kda", action="store_true", help="skip the KDA decode+verify line")
-    ap.add_argument("--plan", default="auto", choices=["auto", "rows", "pipe"],
+    ap.add_argument("--plan", default="auto", choices=["auto", "rows", "pipe", "tc"],
                     help="kernel family for GDN decode/verify (rssm_set_plan)")
     ap.add_argument("--sweep", action="store_true",
                     help="print the steady-state grid (batch, L, T, state dtype, GDN/KDA)")

@@ -101,7 +101,7 @@ enum { RSSM_CONV_ACT_NONE = 0, RSSM_CONV_ACT_SILU = 1 };
 enum { RSSM_COMMIT_LAZY = 0, RSSM_COMMIT_FOLD_EVERY = 1 };
 
 /* Kernel family serving rssm_decode / rssm_verify (rssm_set_plan). */
-enum { RSSM_PLAN_AUTO = 0, RSSM_PLAN_ROWS = 1, RSSM_PLAN_PIPE = 2 };
+enum { RSSM_PLAN_AUTO = 0, RSSM_PLAN_ROWS = 1, RSSM_PLAN_PIPE = 2, RSSM_PLAN_TC = 3 };
 
 /* Bits of the device error word. */
 enum {
@@ -368,8 +368,16 @@ rssm_status rssm_get_device_error(rssm_handle *h, uint32_t *out, int32_t clear,
  *    It serves GDN stores with dk = dv = 128, L <= 16 and L a multiple of 4,
  *    fp32 or fp16 deltas, calls with T <= 8 and B <= 512 (uniform windows);
  *    calls outside that run on the per-row kernel.
+ *  - RSSM_PLAN_TC: the per-row kernel, whose GDN windows of 3..8 tokens
+ *    (uniform, not ragged) stream the checkpoint tile through the
+ *    5th-generation tensor cores (tcgen05 MMAs, tensor-memory accumulators;
+ *    fp32 operands as tf32 hi + lo pairs, so the products keep fp32
+ *    accuracy); a fold of up to 16 records runs there too. It serves GDN
+ *    stores with dv = 128 and dk a multiple of 32; other calls of such a
+ *    store run as RSSM_PLAN_ROWS.
  *  - RSSM_PLAN_AUTO (after rssm_alloc): the per-row kernel.
- * RSSM_PLAN_PIPE on a store it cannot serve returns RSSM_ERR_UNSUPPORTED. Host
+ * RSSM_PLAN_PIPE or RSSM_PLAN_TC on a store it cannot serve returns
+ * RSSM_ERR_UNSUPPORTED. Host
  * state only; takes effect at the next launch.
  */
 rssm_status rssm_set_plan(rssm_handle *h, int32_t plan);

@@ -234,11 +234,11 @@ def rssm_get_device_error(handle, clear=True, stream=None) -> int:
     return int(word.value)
 
 
-PLAN = {"auto": 0, "rows": 1, "pipe": 2}
+PLAN = {"auto": 0, "rows": 1, "pipe": 2, "tc": 3}
 
 
 def rssm_set_plan(handle, plan):
-    """Kernel family for decode and verify: "auto", "rows" or "pipe"."""
+    """Kernel family for decode and verify: "auto", "rows", "pipe" or "tc"."""
     _check(load().rssm_set_plan(handle, PLAN[plan] if isinstance(plan, str) else int(plan)),
            "rssm_set_plan")
 

@@ -44,6 +44,7 @@
 #include "rssm_common.cuh"
 #include "rssm_history.cuh"
 #include "rssm_mma.cuh"
+#include "rssm_tc.cuh"
 
 #include <type_traits>
 
@@ -547,7 +548,9 @@ __device__ __forceinline__ bool stream_mma_dt(const TilePipe<ST>& pipe, int in_d
 // LONG: GDN decode on a ring longer than 16 records, whose own folds carry
 // more than 16 records; it leaves out the tensor-core fold (up to 16 records),
 // whose code slows the general fold when both are compiled into one kernel.
-template <int ALGO, typename ST, int NT, bool RAGGED, bool LONG = false>
+// TC: GDN windows of 3..8 tokens (NT 4 and 8) with 128 value columns stream on
+// the 5th-generation tensor cores when p.tc is set (stream_tc).
+template <int ALGO, typename ST, int NT, bool RAGGED, bool LONG = false, bool TC = false>
 __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     replay_kernel(const ReplayParams p) {
   constexpr int NV = 2 * NT;             // mat-vec vectors: k_i at [0, NT), q_i at [NT, 2NT)
@@ -680,6 +683,14 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     mbar_init(&mbar[kMbarWin], 1);
     mbar_init(&mbar[kMbarHist], 1);
     TilePipe<ST>::init_full(mbar);
+    if (TC) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&mbar[kMbarAFull + b], kWarps);
+        mbar_init(&mbar[kMbarAEmpty + b], 1);
+      }
+      mbar_init(&mbar[kMbarFoldTc], 1);
+      mbar_init(&mbar[kMbarYDone], 1);
+    }
     fence_mbar_init();
     issue_window(tok0);
   }
@@ -713,14 +724,17 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   const bool fold = (p.force != nullptr && p.force[r] != 0) || (c + T > L);
   const int base = fold ? 0 : c;
   const int nh = c;
-  const bool split = can_split(ALGO, NT) && !fold;
+  // the 5th-generation tensor-core stream: one thread per value column
+  const bool tc = TC && p.tc != 0 && dv == kThreads && dk % 32 == 0 &&
+                  (!fold || (nh <= 16 && L >= 16));
+  const bool split = can_split(ALGO, NT) && !fold && !tc;
   const int sw = split ? kSplitWarps : kWarps;  // warps that stream the tile
   // Four- and eight-token GDN windows with 128 value columns stream on the
   // tensor cores (mat-vec inputs and fold keys in fragment order, column sums
   // in ymm); a fold there takes at most 16 records and a ring of at least 16.
   constexpr bool kMmaNT = ALGO == ALGO_GDN && (NT == 4 || NT == 8);
   constexpr int NTN = NV >= 8 ? NV / 8 : 1;  // n-tiles of eight vectors
-  const bool mmas = kMmaNT && dv == 128 && pipe.tr.cr % 8 == 0 &&
+  const bool mmas = !TC && kMmaNT && dv == 128 && pipe.tr.cr % 8 == 0 &&
                     (!fold || (nh <= 16 && L >= 16));
   const size_t kbase = ((size_t)s * HV + h) * L * dk;
   const size_t dbase = ((size_t)s * HV + h) * L * dv;
@@ -742,7 +756,26 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     widen16(wk, wraw + T * qrow, T * dk, p.in_dt, tid, kThreads);
     widen16(wv, wraw + 2 * T * qrow, T * dv, p.in_dt, tid, kThreads);
   }
-  if (ALGO == ALGO_GDN) {
+  if (TC && tc) {
+    // K-major X [16 vectors x dk rows]; fp32 inputs split into hi (xh) and lo
+    const void* qsrc = f32in ? static_cast<const void*>(wq) : wraw;
+    const void* ksrc = f32in ? static_cast<const void*>(wk) : wraw + T * qrow;
+    float* xl = reinterpret_cast<float*>(smem + p.sm.xl);
+    for (int e = tid; e < dk * kTcN; e += kThreads) {
+      int ch, vv;
+      x_slot_tc(e, ch, vv);
+      const int i = vv < NT ? vv : vv - NT;
+      const float x = vv < NV && i < T ? ld_f32(vv < NT ? ksrc : qsrc, (size_t)i * dk + ch, p.in_dt)
+                                       : 0.f;
+      if (f32in) {
+        xh[e] = tf32_hi(x);
+        xl[e] = x - tf32_hi(x);
+      } else {
+        xh[e] = x;
+      }
+    }
+    fence_async_smem();
+  } else if (ALGO == ALGO_GDN) {
     const void* qsrc = f32in ? static_cast<const void*>(wq) : wraw;
     const void* ksrc = f32in ? static_cast<const void*>(wk) : wraw + T * qrow;
     for (int e = tid; e < dk * NV; e += kThreads) {
@@ -778,6 +811,28 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
       pipe.drain();
     }
     return;
+  }
+
+  // tensor memory of the tensor-core stream (freed at the end of the kernel)
+  TcStream tcs{};
+  if (TC && tc) {
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(&mbar[kMbarTmem]);
+    if (warp == 0) {
+      __syncwarp();
+      tmem_alloc(tslot);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tcs.tbase = *tslot;
+    tcs.afull = &mbar[kMbarAFull];
+    tcs.aempty = &mbar[kMbarAEmpty];
+    tcs.fbar = &mbar[kMbarFoldTc];
+    tcs.ydone = &mbar[kMbarYDone];
+    tcs.xh = xh;
+    tcs.xl = f32in ? reinterpret_cast<const float*>(smem + p.sm.xl) : nullptr;
+    tcs.kh = hk;
+    tcs.kl = p.rk_dt == DT_F32 ? reinterpret_cast<const float*>(smem + p.sm.kl) : nullptr;
   }
 
   // ---- records that need no result of the solve: keys, gates and betas at
@@ -881,7 +936,11 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   } else {
     // A wide GDN window without a fold streams first, while its history lands.
     const bool early = ALGO == ALGO_GDN && !fold;
-    if (early) {
+    if (early && TC && tc) {
+      if constexpr (TC) {
+        copies_ok = stream_tc<ST, false>(pipe, tcs, gtile, 1.f, tid, warp, lane) && copies_ok;
+      }
+    } else if (early) {
       if (mmas) {
         if constexpr (kMmaNT) {
           copies_ok = stream_mma_dt<ST, NTN, 2, false>(pipe, p.in_dt, p.rk_dt, hk, hd, hf, 0, 1.f,
@@ -899,7 +958,11 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     if (nh > 0) {
       if (p.rd_dt != DT_F32) widen16(hd, hdraw, nh * dv, p.rd_dt, tid, kThreads);
       if (ALGO == ALGO_GDN) {
-        if (fold && mmas) {
+        if (fold && TC && tc) {
+          float* kl = p.rk_dt == DT_F32 ? reinterpret_cast<float*>(smem + p.sm.kl) : nullptr;
+          tc_fold_keys(hk, kl, hkraw, nh, dk, p.rk_dt, tid, kThreads);
+          fence_async_smem();
+        } else if (fold && mmas) {
           frag_keys16(hk, hkraw, nh, dk, p.rk_dt, tid, kThreads);
         } else if (fold) {
           transpose_keys(hk, hkraw, nh, dk, p.rk_dt, tid, kThreads);
@@ -988,7 +1051,15 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
         if constexpr (NT == 1 && ALGO == ALGO_GDN && !LONG) {
           mma_fold = nh <= 16 && dv == 128 && pipe.tr.cr % 16 == 0;
         }
-        if (mmas) {
+        if (TC && tc) {
+          if constexpr (TC) {
+            tc_fold_a(tcs, hd, hf, nh, dv, tid, warp);
+            tc_fence_before();
+            __syncthreads();
+            copies_ok = stream_tc<ST, true>(pipe, tcs, gtile, hscal[1], tid, warp, lane) &&
+                        copies_ok;
+          }
+        } else if (mmas) {
           if constexpr (kMmaNT) {
             copies_ok = stream_mma_dt<ST, NTN, 2, true>(pipe, p.in_dt, p.rk_dt, hk, hd, hf, nh,
                                                         hscal[1], xh, gtile, tid, warp, lane,
@@ -1009,6 +1080,10 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
                                                                nh, ALGO == ALGO_KDA ? hg : hk, hd,
                                                                hf, hscal[1], egam, xh, tid, lane) &&
                       copies_ok;
+        }
+      } else if (TC && tc) {
+        if constexpr (TC) {
+          copies_ok = stream_tc<ST, false>(pipe, tcs, gtile, 1.f, tid, warp, lane) && copies_ok;
         }
       } else if (mmas) {
         if constexpr (kMmaNT) {
@@ -1034,7 +1109,12 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   // free once every warp has consumed the last chunk); a tensor-core fold
   // leaves whole column sums, in the first row-group slot
   __syncthreads();
-  if (mma_fold) {
+  if (TC && tc) {
+    if constexpr (TC) {
+      copies_ok = tc_read_y<NV>(tcs, red, dv, tid, warp) && copies_ok;
+      for (int e = tid; e < (qlay.rgw - 1) * NV * dv; e += kThreads) red[NV * dv + e] = 0.f;
+    }
+  } else if (mma_fold) {
     if constexpr (NT == 1) {
       if (lane < 4) {
 #pragma unroll
@@ -1137,6 +1217,16 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     // CTA leaves (the window's waited above, or the row would not be here)
     if (nh > 0) mbar_wait_bounded(&mbar[kMbarHist], 0, lim);
     pipe.drain_tail();
+  }
+  if (TC && tc) {
+    // every read of tensor memory is done (tc_read_y waited for the last MMA)
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(tcs.tbase);
+    }
   }
 }
 

@@ -9,20 +9,39 @@
 namespace rssm {
 
 // One CTA per (value head, request row).
-template <int ALGO, typename ST, int NT, bool RAGGED, bool LONG = false>
+template <int ALGO, typename ST, int NT, bool RAGGED, bool LONG = false, bool TC = false>
 static cudaError_t replay_launch_one(const ReplayParams& p, cudaStream_t st) {
   const dim3 grid((unsigned)p.HV, (unsigned)p.B, 1);
-  replay_kernel<ALGO, ST, NT, RAGGED, LONG><<<grid, kThreads, p.sm.total, st>>>(p);
+  replay_kernel<ALGO, ST, NT, RAGGED, LONG, TC><<<grid, kThreads, p.sm.total, st>>>(p);
   return cudaGetLastError();
 }
 
-template <int ALGO, typename ST, int NT, bool RAGGED, bool LONG = false>
+template <int ALGO, typename ST, int NT, bool RAGGED, bool LONG = false, bool TC = false>
 static cudaError_t replay_prepare_one(int max_smem) {
-  cudaError_t e = cudaFuncSetAttribute(replay_kernel<ALGO, ST, NT, RAGGED, LONG>,
+  cudaError_t e = cudaFuncSetAttribute(replay_kernel<ALGO, ST, NT, RAGGED, LONG, TC>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(replay_kernel<ALGO, ST, NT, RAGGED, LONG>,
+  return cudaFuncSetAttribute(replay_kernel<ALGO, ST, NT, RAGGED, LONG, TC>,
                               cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+}
+
+// Verify windows of four and eight tokens: GDN takes the tensor-core stream
+// kernel when p.tc is set.
+template <int ALGO, typename ST, int NT>
+static cudaError_t replay_launch_wide(const ReplayParams& p, cudaStream_t st) {
+  if constexpr (ALGO == ALGO_GDN) {
+    if (p.tc) return replay_launch_one<ALGO, ST, NT, false, false, true>(p, st);
+  }
+  return replay_launch_one<ALGO, ST, NT, false>(p, st);
+}
+
+template <int ALGO, typename ST, int NT>
+static cudaError_t replay_prepare_wide(int max_smem) {
+  if constexpr (ALGO == ALGO_GDN) {
+    const cudaError_t e = replay_prepare_one<ALGO, ST, NT, false, false, true>(max_smem);
+    if (e != cudaSuccess) return e;
+  }
+  return replay_prepare_one<ALGO, ST, NT, false>(max_smem);
 }
 
 // Decode: GDN rings longer than 16 records take the kernel without the
@@ -52,8 +71,8 @@ static cudaError_t replay_prepare_decode(int max_smem) {
     switch (NT) {                                                                           \
       case 1: return replay_launch_decode<ALGO, ST>(p, st);                                 \
       case 2: return replay_launch_one<ALGO, ST, 2, false>(p, st);                          \
-      case 4: return replay_launch_one<ALGO, ST, 4, false>(p, st);                          \
-      case 8: return replay_launch_one<ALGO, ST, 8, false>(p, st);                          \
+      case 4: return replay_launch_wide<ALGO, ST, 4>(p, st);                                \
+      case 8: return replay_launch_wide<ALGO, ST, 8>(p, st);                                \
       case 16: return replay_launch_one<ALGO, ST, 16, false>(p, st);                        \
       default: return cudaErrorInvalidValue;                                                \
     }                                                                                       \
@@ -62,8 +81,8 @@ static cudaError_t replay_prepare_decode(int max_smem) {
     cudaError_t e;                                                                          \
     if ((e = replay_prepare_decode<ALGO, ST>(max_smem)) != cudaSuccess) return e;           \
     if ((e = replay_prepare_one<ALGO, ST, 2, false>(max_smem)) != cudaSuccess) return e;    \
-    if ((e = replay_prepare_one<ALGO, ST, 4, false>(max_smem)) != cudaSuccess) return e;    \
-    if ((e = replay_prepare_one<ALGO, ST, 8, false>(max_smem)) != cudaSuccess) return e;    \
+    if ((e = replay_prepare_wide<ALGO, ST, 4>(max_smem)) != cudaSuccess) return e;          \
+    if ((e = replay_prepare_wide<ALGO, ST, 8>(max_smem)) != cudaSuccess) return e;          \
     return replay_prepare_one<ALGO, ST, 16, false>(max_smem);                               \
   }                                                                                         \
   }

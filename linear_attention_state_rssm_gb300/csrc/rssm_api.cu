@@ -116,9 +116,14 @@ cudaError_t replay_prepare(const rssm_config& c, int max_smem) {
   return f32 ? replay_kda_f32_ragged_prepare(max_smem) : replay_kda_bf16_ragged_prepare(max_smem);
 }
 
-ReplaySmem layout_for(const rssm_config& c, int T, int NT) {
+ReplaySmem layout_for(const rssm_config& c, int T, int NT, bool tc = false) {
   return replay_layout(c.algo, (int)esize(c.state_dtype), NT, T, c.L, c.dk, c.dv, c.in_dtype,
-                       c.ring_k_dtype, c.ring_d_dtype);
+                       c.ring_k_dtype, c.ring_d_dtype, tc);
+}
+
+// the tensor-core stream serves GDN windows of 3..8 tokens with 128 value columns
+bool tc_config(const rssm_config& c) {
+  return c.algo == RSSM_ALGO_GDN && c.dv == 128 && c.dk % 32 == 0;
 }
 
 ReplaySmem layout_for(const rssm_config& c, int T) { return layout_for(c, T, nt_for(T)); }
@@ -219,7 +224,8 @@ rssm_status window(rssm_handle* h, int32_t layer, const void* q, const void* k, 
     }
   }
   const int NT = cu != nullptr ? nt_for_ragged(T) : nt_for(T);
-  p.sm = layout_for(h->cfg, T, NT);
+  p.tc = h->plan == RSSM_PLAN_TC && cu == nullptr && tc_config(c) && (NT == 4 || NT == 8);
+  p.sm = layout_for(h->cfg, T, NT, p.tc != 0);
   if ((int)p.sm.total > h->max_smem) return RSSM_ERR_UNSUPPORTED;
   return from_cuda(replay_launch(h->cfg, p, NT, static_cast<cudaStream_t>(stream)));
 }
@@ -569,9 +575,11 @@ rssm_status rssm_get_device_error(rssm_handle* h, uint32_t* out, int32_t clear, 
 
 rssm_status rssm_set_plan(rssm_handle* h, int32_t plan) {
   if (h == nullptr) return RSSM_ERR_INVALID_ARG;
-  if (plan != RSSM_PLAN_AUTO && plan != RSSM_PLAN_ROWS && plan != RSSM_PLAN_PIPE)
+  if (plan != RSSM_PLAN_AUTO && plan != RSSM_PLAN_ROWS && plan != RSSM_PLAN_PIPE &&
+      plan != RSSM_PLAN_TC)
     return RSSM_ERR_INVALID_ARG;
   if (plan == RSSM_PLAN_PIPE && !h->pipe_cfg) return RSSM_ERR_UNSUPPORTED;
+  if (plan == RSSM_PLAN_TC && !tc_config(h->cfg)) return RSSM_ERR_UNSUPPORTED;
   h->plan = plan;
   return RSSM_OK;
 }

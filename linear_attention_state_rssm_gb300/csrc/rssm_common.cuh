@@ -64,7 +64,14 @@ constexpr int kMbarWin = 0;
 constexpr int kMbarHist = 1;
 constexpr int kMbarFull = 2;
 constexpr int kMbarEmpty = 2 + kStages;
-constexpr int kMbars = 2 + 2 * kStages;
+// tensor-core stream (rssm_tc.cuh): A stage written [2], A stage read [2], fold
+// slice done, mat-vec done, and an 8-byte slot for the tensor-memory address
+constexpr int kMbarAFull = 2 + 2 * kStages;
+constexpr int kMbarAEmpty = kMbarAFull + 2;
+constexpr int kMbarFoldTc = kMbarAFull + 4;
+constexpr int kMbarYDone = kMbarAFull + 5;
+constexpr int kMbarTmem = kMbarAFull + 6;
+constexpr int kMbars = kMbarAFull + 7;
 
 // Geometry of the tile ring for a [dk][dv] tile of `state_bytes`-byte elements.
 struct TileRing {
@@ -94,11 +101,13 @@ struct ReplaySmem {
   uint32_t yk;     // KDA [T][dk]: e^{G_i} * k_i (history dots)
   uint32_t yq;     // KDA [T][dk]: e^{G_i} * q_i
   uint32_t scal;   // GDN: es[NT], eG[NT], Gam, e^Gam, G[NT]; KDA: egam[dk], gam[dk]
-  uint32_t xh;     // [dk][2NT] mat-vec inputs
+  uint32_t xh;     // [dk][2NT] mat-vec inputs (tensor-core stream: K-major, 16 vectors)
+  uint32_t xl;     // tensor-core stream, fp32 inputs: the lo parts of xh
   uint32_t am;     // [NT][NT] window coefficients A (strictly lower)
   uint32_t fm;     // [NT][NT] window coefficients F (lower incl. diagonal)
   uint32_t hk;     // [L][dk] fp32 history keys (KDA: decay-scaled), or for a GDN fold the
-                   // transposed keys [dk][round4(n)]
+                   // transposed keys [dk][round4(n)] (tensor-core stream: K-major, 16 records)
+  uint32_t kl;     // tensor-core stream, fp32 ring keys: the lo parts of the fold keys
   uint32_t hkraw;  // [L][dk]  history keys as stored in the ring (landing zone of the copy;
                    // KDA fp32 keys land in hk); split GDN windows reuse it for the history
                    // correction hc [NV][dv]
@@ -182,6 +191,7 @@ struct ReplayParams {
   int in_dt, rk_dt, rd_dt;
   float scale;
   WaitHook hook;
+  int tc;  // GDN windows of 3..8 tokens stream on the 5th-generation tensor cores
   ReplaySmem sm;
 };
 
@@ -332,7 +342,7 @@ constexpr uint32_t kRankBytes = 8u * kThreads + 4u * kWarps;
 // ring of L records.
 __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, int NT, int T,
                                                     int L, int dk, int dv, int in_dt, int rk_dt,
-                                                    int rd_dt) {
+                                                    int rd_dt, bool tc = false) {
   ReplaySmem m{};
   const int NV = 2 * NT;
   const bool kda = algo == ALGO_KDA;
@@ -350,10 +360,12 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
   m.yk = off;    if (kda) off = align16(off + 4u * T * dk);
   m.yq = off;    if (kda) off = align16(off + 4u * T * dk);
   m.scal = off;  off = align16(off + 4u * (kda ? 2 * dk : 3 * NT + 4));
-  m.xh = off;    off = align16(off + 4u * dk * NV);
+  m.xh = off;    off = align16(off + 4u * dk * (tc ? 16 : NV));
+  m.xl = off;    if (tc && in_dt == DT_F32) off = align16(off + 4u * dk * 16);
   m.am = off;    off = align16(off + 4u * NT * NT);
   m.fm = off;    off = align16(off + 4u * NT * NT);
   m.hk = off;    off = align16(off + 4u * round4(L) * dk);
+  m.kl = off;    if (tc && rk_dt == DT_F32) off = align16(off + 4u * 16 * dk);
   {
     // KDA fp32 keys land in hk and are decay-scaled in place
     const uint32_t raw = (!kda || rk_dt != DT_F32) ? (uint32_t)(dtype_bytes(rk_dt) * L * dk) : 0u;
@@ -382,6 +394,9 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
     m.rank = off;
     off = align16(off + kRankBytes);
   }
+  // the tensor-core stream holds kTmemCols of the SM's 512 tensor-memory
+  // columns: at most four such CTAs may share an SM
+  if (tc && off < 47u * 1024u) off = 47u * 1024u;
   m.total = off;
   return m;
 }

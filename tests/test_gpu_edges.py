@@ -333,7 +333,8 @@ def test_decode_fold_of_every_history_length(state, ring_k, plan):
     assert run.store.rssm_get_device_error() == 0
 
 
-@pytest.mark.parametrize("algo,plan", [("gdn", "rows"), ("gdn", "pipe"), ("kda", "rows")])
+@pytest.mark.parametrize("algo,plan", [("gdn", "rows"), ("gdn", "pipe"), ("gdn", "tc"),
+                                       ("kda", "rows")])
 @pytest.mark.parametrize("T", [1, 2, 3, 8])
 @pytest.mark.parametrize("in_dt,ring_k,state", [("f32", "f32", "f32"), ("f32", "bf16", "f32"),
                                                 ("bf16", "f32", "bf16"), ("bf16", "f16", "f32")])

@@ -125,7 +125,7 @@ def _verify_chain(run, T, steps, poison_frac, seed0, check_oracle=True, narrow_t
     return accepted
 
 
-@pytest.mark.parametrize("plan", ["rows", "pipe"])
+@pytest.mark.parametrize("plan", ["rows", "pipe", "tc"])
 @pytest.mark.parametrize("T", [3, 8])
 @pytest.mark.parametrize("state,mode", [("f32", "lazy"), ("bf16", "fold_every")])
 def test_gdn_verify_commit_with_poisoned_drafts(T, state, mode, plan):
@@ -143,7 +143,7 @@ def test_gdn_verify_commit_with_poisoned_drafts(T, state, mode, plan):
     assert run.store.rssm_get_device_error() == 0
 
 
-@pytest.mark.parametrize("plan", ["rows", "pipe"])
+@pytest.mark.parametrize("plan", ["rows", "pipe", "tc"])
 @pytest.mark.parametrize("state,mode", [("f32", "lazy"), ("bf16", "fold_every")])
 def test_poisoned_rejected_drafts_are_bitwise_inert(state, mode, plan):
     """Poisoned vs clean rejected positions: accepted outputs, checkpoints,

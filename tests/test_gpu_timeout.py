@@ -78,7 +78,8 @@ def _clean_step(run, inp, T, step, force=None, decode=False):
     assert run.store.rssm_get_device_error() == 0
 
 
-@pytest.mark.parametrize("algo,plan", [("gdn", "rows"), ("gdn", "pipe"), ("kda", "rows")])
+@pytest.mark.parametrize("algo,plan", [("gdn", "rows"), ("gdn", "pipe"), ("gdn", "tc"),
+                                       ("kda", "rows")])
 @pytest.mark.parametrize("where", ["window", "history", "chunk"])
 def test_wait_that_runs_out_leaves_the_row_untouched(algo, where, plan):
     """A verify window (no fold) whose window, history or checkpoint-chunk wait
@@ -113,7 +114,8 @@ def test_wait_that_runs_out_leaves_the_row_untouched(algo, where, plan):
 @pytest.mark.parametrize("algo,T,plan", [("gdn", 3, "rows"), ("kda", 3, "rows"),
                                          ("gdn", 1, "rows"), ("gdn", 8, "rows"),
                                          ("gdn", 3, "pipe"), ("gdn", 1, "pipe"),
-                                         ("gdn", 8, "pipe")])
+                                         ("gdn", 8, "pipe"), ("gdn", 3, "tc"),
+                                         ("gdn", 8, "tc")])
 def test_folding_row_stops_storing_at_the_failed_chunk(algo, T, plan):
     """A forced fold whose checkpoint chunk 5 never completes (verify, or decode
     for T = 1): no output, fold flag or ring record is written, the checkpoint
