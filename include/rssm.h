@@ -372,9 +372,11 @@ rssm_status rssm_get_device_error(rssm_handle *h, uint32_t *out, int32_t clear,
  *    (uniform, not ragged) stream the checkpoint tile through the
  *    5th-generation tensor cores (tcgen05 MMAs, tensor-memory accumulators;
  *    fp32 operands as tf32 hi + lo pairs, so the products keep fp32
- *    accuracy); a fold of up to 16 records runs there too. It serves GDN
- *    stores with dv = 128 and dk a multiple of 32; other calls of such a
- *    store run as RSSM_PLAN_ROWS.
+ *    accuracy); a fold of up to 16 records runs there too. The folds of
+ *    rssm_commit (fold-every stores) and rssm_fold compute their rank-n
+ *    update on the tensor cores as well when L <= 32. It serves GDN stores
+ *    with dv = 128 and dk a multiple of 32; other calls of such a store run
+ *    as RSSM_PLAN_ROWS.
  *  - RSSM_PLAN_AUTO (after rssm_alloc): the per-row kernel.
  * RSSM_PLAN_PIPE or RSSM_PLAN_TC on a store it cannot serve returns
  * RSSM_ERR_UNSUPPORTED. Host

@@ -126,6 +126,12 @@ bool tc_config(const rssm_config& c) {
   return c.algo == RSSM_ALGO_GDN && c.dv == 128 && c.dk % 32 == 0;
 }
 
+// the tensor-core fold serves GDN stores with 128 value columns and rings of
+// at most 32 records
+bool fold_tc_config(const rssm_config& c) {
+  return tc_config(c) && c.L <= 32;
+}
+
 ReplaySmem layout_for(const rssm_config& c, int T) { return layout_for(c, T, nt_for(T)); }
 
 FoldSmem fold_layout_for(const rssm_config& c) {
@@ -264,7 +270,10 @@ FoldParams fold_params(const rssm_handle* h, const int32_t* slot, const uint8_t*
   p.rd_dt = c.ring_d_dtype;
   p.mode = mode;
   p.hook = h->hook;
-  p.sm = fold_layout_for(c);
+  p.tc = h->plan == RSSM_PLAN_TC && fold_tc_config(c);
+  p.sm = p.tc ? fold_tc_layout((int)esize(c.state_dtype), c.L, c.dk, c.dv, c.ring_k_dtype,
+                               c.ring_d_dtype)
+              : fold_layout_for(c);
   return p;
 }
 

@@ -196,7 +196,7 @@ struct ReplayParams {
 };
 
 struct FoldSmem {
-  uint32_t ring, mbar, hk, hkraw, hd, hdraw, hg, hf, scal, total;
+  uint32_t ring, mbar, hk, hkraw, hd, hdraw, hg, hf, scal, bf, bl, total;
 };
 
 struct FoldParams {
@@ -214,6 +214,7 @@ struct FoldParams {
   int B, T, L, n_slots, HK, HV, G, dk, dv;
   int rk_dt, rd_dt, mode;
   WaitHook hook;
+  int tc;  // GDN folds on the 5th-generation tensor cores (fold_tc_kernel)
   FoldSmem sm;
 };
 
@@ -536,6 +537,32 @@ __host__ __device__ inline FoldSmem fold_layout(int algo, int state_bytes, int L
   m.hg = off;    if (kda) off = align16(off + 4u * L * dk);
   m.hf = off;    off = align16(off + 4u * L);
   m.scal = off;  off = align16(off + 4u * (kda ? 2 * dk : 4));
+  m.total = off;
+  return m;
+}
+
+// Fold on the tensor cores (GDN): ring, barriers, the ring records as copied
+// (keys in any dtype land in hkraw), fp32 deltas, gates, and the fold keys
+// K-major for up to round8(L) records (hi in bf, lo in bl for fp32 keys).
+__host__ __device__ inline FoldSmem fold_tc_layout(int state_bytes, int L, int dk, int dv,
+                                                   int rk_dt, int rd_dt) {
+  FoldSmem m{};
+  const TileRing tr(dk, dv, state_bytes);
+  const int K = (L + 7) & ~7;
+  uint32_t off = 0;
+  m.ring = off;  off = align16(off + tr.ns * tr.chunk_bytes);
+  m.mbar = off;  off = align16(off + 8u * kMbars);
+  m.hkraw = off; off = align16(off + (uint32_t)(dtype_bytes(rk_dt) * L * dk));
+  m.hk = m.hkraw;
+  m.hd = off;    off = align16(off + 4u * L * dv);
+  m.hdraw = off; if (rd_dt != DT_F32) off = align16(off + 2u * L * dv);
+  m.hg = off;
+  m.hf = off;    off = align16(off + 4u * L);
+  m.scal = off;  off = align16(off + 16u);
+  m.bf = off;    off = align16(off + 4u * K * dk);
+  m.bl = off;    if (rk_dt == DT_F32) off = align16(off + 4u * K * dk);
+  // kTmemCols of the SM's 512 tensor-memory columns: at most four CTAs per SM
+  if (off < 47u * 1024u) off = 47u * 1024u;
   m.total = off;
   return m;
 }

@@ -189,6 +189,14 @@ class Run:
         return o.double().cpu().numpy(), o_orc
 
     # ------------------------------------------------------------- inspection
+    def fold(self, slots):
+        """rssm_fold of the given slots on the GPU and in both oracles."""
+        self.store.rssm_fold(torch.as_tensor(np.asarray(slots, dtype=np.int32)).cuda())
+        orc_slots = [self.orc_index[int(s)] for s in slots if int(s) in self.orc_index]
+        for orc in (self.orc, self.orc_r):
+            if orc is not None:
+                orc.fold(orc_slots)
+
     def cursor_gpu(self):
         return self.store.cursor.cpu().numpy()
 

@@ -143,6 +143,35 @@ def test_restore_copy_checkpoint_into_fresh_slot():
         run.check_ring_records()
 
 
+@pytest.mark.parametrize("plan", ["rows", "tc"])
+@pytest.mark.parametrize("L,state,ring_k", [(16, "f32", "f32"), (16, "bf16", "f16"),
+                                            (32, "f32", "f16"), (8, "f32", "bf16")])
+def test_fold_call_of_every_history_length(L, state, ring_k, plan):
+    """rssm_fold with 128-wide GDN heads after L decode steps in which row r
+    (r < L) was forced to fold at step r: the rows fold histories of every
+    length 1..L in one launch; the checkpoint matches the oracle, then the
+    decode carries on from it."""
+    B = L + 1
+    tol = TOL32 if state == "f32" and ring_k == "f32" else TOL16
+    run = Run(algo="gdn", HK=1, HV=2, dk=128, dv=128, L=L, max_T=1,
+              slots=np.arange(B, dtype=np.int32), n_slots=B, state_dtype=state,
+              ring_k_dtype=ring_k, config_id=35, plan=plan)
+    for step in range(L):
+        force = (np.arange(B) == step).astype(np.uint8)
+        run.window(0, run.inputs(step, 0, 1), 1, force=force, decode=True, advance=True)
+    np.testing.assert_array_equal(run.cursor_gpu(), [L - r for r in range(L)] + [L])
+    run.fold(np.arange(B))
+    run.check_cursors()
+    assert run.state_err() <= tol
+    for step in range(L, L + 3):
+        _, o_gpu, o_orc, _, _ = run.window(0, run.inputs(step, 0, 1), 1, decode=True,
+                                           advance=True)
+        assert rel_err(o_gpu, o_orc) <= tol, step
+        run.check_cursors()
+    assert run.state_err() <= tol
+    assert run.store.rssm_get_device_error() == 0
+
+
 def test_runs_are_deterministic():
     res = []
     for _ in range(2):

@@ -142,13 +142,14 @@ def test_folding_row_stops_storing_at_the_failed_chunk(algo, T, plan):
     _clean_step(run, inp, T, 10, force, decode=T == 1)
 
 
-def test_fold_every_commit_stops_storing_at_the_failed_chunk():
+@pytest.mark.parametrize("plan", ["rows", "tc"])
+def test_fold_every_commit_stops_storing_at_the_failed_chunk(plan):
     """The commit's fold kernel: a chunk wait that runs out leaves the
     checkpoint rows from that chunk on untouched and sets the bit."""
     from linear_attention_state_rssm_gb300 import _lib as L_
     T = 3
     run = Run(algo="gdn", HK=2, HV=4, dk=128, dv=128, L=8, max_T=T, slots=[0, 1],
-              config_id=72, commit_mode="fold_every")
+              config_id=72, commit_mode="fold_every", plan=plan)
     inp = run.inputs(0, 0, T)
     run.window(0, inp, T)
     before = run.store.state.clone()
