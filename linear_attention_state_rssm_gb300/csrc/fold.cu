@@ -18,6 +18,57 @@
 
 namespace rssm {
 
+// The tile stream of the fold: thread tid holds d~_m = f_m d_m[col] of its
+// column for the NB records in registers (zero past n) and, per row of the
+// column, adds sum_m k~_m[row] d~_m to decay(row) S[row] with the row's keys
+// read four at a time from hkt [dk][NB] (a broadcast across the warp); the
+// row goes back in the checkpoint dtype. GDN: decay e^Gam, f_m = hf[m];
+// KDA: decay egam[row] and the decayed keys, f_m = 1.
+template <int ALGO, typename ST, int NB>
+__device__ __forceinline__ bool fold_stream(const TilePipe<ST>& pipe, ST* gcol, const ColMap& cm,
+                                            int dv, int n, const float* hkt, const float* hd,
+                                            const float* hf, float decay, const float* egam,
+                                            int tid, int lane) {
+  float dt[NB];
+#pragma unroll
+  for (int m = 0; m < NB; ++m) {
+    const float f = ALGO == ALGO_GDN && m < n ? hf[m] : 1.f;
+    dt[m] = m < n ? f * hd[m * dv + cm.col] : 0.f;
+  }
+  const int rpc = pipe.tr.cr / cm.RG;  // this thread's rows per chunk
+  bool ok = true;
+  for (int j = 0; j < pipe.tr.nchunk; ++j) {
+    // a warp stores no chunk once one of its waits has run out
+    ok = __all_sync(kFull, pipe.wait_full(j) && ok);
+    const ST* stg = pipe.ring + (size_t)(j % pipe.tr.ns) * pipe.tr.cr * dv +
+                    (size_t)cm.rg * dv + cm.col;
+#pragma unroll 4
+    for (int u = 0; u < rpc; ++u) {
+      const int row = cm.row(j * rpc + u);
+      const float sv = st_load<ST>(stg + (size_t)cm.RG * u * dv);
+      float acc = (ALGO == ALGO_GDN ? decay : egam[row]) * sv;
+      const float4* kr = reinterpret_cast<const float4*>(hkt + (size_t)row * NB);
+#pragma unroll
+      for (int q = 0; q < NB / 4; ++q) {
+        const float4 k4 = kr[q];
+        acc = fmaf(k4.x, dt[4 * q], acc);
+        acc = fmaf(k4.y, dt[4 * q + 1], acc);
+        acc = fmaf(k4.z, dt[4 * q + 2], acc);
+        acc = fmaf(k4.w, dt[4 * q + 3], acc);
+      }
+      if (ok) st_store<ST>(gcol + (size_t)row * dv, acc);
+    }
+    pipe.release(j, tid, lane);
+    if (tid == 0 && ok) ok = pipe.refill(j);
+  }
+  return ok;
+}
+
+// Records per fold stream: n rounded up to 4, 8, 16, 32 or 64.
+__host__ __device__ constexpr int fold_nb(int n) {
+  return n <= 4 ? 4 : n <= 8 ? 8 : n <= 16 ? 16 : n <= 32 ? 32 : 64;
+}
+
 template <int ALGO, typename ST>
 __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -105,7 +156,10 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
     }
     return;
   }
-  widen_history(n, dk, dv, p.rk_dt, p.rd_dt, hk, hkraw, hd, hdraw, tid);
+  // 16-bit deltas widened; KDA's 16-bit keys widened (GDN's are read from
+  // the landing zone when they are transposed below)
+  if (p.rd_dt != DT_F32) widen16(hd, hdraw, n * dv, p.rd_dt, tid, kThreads);
+  if (ALGO == ALGO_KDA && p.rk_dt != DT_F32) widen16(hk, hkraw, n * dk, p.rk_dt, tid, kThreads);
   __syncthreads();
   if (ALGO == ALGO_GDN) {
     if (warp == 0) gdn_history_scan(n, hf, scal, lane);
@@ -113,13 +167,40 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
     for (int ch = tid; ch < dk; ch += kThreads) {
       egam[ch] = __expf(kda_history_channel(n, dk, ch, hk, hg));
     }
+    __syncthreads();
+  }
+  // keys transposed to [dk][NB] (zero past n) for the stream's row-wise reads
+  const int NB = fold_nb(n);
+  float* hkt = reinterpret_cast<float*>(smem + p.sm.hkt);
+  const bool raw16 = ALGO == ALGO_GDN && p.rk_dt != DT_F32;
+  for (int e = tid; e < NB * dk; e += kThreads) {
+    const int m = e / dk, row = e - m * dk;
+    float k = 0.f;
+    if (m < n) k = raw16 ? ld_f32(hkraw, (size_t)m * dk + row, p.rk_dt) : hk[m * dk + row];
+    hkt[row * NB + m] = k;
   }
   __syncthreads();
   // a chunk that did not arrive in time: no chunk from there on is stored (the
   // ones before it hold the folded state), and the copies issued are waited for
-  float unused[1] = {0.f};
-  const bool ok = stream_tile<ALGO, ST, 0, true>(pipe, unused, gcol, cm, dk, dv, n, hk, hd, hf,
-                                                 scal[1], egam, nullptr, tid, lane);
+  const float decay = scal[1];
+  bool ok;
+  switch (NB) {
+    case 4:
+      ok = fold_stream<ALGO, ST, 4>(pipe, gcol, cm, dv, n, hkt, hd, hf, decay, egam, tid, lane);
+      break;
+    case 8:
+      ok = fold_stream<ALGO, ST, 8>(pipe, gcol, cm, dv, n, hkt, hd, hf, decay, egam, tid, lane);
+      break;
+    case 16:
+      ok = fold_stream<ALGO, ST, 16>(pipe, gcol, cm, dv, n, hkt, hd, hf, decay, egam, tid, lane);
+      break;
+    case 32:
+      ok = fold_stream<ALGO, ST, 32>(pipe, gcol, cm, dv, n, hkt, hd, hf, decay, egam, tid, lane);
+      break;
+    default:
+      ok = fold_stream<ALGO, ST, 64>(pipe, gcol, cm, dv, n, hkt, hd, hf, decay, egam, tid, lane);
+      break;
+  }
   if (!__syncthreads_and(ok) && tid == 0) {
     atomicOr(p.err, DEVERR_TIMEOUT);
     pipe.drain_tail();

@@ -196,7 +196,7 @@ struct ReplayParams {
 };
 
 struct FoldSmem {
-  uint32_t ring, mbar, hk, hkraw, hd, hdraw, hg, hf, scal, bf, bl, total;
+  uint32_t ring, mbar, hk, hkraw, hd, hdraw, hg, hf, scal, hkt, bf, bl, total;
 };
 
 struct FoldParams {
@@ -527,14 +527,21 @@ __host__ __device__ inline FoldSmem fold_layout(int algo, int state_bytes, int L
   FoldSmem m{};
   const bool kda = algo == ALGO_KDA;
   const TileRing tr(dk, dv, state_bytes);
+  // the fold stream reads the keys transposed, [dk][nb] with the record count
+  // rounded up to 4 .. 64: in hk for GDN 16-bit keys (read from the landing
+  // zone), else in hg (GDN fp32 keys land in hk; KDA's gates are consumed
+  // before its decayed keys are transposed)
+  const int nb = L <= 4 ? 4 : L <= 8 ? 8 : L <= 16 ? 16 : L <= 32 ? 32 : 64;
+  const bool own_hkt = kda || rk_dt == DT_F32;
   uint32_t off = 0;
   m.ring = off;  off = align16(off + tr.ns * tr.chunk_bytes);
   m.mbar = off;  off = align16(off + 8u * kMbars);
-  m.hk = off;    off = align16(off + 4u * L * dk);
+  m.hk = off;    off = align16(off + 4u * nb * dk);
   m.hkraw = off; if (rk_dt != DT_F32) off = align16(off + 2u * L * dk);
   m.hd = off;    off = align16(off + 4u * L * dv);
   m.hdraw = off; if (rd_dt != DT_F32) off = align16(off + 2u * L * dv);
-  m.hg = off;    if (kda) off = align16(off + 4u * L * dk);
+  m.hg = off;    if (own_hkt) off = align16(off + 4u * nb * dk);
+  m.hkt = own_hkt ? m.hg : m.hk;
   m.hf = off;    off = align16(off + 4u * L);
   m.scal = off;  off = align16(off + 4u * (kda ? 2 * dk : 4));
   m.total = off;
