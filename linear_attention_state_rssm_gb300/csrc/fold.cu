@@ -18,45 +18,70 @@
 
 namespace rssm {
 
-// The tile stream of the fold: thread tid holds d~_m = f_m d_m[col] of its
-// column for the NB records in registers (zero past n) and, per row of the
-// column, adds sum_m k~_m[row] d~_m to decay(row) S[row] with the row's keys
-// read four at a time from hkt [dk][NB] (a broadcast across the warp); the
-// row goes back in the checkpoint dtype. GDN: decay e^Gam, f_m = hf[m];
-// KDA: decay egam[row] and the decayed keys, f_m = 1.
+// Two consecutive checkpoint values <-> fp32 (shared loads, global stores in
+// the checkpoint dtype).
+__device__ __forceinline__ float2 ld_pair(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
+__device__ __forceinline__ float2 ld_pair(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ void st_pair(float* p, float a, float b) {
+  *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+__device__ __forceinline__ void st_pair(__nv_bfloat16* p, float a, float b) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+}
+
+// The tile stream of the fold. Thread tid owns the column pair (c0, c0 + 1),
+// c0 = 2 (tid % (dv / 2)), and the rows rg, rg + RG, ... of every chunk
+// (rg = tid / (dv / 2), RG = kThreads / (dv / 2)); it holds d~_m = f_m d_m[c]
+// of both columns for the NB records in registers (zero past n) and, per
+// row, adds sum_m k~_m[row] d~_m to decay(row) S[row][c], with the row's
+// keys read four records at a time from hkt [dk][NB] (one load serves both
+// columns); the pair goes back in the checkpoint dtype. GDN: decay e^Gam,
+// f_m = hf[m]; KDA: decay egam[row] and the decayed keys, f_m = 1.
 template <int ALGO, typename ST, int NB>
-__device__ __forceinline__ bool fold_stream(const TilePipe<ST>& pipe, ST* gcol, const ColMap& cm,
-                                            int dv, int n, const float* hkt, const float* hd,
-                                            const float* hf, float decay, const float* egam,
-                                            int tid, int lane) {
-  float dt[NB];
+__device__ __forceinline__ bool fold_stream(const TilePipe<ST>& pipe, ST* gtile, int dv, int n,
+                                            const float* hkt, const float* hd, const float* hf,
+                                            float decay, const float* egam, int tid, int lane) {
+  const int half = dv / 2;
+  const int c0 = 2 * (tid % half), rg = tid / half, RG = kThreads / half;
+  float d0[NB], d1[NB];
 #pragma unroll
   for (int m = 0; m < NB; ++m) {
     const float f = ALGO == ALGO_GDN && m < n ? hf[m] : 1.f;
-    dt[m] = m < n ? f * hd[m * dv + cm.col] : 0.f;
+    const float2 d = m < n ? *reinterpret_cast<const float2*>(hd + m * dv + c0)
+                           : make_float2(0.f, 0.f);
+    d0[m] = f * d.x;
+    d1[m] = f * d.y;
   }
-  const int rpc = pipe.tr.cr / cm.RG;  // this thread's rows per chunk
+  const int cr = pipe.tr.cr, rpc = cr / RG;  // this thread's rows per chunk
   bool ok = true;
   for (int j = 0; j < pipe.tr.nchunk; ++j) {
     // a warp stores no chunk once one of its waits has run out
     ok = __all_sync(kFull, pipe.wait_full(j) && ok);
-    const ST* stg = pipe.ring + (size_t)(j % pipe.tr.ns) * pipe.tr.cr * dv +
-                    (size_t)cm.rg * dv + cm.col;
+    const ST* stg = pipe.ring + (size_t)(j % pipe.tr.ns) * cr * dv + (size_t)rg * dv + c0;
 #pragma unroll 4
     for (int u = 0; u < rpc; ++u) {
-      const int row = cm.row(j * rpc + u);
-      const float sv = st_load<ST>(stg + (size_t)cm.RG * u * dv);
-      float acc = (ALGO == ALGO_GDN ? decay : egam[row]) * sv;
+      const int row = j * cr + rg + RG * u;
+      const float2 sv = ld_pair(stg + (size_t)RG * u * dv);
+      const float dec = ALGO == ALGO_GDN ? decay : egam[row];
+      float a0 = dec * sv.x, a1 = dec * sv.y;
       const float4* kr = reinterpret_cast<const float4*>(hkt + (size_t)row * NB);
 #pragma unroll
       for (int q = 0; q < NB / 4; ++q) {
         const float4 k4 = kr[q];
-        acc = fmaf(k4.x, dt[4 * q], acc);
-        acc = fmaf(k4.y, dt[4 * q + 1], acc);
-        acc = fmaf(k4.z, dt[4 * q + 2], acc);
-        acc = fmaf(k4.w, dt[4 * q + 3], acc);
+        a0 = fmaf(k4.x, d0[4 * q], a0);
+        a1 = fmaf(k4.x, d1[4 * q], a1);
+        a0 = fmaf(k4.y, d0[4 * q + 1], a0);
+        a1 = fmaf(k4.y, d1[4 * q + 1], a1);
+        a0 = fmaf(k4.z, d0[4 * q + 2], a0);
+        a1 = fmaf(k4.z, d1[4 * q + 2], a1);
+        a0 = fmaf(k4.w, d0[4 * q + 3], a0);
+        a1 = fmaf(k4.w, d1[4 * q + 3], a1);
       }
-      if (ok) st_store<ST>(gcol + (size_t)row * dv, acc);
+      if (ok) st_pair(gtile + (size_t)row * dv + c0, a0, a1);
     }
     pipe.release(j, tid, lane);
     if (tid == 0 && ok) ok = pipe.refill(j);
@@ -69,7 +94,9 @@ __host__ __device__ constexpr int fold_nb(int n) {
   return n <= 4 ? 4 : n <= 8 ? 8 : n <= 16 ? 16 : n <= 32 ? 32 : 64;
 }
 
-template <int ALGO, typename ST>
+// NBMAX: fold_nb(L), the most records a fold of this store carries (its
+// stream variants are the only ones compiled in, which keeps registers low).
+template <int ALGO, typename ST, int NBMAX>
 __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int h = blockIdx.x, r = blockIdx.y, layer = blockIdx.z;
@@ -107,10 +134,8 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
   }
   if (n == 0) return;
 
-  const ColMap cm(dk, dv, tid);
   ST* gtile = static_cast<ST*>(p.state) + layer * p.layer_state +
               ((size_t)s * HV + h) * (size_t)dk * dv;
-  ST* gcol = gtile + cm.col;
 
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + p.sm.mbar);
   float* hk = reinterpret_cast<float*>(smem + p.sm.hk);
@@ -184,22 +209,18 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldParams p) {
   // ones before it hold the folded state), and the copies issued are waited for
   const float decay = scal[1];
   bool ok;
-  switch (NB) {
-    case 4:
-      ok = fold_stream<ALGO, ST, 4>(pipe, gcol, cm, dv, n, hkt, hd, hf, decay, egam, tid, lane);
-      break;
-    case 8:
-      ok = fold_stream<ALGO, ST, 8>(pipe, gcol, cm, dv, n, hkt, hd, hf, decay, egam, tid, lane);
-      break;
-    case 16:
-      ok = fold_stream<ALGO, ST, 16>(pipe, gcol, cm, dv, n, hkt, hd, hf, decay, egam, tid, lane);
-      break;
-    case 32:
-      ok = fold_stream<ALGO, ST, 32>(pipe, gcol, cm, dv, n, hkt, hd, hf, decay, egam, tid, lane);
-      break;
-    default:
-      ok = fold_stream<ALGO, ST, 64>(pipe, gcol, cm, dv, n, hkt, hd, hf, decay, egam, tid, lane);
-      break;
+  if (NB <= 4) {
+    ok = fold_stream<ALGO, ST, 4>(pipe, gtile, dv, n, hkt, hd, hf, decay, egam, tid, lane);
+  } else if (NB <= 8) {
+    ok = fold_stream<ALGO, ST, 8>(pipe, gtile, dv, n, hkt, hd, hf, decay, egam, tid, lane);
+  } else if (NBMAX <= 16 || NB <= 16) {
+    ok = fold_stream<ALGO, ST, 16>(pipe, gtile, dv, n, hkt, hd, hf, decay, egam, tid, lane);
+  } else if (NBMAX <= 32 || NB <= 32) {
+    ok = fold_stream<ALGO, ST, (NBMAX < 32 ? 16 : 32)>(pipe, gtile, dv, n, hkt, hd, hf, decay,
+                                                       egam, tid, lane);
+  } else {
+    ok = fold_stream<ALGO, ST, (NBMAX < 64 ? 16 : 64)>(pipe, gtile, dv, n, hkt, hd, hf, decay,
+                                                       egam, tid, lane);
   }
   if (!__syncthreads_and(ok) && tid == 0) {
     atomicOr(p.err, DEVERR_TIMEOUT);
@@ -492,8 +513,23 @@ static cudaError_t fold_launch_t(const FoldParams& p, int n_layers, cudaStream_t
       return cudaGetLastError();
     }
   }
-  fold_kernel<ALGO, ST><<<grid, kThreads, p.sm.total, st>>>(p);
+  if (p.L <= 16) {
+    fold_kernel<ALGO, ST, 16><<<grid, kThreads, p.sm.total, st>>>(p);
+  } else if (p.L <= 32) {
+    fold_kernel<ALGO, ST, 32><<<grid, kThreads, p.sm.total, st>>>(p);
+  } else {
+    fold_kernel<ALGO, ST, 64><<<grid, kThreads, p.sm.total, st>>>(p);
+  }
   return cudaGetLastError();
+}
+
+template <int ALGO, typename ST, int NBMAX>
+static cudaError_t fold_prepare_nb(int max_smem) {
+  const cudaError_t e = cudaFuncSetAttribute(fold_kernel<ALGO, ST, NBMAX>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(fold_kernel<ALGO, ST, NBMAX>,
+                              cudaFuncAttributePreferredSharedMemoryCarveout, 100);
 }
 
 template <int ALGO, typename ST>
@@ -507,11 +543,9 @@ static cudaError_t fold_prepare_t(int max_smem) {
                              100);
     if (e != cudaSuccess) return e;
   }
-  e = cudaFuncSetAttribute(fold_kernel<ALGO, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           max_smem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(fold_kernel<ALGO, ST>,
-                              cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if ((e = fold_prepare_nb<ALGO, ST, 16>(max_smem)) != cudaSuccess) return e;
+  if ((e = fold_prepare_nb<ALGO, ST, 32>(max_smem)) != cudaSuccess) return e;
+  return fold_prepare_nb<ALGO, ST, 64>(max_smem);
 }
 
 cudaError_t fold_launch(int algo, int state_dt, const FoldParams& p, int n_layers,
