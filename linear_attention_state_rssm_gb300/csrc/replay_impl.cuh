@@ -626,11 +626,11 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   };
   auto issue_hist = [&](int slot, int n) {
     const size_t sh = (size_t)slot * HV + h;
-    void* kdst = (ALGO == ALGO_KDA && p.rk_dt == DT_F32) ? static_cast<void*>(hk) : hkraw;
-    issue_history<ALGO>(n, dk, dv, p.ring_k, sh * L * dk, p.rk_dt, kdst, p.ring_d, sh * L * dv,
+    // (KDA's gates land in hk, where they become the decayed keys)
+    issue_history<ALGO>(n, dk, dv, p.ring_k, sh * L * dk, p.rk_dt, hkraw, p.ring_d, sh * L * dv,
                         p.rd_dt, p.rd_dt == DT_F32 ? static_cast<void*>(hd) : hdraw, p.ring_g,
-                        sh * L * (ALGO == ALGO_GDN ? 1 : dk), hg, &mbar[kMbarHist],
-                        p.hook.extra(WH_HIST));
+                        sh * L * (ALGO == ALGO_GDN ? 1 : dk), ALGO == ALGO_KDA ? hk : hg,
+                        &mbar[kMbarHist], p.hook.extra(WH_HIST));
   };
   // ---- row order. A folding row's CTAs live several times longer than the
   //      others; started last they would set the end of the launch. For
@@ -709,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   }
   ST* gtile = tile_of(s);
   const TilePipe<ST> pipe(reinterpret_cast<ST*>(smem + p.sm.ring), mbar, gtile, dk, dv,
-                          ring_stages(NT, L), p.hook);
+                          (int)p.sm.ns, p.hook);
   if (tid == 0) pipe.prime();
   if (!have_c) c = p.cursor[s];
   if (c < 0 || c > L) {
@@ -996,15 +996,16 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
       if (warp == 0) gdn_gates(nh, T, fold, hf, hscal, wg, gp, eG, es, lane);
       if (flat && early) pad_window();
     } else {
-      // one thread per key channel: decayed history keys k~ (in hk, [nh][dk]),
-      // history decay, window prefix, scaled window vectors
-      const bool f32k = p.rk_dt == DT_F32;
+      // one thread per key channel: decayed history keys k~ (in hk, [nh][dk],
+      // over the record gates that landed there), history decay, window
+      // prefix, scaled window vectors
       for (int ch = tid; ch < dk; ch += kThreads) {
         float suf = 0.f;
         for (int m = nh - 1; m >= 0; --m) {
-          const float kraw = f32k ? hk[m * dk + ch] : ld_f32(hkraw, (size_t)m * dk + ch, p.rk_dt);
+          const float kraw = ld_f32(hkraw, (size_t)m * dk + ch, p.rk_dt);
+          const float gm = hk[m * dk + ch];
           hk[m * dk + ch] = kraw * __expf(suf);
-          suf += hg[m * dk + ch];
+          suf += gm;
         }
         gam[ch] = suf;
         egam[ch] = __expf(suf);
@@ -1030,9 +1031,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     }
     __syncthreads();
 
-    // ---- 2. window coefficients A, F (j <= i only) and history dot coefficients;
-    //         a folding KDA window transposes its decayed keys over its gates
-    if (ALGO == ALGO_KDA && fold && nh > 0) transpose_keys(hg, hk, nh, dk, DT_F32, tid, kThreads);
+    // ---- 2. window coefficients A, F (j <= i only) and history dot coefficients
     if (flat) {
       if (early) window_pairs_flat<NT>(T, dk, kpad, qpad, wpitch, gp, wb, am, fm, tid, kThreads);
     } else {
@@ -1077,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
           }
         } else {
           copies_ok = stream_quads<ALGO, ST, NV, CW, MR, true>(pipe, qlane, acc, gtile, dk, dv,
-                                                               nh, ALGO == ALGO_KDA ? hg : hk, hd,
+                                                               nh, hk, hd,
                                                                hf, hscal[1], egam, xh, tid, lane) &&
                       copies_ok;
         }

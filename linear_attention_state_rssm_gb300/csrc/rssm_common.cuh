@@ -118,6 +118,7 @@ struct ReplaySmem {
   uint32_t hdot;   // [L][2NT] history dot coefficients
   uint32_t red;    // [row groups][2NT][dv] partial column sums (on the ring when it fits)
   uint32_t rank;   // decode row order: [kThreads] (slot, cursor), [kWarps] fold masks
+  uint32_t ns;     // tile ring stages
   uint32_t total;
 };
 
@@ -339,15 +340,17 @@ __host__ __device__ inline PrefillSmem prefill_layout(int algo, int dk, int dv) 
 
 constexpr uint32_t kRankBytes = 8u * kThreads + 4u * kWarps;
 
-// Shared memory plan of the replay kernel for a window of T <= NT tokens and a
-// ring of L records.
-__host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, int NT, int T,
-                                                    int L, int dk, int dv, int in_dt, int rk_dt,
-                                                    int rd_dt, bool tc = false) {
+// Shared memory plan of the replay kernel for a window of T <= NT tokens, a
+// ring of L records and a tile ring of `stages` stages.
+__host__ __device__ inline ReplaySmem replay_layout_ns(int algo, int state_bytes, int NT, int T,
+                                                       int L, int dk, int dv, int in_dt,
+                                                       int rk_dt, int rd_dt, bool tc,
+                                                       int stages) {
   ReplaySmem m{};
   const int NV = 2 * NT;
   const bool kda = algo == ALGO_KDA;
-  const TileRing tr(dk, dv, state_bytes, ring_stages(NT, L));
+  const TileRing tr(dk, dv, state_bytes, stages);
+  m.ns = (uint32_t)tr.ns;
   const QuadLayout ql(dv, quad_width(NT), kWarps);
   uint32_t off = 0;
   m.ring = off;  off = align16(off + tr.ns * tr.chunk_bytes);
@@ -368,15 +371,15 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
   m.hk = off;    off = align16(off + 4u * round4(L) * dk);
   m.kl = off;    if (tc && rk_dt == DT_F32) off = align16(off + 4u * 16 * dk);
   {
-    // KDA fp32 keys land in hk and are decay-scaled in place
-    const uint32_t raw = (!kda || rk_dt != DT_F32) ? (uint32_t)(dtype_bytes(rk_dt) * L * dk) : 0u;
+    // ring keys land in hkraw; KDA's record gates land in hk and become the
+    // decayed keys there
+    const uint32_t raw = (uint32_t)(dtype_bytes(rk_dt) * L * dk);
     const uint32_t hc = can_split(algo, NT) ? 4u * NV * dv : 0u;
     m.hkraw = off; off = align16(off + (raw > hc ? raw : hc));
   }
   m.hd = off;    off = align16(off + 4u * L * dv);
   m.hdraw = off; if (rd_dt != DT_F32) off = align16(off + 2u * L * dv);
-  // KDA gates [L][dk]; a folding KDA window reuses them for its transposed keys
-  m.hg = off;    if (kda) off = align16(off + 4u * round4(L) * dk);
+  m.hg = off;
   m.hf = off;    off = align16(off + 4u * L);
   m.hdot = off;  off = align16(off + 4u * L * NV);
   // partial column sums go to the ring once the tile is consumed, if they fit
@@ -388,10 +391,10 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
     off = align16(off + red_bytes);
   }
   // The decode row order sits in the fp32 history keys: nothing writes there
-  // before the CTA barrier that follows the copies (16-bit ring keys land in
-  // hkraw), unless KDA fp32 keys land in place.
+  // before the CTA barrier that follows the copies (ring keys land in hkraw),
+  // unless KDA's gates land there (they get a region of their own).
   m.rank = m.hk;
-  if (NT == 1 && ((kda && rk_dt == DT_F32) || 4u * round4(L) * dk < kRankBytes)) {
+  if (NT == 1 && (kda || 4u * round4(L) * dk < kRankBytes)) {
     m.rank = off;
     off = align16(off + kRankBytes);
   }
@@ -400,6 +403,26 @@ __host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, i
   if (tc && off < 47u * 1024u) off = 47u * 1024u;
   m.total = off;
   return m;
+}
+
+// CTAs of one kernel that fit an SM's 228 KB of shared memory (1 KB of which
+// each CTA's launch reserves)
+__host__ __device__ constexpr uint32_t ctas_per_sm(uint32_t smem) {
+  return 233472u / (smem + 1024u);
+}
+
+// The replay kernel's plan: ring_stages(NT, L) stages, or one fewer where that
+// fits one more CTA per SM (long KDA rings with 16-bit deltas or checkpoints).
+__host__ __device__ inline ReplaySmem replay_layout(int algo, int state_bytes, int NT, int T,
+                                                    int L, int dk, int dv, int in_dt, int rk_dt,
+                                                    int rd_dt, bool tc = false) {
+  const int st = ring_stages(NT, L);
+  const ReplaySmem m = replay_layout_ns(algo, state_bytes, NT, T, L, dk, dv, in_dt, rk_dt, rd_dt,
+                                        tc, st);
+  if (st <= 2) return m;
+  const ReplaySmem m2 = replay_layout_ns(algo, state_bytes, NT, T, L, dk, dv, in_dt, rk_dt,
+                                         rd_dt, tc, st - 1);
+  return ctas_per_sm(m2.total) > ctas_per_sm(m.total) ? m2 : m;
 }
 
 // ----------------------------------------------------------- pipelined replay

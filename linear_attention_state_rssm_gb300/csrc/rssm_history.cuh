@@ -485,7 +485,35 @@ __device__ __forceinline__ bool stream_quads(const PIPE& pipe, const QuadLane& q
         rows[u] = row0 + lr;
         ld_cols<ST, CW>(stg + (size_t)lr * dv, s[u]);
       }
-      if (FOLD) {
+      if (FOLD && ALGO == ALGO_KDA) {
+        // KDA: the decayed keys as computed, [n][dk] (one broadcast load per
+        // record and row)
+#pragma unroll
+        for (int u = 0; u < RS; ++u) {
+          const float dec = egam[rows[u]];
+#pragma unroll
+          for (int c = 0; c < CW; ++c) s[u][c] *= dec;
+#pragma unroll
+          for (int m = 0; m < MRR; ++m) {
+            if (m < n) {
+              const float k = hkt[(size_t)m * dk + rows[u]];
+#pragma unroll
+              for (int c = 0; c < CW; ++c) s[u][c] = fmaf(k, dr[m][c], s[u][c]);
+            }
+          }
+          for (int m = MRR; m < n; ++m) {
+            float dv4[CW];
+            ld_cols<float, CW>(hd + (size_t)m * dv + ql.col0, dv4);
+            const float k = hkt[(size_t)m * dk + rows[u]];
+#pragma unroll
+            for (int c = 0; c < CW; ++c) s[u][c] = fmaf(k, dv4[c], s[u][c]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < RS; ++u) {
+          if (ok && u0 + u < rpl) st_cols<ST, CW>(gtile + (size_t)rows[u] * dv + ql.col0, s[u]);
+        }
+      } else if (FOLD) {
 #pragma unroll
         for (int u = 0; u < RS; ++u) {
           const float dec = ALGO == ALGO_GDN ? gdn_decay : egam[rows[u]];
