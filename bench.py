@@ -42,7 +42,9 @@ WL = dict(workload="Qwen3.5-4B-shaped GDN decode layer", algo="gdn", HK=16, HV=3
           dv=128, batch=64, null_slots=8, L=16, T=1, in_dtype="bf16", state_dtype="f32",
           ring_k_dtype="f16", ring_d_dtype="f32", layers=48)
 VERIFY = dict(workload="GDN speculative verify+commit", batch=128, T=8, L=16,
-              state_dtype="f32", commit_mode="lazy", layers=48)
+              state_dtype="f32", commit_mode="lazy", layers=48, widths=(8, 3))
+VERIFY_FE = dict(VERIFY, workload="GDN speculative verify + fold-every commit (bf16 checkpoint)",
+                 state_dtype="bf16", commit_mode="fold_every")
 ESZ = {"f32": 4, "bf16": 2, "f16": 2}
 PREFILL = dict(workload="Qwen3.5-4B-shaped GDN replay prefill", prompts=8, tokens=4096,
                in_dtype="bf16", state_dtype="f32")
@@ -95,6 +97,14 @@ def job_throughput(tokens_per_rank: float, world: int, t_max_s: float) -> float:
     return world * tokens_per_rank / t_max_s
 
 
+def nt_for(T):
+    """The kernel's window width for a verify of T tokens (powers of two)."""
+    nt = 1
+    while nt < T:
+        nt *= 2
+    return nt
+
+
 def advance(c, T, L, a):
     fold = c + T > L
     return (0 if fold else c) + a, fold
@@ -109,10 +119,10 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def ncu_traffic():
-    """Bytes per launch from the committed ncu summary, if its kernel sources
+def ncu_traffic(name="replay_gdn_decode_qwen_shapes.md"):
+    """Bytes per launch from a committed ncu summary, if its kernel sources
     still hash to what was profiled; else None."""
-    path = os.path.join(ROOT, "profiles", "replay_gdn_decode_qwen_shapes.md")
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
     vals = {}
@@ -132,7 +142,7 @@ def ncu_traffic():
 # The files that define the decode launch the ncu summary describes (kernel,
 # shared-memory plan, launch); a change to any of them invalidates the traffic.
 DECODE_SOURCES = ("replay_impl.cuh", "rssm_history.cuh", "rssm_common.cuh", "rssm_mma.cuh",
-                  "replay_launch.cuh",
+                  "rssm_tc.cuh", "replay_launch.cuh",
                   "replay_gdn_f32.cu")
 
 
@@ -458,6 +468,10 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.empty_cache()
 
     ver = run_verify(args, torch, dev, rank, peak, local_rank) if not args.no_verify else None
+    ver3 = (run_verify(args, torch, dev, rank, peak, local_rank, T=VERIFY["widths"][1])
+            if not args.no_verify else None)
+    ver_fe = (run_verify(args, torch, dev, rank, peak, local_rank, cfg=VERIFY_FE)
+              if not args.no_verify else None)
     kda = run_kda(args, torch, dev, rank, peak, local_rank) if not args.no_kda else None
     pre = run_prefill(args, torch, dev, rank) if not args.no_prefill else None
     conv = run_conv(args, torch, dev, rank, peak) if not args.no_conv else None
@@ -482,6 +496,10 @@ def run_ours(args, rank, world, local_rank):
         res["native_decode"] = native
     if ver is not None:
         res["verify"] = ver
+    if ver3 is not None:
+        res["verify_t3"] = ver3
+    if ver_fe is not None:
+        res["verify_fold_every"] = ver_fe
     if kda is not None:
         res["kda"] = kda
     if pre is not None:
@@ -631,15 +649,37 @@ def max_sm_mhz(index):
         return 2070
 
 
-def run_verify(args, torch, dev, rank, peak, clk_index):
-    """Speculative verify (T = 8) + lazy commit over 48 layers, batch 128. The
+def commit_summary(t_com, steps, com_bytes, fold_every, peak, v, nl):
+    """The commit's own line: one rssm_commit per step (every layer's fold and
+    the cursor kernel for a fold-every store; the cursor kernel alone for a
+    lazy one), timed between CUDA events around its graph."""
+    launch_ms = t_com * 1e3 / steps
+    res = {"launch_ms": launch_ms, "algorithmic_bytes_per_launch": statistics.mean(com_bytes),
+           "covers": "one rssm_commit (every layer)"}
+    if not fold_every:
+        res["note"] = "lazy commit: the cursor kernel only (no state bytes)"
+        return res
+    achieved = statistics.mean(com_bytes) / (launch_ms / 1e3) / 1e9
+    res["note"] = "fold kernel over all layers + cursor kernel"
+    res["per_layer_us"] = launch_ms * 1e3 / nl
+    res["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                       "frac": achieved / peak, "traffic": None,
+                       "kernel": "fold_kernel<GDN, %s, 16>" % v["state_dtype"],
+                       "bytes": "per row with n = base + a > 0 records: checkpoint read and "
+                                "written once + n records (key, delta, gate) read"}
+    return res
+
+
+def run_verify(args, torch, dev, rank, peak, clk_index, T=None, cfg=None):
+    """Speculative verify (T = 8, or 3) + lazy commit over 48 layers, batch 128. The
     verify launches and the commit are captured in two CUDA graphs and timed
     apart (CUDA events between them), so the verify kernel's own launch time
     and bandwidth come out; the host follows the rows' cursors to count each
     launch's algorithmic bytes."""
     from linear_attention_state_rssm_gb300.store import ReplayStore
-    w, v = WL, VERIFY
-    nl, B, T, L = args.layers, v["batch"], v["T"], v["L"]
+    w, v = WL, (VERIFY if cfg is None else cfg)
+    nl, B, L = args.layers, v["batch"], v["L"]
+    T = v["T"] if T is None else T
     HK, HV, dk, dv = w["HK"], w["HV"], w["dk"], w["dv"]
     gen = torch.Generator(device=dev)
     gen.manual_seed(2000 + rank)
@@ -679,7 +719,7 @@ def run_verify(args, torch, dev, rank, peak, clk_index):
             c = cur[r]
             nxt, fold = advance(c, T, L, acc_h[i][r])
             tot += row_bytes(c, T, fold, HK, HV, dk, dv, s_state, 2, 2, 4)
-            if fold_every:  # the commit folds every layer
+            if fold_every and nxt > 0:  # the commit folds every layer (rows with records)
                 ctot += nl * commit_bytes(nxt, HK, HV, dk, dv, s_state, 2, 4)
             cur[r] = 0 if fold_every else nxt
         return tot, ctot
@@ -731,14 +771,12 @@ def run_verify(args, torch, dev, rank, peak, clk_index):
            "accepted_tokens_per_s_per_layer": acc_sum * nl / (t_ver + t_com),
            "ms_per_step": (t_ver + t_com) * 1e3 / args.steps,
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                        "frac": achieved / peak, "traffic": None,
-                        "kernel": "replay_kernel<GDN, f32, 8>",
+                        "frac": achieved / peak,
+                        "traffic": (ncu_traffic("replay_gdn_verify_t8_qwen_shapes.md")
+                                    if T == 8 and v["state_dtype"] == "f32" else None),
+                        "kernel": "replay_kernel<GDN, %s, %d>" % (v["state_dtype"], nt_for(T)),
                         "algorithmic_bytes_per_launch": bytes_launch, "launch_ms": launch_ms},
-           "commit": {"launch_ms": t_com * 1e3 / args.steps,
-                      "algorithmic_bytes_per_launch": statistics.mean(com_bytes),
-                      "covers": "one rssm_commit (every layer)",
-                      "note": "lazy commit: the cursor kernel only (no state bytes)"
-                      if not fold_every else "fold kernel over all layers + cursor kernel"},
+           "commit": commit_summary(t_com, args.steps, com_bytes, fold_every, peak, v, nl),
            "clocks": clk.summary(), "device_error_word": err}
     return res
 
@@ -810,7 +848,7 @@ def run_kda(args, torch, dev, rank, peak, clk_index):
                 c = nxt
                 nxt, fold = advance(c, T, L, acc_h[i][r])
                 vb += row_bytes(c, T, fold, HK, HV, dk, dv, s_state, 2, 2, s_d, dk)
-                if fold_every:  # the commit folds every layer
+                if fold_every and nxt > 0:  # the commit folds every layer (rows with records)
                     cb += nl * commit_bytes(nxt, HK, HV, dk, dv, s_state, 2, s_d, dk)
                 cur[r] = 0 if fold_every else nxt
             if record:
@@ -873,7 +911,7 @@ def run_kda(args, torch, dev, rank, peak, clk_index):
             ach = cbl / (cms / 1e3) / 1e9
             res["commit"]["roofline"] = {"bound": "hbm", "achieved": ach, "peak": peak,
                                          "unit": "GB/s", "frac": ach / peak,
-                                         "kernel": f"fold_kernel<KDA, {sdt}>"}
+                                         "kernel": f"fold_kernel<KDA, {sdt}, 32>"}
         out_all.append(res)
     return {"workload": k_["workload"], "batch": B, "L": L, "HK": HK, "HV": HV, "dk": dk,
             "dv": dv, "layers": nl, "in_dtype": "bf16",
