@@ -183,72 +183,99 @@ __device__ __forceinline__ void decode_dots(int nh, int dk, const void* hkraw, i
   }
 }
 
-// GDN window coefficients with one thread per pair (i, j), j <= i: plain dot
-// products over copies of the window keys and queries whose rows are padded
-// to `pitch` floats (so the rows a warp reads fall in different banks); no
-// shuffles. gp holds the inclusive gate prefixes.
+// GDN window coefficients, four consecutive threads per pair (i, j), j <= i:
+// thread q of a pair takes the channels 4q + 16 s (so the four read one 64-byte
+// span of a row) of copies of the window keys and queries whose rows are
+// padded to `pitch` floats; two shuffles finish each sum. gp holds the
+// inclusive gate prefixes. Every thread of the CTA (t < nt, nt a multiple of
+// 32) runs the same number of rounds.
 template <int NT>
 __device__ __forceinline__ void window_pairs_flat(int T, int dk, const float* kp,
                                                   const float* qp, int pitch, const float* gp,
                                                   const float* wb, float* am, float* fm, int t,
                                                   int nt) {
+  constexpr int S = 4;  // threads per pair
   const int npairs = T * (T + 1) / 2;
-  for (int pidx = t; pidx < npairs; pidx += nt) {
-    int i = 0;
-    while ((i + 1) * (i + 2) / 2 <= pidx) ++i;
-    const int j = pidx - i * (i + 1) / 2;
-    const float* kj = kp + j * pitch;
-    const float* ki = kp + i * pitch;
-    const float* qi = qp + i * pitch;
-    float sk0 = 0.f, sk1 = 0.f, sq0 = 0.f, sq1 = 0.f;
-    for (int c4 = 0; c4 < dk; c4 += 8) {
-      const float4 a = ld4(kj + c4), b = ld4(ki + c4), c = ld4(qi + c4);
-      const float4 a2 = ld4(kj + c4 + 4), b2 = ld4(ki + c4 + 4), c2 = ld4(qi + c4 + 4);
-      sk0 = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, sk0))));
-      sq0 = fmaf(a.x, c.x, fmaf(a.y, c.y, fmaf(a.z, c.z, fmaf(a.w, c.w, sq0))));
-      sk1 = fmaf(a2.x, b2.x, fmaf(a2.y, b2.y, fmaf(a2.z, b2.z, fmaf(a2.w, b2.w, sk1))));
-      sq1 = fmaf(a2.x, c2.x, fmaf(a2.y, c2.y, fmaf(a2.z, c2.z, fmaf(a2.w, c2.w, sq1))));
+  for (int base = 0; base < npairs * S; base += nt) {
+    const int pidx = (base + t) / S, q = (base + t) % S;
+    const bool act = pidx < npairs;
+    int i = 0, j = 0;
+    float sk = 0.f, sq = 0.f;
+    if (act) {
+      while ((i + 1) * (i + 2) / 2 <= pidx) ++i;
+      j = pidx - i * (i + 1) / 2;
+      const float* kj = kp + j * pitch;
+      const float* ki = kp + i * pitch;
+      const float* qi = qp + i * pitch;
+      float sk1 = 0.f, sq1 = 0.f;
+      for (int c4 = 4 * q; c4 < dk; c4 += 8 * S) {
+        const float4 a = ld4(kj + c4), b = ld4(ki + c4), c = ld4(qi + c4);
+        sk = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, sk))));
+        sq = fmaf(a.x, c.x, fmaf(a.y, c.y, fmaf(a.z, c.z, fmaf(a.w, c.w, sq))));
+        if (c4 + 4 * S < dk) {
+          const float4 a2 = ld4(kj + c4 + 4 * S), b2 = ld4(ki + c4 + 4 * S),
+                       c2 = ld4(qi + c4 + 4 * S);
+          sk1 = fmaf(a2.x, b2.x, fmaf(a2.y, b2.y, fmaf(a2.z, b2.z, fmaf(a2.w, b2.w, sk1))));
+          sq1 = fmaf(a2.x, c2.x, fmaf(a2.y, c2.y, fmaf(a2.z, c2.z, fmaf(a2.w, c2.w, sq1))));
+        }
+      }
+      sk += sk1;
+      sq += sq1;
     }
-    const float wgt = __expf(gp[i] - gp[j]);
-    fm[i * NT + j] = wgt * (sq0 + sq1);
-    am[i * NT + j] = (j < i) ? wb[i] * wgt * (sk0 + sk1) : 0.f;
+#pragma unroll
+    for (int off = 1; off < S; off <<= 1) {
+      sk += __shfl_xor_sync(kFull, sk, off);
+      sq += __shfl_xor_sync(kFull, sq, off);
+    }
+    if (act && q == 0) {
+      const float wgt = __expf(gp[i] - gp[j]);
+      fm[i * NT + j] = wgt * sq;
+      am[i * NT + j] = (j < i) ? wb[i] * wgt * sk : 0.f;
+    }
   }
 }
 
-// History dot coefficients hdot[m][v] of the records m = w, w + nw, ...:
-// GDN: raw keys against raw window vectors, times hf[m] e^{G_i};
-// KDA: decayed keys against e^{G_i} x (xk, xq = yk, yq).
+// History dot coefficients hdot[m][v]: GDN: raw keys against raw window
+// vectors, times hf[m] e^{G_i}; KDA: decayed keys against e^{G_i} x (xk, xq =
+// yk, yq). Warp w takes the groups of 32 / NV records starting at record
+// (w + k nw) 32 / NV; each lane sums its channels' products for every (record,
+// vector) of the group and one reduce-scatter leaves the full sum of value l in
+// lane l (31 shuffles per group instead of five per value).
 template <int ALGO, int NT>
 __device__ __forceinline__ void history_dots(int nh, int T, int dk, const float* hk,
                                              const float* xk, const float* xq, const float* hf,
                                              const float* eG, float* hdot, int w, int nw,
                                              int lane) {
   constexpr int NV = 2 * NT;
-  for (int m = w; m < nh; m += nw) {
-    float part[NV];
+  static_assert(32 % NV == 0, "vectors per record divide the warp");
+  constexpr int RPI = 32 / NV;  // records per reduce-scatter
+  for (int m0 = w * RPI; m0 < nh; m0 += nw * RPI) {
+    float v[32];
 #pragma unroll
-    for (int vv = 0; vv < NV; ++vv) part[vv] = 0.f;
+    for (int e = 0; e < 32; ++e) v[e] = 0.f;
     for (int c4 = 4 * lane; c4 < dk; c4 += 128) {
-      const float4 km = ld4(hk + m * dk + c4);
 #pragma unroll
       for (int vv = 0; vv < NV; ++vv) {
         const int i = vv < NT ? vv : vv - NT;
         if (i < T) {
           const float4 x = ld4((vv < NT ? xk : xq) + i * dk + c4);
-          part[vv] = fmaf(km.x, x.x, fmaf(km.y, x.y, fmaf(km.z, x.z, fmaf(km.w, x.w, part[vv]))));
+#pragma unroll
+          for (int r = 0; r < RPI; ++r) {
+            if (m0 + r < nh) {
+              const float4 km = ld4(hk + (m0 + r) * dk + c4);
+              float& a = v[r * NV + vv];
+              a = fmaf(km.x, x.x, fmaf(km.y, x.y, fmaf(km.z, x.z, fmaf(km.w, x.w, a))));
+            }
+          }
         }
       }
     }
-#pragma unroll
-    for (int vv = 0; vv < NV; ++vv) part[vv] = warp_sum(part[vv]);
-    if (lane == 0) {
-#pragma unroll
-      for (int vv = 0; vv < NV; ++vv) {
-        const int i = vv < NT ? vv : vv - NT;
-        float hv = 0.f;
-        if (i < T) hv = (ALGO == ALGO_GDN) ? part[vv] * hf[m] * eG[i] : part[vv];
-        hdot[m * NV + vv] = hv;
-      }
+    const float sum = warp_reduce_scatter32(v, lane);
+    const int m = m0 + lane / NV, vv = lane % NV, i = vv < NT ? vv : vv - NT;
+    if (m < nh) {
+      float hv = 0.f;
+      if (i < T) hv = (ALGO == ALGO_GDN) ? sum * hf[m] * eG[i] : sum;
+      hdot[m * NV + vv] = hv;
     }
   }
 }
