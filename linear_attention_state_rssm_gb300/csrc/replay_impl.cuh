@@ -983,7 +983,8 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     }
     if (nh > 0 && !fold) copies_ok = mbar_wait_bounded(&mbar[kMbarHist], 0, lim) && copies_ok;
     if (nh > 0) {
-      if (p.rd_dt != DT_F32) widen16(hd, hdraw, nh * dv, p.rd_dt, tid, kThreads);
+      // (KDA reads fp16 deltas as they landed)
+      if (p.rd_dt != DT_F32 && ALGO == ALGO_GDN) widen16(hd, hdraw, nh * dv, p.rd_dt, tid, kThreads);
       if (ALGO == ALGO_GDN) {
         if (fold && TC && tc) {
           float* kl = p.rk_dt == DT_F32 ? reinterpret_cast<float*>(smem + p.sm.kl) : nullptr;
@@ -1102,9 +1103,9 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
                         copies_ok;
           }
         } else {
-          copies_ok = stream_quads<ALGO, ST, NV, CW, MR, true>(pipe, qlane, acc, gtile, dk, dv,
-                                                               nh, hk, hd,
-                                                               hf, hscal[1], egam, xh, tid, lane) &&
+          copies_ok = stream_quads<ALGO, ST, NV, CW, MR, true>(
+                          pipe, qlane, acc, gtile, dk, dv, nh, hk, hd, hf, hscal[1], egam, xh, tid,
+                          lane, ALGO == ALGO_KDA ? p.rd_dt : (int)DT_F32) &&
                       copies_ok;
         }
       } else if (TC && tc) {
@@ -1207,8 +1208,10 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
 #pragma unroll
       for (int vv = 0; vv < NV; ++vv) y[vv] += hc[vv * dv + col];
     } else if (!fold) {
+      const bool d16 = ALGO == ALGO_KDA && p.rd_dt != DT_F32;
       for (int m = 0; m < nh; ++m) {
-        const float dm = hd[m * dv + col];
+        const float dm = d16 ? __half2float(reinterpret_cast<const __half*>(hd)[m * dv + col])
+                             : hd[m * dv + col];
         const float* hm = hdot + m * NV;
 #pragma unroll
         for (int vv = 0; vv < NV; ++vv) y[vv] = fmaf(hm[vv], dm, y[vv]);

@@ -377,8 +377,11 @@ __host__ __device__ inline ReplaySmem replay_layout_ns(int algo, int state_bytes
     const uint32_t hc = can_split(algo, NT) ? 4u * NV * dv : 0u;
     m.hkraw = off; off = align16(off + (raw > hc ? raw : hc));
   }
-  m.hd = off;    off = align16(off + 4u * L * dv);
+  // (KDA reads 16-bit deltas where they landed: no widened copy)
+  const bool kda_d16 = kda && rd_dt != DT_F32;
+  m.hd = off;    if (!kda_d16) off = align16(off + 4u * L * dv);
   m.hdraw = off; if (rd_dt != DT_F32) off = align16(off + 2u * L * dv);
+  if (kda_d16) m.hd = m.hdraw;
   m.hg = off;
   m.hf = off;    off = align16(off + 4u * L);
   m.hdot = off;  off = align16(off + 4u * L * NV);

@@ -445,13 +445,17 @@ struct QuadLane {
 // [n][dv]. Then acc[v] += x_v[row] S[row] for the NV mat-vec vectors (xh
 // [dk][NV]). Sums over the rows of one warp instruction are reduced before
 // returning.
+// hd_dt: the dtype of the deltas at hd (fp32, or fp16 read as they landed).
 template <int ALGO, typename ST, int NV, int CW, int MR, bool FOLD, class PIPE>
 __device__ __forceinline__ bool stream_quads(const PIPE& pipe, const QuadLane& ql,
                                              float (&acc)[NV][CW], ST* gtile, int dk, int dv,
                                              int n, const float* hkt, const float* hd,
                                              const float* hf, float gdn_decay,
                                              const float* egam, const float* xh, int tid,
-                                             int lane) {
+                                             int lane, int hd_dt = DT_F32) {
+  auto hd_at = [&](size_t i) {
+    return hd_dt == DT_F32 ? hd[i] : __half2float(reinterpret_cast<const __half*>(hd)[i]);
+  };
   constexpr int RS = FOLD ? 2 : 4;  // rows held in registers at a time
   constexpr int MRR = FOLD ? MR : 1;
   const int ks = round4(n);
@@ -464,7 +468,7 @@ __device__ __forceinline__ bool stream_quads(const PIPE& pipe, const QuadLane& q
       if (m < n) {
         const float f = ALGO == ALGO_GDN ? hf[m] : 1.f;
 #pragma unroll
-        for (int c = 0; c < CW; ++c) dr[m][c] = f * hd[(size_t)m * dv + ql.col0 + c];
+        for (int c = 0; c < CW; ++c) dr[m][c] = f * hd_at((size_t)m * dv + ql.col0 + c);
       }
     }
   }
@@ -503,7 +507,12 @@ __device__ __forceinline__ bool stream_quads(const PIPE& pipe, const QuadLane& q
           }
           for (int m = MRR; m < n; ++m) {
             float dv4[CW];
-            ld_cols<float, CW>(hd + (size_t)m * dv + ql.col0, dv4);
+            if (hd_dt == DT_F32) {
+              ld_cols<float, CW>(hd + (size_t)m * dv + ql.col0, dv4);
+            } else {
+#pragma unroll
+              for (int c = 0; c < CW; ++c) dv4[c] = hd_at((size_t)m * dv + ql.col0 + c);
+            }
             const float k = hkt[(size_t)m * dk + rows[u]];
 #pragma unroll
             for (int c = 0; c < CW; ++c) s[u][c] = fmaf(k, dv4[c], s[u][c]);
