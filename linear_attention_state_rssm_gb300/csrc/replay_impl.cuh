@@ -1133,13 +1133,12 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     }
   }
   // partial column sums of the warp row groups -> shared memory (the ring is
-  // free once every warp has consumed the last chunk); a tensor-core fold
-  // leaves whole column sums, in the first row-group slot
+  // free once every warp has consumed the last chunk); the tensor-core streams
+  // leave whole column sums, in the first row-group slot
   __syncthreads();
   if (TC && tc) {
     if constexpr (TC) {
       copies_ok = tc_read_y<NV>(tcs, red, dv, tid, warp) && copies_ok;
-      for (int e = tid; e < (qlay.rgw - 1) * NV * dv; e += kThreads) red[NV * dv + e] = 0.f;
     }
   } else if (mma_fold) {
     if constexpr (NT == 1) {
@@ -1154,7 +1153,6 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
           }
         }
       }
-      for (int e = tid; e < (qlay.rgw - 1) * NV * dv; e += kThreads) red[NV * dv + e] = 0.f;
     }
   } else if (mmas) {
     if constexpr (kMmaNT) {
@@ -1167,7 +1165,6 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
       } else {
         red_mma<NTN, 2>(red, ymm, warp, lane);
       }
-      for (int e = tid; e < (qlay.rgw - 1) * NV * dv; e += kThreads) red[NV * dv + e] = 0.f;
     }
   } else if (warp < sw && qlane.first) {
 #pragma unroll
@@ -1186,13 +1183,15 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   if (fold && all_ok) write_kgb();
 
   // ---- 4. per value column: corrections, triangular solve, outputs, deltas
+  //      (the tensor-core streams leave whole column sums in row group 0)
+  const int rgu = (tc || mma_fold || mmas) ? 1 : qlay.rgw;
   if (tid < dv && all_ok) {
     const int col = tid;
     float y[NV];
 #pragma unroll
     for (int vv = 0; vv < NV; ++vv) {
       float sum = 0.f;
-      for (int g2 = 0; g2 < qlay.rgw; ++g2) sum += red[(g2 * NV + vv) * dv + col];
+      for (int g2 = 0; g2 < rgu; ++g2) sum += red[(g2 * NV + vv) * dv + col];
       y[vv] = sum;
     }
     if (ALGO == ALGO_GDN) {
