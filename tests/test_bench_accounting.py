@@ -55,3 +55,21 @@ def test_commit_bytes_fold_every():
     # KDA: a gate per key channel, bf16 checkpoint, fp16 keys and deltas
     assert bench.commit_bytes(3, 32, 32, 128, 128, 2, 2, 2, 128) == \
         2 * 32 * 128 * 128 * 2 + 3 * (32 * 128 * 2 + 32 * 128 * 2 + 32 * 128 * 4)
+
+
+@pytest.mark.parametrize("T,nt", [(1, 1), (2, 2), (3, 4), (4, 4), (5, 8), (8, 8), (9, 16)])
+def test_window_width_of_the_kernel(T, nt):
+    """The verify line names the kernel by its window width: the smallest
+    power of two at least T (the library's own choice of instantiation)."""
+    assert bench.nt_for(T) == nt
+
+
+def test_commit_summary_carries_a_roofline_only_for_a_folding_commit():
+    v = {"state_dtype": "bf16"}
+    lazy = bench.commit_summary(0.001, 10, [0.0, 0.0], False, 6000.0, v, 48)
+    assert "roofline" not in lazy and lazy["launch_ms"] == pytest.approx(0.1)
+    # 3 MB per step in 60 us per step: 50 GB/s
+    fe = bench.commit_summary(0.0006, 10, [3e6, 3e6], True, 6000.0, v, 48)
+    assert fe["roofline"]["achieved"] == pytest.approx(50.0)
+    assert fe["roofline"]["frac"] == pytest.approx(50.0 / 6000.0)
+    assert fe["per_layer_us"] == pytest.approx(60.0 / 48)
