@@ -779,9 +779,15 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   //      vectors (their scalar decay goes on the column results)
   bool copies_ok = mbar_wait_bounded(&mbar[kMbarWin], 0, lim);
   if (!f32in) {
-    widen16(wq, wraw, T * dk, p.in_dt, tid, kThreads);
-    widen16(wk, wraw + T * qrow, T * dk, p.in_dt, tid, kThreads);
-    widen16(wv, wraw + 2 * T * qrow, T * dv, p.in_dt, tid, kThreads);
+    if constexpr (NT >= 4) {  // (dk and dv are multiples of 32)
+      widen16x8(wq, wraw, T * dk, p.in_dt, tid, kThreads);
+      widen16x8(wk, wraw + T * qrow, T * dk, p.in_dt, tid, kThreads);
+      widen16x8(wv, wraw + 2 * T * qrow, T * dv, p.in_dt, tid, kThreads);
+    } else {
+      widen16(wq, wraw, T * dk, p.in_dt, tid, kThreads);
+      widen16(wk, wraw + T * qrow, T * dk, p.in_dt, tid, kThreads);
+      widen16(wv, wraw + 2 * T * qrow, T * dv, p.in_dt, tid, kThreads);
+    }
   }
   if (TC && tc) {
     // K-major X [16 vectors x dk rows]; fp32 inputs split into hi (xh) and lo
@@ -802,18 +808,37 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
       }
     }
     fence_async_smem();
+  } else if (ALGO == ALGO_GDN && mmas) {
+    if constexpr (kMmaNT) {
+      // fragment order (x_slot): a lane-step of 2 NTN consecutive slots holds
+      // the channel pair (c, c + 1) of NTN vectors, one paired load each
+      const void* qsrc = f32in ? static_cast<const void*>(wq) : wraw;
+      const void* ksrc = f32in ? static_cast<const void*>(wk) : wraw + T * qrow;
+      constexpr int CPL = 2 * NTN;
+      for (int st = tid; st < dk * NV / CPL; st += kThreads) {
+        const int ln = st & 31, c = 8 * (st >> 5) + 2 * (ln & 3), vl = ln >> 2;
+        float x[CPL];
+#pragma unroll
+        for (int m = 0; m < NTN; ++m) {
+          const int v = 8 * m + vl, i = v < NT ? v : v - NT;
+          float2 pr = make_float2(0.f, 0.f);
+          if (i < T) pr = ld2_f32(v < NT ? ksrc : qsrc, (size_t)i * dk + c, p.in_dt);
+          x[2 * m] = pr.x;
+          x[2 * m + 1] = pr.y;
+        }
+        if constexpr (CPL == 4) {
+          *reinterpret_cast<float4*>(xh + 4 * st) = make_float4(x[0], x[1], x[2], x[3]);
+        } else {
+          *reinterpret_cast<float2*>(xh + 2 * st) = make_float2(x[0], x[1]);
+        }
+      }
+    }
   } else if (ALGO == ALGO_GDN) {
     const void* qsrc = f32in ? static_cast<const void*>(wq) : wraw;
     const void* ksrc = f32in ? static_cast<const void*>(wk) : wraw + T * qrow;
     for (int e = tid; e < dk * NV; e += kThreads) {
-      // slot e holds (row ch, vector vv): row-major, or in fragment order
-      int ch, vv;
-      if (mmas) {
-        x_slot<NTN>(e, ch, vv);
-      } else {
-        ch = e / NV;
-        vv = e - ch * NV;
-      }
+      // slot e holds (row ch, vector vv), row-major
+      const int ch = e / NV, vv = e - ch * NV;
       const int i = vv < NT ? vv : vv - NT;
       xh[e] = i < T ? ld_f32(vv < NT ? ksrc : qsrc, (size_t)i * dk + ch, p.in_dt) : 0.f;
     }

@@ -609,6 +609,44 @@ __device__ __forceinline__ float ld_f32(const void* base, size_t i, int dt) {
   return __half2float(static_cast<const __half*>(base)[i]);
 }
 
+// Two consecutive values at element i (i even) as fp32.
+__device__ __forceinline__ float2 ld2_f32(const void* base, size_t i, int dt) {
+  if (dt == DT_F32) return *reinterpret_cast<const float2*>(static_cast<const float*>(base) + i);
+  if (dt == DT_BF16) {
+    return __bfloat1622float2(
+        *reinterpret_cast<const __nv_bfloat162*>(static_cast<const __nv_bfloat16*>(base) + i));
+  }
+  return __half22float2(*reinterpret_cast<const __half2*>(static_cast<const __half*>(base) + i));
+}
+
+// Widen n 16-bit values (bf16 or fp16) in shared memory to fp32, eight at a
+// time (n a multiple of 8, both buffers 16-byte aligned).
+__device__ __forceinline__ void widen16x8(float* dst, const void* src, int n, int dt, int tid,
+                                          int nthreads) {
+  {
+    const uint4* s8 = static_cast<const uint4*>(src);
+    float4* d4 = reinterpret_cast<float4*>(dst);
+    for (int e = tid; e < n / 8; e += nthreads) {
+      const uint4 u = s8[e];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      float f[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float2 t;
+        if (dt == DT_BF16) {
+          t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+        } else {
+          t = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+        }
+        f[2 * k] = t.x;
+        f[2 * k + 1] = t.y;
+      }
+      d4[2 * e] = make_float4(f[0], f[1], f[2], f[3]);
+      d4[2 * e + 1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+  }
+}
+
 // Widen n 16-bit values (bf16 or fp16) in shared memory to fp32.
 __device__ __forceinline__ void widen16(float* dst, const void* src, int n, int dt, int tid,
                                         int nthreads) {
