@@ -1063,6 +1063,12 @@ SWEEP = [  # (algo, B, L, T, state dtype, commit mode); decode when T == 1
 ]
 
 
+# the full throughput grid: GDN and KDA x batch x ring length x window width x
+# checkpoint dtype, lazy commit
+GRID = [(algo, B, L, T, st, "lazy") for algo in ("gdn", "kda") for st in ("f32", "bf16")
+        for L in (16, 32, 64) for T in (1, 3, 8) for B in (1, 8, 64, 128, 256)]
+
+
 def sweep_point(torch, dev, algo, B, L, T, state_dtype, mode, steps, warmup, peak, plan="auto"):
     """Steady-state decode (T = 1) or verify + commit (T > 1) over enough
     stacked layers that the checkpoints exceed L2; per-layer time from CUDA
@@ -1160,9 +1166,11 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     peak, peak_kind = peaks()
-    pts = [sweep_point(torch, dev, *pt, steps=args.steps, warmup=args.warmup, peak=peak,
-                       plan=args.plan)
-           for pt in SWEEP]
+    pts = []
+    for pt in (GRID if args.grid == "full" else SWEEP):
+        pts.append(sweep_point(torch, dev, *pt, steps=args.steps, warmup=args.warmup, peak=peak,
+                               plan=args.plan))
+        print(json.dumps(pts[-1]), file=sys.stderr, flush=True)  # progress
     return {"sweep": pts, "peak_gbs": peak, "peak_kind": peak_kind,
             "note": "per-layer time includes the step's cursor advance (decode) or commit "
                     "(verify); bytes count the replay launches only"}
@@ -1186,6 +1194,8 @@ def main():
                     help="kernel family for GDN decode/verify (rssm_set_plan)")
     ap.add_argument("--sweep", action="store_true",
                     help="print the steady-state grid (batch, L, T, state dtype, GDN/KDA)")
+    ap.add_argument("--grid", default="short", choices=["short", "full"],
+                    help="--sweep over the short list or the full batch x L x T x dtype grid")
     ap.add_argument("--prefill-prompts", type=int, default=PREFILL["prompts"])
     ap.add_argument("--prefill-tokens", type=int, default=PREFILL["tokens"])
     args = ap.parse_args()

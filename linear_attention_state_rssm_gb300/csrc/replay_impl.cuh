@@ -316,18 +316,21 @@ __device__ __forceinline__ int swap_rank(const unsigned* fmask, int y) {
   return y;
 }
 
-// Decode fold of a GDN window with at most 16 history records and 128 value
-// columns on the tensor cores: each 16-row tile of the checkpoint is folded as
-//     S <- e^Gam S + K~^T D~,   K~^T [16 rows x 16 records], D~ [16 records x 128]
+// Decode fold of a GDN window with at most 16 history records (LONG: up to
+// kMmaFoldRecords) and 128 value columns on the tensor cores: each 16-row tile
+// of the checkpoint is folded as
+//     S <- e^Gam S + K~^T D~,   K~^T [16 rows x n records], D~ [n records x 128]
 // with the keys transposed in hkt (row stride round4(n); records >= n read as
-// zero), D~ = f_m d_m held as tensor-core fragments for the whole tile (f_m =
-// hf[m], the decay from record m to the end of the history), the tile rows
-// from the ring stage as the fp32 accumulator, the folded rows stored back to
-// the checkpoint and fed to the mat-vec y_v = S^T x_v (x from xh [dk][2]). Warp w owns value columns
+// zero), D~ = f_m d_m (f_m = hf[m], the decay from record m to the end of the
+// history), the tile rows from the ring stage as the fp32 accumulator, the
+// folded rows stored back to the checkpoint and fed to the mat-vec
+// y_v = S^T x_v (x from xh [dk][2]). The D~ fragments of records [0, 16) stay
+// in registers for the whole tile; those of later records (LONG) come from
+// hd, which holds f_m d_m in place for m >= 16. Warp w owns value columns
 // [32w, 32w + 32); y[nt][c][v] ends as the column sums of its columns
 // 32w + 8nt + 2t + c in the lanes with g = 0. Keys from a 16-bit ring are
 // exact in tf32 (EXACT_K).
-template <typename ST, bool EXACT_K>
+template <typename ST, bool EXACT_K, bool LONG>
 __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const float* hkt,
                                                 const float* hd, const float* hf, int n,
                                                 float decay, const float* xh, ST* gtile, int tid,
@@ -354,6 +357,14 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
       y[nt][c][1] = 0.f;
     }
   }
+  // A fragment of records ma = 8 kq + t and ma + 4 for rows ra and ra + 8
+  auto key_frag = [&](int ra, int kq, Tf32 (&a)[4]) {
+    const int rb = ra + 8, ma = 8 * kq + t, mb = ma + 4;
+    a[0] = tf32_split<EXACT_K>(ma < n ? hkt[ra * ks + ma] : 0.f);
+    a[1] = tf32_split<EXACT_K>(ma < n ? hkt[rb * ks + ma] : 0.f);
+    a[2] = tf32_split<EXACT_K>(mb < n ? hkt[ra * ks + mb] : 0.f);
+    a[3] = tf32_split<EXACT_K>(mb < n ? hkt[rb * ks + mb] : 0.f);
+  };
   bool ok = true;
   const int cr = pipe.tr.cr;
   for (int j = 0; j < pipe.tr.nchunk; ++j) {
@@ -363,24 +374,12 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
       const int ra = j * cr + m0 + g, rb = ra + 8;  // this lane's two tile rows
       Tf32 af[2][4];
 #pragma unroll
-      for (int kq = 0; kq < 2; ++kq) {
-        const int ma = 8 * kq + t, mb = ma + 4;
-        af[kq][0] = tf32_split<EXACT_K>(ma < n ? hkt[ra * ks + ma] : 0.f);
-        af[kq][1] = tf32_split<EXACT_K>(ma < n ? hkt[rb * ks + ma] : 0.f);
-        af[kq][2] = tf32_split<EXACT_K>(mb < n ? hkt[ra * ks + mb] : 0.f);
-        af[kq][3] = tf32_split<EXACT_K>(mb < n ? hkt[rb * ks + mb] : 0.f);
-      }
+      for (int kq = 0; kq < 2; ++kq) key_frag(ra, kq, af[kq]);
       const float xa0 = xh[ra * NV], xa1 = xh[ra * NV + 1];
       const float xb0 = xh[rb * NV], xb1 = xh[rb * NV + 1];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
+      // fold of one n-tile's accumulator done: store it back, mat-vec
+      auto finish = [&](int nt, const float (&acc)[4]) {
         const int col = c0 + 8 * nt + 2 * t;
-        float sa[2], sb[2];
-        ld_cols<ST, 2>(stg + (size_t)(m0 + g) * DV + col, sa);
-        ld_cols<ST, 2>(stg + (size_t)(m0 + g + 8) * DV + col, sb);
-        float acc[4] = {decay * sa[0], decay * sa[1], decay * sb[0], decay * sb[1]};
-        mma_split<EXACT_K, false>(acc, af[0], bf[0][nt]);
-        if (n > 8) mma_split<EXACT_K, false>(acc, af[1], bf[1][nt]);
         float wa[2] = {acc[0], acc[1]}, wb[2] = {acc[2], acc[3]};
         if (ok) {
           st_cols<ST, 2>(gtile + (size_t)ra * DV + col, wa);
@@ -391,6 +390,49 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
         y[nt][0][1] = fmaf(wa[0], xa1, fmaf(wb[0], xb1, y[nt][0][1]));
         y[nt][1][0] = fmaf(wa[1], xa0, fmaf(wb[1], xb0, y[nt][1][0]));
         y[nt][1][1] = fmaf(wa[1], xa1, fmaf(wb[1], xb1, y[nt][1][1]));
+      };
+      if constexpr (!LONG) {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const int col = c0 + 8 * nt + 2 * t;
+          float sa[2], sb[2];
+          ld_cols<ST, 2>(stg + (size_t)(m0 + g) * DV + col, sa);
+          ld_cols<ST, 2>(stg + (size_t)(m0 + g + 8) * DV + col, sb);
+          float acc[4] = {decay * sa[0], decay * sa[1], decay * sb[0], decay * sb[1]};
+          mma_split<EXACT_K, false>(acc, af[0], bf[0][nt]);
+          if (n > 8) mma_split<EXACT_K, false>(acc, af[1], bf[1][nt]);
+          finish(nt, acc);
+        }
+      } else {
+        // all four n-tiles' accumulators stay live over the later records
+        float acc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const int col = c0 + 8 * nt + 2 * t;
+          float sa[2], sb[2];
+          ld_cols<ST, 2>(stg + (size_t)(m0 + g) * DV + col, sa);
+          ld_cols<ST, 2>(stg + (size_t)(m0 + g + 8) * DV + col, sb);
+          acc[nt][0] = decay * sa[0];
+          acc[nt][1] = decay * sa[1];
+          acc[nt][2] = decay * sb[0];
+          acc[nt][3] = decay * sb[1];
+          mma_split<EXACT_K, false>(acc[nt], af[0], bf[0][nt]);
+          if (n > 8) mma_split<EXACT_K, false>(acc[nt], af[1], bf[1][nt]);
+        }
+        for (int kq = 2; 8 * kq < n; ++kq) {
+          Tf32 ak[4];
+          key_frag(ra, kq, ak);
+          const int ma = 8 * kq + t, mb = ma + 4;
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) {
+            const int cb = c0 + 8 * nt + g;
+            const Tf32 b[2] = {tf32_split<false>(ma < n ? hd[ma * DV + cb] : 0.f),
+                               tf32_split<false>(mb < n ? hd[mb * DV + cb] : 0.f)};
+            mma_split<EXACT_K, false>(acc[nt], ak, b);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) finish(nt, acc[nt]);
       }
     }
     ok = pipe.done(j, tid, lane, ok) && ok;
@@ -415,14 +457,17 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
 
 // Tile stream of a GDN window with 8 NTN mat-vec vectors (four or eight
 // tokens) and 128 value columns on the tensor cores, with the fold of a
-// history of at most 16 records when FOLD. Both products take the value
-// columns as the m index and the checkpoint rows as the reduction or n index,
-// so the fold's accumulator fragment is the mat-vec's A fragment as it stands:
+// history of n records when FOLD. Both products take the value columns as
+// the m index and the checkpoint rows as the reduction or n index, so the
+// fold's accumulator fragment is the mat-vec's A fragment as it stands:
 //     fold     S^T <- e^Gam S^T + D~^T K~     D~^T [128 x n records], K~ [n x rows]
 //     mat-vec  Y^T += S^T X                   X [rows x 8 NTN]
-// with D~ = f_m d_m (f_m = hf[m]). The raw keys (hkf, from frag_keys16) and
-// the window vectors X (xf, see x_slot) are stored in fragment order: one
-// load per lane and step gives all of the step's fragments of each.
+// with D~ = f_m d_m (f_m = hf[m]). The raw keys (hkf, from frag_keys) and the
+// window vectors X (xf, see x_slot) are stored in fragment order: one load
+// per lane and step gives all of the step's fragments of each (of one group
+// of 16 records, for the keys). The D~ fragments of records [0, 16) stay in
+// registers for the whole tile; a longer history (LONG) reads those of each
+// later group at every step from hd, which holds f_m d_m in place for m >= 16.
 // The 128 / (16 MT) streaming warps own 16 MT columns each; lane (g, t) of warp
 // w reads, for each of its MT / 2 column quads q, the four columns
 // 16 MT w + 32 q + 4g .. + 3 of rows 2t and 2t + 1 of each eight-row step (one
@@ -435,7 +480,7 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
 // vector 8 nt + 2t), 1 (same column, next vector), 2 and 3 (the next column).
 // 16-bit checkpoint values, 16-bit inputs (EXACT_X) and 16-bit ring keys
 // (EXACT_K) are exact in tf32. A fold runs on four warps (MT = 2).
-template <typename ST, int NTN, int MT, bool FOLD, bool EXACT_X, bool EXACT_K>
+template <typename ST, int NTN, int MT, bool FOLD, bool EXACT_X, bool EXACT_K, bool LONG>
 __device__ __forceinline__ bool stream_mma(const TilePipe<ST>& pipe, const float* hkf,
                                            const float* hd, const float* hf, int n, float decay,
                                            const float* xf, ST* gtile, int tid, int warp,
@@ -446,18 +491,42 @@ __device__ __forceinline__ bool stream_mma(const TilePipe<ST>& pipe, const float
   constexpr bool EXACT_S = !std::is_same<ST, float>::value;
   const int g = lane >> 2, t = lane & 3, col = warp * 16 * MT + 4 * g;
   const float4* kf4 = reinterpret_cast<const float4*>(hkf);
-  Tf32 df[2][2][4];  // fold A fragments: [m-tile][record step][4]
-  if (FOLD) {
+  const int ng = FOLD && LONG ? (n + 15) >> 4 : 1;  // groups of 16 history records
+  // fold A fragments of records m0 = t (+ 8 kq), m0 + 4 and value columns c,
+  // c + 1: one float4 of hd row m holds columns [col, col + 4), i.e. both
+  // m-tiles; f scales the rows that hd does not hold scaled
+  auto d_frag = [&](int m0, float f0, float f1, Tf32 (&a)[2][4]) {
+    const int m1 = m0 + 4;
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f), w = u;
+    if (m0 < n) u = *reinterpret_cast<const float4*>(hd + m0 * DV + col);
+    if (m1 < n) w = *reinterpret_cast<const float4*>(hd + m1 * DV + col);
+    a[0][0] = tf32_split<false>(f0 * u.x);
+    a[0][1] = tf32_split<false>(f0 * u.y);
+    a[0][2] = tf32_split<false>(f1 * w.x);
+    a[0][3] = tf32_split<false>(f1 * w.y);
+    a[1][0] = tf32_split<false>(f0 * u.z);
+    a[1][1] = tf32_split<false>(f0 * u.w);
+    a[1][2] = tf32_split<false>(f1 * w.z);
+    a[1][3] = tf32_split<false>(f1 * w.w);
+  };
+  Tf32 df[2][2][4];  // fold A fragments of records [0, 16): [record step][m-tile][4]
+  if (FOLD && LONG) {
+#pragma unroll
+    for (int kq = 0; kq < 2; ++kq) {
+      const int m0 = 8 * kq + t, m1 = m0 + 4;
+      d_frag(m0, m0 < n ? hf[m0] : 0.f, m1 < n ? hf[m1] : 0.f, df[kq]);
+    }
+  } else if (FOLD) {
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
       for (int kq = 0; kq < 2; ++kq) {
         const int m0 = 8 * kq + t, m1 = m0 + 4, c0 = col + 2 * mt;
         const float f0 = m0 < n ? hf[m0] : 0.f, f1 = m1 < n ? hf[m1] : 0.f;
-        df[mt][kq][0] = tf32_split<false>(m0 < n ? f0 * hd[m0 * DV + c0] : 0.f);
-        df[mt][kq][1] = tf32_split<false>(m0 < n ? f0 * hd[m0 * DV + c0 + 1] : 0.f);
-        df[mt][kq][2] = tf32_split<false>(m1 < n ? f1 * hd[m1 * DV + c0] : 0.f);
-        df[mt][kq][3] = tf32_split<false>(m1 < n ? f1 * hd[m1 * DV + c0 + 1] : 0.f);
+        df[kq][mt][0] = tf32_split<false>(m0 < n ? f0 * hd[m0 * DV + c0] : 0.f);
+        df[kq][mt][1] = tf32_split<false>(m0 < n ? f0 * hd[m0 * DV + c0 + 1] : 0.f);
+        df[kq][mt][2] = tf32_split<false>(m1 < n ? f1 * hd[m1 * DV + c0] : 0.f);
+        df[kq][mt][3] = tf32_split<false>(m1 < n ? f1 * hd[m1 * DV + c0 + 1] : 0.f);
       }
     }
   }
@@ -471,14 +540,15 @@ __device__ __forceinline__ bool stream_mma(const TilePipe<ST>& pipe, const float
     const ST* stg = pipe.stage(j);
     for (int kb = 0; kb < cr; kb += 8) {
       const int r0 = j * cr + kb + 2 * t, r1 = r0 + 1;  // this lane's two tile rows
-      const int fi = ((j * cr + kb) >> 3) * 32 + lane;   // fragment slot of this step
+      const int step = (j * cr + kb) >> 3;
+      const int fi = step * 32 + lane;                    // fragment slot of this step
       float s0[NQ][4], s1[NQ][4];
 #pragma unroll
       for (int q = 0; q < NQ; ++q) {
         ld_cols<ST, 4>(stg + (size_t)(kb + 2 * t) * DV + col + 32 * q, s0[q]);
         ld_cols<ST, 4>(stg + (size_t)(kb + 2 * t + 1) * DV + col + 32 * q, s1[q]);
       }
-      if constexpr (FOLD) {
+      if constexpr (FOLD && !LONG) {
         const float4 k4 = kf4[fi];  // row kb + g: records t, t + 4, 8 + t, 12 + t
         const Tf32 kf[2][2] = {{tf32_split<EXACT_K>(k4.x), tf32_split<EXACT_K>(k4.y)},
                                {tf32_split<EXACT_K>(k4.z), tf32_split<EXACT_K>(k4.w)}};
@@ -486,12 +556,58 @@ __device__ __forceinline__ bool stream_mma(const TilePipe<ST>& pipe, const float
         for (int mt = 0; mt < 2; ++mt) {
           float c[4] = {decay * s0[0][2 * mt], decay * s1[0][2 * mt], decay * s0[0][2 * mt + 1],
                         decay * s1[0][2 * mt + 1]};
-          mma_split<false, EXACT_K>(c, df[mt][0], kf[0]);
-          if (n > 8) mma_split<false, EXACT_K>(c, df[mt][1], kf[1]);
+          mma_split<false, EXACT_K>(c, df[0][mt], kf[0]);
+          if (n > 8) mma_split<false, EXACT_K>(c, df[1][mt], kf[1]);
           s0[0][2 * mt] = c[0];
           s1[0][2 * mt] = c[1];
           s0[0][2 * mt + 1] = c[2];
           s1[0][2 * mt + 1] = c[3];
+        }
+        if (ok) {
+          st_cols<ST, 4>(gtile + (size_t)r0 * DV + col, s0[0]);
+          st_cols<ST, 4>(gtile + (size_t)r1 * DV + col, s1[0]);
+        }
+      } else if constexpr (FOLD) {
+        float c[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          c[mt][0] = decay * s0[0][2 * mt];
+          c[mt][1] = decay * s1[0][2 * mt];
+          c[mt][2] = decay * s0[0][2 * mt + 1];
+          c[mt][3] = decay * s1[0][2 * mt + 1];
+        }
+        {
+          // row kb + g: records t, t + 4, t + 8, t + 12
+          const float4 k4 = kf4[step * ng * 32 + lane];
+          const Tf32 kf[2][2] = {{tf32_split<EXACT_K>(k4.x), tf32_split<EXACT_K>(k4.y)},
+                                 {tf32_split<EXACT_K>(k4.z), tf32_split<EXACT_K>(k4.w)}};
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            mma_split<false, EXACT_K>(c[mt], df[0][mt], kf[0]);
+            if (n > 8) mma_split<false, EXACT_K>(c[mt], df[1][mt], kf[1]);
+          }
+        }
+        for (int q = 1; q < ng; ++q) {
+          // records 16q + t, + t + 4, + t + 8, + t + 12
+          const float4 k4 = kf4[(step * ng + q) * 32 + lane];
+          const Tf32 kf[2][2] = {{tf32_split<EXACT_K>(k4.x), tf32_split<EXACT_K>(k4.y)},
+                                 {tf32_split<EXACT_K>(k4.z), tf32_split<EXACT_K>(k4.w)}};
+#pragma unroll
+          for (int kq = 0; kq < 2; ++kq) {
+            if (16 * q + 8 * kq < n) {
+              Tf32 a[2][4];
+              d_frag(16 * q + 8 * kq + t, 1.f, 1.f, a);
+#pragma unroll
+              for (int mt = 0; mt < 2; ++mt) mma_split<false, EXACT_K>(c[mt], a[mt], kf[kq]);
+            }
+          }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          s0[0][2 * mt] = c[mt][0];
+          s1[0][2 * mt] = c[mt][1];
+          s0[0][2 * mt + 1] = c[mt][2];
+          s1[0][2 * mt + 1] = c[mt][3];
         }
         if (ok) {
           st_cols<ST, 4>(gtile + (size_t)r0 * DV + col, s0[0]);
@@ -549,22 +665,22 @@ __device__ __forceinline__ void red_mma(float* red, const float (&y)[16], int wa
 
 // stream_mma with the exact-operand variants chosen by the input and ring-key
 // dtypes.
-template <typename ST, int NTN, int MT, bool FOLD>
+template <typename ST, int NTN, int MT, bool FOLD, bool LONG = false>
 __device__ __forceinline__ bool stream_mma_dt(const TilePipe<ST>& pipe, int in_dt, int rk_dt,
                                               const float* hkf, const float* hd, const float* hf,
                                               int n, float decay, const float* xf, ST* gtile,
                                               int tid, int warp, int lane, float (&y)[16]) {
   const bool xk = in_dt != DT_F32, kk = FOLD && rk_dt != DT_F32;
   if (xk) {
-    return kk ? stream_mma<ST, NTN, MT, FOLD, true, true>(pipe, hkf, hd, hf, n, decay, xf, gtile,
-                                                          tid, warp, lane, y)
-              : stream_mma<ST, NTN, MT, FOLD, true, false>(pipe, hkf, hd, hf, n, decay, xf, gtile,
-                                                           tid, warp, lane, y);
+    return kk ? stream_mma<ST, NTN, MT, FOLD, true, true, LONG>(pipe, hkf, hd, hf, n, decay, xf,
+                                                                gtile, tid, warp, lane, y)
+              : stream_mma<ST, NTN, MT, FOLD, true, false, LONG>(pipe, hkf, hd, hf, n, decay, xf,
+                                                                 gtile, tid, warp, lane, y);
   }
-  return kk ? stream_mma<ST, NTN, MT, FOLD, false, true>(pipe, hkf, hd, hf, n, decay, xf, gtile,
-                                                         tid, warp, lane, y)
-            : stream_mma<ST, NTN, MT, FOLD, false, false>(pipe, hkf, hd, hf, n, decay, xf, gtile,
-                                                          tid, warp, lane, y);
+  return kk ? stream_mma<ST, NTN, MT, FOLD, false, true, LONG>(pipe, hkf, hd, hf, n, decay, xf,
+                                                               gtile, tid, warp, lane, y)
+            : stream_mma<ST, NTN, MT, FOLD, false, false, LONG>(pipe, hkf, hd, hf, n, decay, xf,
+                                                                gtile, tid, warp, lane, y);
 }
 
 // Narrow windows keep four CTAs per SM (at most 128 registers per thread),
@@ -572,12 +688,12 @@ __device__ __forceinline__ bool stream_mma_dt(const TilePipe<ST>& pipe, int in_d
 // the widest trade occupancy for their larger accumulator tiles.
 // RAGGED: windows of different lengths from p.cu (verify widths only); the
 // uniform kernels keep the window length a launch constant.
-// LONG: GDN decode on a ring longer than 16 records, whose own folds carry
-// more than 16 records; it leaves out the tensor-core fold (up to 16 records),
-// whose code slows the general fold when both are compiled into one kernel.
 // TC: GDN windows of 3..8 tokens (NT 4 and 8) with 128 value columns stream on
 // the 5th-generation tensor cores when p.tc is set (stream_tc).
-template <int ALGO, typename ST, int NT, bool RAGGED, bool LONG = false, bool TC = false>
+// LONG: GDN decode and four- and eight-token windows on rings longer than 16
+// records: their tensor-core folds take up to kMmaFoldRecords records (the
+// kernels of shorter rings keep the tighter code of folds of at most 16).
+template <int ALGO, typename ST, int NT, bool RAGGED, bool TC = false, bool LONG = false>
 __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     replay_kernel(const ReplayParams p) {
   constexpr int NV = 2 * NT;             // mat-vec vectors: k_i at [0, NT), q_i at [NT, 2NT)
@@ -758,11 +874,14 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
   const int sw = split ? kSplitWarps : kWarps;  // warps that stream the tile
   // Four- and eight-token GDN windows with 128 value columns stream on the
   // tensor cores (mat-vec inputs and fold keys in fragment order, column sums
-  // in ymm); a fold there takes at most 16 records and a ring of at least 16.
+  // in ymm); a fold there takes at most 16 records (LONG: up to
+  // kMmaFoldRecords, as many groups of 16 as the key buffer holds).
   constexpr bool kMmaNT = ALGO == ALGO_GDN && (NT == 4 || NT == 8);
   constexpr int NTN = NV >= 8 ? NV / 8 : 1;  // n-tiles of eight vectors
+  constexpr int kFoldMax = LONG ? kMmaFoldRecords : 16;
   const bool mmas = !TC && kMmaNT && dv == 128 && pipe.tr.cr % 8 == 0 &&
-                    (!fold || (nh <= 16 && L >= 16));
+                    (!fold || (LONG ? nh <= kFoldMax && ((nh + 15) & ~15) <= round4(L)
+                                    : nh <= 16 && L >= 16));
   const size_t kbase = ((size_t)s * HV + h) * L * dk;
   const size_t dbase = ((size_t)s * HV + h) * L * dv;
   const size_t gbase = ((size_t)s * HV + h) * L * (ALGO == ALGO_GDN ? 1 : dk);
@@ -1016,7 +1135,11 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
           tc_fold_keys(hk, kl, hkraw, nh, dk, p.rk_dt, tid, kThreads);
           fence_async_smem();
         } else if (fold && mmas) {
-          frag_keys16(hk, hkraw, nh, dk, p.rk_dt, tid, kThreads);
+          if (LONG) {
+            frag_keys(hk, hkraw, nh, dk, p.rk_dt, tid, kThreads);
+          } else {
+            frag_keys16(hk, hkraw, nh, dk, p.rk_dt, tid, kThreads);
+          }
         } else if (fold) {
           transpose_keys(hk, hkraw, nh, dk, p.rk_dt, tid, kThreads);
         } else {
@@ -1100,8 +1223,23 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
     if (!early) {
       __syncthreads();
       if (fold && nh > 0) {
-        if constexpr (NT == 1 && ALGO == ALGO_GDN && !LONG) {
-          mma_fold = nh <= 16 && dv == 128 && pipe.tr.cr % 16 == 0;
+        if constexpr (NT == 1 && ALGO == ALGO_GDN) {
+          mma_fold = nh <= kFoldMax && dv == 128 && pipe.tr.cr % 16 == 0;
+        }
+        // the tensor-core folds read the deltas of records m >= 16 as f_m d_m,
+        // scaled in place over the gate factors of step 1 (a folding window
+        // reads hd nowhere else)
+        if (LONG && (mmas || mma_fold) && nh > 16) {
+          for (int e = 16 * (dv / 4) + tid; e < nh * (dv / 4); e += kThreads) {
+            const float f = hf[e / (dv / 4)];
+            float4 d4 = reinterpret_cast<float4*>(hd)[e];
+            d4.x *= f;
+            d4.y *= f;
+            d4.z *= f;
+            d4.w *= f;
+            reinterpret_cast<float4*>(hd)[e] = d4;
+          }
+          __syncthreads();
         }
         if (TC && tc) {
           if constexpr (TC) {
@@ -1113,18 +1251,18 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
           }
         } else if (mmas) {
           if constexpr (kMmaNT) {
-            copies_ok = stream_mma_dt<ST, NTN, 2, true>(pipe, p.in_dt, p.rk_dt, hk, hd, hf, nh,
-                                                        hscal[1], xh, gtile, tid, warp, lane,
-                                                        ymm) &&
+            copies_ok = stream_mma_dt<ST, NTN, 2, true, LONG>(pipe, p.in_dt, p.rk_dt, hk, hd, hf,
+                                                              nh, hscal[1], xh, gtile, tid, warp,
+                                                              lane, ymm) &&
                         copies_ok;
           }
         } else if (mma_fold) {
-          if constexpr (NT == 1 && ALGO == ALGO_GDN && !LONG) {
+          if constexpr (NT == 1 && ALGO == ALGO_GDN) {
             copies_ok = (p.rk_dt == DT_F32
-                             ? fold_stream_mma<ST, false>(pipe, hk, hd, hf, nh, hscal[1], xh, gtile,
-                                                          tid, warp, lane, ymma)
-                             : fold_stream_mma<ST, true>(pipe, hk, hd, hf, nh, hscal[1], xh, gtile,
-                                                         tid, warp, lane, ymma)) &&
+                             ? fold_stream_mma<ST, false, LONG>(pipe, hk, hd, hf, nh, hscal[1], xh,
+                                                                gtile, tid, warp, lane, ymma)
+                             : fold_stream_mma<ST, true, LONG>(pipe, hk, hd, hf, nh, hscal[1], xh,
+                                                               gtile, tid, warp, lane, ymma)) &&
                         copies_ok;
           }
         } else {

@@ -155,6 +155,8 @@ __host__ __device__ constexpr int ring_stages(int NT, int L) {
 // the checkpoint tile while the others stage the history and compute the
 // window and history coefficients.
 constexpr int kSplitWarps = 2;
+// longest history the verify kernel's tensor-core fold takes (in groups of 16)
+constexpr int kMmaFoldRecords = 64;
 __host__ __device__ constexpr bool can_split(int algo, int NT) {
   return algo == ALGO_GDN && NT <= 4;
 }

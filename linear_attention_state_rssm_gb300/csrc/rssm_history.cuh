@@ -106,6 +106,26 @@ __device__ __forceinline__ void frag_keys16(float* hkf, const void* raw, int n, 
   }
 }
 
+// The same for any n, in ng = ceil(n / 16) groups of 16 records: for rows [8s, 8s + 8) and group q lane (g, t) finds at
+// hkf[4 (32 (ng s + q) + 4 g + t)] the keys of row 8s + g from records
+// 16q + t, 16q + t + 4, 16q + t + 8 and 16q + t + 12 (zero for records >= n).
+// hkf holds dk * 16 * ng floats.
+__device__ __forceinline__ void frag_keys(float* hkf, const void* raw, int n, int dk, int dt,
+                                          int t, int nt) {
+  const int ng = (n + 15) >> 4;
+  for (int e = t; e < dk * 4 * ng; e += nt) {
+    const int blk = e >> 5, ln = e & 31, s8 = blk / ng, q = blk - s8 * ng;
+    const int row = 8 * s8 + (ln >> 2), m0 = 16 * q + (ln & 3);
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int m = m0 + 4 * j;
+      v[j] = m < n ? ld_f32(raw, (size_t)m * dk + row, dt) : 0.f;
+    }
+    *reinterpret_cast<float4*>(hkf + 4 * e) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
 // GDN, warp 0: hf[m] holds the raw record gates g_m; replaces them with
 // exp(sum_{m' > m} g_m') and writes Gam, exp(Gam) to scal[0], scal[1].
 __device__ __forceinline__ void gdn_history_scan(int n, float* hf, float* scal, int lane) {
