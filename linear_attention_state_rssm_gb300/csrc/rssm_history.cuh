@@ -106,7 +106,8 @@ __device__ __forceinline__ void frag_keys16(float* hkf, const void* raw, int n, 
   }
 }
 
-// The same for any n, in ng = ceil(n / 16) groups of 16 records: for rows [8s, 8s + 8) and group q lane (g, t) finds at
+// The same for any n, in ng = ceil(n / 16) groups of 16 records: for rows
+// [8s, 8s + 8) and group q lane (g, t) finds at
 // hkf[4 (32 (ng s + q) + 4 g + t)] the keys of row 8s + g from records
 // 16q + t, 16q + t + 4, 16q + t + 8 and 16q + t + 12 (zero for records >= n).
 // hkf holds dk * 16 * ng floats.
