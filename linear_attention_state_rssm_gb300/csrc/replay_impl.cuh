@@ -321,8 +321,9 @@ __device__ __forceinline__ int swap_rank(const unsigned* fmask, int y) {
 // of the checkpoint is folded as
 //     S <- e^Gam S + K~^T D~,   K~^T [16 rows x n records], D~ [n records x 128]
 // with the keys transposed in hkt (row stride round4(n); records >= n read as
-// zero), D~ = f_m d_m (f_m = hf[m], the decay from record m to the end of the
-// history), the tile rows from the ring stage as the fp32 accumulator, the
+// zero; LONG with kdt 16-bit: the ring's keys transposed in place, which are
+// exact in tf32), D~ = f_m d_m (f_m = hf[m], the decay from record m to the
+// end of the history), the tile rows from the ring stage as the fp32 accumulator, the
 // folded rows stored back to the checkpoint and fed to the mat-vec
 // y_v = S^T x_v (x from xh [dk][2]). The D~ fragments of records [0, 16) stay
 // in registers for the whole tile; those of later records (LONG) come from
@@ -334,7 +335,8 @@ template <typename ST, bool EXACT_K, bool LONG>
 __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const float* hkt,
                                                 const float* hd, const float* hf, int n,
                                                 float decay, const float* xh, ST* gtile, int tid,
-                                                int warp, int lane, float (&y)[4][2][2]) {
+                                                int warp, int lane, float (&y)[4][2][2],
+                                                int kdt = DT_F32) {
   constexpr int DV = 128, NV = 2;
   const int g = lane >> 2, t = lane & 3, c0 = warp * 32, ks = round4(n);
   Tf32 bf[2][4][2];
@@ -357,13 +359,20 @@ __device__ __forceinline__ bool fold_stream_mma(const TilePipe<ST>& pipe, const 
       y[nt][c][1] = 0.f;
     }
   }
+  // transposed key i: fp32, or (LONG, kdt 16-bit) the ring's own 16-bit keys
+  auto key = [&](int i) -> float {
+    if constexpr (LONG) {
+      if (kdt != DT_F32) return ld_f32(hkt, (size_t)i, kdt);
+    }
+    return hkt[i];
+  };
   // A fragment of records ma = 8 kq + t and ma + 4 for rows ra and ra + 8
   auto key_frag = [&](int ra, int kq, Tf32 (&a)[4]) {
     const int rb = ra + 8, ma = 8 * kq + t, mb = ma + 4;
-    a[0] = tf32_split<EXACT_K>(ma < n ? hkt[ra * ks + ma] : 0.f);
-    a[1] = tf32_split<EXACT_K>(ma < n ? hkt[rb * ks + ma] : 0.f);
-    a[2] = tf32_split<EXACT_K>(mb < n ? hkt[ra * ks + mb] : 0.f);
-    a[3] = tf32_split<EXACT_K>(mb < n ? hkt[rb * ks + mb] : 0.f);
+    a[0] = tf32_split<EXACT_K>(ma < n ? key(ra * ks + ma) : 0.f);
+    a[1] = tf32_split<EXACT_K>(ma < n ? key(rb * ks + ma) : 0.f);
+    a[2] = tf32_split<EXACT_K>(mb < n ? key(ra * ks + mb) : 0.f);
+    a[3] = tf32_split<EXACT_K>(mb < n ? key(rb * ks + mb) : 0.f);
   };
   bool ok = true;
   const int cr = pipe.tr.cr;
@@ -1134,6 +1143,9 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
           float* kl = p.rk_dt == DT_F32 ? reinterpret_cast<float*>(smem + p.sm.kl) : nullptr;
           tc_fold_keys(hk, kl, hkraw, nh, dk, p.rk_dt, tid, kThreads);
           fence_async_smem();
+        } else if (fold && LONG && p.sm.kip) {
+          // (every fold of this plan runs on the tensor cores: mma_fold below)
+          transpose_keys16_inplace(reinterpret_cast<uint16_t*>(hkraw), nh, dk, tid, kThreads);
         } else if (fold && mmas) {
           if (LONG) {
             frag_keys(hk, hkraw, nh, dk, p.rk_dt, tid, kThreads);
@@ -1258,11 +1270,14 @@ __global__ void __launch_bounds__(kThreads, NT <= 4 ? 4 : NT == 8 ? 3 : 2)
           }
         } else if (mma_fold) {
           if constexpr (NT == 1 && ALGO == ALGO_GDN) {
+            const bool kip = LONG && p.sm.kip;
+            const float* hkt = kip ? reinterpret_cast<const float*>(hkraw) : hk;
             copies_ok = (p.rk_dt == DT_F32
-                             ? fold_stream_mma<ST, false, LONG>(pipe, hk, hd, hf, nh, hscal[1], xh,
+                             ? fold_stream_mma<ST, false, LONG>(pipe, hkt, hd, hf, nh, hscal[1], xh,
                                                                 gtile, tid, warp, lane, ymma)
-                             : fold_stream_mma<ST, true, LONG>(pipe, hk, hd, hf, nh, hscal[1], xh,
-                                                               gtile, tid, warp, lane, ymma)) &&
+                             : fold_stream_mma<ST, true, LONG>(pipe, hkt, hd, hf, nh, hscal[1], xh,
+                                                               gtile, tid, warp, lane, ymma,
+                                                               kip ? p.rk_dt : (int)DT_F32)) &&
                         copies_ok;
           }
         } else {

@@ -118,6 +118,8 @@ struct ReplaySmem {
   uint32_t hdot;   // [L][2NT] history dot coefficients
   uint32_t red;    // [row groups][2NT][dv] partial column sums (on the ring when it fits)
   uint32_t rank;   // decode row order: [kThreads] (slot, cursor), [kWarps] fold masks
+  uint32_t kip;    // 1: GDN decode on a long ring with 16-bit keys; a fold transposes the
+                   // landed keys in place ([dk][round4(n)], 16-bit) and hk is empty
   uint32_t ns;     // tile ring stages
   uint32_t total;
 };
@@ -370,12 +372,20 @@ __host__ __device__ inline ReplaySmem replay_layout_ns(int algo, int state_bytes
   m.xl = off;    if (tc && in_dt == DT_F32) off = align16(off + 4u * dk * 16);
   m.am = off;    off = align16(off + 4u * NT * NT);
   m.fm = off;    off = align16(off + 4u * NT * NT);
-  m.hk = off;    off = align16(off + 4u * round4(L) * dk);
+  // GDN decode on a ring of 17..kMmaFoldRecords records with 16-bit keys and
+  // 128 value columns: every fold runs on the tensor cores, which take the
+  // keys transposed in place in their landing zone (at most eight 16-byte
+  // rows of keys per thread), so the fp32 key region is left out
+  const bool kip = algo == ALGO_GDN && NT == 1 && L > 16 && L <= kMmaFoldRecords &&
+                   rk_dt != DT_F32 && dv == 128 && dk % 16 == 0 && dk >= 32 &&
+                   round4(L) * dk <= 64 * kThreads;
+  m.kip = kip ? 1u : 0u;
+  m.hk = off;    if (!kip) off = align16(off + 4u * round4(L) * dk);
   m.kl = off;    if (tc && rk_dt == DT_F32) off = align16(off + 4u * 16 * dk);
   {
     // ring keys land in hkraw; KDA's record gates land in hk and become the
     // decayed keys there
-    const uint32_t raw = (uint32_t)(dtype_bytes(rk_dt) * L * dk);
+    const uint32_t raw = (uint32_t)(kip ? 2 * round4(L) * dk : dtype_bytes(rk_dt) * L * dk);
     const uint32_t hc = can_split(algo, NT) ? 4u * NV * dv : 0u;
     m.hkraw = off; off = align16(off + (raw > hc ? raw : hc));
   }
@@ -399,7 +409,7 @@ __host__ __device__ inline ReplaySmem replay_layout_ns(int algo, int state_bytes
   // before the CTA barrier that follows the copies (ring keys land in hkraw),
   // unless KDA's gates land there (they get a region of their own).
   m.rank = m.hk;
-  if (NT == 1 && (kda || 4u * round4(L) * dk < kRankBytes)) {
+  if (NT == 1 && (kda || kip || 4u * round4(L) * dk < kRankBytes)) {
     m.rank = off;
     off = align16(off + kRankBytes);
   }

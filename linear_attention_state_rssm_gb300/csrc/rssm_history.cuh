@@ -87,6 +87,43 @@ __device__ __forceinline__ void transpose_keys(float* hkt, const void* raw, int 
   }
 }
 
+// Keys of n records as they landed, [n][dk] 16-bit, transposed in place to
+// [dk][ks] 16-bit (ks = round4(n), entries m in [n, ks) zero). Every one of
+// the nt threads of the CTA (t its index) takes part, with two CTA barriers:
+// each first holds at most kKipVec 16-byte rows of eight keys in registers,
+// so n * dk <= 8 * kKipVec * nt. Consecutive threads take consecutive
+// records, so the 2-byte stores of a warp land in consecutive halves.
+constexpr int kKipVec = 8;
+__device__ __forceinline__ void transpose_keys16_inplace(uint16_t* raw, int n, int dk, int t,
+                                                         int nt) {
+  const int ks = round4(n), c8n = dk / 8, nvec = n * c8n;
+  uint4 v[kKipVec];
+#pragma unroll
+  for (int i = 0; i < kKipVec; ++i) {
+    const int e = t + i * nt;
+    if (e < nvec) {
+      const int m = e % n, c8 = e / n;
+      v[i] = reinterpret_cast<const uint4*>(raw)[m * c8n + c8];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kKipVec; ++i) {
+    const int e = t + i * nt;
+    if (e < nvec) {
+      const int m = e % n, c8 = e / n;
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        raw[(8 * c8 + j) * ks + m] = (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
+      }
+    }
+  }
+  const int pad = ks - n;
+  for (int e = t; e < dk * pad; e += nt) raw[(e / pad) * ks + n + e % pad] = 0;
+  __syncthreads();
+}
+
 // The raw keys of n <= 16 records in the order of the B fragments of an
 // m16n8k8 product with the records as k and eight rows as n: for rows
 // [8s, 8s + 8) lane (g, t) finds at hkf[4 (32 s + 4 g + t)] the keys of row
