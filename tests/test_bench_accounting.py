@@ -73,3 +73,16 @@ def test_commit_summary_carries_a_roofline_only_for_a_folding_commit():
     assert fe["roofline"]["achieved"] == pytest.approx(50.0)
     assert fe["roofline"]["frac"] == pytest.approx(50.0 / 6000.0)
     assert fe["per_layer_us"] == pytest.approx(60.0 / 48)
+
+
+def test_full_grid_covers_every_throughput_configuration():
+    """--sweep --grid full: GDN and KDA, batch {1, 8, 64, 128, 256}, ring length
+    {16, 32, 64}, window {1, 3, 8}, fp32 and bf16 checkpoints, each once."""
+    grid = bench.GRID
+    assert len(grid) == len(set(grid)) == 2 * 5 * 3 * 3 * 2
+    assert {g[0] for g in grid} == {"gdn", "kda"}
+    assert {g[1] for g in grid} == {1, 8, 64, 128, 256}
+    assert {g[2] for g in grid} == {16, 32, 64}
+    assert {g[3] for g in grid} == {1, 3, 8}
+    assert {g[4] for g in grid} == {"f32", "bf16"}
+    assert all(g[5] == "lazy" and g[3] <= g[2] for g in grid)
