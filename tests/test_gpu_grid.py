@@ -24,16 +24,12 @@ def _lib():
     build.build()
 
 
-@pytest.mark.parametrize("state", ["f32", "bf16"])
-@pytest.mark.parametrize("T", [1, 3, 8])
-@pytest.mark.parametrize("L", [16, 32, 64])
-@pytest.mark.parametrize("algo", ["gdn", "kda"])
-def test_grid_configuration(algo, L, T, state):
+def _chain(algo, L, T, state, ring_k="f16"):
     B = 5
     HK, HV = (1, 2) if algo == "gdn" else (2, 2)
     run = Run(algo=algo, HK=HK, HV=HV, dk=128, dv=128, L=L, max_T=T,
               slots=np.arange(B, dtype=np.int32), n_slots=B, in_dtype="bf16",
-              state_dtype=state, ring_k_dtype="f16", config_id=40 + L + T)
+              state_dtype=state, ring_k_dtype=ring_k, config_id=40 + L + T)
     steps = L + 6 if T == 1 else -(-5 * L // (2 * T)) + 4
     folds = np.zeros(B, dtype=np.int64)
     overflow = False
@@ -60,3 +56,19 @@ def test_grid_configuration(algo, L, T, state):
     assert overflow, "no window folded for lack of ring room"
     assert run.ring_d_err() <= TOL16
     assert run.store.rssm_get_device_error() == 0
+
+
+@pytest.mark.parametrize("state", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 3, 8])
+@pytest.mark.parametrize("L", [16, 32, 64])
+@pytest.mark.parametrize("algo", ["gdn", "kda"])
+def test_grid_configuration(algo, L, T, state):
+    _chain(algo, L, T, state)
+
+
+@pytest.mark.parametrize("state", ["f32", "bf16"])
+@pytest.mark.parametrize("L", [32, 64])
+def test_long_ring_decode_with_bf16_ring_keys(L, state):
+    """GDN decode on long rings with bf16 ring keys: the fold reads the keys as
+    they landed, transposed in place (the 16-bit key path of long rings)."""
+    _chain("gdn", L, 1, state, ring_k="bf16")
