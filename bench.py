@@ -1157,6 +1157,27 @@ def sweep_point(torch, dev, algo, B, L, T, state_dtype, mode, steps, warmup, pea
             "replay_gbs": gbs, "frac_of_hbm_peak": gbs / peak, "device_error_word": err}
 
 
+def grid_summary():
+    """The full throughput grid (GRID: GDN and KDA x batch x ring length x
+    window x checkpoint dtype, lazy commit), five timed steps after three
+    warm-up steps per point, as compact rows for the bench line."""
+    import torch
+    dev = torch.device("cuda", 0)
+    peak, peak_kind = peaks()
+    rows, err = [], 0
+    for pt in GRID:
+        p = sweep_point(torch, dev, *pt, steps=5, warmup=3, peak=peak)
+        rows.append([p["algo"], p["batch"], p["L"], p["T"], p["state_dtype"],
+                     round(p["ms_per_layer"] * 1e3, 2), round(p["frac_of_hbm_peak"], 4)])
+        err |= p["device_error_word"]
+    return {"columns": ["algo", "batch", "L", "T", "state_dtype", "us_per_layer",
+                        "frac_of_hbm_peak"],
+            "rows": rows, "commit_mode": "lazy", "steps": 5, "warmup": 3, "peak_gbs": peak,
+            "peak_kind": peak_kind, "device_error_word": err,
+            "note": "per-layer time includes the step's cursor advance or commit; bytes count "
+                    "the replay launches"}
+
+
 def run_sweep(args):
     """--sweep: a steady-state grid of decode and verify launches over batch,
     ring length, window width, state dtype, and GDN and KDA heads."""
@@ -1190,6 +1211,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the replay prefill line")
     ap.add_argument("--no-conv", action="store_true", help="skip the conv window line")
     ap.add_argument("--no-kda", action="store_true", help="skip the KDA decode+verify line")
+    ap.add_argument("--no-grid", action="store_true",
+                    help="skip the full throughput grid summary (N = 1 only)")
     ap.add_argument("--plan", default="auto", choices=["auto", "rows", "pipe", "tc"],
                     help="kernel family for GDN decode/verify (rssm_set_plan)")
     ap.add_argument("--sweep", action="store_true",
@@ -1221,6 +1244,11 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
+        if world == 1 and not args.no_grid:
+            try:
+                res["grid"] = grid_summary()
+            except Exception as e:  # the headline line stands on its own
+                res["grid"] = {"error": f"{type(e).__name__}: {e}"}
         if world == 1 and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline()
         print(json.dumps(res), flush=True)
