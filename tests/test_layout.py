@@ -104,3 +104,24 @@ def test_long_ring_decode_keys_in_place(probe):
 ])
 def test_ctas_per_sm(probe, cfg, ctas):
     assert probe([cfg])[0]["ctas"] == ctas
+
+
+def _nt_for(T):
+    return 1 if T == 1 else 2 if T == 2 else 4 if T <= 4 else 8 if T <= 8 else 16
+
+
+def test_no_narrower_window_outgrows_the_widest(probe):
+    """rssm_alloc checks that the widest window a store allows fits in shared
+    memory; no narrower window of the same store may need more than the limit
+    (the plans are not monotone in T: eight-token windows drop a ring stage)."""
+    cfgs = [(algo, sb, _nt_for(T), T, L, dk, dv, BF16, rk, rd, 0)
+            for algo in (GDN, KDA) for sb in (4, 2) for L in (16, 20, 32, 64, 128, 256)
+            for dk, dv in ((128, 128), (256, 128), (128, 256), (256, 256))
+            for rk in (F32, F16) for rd in (F32, F16) for T in range(1, 17) if T <= L]
+    total = {}
+    for cfg, m in zip(cfgs, probe(cfgs)):
+        total.setdefault(cfg[:2] + cfg[4:], {})[cfg[3]] = m["total"]
+    for key, by_t in total.items():
+        for max_t, worst in by_t.items():
+            if worst <= MAX_SMEM:
+                assert all(by_t[t] <= MAX_SMEM for t in by_t if t <= max_t), (key, max_t)
