@@ -114,8 +114,10 @@ enum {
 
 /*
  * Store configuration. Supported: dk, dv in {32, 64, 128}; HV a multiple of HK;
- * 1 <= max_T <= 16; max_T <= L <= 256 (a ring shorter than
- * the widest window is refused, SGLang fork PR jianc99/sglang#2, first commit);
+ * 1 <= max_T <= 16; max_T <= L <= 64 (a ring shorter than
+ * the widest window is refused, SGLang fork PR jianc99/sglang#2, first commit;
+ * a longer ring is RSSM_ERR_UNSUPPORTED: a fold carries the whole history and
+ * the fold kernel takes at most 64 records);
  * in_dtype F32|BF16; state_dtype F32|BF16; ring_k_dtype F32|F16|BF16;
  * ring_d_dtype F32|F16. commit_mode selects what rssm_commit does.
  */

@@ -24,7 +24,10 @@ struct rssm_handle {
 
 namespace {
 
-constexpr int kMaxL = 256;
+// Rings of up to 64 records: a fold (rssm_fold, a fold-every commit after
+// decode history) carries the whole history, and the fold kernel's streams
+// take at most 64 records.
+constexpr int kMaxL = 64;
 constexpr int kMaxT = 16;
 constexpr int kMaxGrid = 65535;
 

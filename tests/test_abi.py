@@ -65,6 +65,7 @@ def test_required_bytes_matches_layouts(lib):
     (dict(ring_d_dtype="bf16"), 2),      # bf16 deltas not built
     (dict(n_slots=0), 1),
     (dict(L=300, max_T=1), 2),
+    (dict(L=65, max_T=1), 2),            # a fold carries at most 64 records
 ])
 def test_host_validation(lib, kw, status):
     base = dict(algo="gdn", n_layers=1, n_slots=2, HK=2, HV=4, dk=64, dv=64, L=8, max_T=2,
@@ -74,6 +75,11 @@ def test_host_validation(lib, kw, status):
     with pytest.raises(_lib.RssmError) as e:
         _lib.rssm_required_bytes(cfg)
     assert e.value.status == status
+
+
+def test_longest_ring_is_accepted(lib):
+    cfg = _lib.make_config("gdn", 1, 2, 2, 4, 128, 128, 64, 16, "bf16", "f32")
+    assert _lib.rssm_required_bytes(cfg).state == 2 * 4 * 128 * 128 * 4
 
 
 def test_alloc_refuses_bad_buffers_before_touching_the_device(lib):
