@@ -86,3 +86,20 @@ def test_full_grid_covers_every_throughput_configuration():
     assert {g[3] for g in grid} == {1, 3, 8}
     assert {g[4] for g in grid} == {"f32", "bf16"}
     assert all(g[5] == "lazy" and g[3] <= g[2] for g in grid)
+
+
+def test_grid_summary_rows(monkeypatch):
+    """The bench line's grid object: one compact row per grid point, in GRID
+    order, device error words OR-ed (sweep_point stubbed: no GPU here)."""
+    def fake_point(torch, dev, algo, B, L, T, state, mode, steps, warmup, peak, plan="auto"):
+        assert (mode, steps, warmup) == ("lazy", 5, 3)
+        return {"algo": algo, "batch": B, "L": L, "T": T, "state_dtype": state,
+                "ms_per_layer": 0.001 * L, "frac_of_hbm_peak": 0.5,
+                "device_error_word": 8 if (algo, B, L, T) == ("kda", 8, 32, 3) else 0}
+    monkeypatch.setattr(bench, "sweep_point", fake_point)
+    g = bench.grid_summary()
+    assert g["columns"] == ["algo", "batch", "L", "T", "state_dtype", "us_per_layer",
+                            "frac_of_hbm_peak"]
+    assert [tuple(r[:5]) for r in g["rows"]] == [pt[:5] for pt in bench.GRID]
+    assert all(r[5] == r[2] for r in g["rows"])  # 0.001 ms per record -> L us
+    assert g["device_error_word"] == 8 and g["commit_mode"] == "lazy"
